@@ -1,0 +1,177 @@
+/*
+ * lora_mixed.h -- C ABI of the mixed-batch multi-adapter LoRA linear layer.
+ *
+ * One call computes, for a batch whose tokens are split into segments that
+ * each name their own adapter (decode tokens, prefill segments and
+ * fine-tuning segments alike):
+ *
+ *     y[t,:] = x[t,:] W + s_a * (x[t,:] A_a) B_a          (row-vector form)
+ *
+ * which is the LoRA layer W_eff = W + BA ("DeltaServe: Host-Agnostic
+ * Co-Serving of Inference and Fine-Tuning for LLMs", section 2.2; "MOLT: A
+ * Fine-Grained GPU Memory Sharing System for LLM Serving with Opportunistic
+ * Fine-Tuning", section 2.1, h(x) = Wx + BAx) batched over many adapters in
+ * one base-model pass (multi-LoRA batching, DeltaServe section 2.2), with
+ * fine-tuning samples carried as ordinary prefill-like entries on their own
+ * adapter (DeltaServe section 3.2, "Mixed forward batch").  A second call
+ * computes the LoRA backward of the fine-tuning segments (DeltaServe section
+ * 3.2, "Backward subprocess": LoRA gradients from captured activations, with
+ * unsaved intermediates recomputed):
+ *
+ *     v      = dY B_a^T
+ *     dX     = dY W^T + s_a * v A_a^T
+ *     dB_a  += s_a * (x A_a)^T dY          summed over a's fine-tuning tokens
+ *     dA_a  += s_a * x^T v                 (stored transposed, see below)
+ *
+ * Layouts (all row-major, element offsets, no padding):
+ *   x   [T,K]          layer input, one row per token
+ *   Wt  [N,K]          the frozen weight stored transposed (nn.Linear layout)
+ *   A   pool of blocks; adapter a's block is A_a stored as [r_a, K]
+ *       (the paper's A in R^{r x k}), starting at element a_off[a]
+ *   B   pool of blocks; adapter a's block is [r_a, N] (the paper's B^T),
+ *       starting at element b_off[a]
+ *   y   [T,N]
+ *   dA, dB  float32, shaped exactly like the A and B pools (same offsets)
+ *
+ * Conventions shared by every entry point:
+ *   - Device pointers unless marked HOST.  The caller owns every buffer; the
+ *     library allocates no device memory and keeps no pointer after a call.
+ *   - Everything is validated on the host before anything is launched.  On
+ *     error the call returns a negative LORA_ERR_* code, writes nothing,
+ *     launches nothing, and lora_last_error() describes the problem.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without waiting for it.  Segment-table
+ *     planning happens on the host; the plan is copied into `workspace` with
+ *     an asynchronous copy from pageable host memory, so the host-side
+ *     segment array may be reused as soon as the call returns.
+ *   - Two calls that share a workspace must not overlap on the GPU.
+ *   - Kernels never wait without a bound.  If one gives up, it records a
+ *     nonzero code in the workspace's status word; lora_workspace_status()
+ *     reads it.
+ */
+#ifndef LORA_MIXED_H
+#define LORA_MIXED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* One batch segment: tokens [start, start+len) use adapter `adapter_id`
+ * (-1: base projection only).  is_train != 0 marks a fine-tuning segment;
+ * it must name an adapter (>= 0).  The segments of a call must cover [0, T)
+ * exactly once, in any order; zero-length segments are ignored. */
+typedef struct lora_segment {
+    int32_t start;
+    int32_t len;
+    int32_t adapter_id;
+    int32_t is_train;
+} lora_segment_t;
+
+/* The stacked adapter pool (MOLT section 2.1: each adapter holds r(d+k)
+ * trainable values; here each adapter keeps its own rank, no padding to a
+ * common maximum). */
+typedef struct lora_pool {
+    const void* A;          /* device, element type of the call; blocks [r_a, K] */
+    const void* B;          /* device, element type of the call; blocks [r_a, N] */
+    const int64_t* a_off;   /* HOST [n_adapters]; a multiple of K */
+    const int64_t* b_off;   /* HOST [n_adapters]; a multiple of N */
+    const int32_t* rank;    /* HOST [n_adapters]; 1 <= r_a <= 128 */
+    const float* scale;     /* HOST [n_adapters]; s_a (LoRA alpha / r) */
+    int32_t n_adapters;
+} lora_pool_t;
+
+typedef enum lora_dtype { LORA_BF16 = 0, LORA_F32 = 1 } lora_dtype_t;
+
+/* flags */
+enum {
+    LORA_SAVE_XA = 1,          /* forward: write x A_a of fine-tuning rows to xa_save */
+    LORA_RECOMPUTE_XA = 2,     /* backward: recompute x A_a even if xa_saved is given */
+    LORA_ACCUMULATE_GRAD = 4,  /* backward: add into dA/dB instead of overwriting */
+    LORA_DEBUG_CHECKS = 8      /* reserved: extra host-side checks */
+};
+
+/* return codes */
+enum {
+    LORA_OK = 0,
+    LORA_ERR_INVALID_ARG = -1,  /* null pointer, negative size, bad flag combination */
+    LORA_ERR_SEGMENTS = -2,     /* segments overlap, leave a gap, or leave [0,T) */
+    LORA_ERR_ADAPTER = -3,      /* adapter id out of range, or pool offsets out of shape */
+    LORA_ERR_TRAIN_BASE = -4,   /* fine-tuning segment on adapter -1 */
+    LORA_ERR_ALIGNMENT = -5,    /* bf16: x/Wt/A/B/y/dY/dX not 16-byte aligned, or K, N not multiples of 8 */
+    LORA_ERR_WORKSPACE = -6,    /* workspace missing, too small or not 256-byte aligned */
+    LORA_ERR_DTYPE = -7,        /* unknown dtype */
+    LORA_ERR_CUDA = -8,         /* a CUDA runtime call failed (message in lora_last_error) */
+    LORA_ERR_RANK = -9,         /* rank outside [1, 128] */
+    LORA_ERR_LIMIT = -10,       /* beyond a documented size limit (see below) */
+    LORA_ERR_TIMEOUT = -11      /* reported by lora_workspace_status: a kernel gave up waiting */
+};
+
+/* Limits: T, K, N < 2^31; sum over segments of len*r fits in int32;
+ * at most 48 fine-tuning segments per call; bf16 path: K, N multiples of 8. */
+#define LORA_MAX_RANK 128
+#define LORA_MAX_TRAIN_SEGMENTS 48
+
+/* Bytes of device workspace that lora_mixed_forward and lora_mixed_backward
+ * need for this segment table (the larger of the two).  Returns 0 and sets
+ * lora_last_error on invalid input; a valid empty batch still needs a small
+ * nonzero workspace (the status word). */
+size_t lora_workspace_size(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool,
+                           const lora_segment_t* segs /* HOST */, int32_t n_segs);
+
+/* Bytes of the saved-activation buffer: for every fine-tuning segment, in
+ * increasing start order, a [len, r_a] row-major block of x A_a in the call's
+ * element type (DeltaServe section 3.2: activation capture for the
+ * fine-tuning rows of a mixed batch).  Returns 0 on invalid input. */
+size_t lora_xa_size(lora_dtype_t dt, const lora_pool_t* pool, const lora_segment_t* segs /* HOST */,
+                    int32_t n_segs);
+
+/* Forward over every segment of the batch.
+ *   x [T,K], Wt [N,K], y [T,N] in element type dt; y is written for all T rows.
+ *   xa_save: with LORA_SAVE_XA, receives x A_a of the fine-tuning rows
+ *            (layout of lora_xa_size); otherwise ignored, may be NULL.
+ *   workspace: device, 256-byte aligned, >= lora_workspace_size bytes. */
+int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                       const lora_pool_t* pool, const lora_segment_t* segs /* HOST */, int32_t n_segs, void* y,
+                       void* xa_save, uint32_t flags, void* workspace, size_t ws_bytes, void* stream);
+
+/* LoRA backward of the fine-tuning segments.
+ *   dY [T,N]: only fine-tuning rows are read.
+ *   xa_saved: the forward's xa_save for the same segment table, or NULL to
+ *             recompute x A_a (also recomputed under LORA_RECOMPUTE_XA).
+ *   dX [T,K]: only fine-tuning rows are written.  May be NULL (skipped).
+ *   dA, dB:   float32, pool-shaped.  Blocks of adapters with a fine-tuning
+ *             segment are overwritten (or added to, LORA_ACCUMULATE_GRAD);
+ *             all other entries are left untouched.  Contributions of
+ *             several segments on one adapter are summed in a fixed order,
+ *             so repeated calls give bitwise-identical results.  */
+int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                        const lora_pool_t* pool, const lora_segment_t* segs /* HOST */, int32_t n_segs,
+                        const void* dY, const void* xa_saved, void* dX, float* dA, float* dB, uint32_t flags,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* lora_last_error(void);
+
+/* Waits for `stream`, then reads the workspace status word of the last call
+ * that used `workspace`: LORA_OK, or LORA_ERR_TIMEOUT if a kernel gave up a
+ * bounded wait (its outputs are then incomplete).  Blocking. */
+int lora_workspace_status(const void* workspace, void* stream);
+
+/* Diagnostic: the forward tile plan of a segment table, for host-side tests.
+ *   n_tiles_out: number of 128-row tiles.
+ *   rows_out [cap*128]: token row held by each tile row, -1 for none.
+ *   info_out [cap*4]: per tile {gathered (1: rows copied out of x, 0: a
+ *              contiguous window of x), number of adapters, LoRA columns
+ *              (sum of ranks rounded up to 16), first x row of the window}.
+ * Returns LORA_OK, a validation error, or LORA_ERR_LIMIT if cap is short. */
+int lora_plan_describe(int32_t T, int32_t K, int32_t N, const lora_pool_t* pool, const lora_segment_t* segs,
+                       int32_t n_segs, int32_t* n_tiles_out, int32_t* rows_out, int32_t* info_out, int32_t cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_MIXED_H */

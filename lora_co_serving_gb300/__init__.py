@@ -1,0 +1,235 @@
+"""Python binding of the mixed-batch multi-adapter LoRA layer library (``liblora_mixed.so``).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  The entry points mirror
+``include/lora_mixed.h``:
+
+    forward(x, Wt, pool, segs, ...)         -> y   (and the saved xA when asked)
+    backward(x, Wt, pool, segs, dY, ...)    -> dX, dA, dB
+
+``segs`` is an int32 array (or list) of rows {start, len, adapter_id, is_train};
+``Pool`` holds the stacked adapter factors (A blocks [r_a, K], B blocks [r_a, N])
+on the device plus their host-side offsets, ranks and scales.
+
+If the compiled library is missing, calls raise ``LibraryNotBuilt``: there is no
+fallback path.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import _build
+
+__all__ = ["Pool", "forward", "backward", "workspace_size", "xa_size", "workspace_status", "plan_describe",
+           "LoraError", "LibraryNotBuilt", "library", "build", "SAVE_XA", "RECOMPUTE_XA", "ACCUMULATE_GRAD"]
+
+SAVE_XA = 1
+RECOMPUTE_XA = 2
+ACCUMULATE_GRAD = 4
+BF16 = 0
+F32 = 1
+
+ERRORS = {0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_SEGMENTS", -3: "LORA_ERR_ADAPTER",
+          -4: "LORA_ERR_TRAIN_BASE", -5: "LORA_ERR_ALIGNMENT", -6: "LORA_ERR_WORKSPACE", -7: "LORA_ERR_DTYPE",
+          -8: "LORA_ERR_CUDA", -9: "LORA_ERR_RANK", -10: "LORA_ERR_LIMIT", -11: "LORA_ERR_TIMEOUT"}
+
+EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_mixed_backward", "lora_last_error",
+            "lora_workspace_status", "lora_plan_describe"]
+
+
+class LoraError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("%s (%d): %s" % (ERRORS.get(code, "?"), code, msg))
+        self.code = code
+
+
+class LibraryNotBuilt(ImportError):
+    pass
+
+
+class _Segment(ctypes.Structure):
+    _fields_ = [("start", ctypes.c_int32), ("len", ctypes.c_int32), ("adapter_id", ctypes.c_int32),
+                ("is_train", ctypes.c_int32)]
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("a_off", ctypes.c_void_p),
+                ("b_off", ctypes.c_void_p), ("rank", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("n_adapters", ctypes.c_int32)]
+
+
+_LIB = None
+
+
+def build(force=False):
+    """Compile the CUDA library for sm_103a (in-tree) and return its path."""
+    return _build.build(force=force)
+
+
+def library(path=None):
+    """The loaded ``liblora_mixed.so`` (ctypes); raises LibraryNotBuilt if it has not been built."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise LibraryNotBuilt("liblora_mixed.so is not built; run lora_co_serving_gb300.build()")
+    lib = ctypes.CDLL(p)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    lib.lora_workspace_size.argtypes = [I32, I32, I32, ctypes.c_int, P, P, I32]
+    lib.lora_workspace_size.restype = SZ
+    lib.lora_xa_size.argtypes = [ctypes.c_int, P, P, I32]
+    lib.lora_xa_size.restype = SZ
+    lib.lora_mixed_forward.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, I32, P, P, ctypes.c_uint32, P, SZ, P]
+    lib.lora_mixed_forward.restype = ctypes.c_int
+    lib.lora_mixed_backward.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, I32, P, P, P, P, P, ctypes.c_uint32,
+                                        P, SZ, P]
+    lib.lora_mixed_backward.restype = ctypes.c_int
+    lib.lora_last_error.argtypes = []
+    lib.lora_last_error.restype = ctypes.c_char_p
+    lib.lora_workspace_status.argtypes = [P, P]
+    lib.lora_workspace_status.restype = ctypes.c_int
+    lib.lora_plan_describe.argtypes = [I32, I32, I32, P, P, I32, P, P, P, I32]
+    lib.lora_plan_describe.restype = ctypes.c_int
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _check(rc):
+    if rc != 0:
+        raise LoraError(rc, library().lora_last_error().decode())
+
+
+def _ptr(t):
+    """Raw address of a torch tensor / numpy array (None -> NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("unsupported dtype %s (bf16 or float32)" % t.dtype)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def segments(segs):
+    """Segment table as a contiguous int32 [n, 4] numpy array."""
+    a = np.ascontiguousarray(np.asarray(segs, dtype=np.int32).reshape(-1, 4))
+    return a
+
+
+class Pool:
+    """Stacked adapter pool: A (concatenated [r_a, K] blocks) and B (concatenated [r_a, N] blocks) on the device,
+    with host arrays of element offsets, ranks and scales."""
+
+    def __init__(self, A, B, a_off, b_off, rank, scale):
+        self.A = A
+        self.B = B
+        self.a_off = np.ascontiguousarray(a_off, dtype=np.int64)
+        self.b_off = np.ascontiguousarray(b_off, dtype=np.int64)
+        self.rank = np.ascontiguousarray(rank, dtype=np.int32)
+        self.scale = np.ascontiguousarray(scale, dtype=np.float32)
+        n = self.rank.shape[0]
+        self._c = _Pool(_ptr(A), _ptr(B), _ptr(self.a_off), _ptr(self.b_off), _ptr(self.rank), _ptr(self.scale), n)
+
+    @property
+    def n_adapters(self):
+        return int(self.rank.shape[0])
+
+    def cptr(self):
+        return ctypes.addressof(self._c)
+
+
+def workspace_size(T, K, N, dtype_code, pool, segs):
+    s = segments(segs)
+    n = library().lora_workspace_size(T, K, N, dtype_code, pool.cptr(), _ptr(s), s.shape[0])
+    if n == 0:
+        raise LoraError(-1, library().lora_last_error().decode())
+    return int(n)
+
+
+def xa_size(dtype_code, pool, segs):
+    s = segments(segs)
+    return int(library().lora_xa_size(dtype_code, pool.cptr(), _ptr(s), s.shape[0]))
+
+
+def _workspace(T, K, N, code, pool, s, workspace, device):
+    import torch
+    need = workspace_size(T, K, N, code, pool, s)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace
+
+
+def forward(x, Wt, pool, segs, y=None, xa_save=None, save_xa=False, workspace=None, stream=None):
+    """y [T, N] = x W + per-segment LoRA; returns y, or (y, xa_save) when save_xa is set."""
+    import torch
+    T, K = x.shape
+    N = Wt.shape[0]
+    code = _dtype_code(x)
+    s = segments(segs)
+    if y is None:
+        y = torch.empty((T, N), dtype=x.dtype, device=x.device)
+    if save_xa and xa_save is None:
+        n = xa_size(code, pool, s) // x.element_size()
+        xa_save = torch.empty(max(n, 1), dtype=x.dtype, device=x.device)
+    ws = _workspace(T, K, N, code, pool, s, workspace, x.device)
+    flags = SAVE_XA if save_xa else 0
+    _check(library().lora_mixed_forward(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), _ptr(s), s.shape[0], _ptr(y),
+                                        _ptr(xa_save), flags, _ptr(ws), ws.numel(), _stream_ptr(stream)))
+    return (y, xa_save) if save_xa else y
+
+
+def backward(x, Wt, pool, segs, dY, xa_saved=None, dX=None, dA=None, dB=None, want_dx=True, want_grads=True,
+             recompute=False, accumulate=False, workspace=None, stream=None):
+    """LoRA backward of the fine-tuning segments; returns (dX, dA, dB) (dA/dB float32, pool-shaped)."""
+    import torch
+    T, K = x.shape
+    N = Wt.shape[0]
+    code = _dtype_code(x)
+    s = segments(segs)
+    if want_dx and dX is None:
+        dX = torch.zeros((T, K), dtype=x.dtype, device=x.device)
+    if want_grads and dA is None:
+        dA = torch.zeros(pool.A.numel(), dtype=torch.float32, device=x.device)
+    if want_grads and dB is None:
+        dB = torch.zeros(pool.B.numel(), dtype=torch.float32, device=x.device)
+    ws = _workspace(T, K, N, code, pool, s, workspace, x.device)
+    flags = (RECOMPUTE_XA if recompute else 0) | (ACCUMULATE_GRAD if accumulate else 0)
+    _check(library().lora_mixed_backward(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), _ptr(s), s.shape[0],
+                                         _ptr(dY), _ptr(xa_saved), _ptr(dX) if want_dx else None,
+                                         _ptr(dA) if want_grads else None, _ptr(dB) if want_grads else None, flags,
+                                         _ptr(ws), ws.numel(), _stream_ptr(stream)))
+    return dX, dA, dB
+
+
+def workspace_status(workspace, stream=None):
+    """Raise LoraError if a kernel of the last call on this workspace gave up a bounded wait."""
+    _check(library().lora_workspace_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def plan_describe(T, K, N, pool, segs, cap=None):
+    """(rows [n_tiles, 128], info [n_tiles, 4]) of the forward tile plan; info = gathered, adapters, LoRA cols, x row."""
+    s = segments(segs)
+    cap = cap or (T // 128 + 2 * s.shape[0] + 8)
+    rows = np.zeros((cap, 128), np.int32)
+    info = np.zeros((cap, 4), np.int32)
+    nt = ctypes.c_int32(0)
+    _check(library().lora_plan_describe(T, K, N, pool.cptr(), _ptr(s), s.shape[0], ctypes.addressof(nt), _ptr(rows),
+                                        _ptr(info), cap))
+    return rows[:nt.value], info[:nt.value]

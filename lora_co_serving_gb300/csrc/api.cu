@@ -1,0 +1,523 @@
+// api.cu -- the C ABI (include/lora_mixed.h): validation, planning, staging, tensor maps and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "lora_mixed.h"
+#include "plan.h"
+#include "simt.h"
+#include "tc_kernel.h"
+
+using namespace lora;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+    g_err = msg;
+    return code;
+}
+
+#define CUDA_TRY(expr)                                                                         \
+    do {                                                                                       \
+        cudaError_t e_ = (expr);                                                               \
+        if (e_ != cudaSuccess) return fail(LORA_ERR_CUDA, std::string(#expr) + ": " + cudaGetErrorString(e_)); \
+    } while (0)
+
+// ------------------------------------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] with row stride `ld` elements, 128-byte swizzled boxes {box_in, box_out}.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_in,
+               uint32_t box_out, std::string* err) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) { *err = "cuTensorMapEncodeTiled is not available from the driver"; return false; }
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_in, box_out};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ") for a [" + std::to_string(outer) +
+               ", " + std::to_string(inner) + "] tensor";
+        return false;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------------------------------------ device info
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 64 && cache[dev]) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+// ------------------------------------------------------------------------------------------------ host staging
+// The plan travels host -> workspace through a small ring of pinned buffers per device, so the copy is
+// truly asynchronous.  A slot is reused only after the event recorded behind its copy has completed.
+struct StagingRing {
+    static constexpr int kSlots = 8;
+    struct Slot {
+        void* host = nullptr;
+        size_t cap = 0;
+        cudaEvent_t ev = nullptr;
+        bool pending = false;
+    };
+    std::mutex mu;
+    Slot slot[kSlots];
+    int next = 0;
+};
+StagingRing g_rings[64];
+
+int stage_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
+    if (bytes == 0) return LORA_OK;
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    if (dev >= 64) {   // unusual device index: fall back to a pageable copy
+        CUDA_TRY(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, stream));
+        return LORA_OK;
+    }
+    StagingRing& R = g_rings[dev];
+    std::lock_guard<std::mutex> lock(R.mu);
+    StagingRing::Slot& s = R.slot[R.next];
+    R.next = (R.next + 1) % StagingRing::kSlots;
+    if (s.pending) {
+        CUDA_TRY(cudaEventSynchronize(s.ev));
+        s.pending = false;
+    }
+    if (!s.ev) CUDA_TRY(cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming));
+    if (s.cap < bytes) {
+        if (s.host) CUDA_TRY(cudaFreeHost(s.host));
+        s.host = nullptr;
+        size_t cap = std::max<size_t>(bytes, 1 << 16);
+        CUDA_TRY(cudaHostAlloc(&s.host, cap, cudaHostAllocPortable));
+        s.cap = cap;
+    }
+    std::memcpy(s.host, src, bytes);
+    CUDA_TRY(cudaMemcpyAsync(dst, s.host, bytes, cudaMemcpyHostToDevice, stream));
+    CUDA_TRY(cudaEventRecord(s.ev, stream));
+    s.pending = true;
+    return LORA_OK;
+}
+
+template <class T>
+void put(std::vector<uint8_t>& blob, size_t off, const std::vector<T>& v) {
+    if (!v.empty()) std::memcpy(blob.data() + off, v.data(), sizeof(T) * v.size());
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Write the plan (tiles ... per-CTA lists) into a host blob laid out exactly like the workspace prefix.
+void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&off)[2],
+                const std::vector<int32_t> (&lst)[2], std::vector<uint8_t>* blob) {
+    blob->assign(L.plan_end - L.tiles, 0);
+    auto at = [&](size_t o) { return o - L.tiles; };
+    std::vector<uint8_t>& b = *blob;
+    put(b, at(L.tiles), pl.tiles);
+    put(b, at(L.chunks), pl.chunks);
+    put(b, at(L.rowmap), pl.rowmap);
+    put(b, at(L.rowchunk), pl.rowchunk);
+    put(b, at(L.rowaux), pl.rowaux);
+    put(b, at(L.groups), pl.groups);
+    put(b, at(L.tsegs), pl.tsegs);
+    for (int k = 0; k < 2; ++k) {
+        put(b, at(L.items[k]), pl.items[k]);
+        put(b, at(L.cta_off[k]), off[k]);
+        put(b, at(L.cta_list[k]), lst[k]);
+    }
+}
+
+void fill_plan_pointers(KParams* P, uint8_t* ws, const Layout& L, int launch) {
+    P->tiles = reinterpret_cast<const TileDesc*>(ws + L.tiles);
+    P->chunks = reinterpret_cast<const Chunk*>(ws + L.chunks);
+    P->rowmap = reinterpret_cast<const int32_t*>(ws + L.rowmap);
+    P->rowchunk = reinterpret_cast<const int32_t*>(ws + L.rowchunk);
+    P->rowaux = reinterpret_cast<const int32_t*>(ws + L.rowaux);
+    P->groups = reinterpret_cast<const GradGroup*>(ws + L.groups);
+    P->tsegs = reinterpret_cast<const TrainSeg*>(ws + L.tsegs);
+    P->items = reinterpret_cast<const WorkItem*>(ws + L.items[launch]);
+    P->cta_off = reinterpret_cast<const int32_t*>(ws + L.cta_off[launch]);
+    P->cta_list = reinterpret_cast<const int32_t*>(ws + L.cta_list[launch]);
+    P->status = reinterpret_cast<int32_t*>(ws + L.status);
+}
+
+int check_workspace(void* workspace, size_t ws_bytes, size_t need) {
+    if (!workspace) return fail(LORA_ERR_WORKSPACE, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+        return fail(LORA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < need)
+        return fail(LORA_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes, got " +
+                                            std::to_string(ws_bytes));
+    return LORA_OK;
+}
+
+// ------------------------------------------------------------------------------------------------ float32 path
+struct F32Blob {
+    std::vector<uint8_t> bytes;
+    size_t tok = 0, ad = 0, segs = 0, xa = 0, dyb = 0;
+};
+
+void f32_layout(const Problem& p, size_t base, F32Blob* fb) {
+    auto al = [](size_t v) { return (v + 255) & ~size_t(255); };
+    fb->tok = base;
+    fb->ad = fb->tok + al(sizeof(int32_t) * (size_t)p.T);
+    fb->segs = fb->ad + al(32 * (size_t)(p.n_adapters + 1));
+    fb->xa = fb->segs + al(32 * (size_t)(p.segs.size() + 1));
+    fb->dyb = fb->xa + al(sizeof(float) * (size_t)p.T * 128);
+    fb->bytes.assign(fb->xa - fb->tok, 0);
+    std::vector<int32_t> tok(p.T, -1);
+    std::vector<F32Seg> segs(p.segs.size());
+    int64_t xo = 0;
+    for (size_t i = 0; i < p.segs.size(); ++i) {
+        const auto& s = p.segs[i];
+        for (int32_t t = s.start; t < s.start + s.len; ++t) tok[t] = s.adapter_id;
+        F32Seg f{};
+        f.start = s.start; f.len = s.len; f.adapter = s.adapter_id; f.is_train = s.is_train;
+        f.xoff = -1;
+        if (s.is_train) { f.xoff = int32_t(xo); xo += (int64_t)s.len * p.rank[s.adapter_id]; }
+        segs[i] = f;
+    }
+    std::vector<AdapterRec> ad(p.n_adapters);
+    for (int32_t a = 0; a < p.n_adapters; ++a) {
+        ad[a] = AdapterRec{p.a_off[a], p.b_off[a], p.rank[a], p.scale[a], 0, 0};
+    }
+    put(fb->bytes, fb->tok - base, tok);
+    put(fb->bytes, fb->ad - base, ad);
+    put(fb->bytes, fb->segs - base, segs);
+}
+
+int begin_call(const Layout& L, void* ws, size_t bytes_plan, const void* blob, cudaStream_t stream) {
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    CUDA_TRY(cudaMemsetAsync(w + L.status, 0, 256, stream));
+    return stage_copy(w + L.tiles, blob, bytes_plan, stream);
+}
+
+}  // namespace
+
+// ================================================================================================== C ABI
+extern "C" {
+
+const char* lora_last_error(void) { return g_err.c_str(); }
+
+size_t lora_workspace_size(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool,
+                           const lora_segment_t* segs, int32_t n_segs) {
+    Problem p;
+    std::string err;
+    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err);
+    if (rc != LORA_OK) { g_err = err; return 0; }
+    Plan f, b;
+    plan_forward(p, &f);
+    plan_backward(p, true, true, true, true, &b);
+    return std::max(layout_of(p, f, false).total, layout_of(p, b, true).total);
+}
+
+size_t lora_xa_size(lora_dtype_t dt, const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs) {
+    if (dt != LORA_BF16 && dt != LORA_F32) { g_err = "unknown dtype"; return 0; }
+    if (!pool || (n_segs > 0 && !segs) || n_segs < 0) { g_err = "NULL pool or segments"; return 0; }
+    size_t elems = 0;
+    for (int32_t i = 0; i < n_segs; ++i) {
+        const lora_segment_t& s = segs[i];
+        if (!s.is_train || s.len <= 0) continue;
+        if (s.adapter_id < 0 || s.adapter_id >= pool->n_adapters || !pool->rank) { g_err = "bad adapter id"; return 0; }
+        elems += (size_t)s.len * (size_t)pool->rank[s.adapter_id];
+    }
+    return elems * (dt == LORA_BF16 ? 2 : 4);
+}
+
+int lora_workspace_status(const void* workspace, void* stream) {
+    if (!workspace) return fail(LORA_ERR_WORKSPACE, "workspace is NULL");
+    CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    int32_t st = 0;
+    CUDA_TRY(cudaMemcpy(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost));
+    if (st != 0) return fail(st, "a kernel gave up a bounded wait; outputs of that call are incomplete");
+    return LORA_OK;
+}
+
+int lora_plan_describe(int32_t T, int32_t K, int32_t N, const lora_pool_t* pool, const lora_segment_t* segs,
+                       int32_t n_segs, int32_t* n_tiles_out, int32_t* rows_out, int32_t* info_out, int32_t cap) {
+    Problem p;
+    std::string err;
+    int rc = validate(T, K, N, LORA_BF16, pool, segs, n_segs, &p, &err);
+    if (rc != LORA_OK) return fail(rc, err);
+    Plan pl;
+    plan_forward(p, &pl);
+    const int32_t nt = int32_t(pl.tiles.size());
+    if (n_tiles_out) *n_tiles_out = nt;
+    if (nt > cap) return fail(LORA_ERR_LIMIT, "capacity too small for " + std::to_string(nt) + " tiles");
+    for (int32_t i = 0; i < nt; ++i) {
+        if (rows_out) std::memcpy(rows_out + (size_t)i * kTileM, &pl.rowmap[(size_t)i * kTileM], sizeof(int32_t) * kTileM);
+        if (info_out) {
+            info_out[4 * i + 0] = pl.tiles[i].a_src;
+            info_out[4 * i + 1] = pl.tiles[i].nchunk;
+            info_out[4 * i + 2] = pl.tiles[i].ext_k;
+            info_out[4 * i + 3] = pl.tiles[i].a_src ? -1 : pl.tiles[i].a_row0;
+        }
+    }
+    return LORA_OK;
+}
+
+int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                       const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, void* y, void* xa_save,
+                       uint32_t flags, void* workspace, size_t ws_bytes, void* stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    Problem p;
+    std::string err;
+    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err);
+    if (rc != LORA_OK) return fail(rc, err);
+    if (flags & ~uint32_t(LORA_SAVE_XA | LORA_RECOMPUTE_XA | LORA_ACCUMULATE_GRAD | LORA_DEBUG_CHECKS))
+        return fail(LORA_ERR_INVALID_ARG, "unknown flag bits");
+    const bool save = (flags & LORA_SAVE_XA) && p.xa_elems > 0;
+    if (T > 0 && (!x || !Wt || !y)) return fail(LORA_ERR_INVALID_ARG, "x, Wt and y must be non-NULL");
+    if (p.n_adapters > 0 && (!pool->A || !pool->B)) return fail(LORA_ERR_INVALID_ARG, "pool A/B must be non-NULL");
+    if (save && !xa_save) return fail(LORA_ERR_INVALID_ARG, "LORA_SAVE_XA needs xa_save");
+    if (dt == LORA_BF16 && T > 0 &&
+        (!aligned16(x) || !aligned16(Wt) || !aligned16(y) || (p.n_adapters && (!aligned16(pool->A) || !aligned16(pool->B)))))
+        return fail(LORA_ERR_ALIGNMENT, "x, Wt, y, A and B must be 16-byte aligned");
+
+    if (dt == LORA_F32) {
+        Plan empty;
+        Layout L = layout_of(p, empty, false);
+        rc = check_workspace(workspace, ws_bytes, L.total);
+        if (rc) return rc;
+        if (T == 0) return LORA_OK;
+        F32Blob fb;
+        f32_layout(p, L.simt, &fb);
+        uint8_t* w = static_cast<uint8_t*>(workspace);
+        CUDA_TRY(cudaMemsetAsync(w + L.status, 0, 256, stream));
+        rc = stage_copy(w + fb.tok, fb.bytes.data(), fb.bytes.size(), stream);
+        if (rc) return rc;
+        F32Args a{};
+        a.T = T; a.K = K; a.N = N;
+        a.x = static_cast<const float*>(x); a.Wt = static_cast<const float*>(Wt);
+        a.A = static_cast<const float*>(pool->A); a.B = static_cast<const float*>(pool->B);
+        a.ad = reinterpret_cast<const AdapterRec*>(w + fb.ad);
+        a.tok_ad = reinterpret_cast<const int32_t*>(w + fb.tok);
+        a.segs = reinterpret_cast<const F32Seg*>(w + fb.segs);
+        a.n_segs = int32_t(p.segs.size());
+        a.xa = reinterpret_cast<float*>(w + fb.xa);
+        a.y = static_cast<float*>(y);
+        a.xa_save = save ? static_cast<float*>(xa_save) : nullptr;
+        a.xa_elems = p.xa_elems;
+        CUDA_TRY(f32_forward(a, stream));
+        return LORA_OK;
+    }
+
+    Plan pl;
+    plan_forward(p, &pl);
+    Layout L = layout_of(p, pl, false);
+    rc = check_workspace(workspace, ws_bytes, L.total);
+    if (rc) return rc;
+    if (T == 0) return LORA_OK;
+    const int sms = sm_count();
+    if (sms <= 0) return fail(LORA_ERR_CUDA, "no CUDA device available");
+    std::vector<int32_t> off[2], lst[2];
+    int grid[2];
+    for (int k = 0; k < 2; ++k) {
+        grid[k] = std::min<int>(std::min(sms, kMaxCtas), (int)pl.items[k].size());
+        if (grid[k] > 0) assign_items(pl.items[k], pl, grid[k], &off[k], &lst[k]);
+    }
+    std::vector<uint8_t> blob;
+    build_blob(pl, L, off, lst, &blob);
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    KParams P;
+    std::memset(&P, 0, sizeof(P));
+    if (!encode_2d(&P.tm_x, x, K, T, K, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
+    if (pl.n_gtiles > 0 && !encode_2d(&P.tm_xg, ws + L.xg, K, (uint64_t)pl.n_gtiles * kTileM, K, 64, 128, &err))
+        return fail(LORA_ERR_CUDA, err);
+    if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 256, &err)) return fail(LORA_ERR_CUDA, err);
+    if (p.rows_a > 0 && !encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    if (p.rows_b > 0 && !encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    P.zin = ws + L.z;
+    P.zout = ws + L.z;
+    P.out = static_cast<__nv_bfloat16*>(y);
+    P.out_ld = N;
+    P.out_cols = N;
+    P.xa_save = save ? static_cast<__nv_bfloat16*>(xa_save) : nullptr;
+    P.K = K;
+    P.N = N;
+
+    rc = begin_call(L, workspace, blob.size(), blob.data(), stream);
+    if (rc) return rc;
+    if (pl.n_gtiles > 0) {
+        const int32_t first = int32_t(pl.tiles.size()) - pl.n_gtiles;
+        CUDA_TRY(gather_rows(x, K, reinterpret_cast<const int32_t*>(ws + L.rowmap) + (size_t)first * kTileM,
+                             ws + L.xg, pl.n_gtiles * kTileM, stream));
+    }
+    for (int k = 0; k < 2; ++k) {
+        if (grid[k] == 0) continue;
+        fill_plan_pointers(&P, ws, L, k);
+        CUDA_TRY(tc_launch(P, grid[k], stream));
+    }
+    return LORA_OK;
+}
+
+int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                        const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, const void* dY,
+                        const void* xa_saved, void* dX, float* dA, float* dB, uint32_t flags, void* workspace,
+                        size_t ws_bytes, void* stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    Problem p;
+    std::string err;
+    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err);
+    if (rc != LORA_OK) return fail(rc, err);
+    if (flags & ~uint32_t(LORA_SAVE_XA | LORA_RECOMPUTE_XA | LORA_ACCUMULATE_GRAD | LORA_DEBUG_CHECKS))
+        return fail(LORA_ERR_INVALID_ARG, "unknown flag bits");
+    const bool recompute = (xa_saved == nullptr) || (flags & LORA_RECOMPUTE_XA);
+    const bool acc = (flags & LORA_ACCUMULATE_GRAD) != 0;
+    if (p.n_train > 0) {
+        if (!x || !Wt || !dY) return fail(LORA_ERR_INVALID_ARG, "x, Wt and dY must be non-NULL");
+        if (!pool->A || !pool->B) return fail(LORA_ERR_INVALID_ARG, "pool A/B must be non-NULL");
+        if (dt == LORA_BF16 && (!aligned16(x) || !aligned16(Wt) || !aligned16(dY) || (dX && !aligned16(dX)) ||
+                                !aligned16(pool->A) || !aligned16(pool->B)))
+            return fail(LORA_ERR_ALIGNMENT, "x, Wt, dY, dX, A and B must be 16-byte aligned");
+        if ((dA && (reinterpret_cast<uintptr_t>(dA) & 3)) || (dB && (reinterpret_cast<uintptr_t>(dB) & 3)))
+            return fail(LORA_ERR_ALIGNMENT, "dA and dB must be 4-byte aligned");
+    }
+
+    if (dt == LORA_F32) {
+        Plan empty;
+        Layout L = layout_of(p, empty, true);
+        rc = check_workspace(workspace, ws_bytes, L.total);
+        if (rc) return rc;
+        if (p.n_train == 0) return LORA_OK;
+        F32Blob fb;
+        f32_layout(p, L.simt, &fb);
+        uint8_t* w = static_cast<uint8_t*>(workspace);
+        CUDA_TRY(cudaMemsetAsync(w + L.status, 0, 256, stream));
+        rc = stage_copy(w + fb.tok, fb.bytes.data(), fb.bytes.size(), stream);
+        if (rc) return rc;
+        // adapter groups in order of first appearance by start (host arrays)
+        std::vector<int32_t> g_ad, g_r;
+        std::vector<float> g_s;
+        std::vector<int64_t> g_ao, g_bo;
+        int32_t train_tokens = 0;
+        for (const auto& s : p.segs) {
+            if (!s.is_train) continue;
+            train_tokens += s.len;
+            if (std::find(g_ad.begin(), g_ad.end(), s.adapter_id) == g_ad.end()) {
+                g_ad.push_back(s.adapter_id);
+                g_r.push_back(p.rank[s.adapter_id]);
+                g_s.push_back(p.scale[s.adapter_id]);
+                g_ao.push_back(p.a_off[s.adapter_id]);
+                g_bo.push_back(p.b_off[s.adapter_id]);
+            }
+        }
+        F32Args a{};
+        a.T = T; a.K = K; a.N = N;
+        a.x = static_cast<const float*>(x); a.Wt = static_cast<const float*>(Wt);
+        a.A = static_cast<const float*>(pool->A); a.B = static_cast<const float*>(pool->B);
+        a.ad = reinterpret_cast<const AdapterRec*>(w + fb.ad);
+        a.tok_ad = reinterpret_cast<const int32_t*>(w + fb.tok);
+        a.segs = reinterpret_cast<const F32Seg*>(w + fb.segs);
+        a.n_segs = int32_t(p.segs.size());
+        a.xa = reinterpret_cast<float*>(w + fb.xa);
+        a.dyb = reinterpret_cast<float*>(w + fb.dyb);
+        a.xa_saved = recompute ? nullptr : static_cast<const float*>(xa_saved);
+        a.xa_elems = p.xa_elems;
+        a.dY = static_cast<const float*>(dY);
+        a.dX = static_cast<float*>(dX);
+        a.dA = dA; a.dB = dB;
+        a.accumulate = acc ? 1 : 0;
+        a.train_tokens = train_tokens;
+        a.n_groups = int32_t(g_ad.size());
+        a.group_adapter = g_ad.data(); a.group_r = g_r.data(); a.group_scale = g_s.data();
+        a.group_a_off = g_ao.data(); a.group_b_off = g_bo.data();
+        CUDA_TRY(f32_backward(a, stream));
+        return LORA_OK;
+    }
+
+    Plan pl;
+    plan_backward(p, dX != nullptr, dA != nullptr, dB != nullptr, recompute, &pl);
+    Layout L = layout_of(p, pl, true);
+    rc = check_workspace(workspace, ws_bytes, L.total);
+    if (rc) return rc;
+    if (p.n_train == 0) return LORA_OK;
+    const int sms = sm_count();
+    if (sms <= 0) return fail(LORA_ERR_CUDA, "no CUDA device available");
+    std::vector<int32_t> off[2], lst[2];
+    int grid[2];
+    for (int k = 0; k < 2; ++k) {
+        grid[k] = std::min<int>(std::min(sms, kMaxCtas), (int)pl.items[k].size());
+        if (grid[k] > 0) assign_items(pl.items[k], pl, grid[k], &off[k], &lst[k]);
+    }
+    std::vector<uint8_t> blob;
+    build_blob(pl, L, off, lst, &blob);
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    KParams P;
+    std::memset(&P, 0, sizeof(P));
+    const uint64_t Pcols = (uint64_t)pl.tcols;
+    if (!encode_2d(&P.tm_x, x, K, T, K, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
+    if (!encode_2d(&P.tm_dy, dY, N, T, N, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
+    if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
+    if (!encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    if (!encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    if (!encode_2d(&P.tm_xat, ws + L.xat, Pcols, LORA_MAX_RANK, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    if (!encode_2d(&P.tm_dybt, ws + L.dybt, Pcols, LORA_MAX_RANK, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    const __nv_bfloat16* db = static_cast<const __nv_bfloat16*>(dY);
+    int32_t max_len = 0;
+    for (size_t q = 0; q < pl.tsegs.size(); ++q) {
+        const TrainSeg& s = pl.tsegs[q];
+        max_len = std::max(max_len, s.len);
+        if (!encode_2d(&P.tm_seg_dy[q], db + (size_t)s.start * N, N, s.len, N, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
+        if (!encode_2d(&P.tm_seg_x[q], xb + (size_t)s.start * K, K, s.len, K, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
+    }
+    P.zin = ws + L.z;
+    P.zout = ws + L.z;
+    P.out = static_cast<__nv_bfloat16*>(dX);
+    P.out_ld = K;
+    P.out_cols = K;
+    P.xat = reinterpret_cast<__nv_bfloat16*>(ws + L.xat);
+    P.dybt = reinterpret_cast<__nv_bfloat16*>(ws + L.dybt);
+    P.t_ld = int32_t(Pcols);
+    P.dA = dA;
+    P.dB = dB;
+    P.K = K;
+    P.N = N;
+    P.accumulate = acc ? 1 : 0;
+
+    rc = begin_call(L, workspace, blob.size(), blob.data(), stream);
+    if (rc) return rc;
+    if (!recompute && dB)
+        CUDA_TRY(xat_from_saved(xa_saved, reinterpret_cast<const TrainSeg*>(ws + L.tsegs), int32_t(pl.tsegs.size()),
+                                max_len, ws + L.xat, int32_t(Pcols), stream));
+    for (int k = 0; k < 2; ++k) {
+        if (grid[k] == 0) continue;
+        fill_plan_pointers(&P, ws, L, k);
+        CUDA_TRY(tc_launch(P, grid[k], stream));
+    }
+    return LORA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// common.h -- plan structures shared by the host planner and the sm_103a kernels.
+//
+// The layer is executed as lists of work items over 128-row tiles of tokens:
+//   * a tile is a window of 128 consecutive rows of x (or dY), or 128 rows
+//     copied out of x into a gathered buffer (short decode segments sorted by
+//     adapter, so that one tile meets few adapters);
+//   * each tile carries the list of adapters ("chunks") its rows use; chunk c
+//     owns LoRA columns [zcol, zcol + roundup(r,16)) of the tile;
+//   * the shrink x*A of every tile row is written, scaled and masked to its
+//     own chunk, as the tile's "Z" matrix [128, sum of padded ranks]; the
+//     expand (Z * stacked B) is then extra K-steps of the base GEMM, so the
+//     LoRA term lands in the same accumulator and y is written once.
+#pragma once
+#include <stdint.h>
+
+namespace lora {
+
+constexpr int kTileM = 128;       // rows per tile (MMA M)
+constexpr int kBN = 256;          // output columns per main work item (MMA N)
+constexpr int kBK = 64;           // K elements per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int kStages = 4;
+constexpr int kZBlockBytes = kTileM * kBK * 2;   // one 128x64 bf16 Z block in its shared-memory image
+constexpr int kMaxTrainSegs = 48;
+constexpr int kPassCols = 256;    // LoRA columns per shrink pass (MMA N limit)
+
+enum ItemKind : int32_t {
+    kShrinkFwd = 0,   // Z <- s * mask(x A^T), xa_save <- x A^T           (A: x rows, B: A-pool rows, K-major)
+    kMainFwd = 1,     // y <- x Wt^T + Z Bstack                             (B: Wt K-major; ext: B-pool MN-major)
+    kShrinkDyb = 2,   // Z <- s * mask(dY B^T), dYB^T (transposed) <- dY B^T (A: dY rows, B: B-pool rows)
+    kShrinkXa = 3,    // xA^T (transposed) <- x A^T                         (A: x rows, B: A-pool rows)
+    kMainDx = 4,      // dX <- dY Wt + Z Astack                             (B: Wt MN-major; ext: A-pool MN-major)
+    kGradDb = 5,      // dB^T[n, j] = s * sum_t dY[t,n] xA[t,j]             (A: dY^T MN-major, B: xA^T K-major)
+    kGradDa = 6       // dA^T[k, j] = s * sum_t x[t,k] dYB[t,j]             (A: x^T MN-major, B: dYB^T K-major)
+};
+
+struct TileDesc {
+    int32_t a_row0;   // first row of the window in the row source (x, dY or the gathered buffer)
+    int32_t a_src;    // 0: x / dY window; 1: gathered buffer
+    int32_t chunk0;   // first chunk (index into the chunk array)
+    int32_t nchunk;
+    int32_t ext_k;    // LoRA columns: sum over chunks of roundup(r,16)
+    int32_t z_blk0;   // first Z block of this tile
+    int32_t tpos0;    // backward tiles: column of tile row 0 in the transposed buffers; -1 otherwise
+    int32_t pad;
+};
+
+struct Chunk {
+    int32_t adapter;
+    int32_t zcol;     // multiple of 16
+    int32_t r;
+    int32_t prow_a;   // first row of the adapter's block in the A pool viewed as [rows, K]
+    int32_t prow_b;   // first row of the adapter's block in the B pool viewed as [rows, N]
+    float scale;
+    int32_t pad0, pad1;
+};
+
+struct WorkItem {
+    int32_t kind;
+    int32_t tile;     // tile index; for grad items: grad-group index
+    int32_t n0;       // main: first output column; shrink: first LoRA column of the pass; grad: first row m0
+    int32_t nk;       // main/shrink: k-blocks of the dense loop; grad: total token blocks
+    int32_t mma_n;    // N of the MMA
+    int32_t n_ext;    // main: LoRA k-blocks after the dense loop
+    int32_t pad0, pad1;
+};
+
+struct GradGroup {    // one fine-tuning adapter of a backward call
+    int32_t adapter;
+    int32_t r;
+    int32_t seg0;     // first entry in the train-segment arrays
+    int32_t nseg;
+    int32_t prow_a, prow_b;
+    float scale;
+    int32_t pad;
+};
+
+struct TrainSeg {     // fine-tuning segment; grouped by adapter, increasing start within a group
+    int32_t start;
+    int32_t len;
+    int32_t tpos0;    // first column in the transposed buffers (multiple of 128)
+    int32_t group;
+    int32_t xoff;     // element offset of the segment's [len, r] block in the saved-activation buffer
+    int32_t r;
+    int32_t pad0, pad1;
+};
+
+}  // namespace lora

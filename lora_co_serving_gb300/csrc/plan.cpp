@@ -1,0 +1,396 @@
+// plan.cpp -- host-side validation and tile planning (no CUDA calls).
+#include "plan.h"
+
+#include <algorithm>
+#include <cstring>
+#include <queue>
+#include <utility>
+
+namespace lora {
+
+static inline int32_t pad16(int32_t r) { return (r + 15) & ~15; }
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool, const lora_segment_t* segs,
+             int32_t n_segs, Problem* out, std::string* err) {
+    if (dt != LORA_BF16 && dt != LORA_F32) { *err = "unknown dtype"; return LORA_ERR_DTYPE; }
+    if (T < 0 || K <= 0 || N <= 0 || n_segs < 0) { *err = "T must be >= 0, K and N > 0, n_segs >= 0"; return LORA_ERR_INVALID_ARG; }
+    if (dt == LORA_BF16 && ((K % 8) != 0 || (N % 8) != 0)) {
+        *err = "bf16 layers need K and N to be multiples of 8 (16-byte rows)";
+        return LORA_ERR_ALIGNMENT;
+    }
+    if (n_segs > 0 && segs == nullptr) { *err = "segs is NULL"; return LORA_ERR_INVALID_ARG; }
+    if (pool == nullptr) { *err = "pool is NULL"; return LORA_ERR_INVALID_ARG; }
+    if (pool->n_adapters < 0) { *err = "pool->n_adapters < 0"; return LORA_ERR_INVALID_ARG; }
+    if (pool->n_adapters > 0 && (!pool->a_off || !pool->b_off || !pool->rank || !pool->scale)) {
+        *err = "pool host arrays (a_off, b_off, rank, scale) must be non-NULL";
+        return LORA_ERR_INVALID_ARG;
+    }
+    Problem& p = *out;
+    p = Problem();
+    p.T = T; p.K = K; p.N = N; p.dt = dt;
+    p.n_adapters = pool->n_adapters;
+    p.a_off = pool->a_off; p.b_off = pool->b_off; p.rank = pool->rank; p.scale = pool->scale;
+    for (int32_t a = 0; a < pool->n_adapters; ++a) {
+        int32_t r = pool->rank[a];
+        if (r < 1 || r > LORA_MAX_RANK) { *err = "adapter " + std::to_string(a) + ": rank outside [1,128]"; return LORA_ERR_RANK; }
+        int64_t ao = pool->a_off[a], bo = pool->b_off[a];
+        if (ao < 0 || bo < 0 || ao % K != 0 || bo % N != 0) {
+            *err = "adapter " + std::to_string(a) + ": a_off must be a non-negative multiple of K and b_off of N";
+            return LORA_ERR_ADAPTER;
+        }
+        p.rows_a = std::max<int64_t>(p.rows_a, ao / K + r);
+        p.rows_b = std::max<int64_t>(p.rows_b, bo / N + r);
+        if (p.rows_a > INT32_MAX || p.rows_b > INT32_MAX) { *err = "pool too large"; return LORA_ERR_LIMIT; }
+    }
+    p.segs.reserve(n_segs);
+    for (int32_t i = 0; i < n_segs; ++i) {
+        const lora_segment_t& s = segs[i];
+        if (s.len < 0 || s.start < 0 || (int64_t)s.start + s.len > T) {
+            *err = "segment " + std::to_string(i) + " lies outside [0,T)";
+            return LORA_ERR_SEGMENTS;
+        }
+        if (s.adapter_id < -1 || s.adapter_id >= pool->n_adapters) {
+            *err = "segment " + std::to_string(i) + ": adapter id out of range";
+            return LORA_ERR_ADAPTER;
+        }
+        if (s.is_train && s.adapter_id < 0) {
+            *err = "segment " + std::to_string(i) + ": fine-tuning segment on adapter -1";
+            return LORA_ERR_TRAIN_BASE;
+        }
+        if (s.len > 0) {
+            lora_segment_t c = s;
+            c.is_train = s.is_train ? 1 : 0;
+            p.segs.push_back(c);
+        }
+    }
+    std::stable_sort(p.segs.begin(), p.segs.end(),
+                     [](const lora_segment_t& a, const lora_segment_t& b) { return a.start < b.start; });
+    int64_t at = 0;
+    for (const auto& s : p.segs) {
+        if (s.start != at) {
+            *err = s.start < at ? "segments overlap at token " + std::to_string(s.start)
+                                : "tokens " + std::to_string(at) + ".." + std::to_string(s.start - 1) + " are in no segment";
+            return LORA_ERR_SEGMENTS;
+        }
+        at = (int64_t)s.start + s.len;
+    }
+    if (at != T) { *err = "segments do not cover [0,T)"; return LORA_ERR_SEGMENTS; }
+    for (const auto& s : p.segs) {
+        if (s.is_train) {
+            p.n_train++;
+            p.xa_elems += (int64_t)s.len * p.rank[s.adapter_id];
+        }
+    }
+    if (p.n_train > kMaxTrainSegs) { *err = "more than 48 fine-tuning segments in one call"; return LORA_ERR_LIMIT; }
+    if (p.xa_elems > INT32_MAX) { *err = "saved-activation buffer exceeds 2^31 elements"; return LORA_ERR_LIMIT; }
+    return LORA_OK;
+}
+
+// Build the chunk list of one tile from the adapters of its valid rows (increasing adapter id).
+static void make_chunks(const Problem& p, const int32_t* row_adapter, Plan* pl, TileDesc* td, int32_t* rowchunk) {
+    int32_t ids[kTileM];
+    int n = 0;
+    for (int i = 0; i < kTileM; ++i)
+        if (row_adapter[i] >= 0) ids[n++] = row_adapter[i];
+    std::sort(ids, ids + n);
+    n = int(std::unique(ids, ids + n) - ids);
+    td->chunk0 = int32_t(pl->chunks.size());
+    td->nchunk = n;
+    int32_t zcol = 0;
+    for (int c = 0; c < n; ++c) {
+        int32_t a = ids[c];
+        Chunk ch{};
+        ch.adapter = a;
+        ch.zcol = zcol;
+        ch.r = p.rank[a];
+        ch.prow_a = int32_t(p.a_off[a] / p.K);
+        ch.prow_b = int32_t(p.b_off[a] / p.N);
+        ch.scale = p.scale[a];
+        pl->chunks.push_back(ch);
+        zcol += pad16(ch.r);
+    }
+    td->ext_k = zcol;
+    td->z_blk0 = int32_t(pl->z_blocks);
+    pl->z_blocks += cdiv(zcol, kBK);
+    for (int i = 0; i < kTileM; ++i) {
+        rowchunk[i] = -1;
+        if (row_adapter[i] >= 0)
+            rowchunk[i] = td->chunk0 + int32_t(std::lower_bound(ids, ids + n, row_adapter[i]) - ids);
+    }
+}
+
+void plan_forward(const Problem& p, Plan* out) {
+    Plan& pl = *out;
+    pl = Plan();
+    // xa_save offsets of fine-tuning segments (increasing start)
+    std::vector<int64_t> seg_xoff(p.segs.size(), -1);
+    int64_t xo = 0;
+    for (size_t i = 0; i < p.segs.size(); ++i)
+        if (p.segs[i].is_train) { seg_xoff[i] = xo; xo += (int64_t)p.segs[i].len * p.rank[p.segs[i].adapter_id]; }
+
+    // classify rows: long (windowed) or short (gathered)
+    std::vector<int32_t> row_seg(p.T);
+    std::vector<uint8_t> is_long(p.T, 0);
+    std::vector<std::pair<int64_t, int32_t>> gathered;   // (sort key, row)
+    for (size_t i = 0; i < p.segs.size(); ++i) {
+        const auto& s = p.segs[i];
+        bool shortseg = s.len < kShortSegment && !s.is_train;
+        for (int32_t t = s.start; t < s.start + s.len; ++t) {
+            row_seg[t] = int32_t(i);
+            if (shortseg) gathered.push_back({((int64_t)(s.adapter_id + 1) << 32) | (uint32_t)t, t});
+            else is_long[t] = 1;
+        }
+    }
+    auto add_tile = [&](int32_t a_row0, int32_t a_src, const int32_t* rows) {
+        TileDesc td{};
+        td.a_row0 = a_row0;
+        td.a_src = a_src;
+        td.tpos0 = -1;
+        int32_t row_ad[kTileM];
+        size_t base = pl.rowmap.size();
+        pl.rowmap.resize(base + kTileM);
+        pl.rowchunk.resize(base + kTileM);
+        pl.rowaux.resize(base + kTileM);
+        for (int i = 0; i < kTileM; ++i) {
+            int32_t t = rows[i];
+            pl.rowmap[base + i] = t;
+            row_ad[i] = -1;
+            pl.rowaux[base + i] = -1;
+            if (t >= 0) {
+                const auto& s = p.segs[row_seg[t]];
+                row_ad[i] = s.adapter_id;
+                if (s.is_train) pl.rowaux[base + i] = int32_t(seg_xoff[row_seg[t]] + (int64_t)(t - s.start) * p.rank[s.adapter_id]);
+            }
+        }
+        make_chunks(p, row_ad, &pl, &td, &pl.rowchunk[base]);
+        pl.tiles.push_back(td);
+    };
+    // windows over the long rows
+    int32_t rows[kTileM];
+    for (int32_t t = 0; t < p.T;) {
+        if (!is_long[t]) { ++t; continue; }
+        int32_t w0 = t;
+        for (int i = 0; i < kTileM; ++i) {
+            int32_t r = w0 + i;
+            rows[i] = (r < p.T && is_long[r]) ? r : -1;
+        }
+        add_tile(w0, 0, rows);
+        t = w0 + kTileM;
+    }
+    // gathered tiles: short rows sorted by (adapter, row)
+    std::sort(gathered.begin(), gathered.end());
+    for (size_t g0 = 0; g0 < gathered.size(); g0 += kTileM) {
+        for (int i = 0; i < kTileM; ++i) rows[i] = (g0 + i < gathered.size()) ? gathered[g0 + i].second : -1;
+        add_tile(int32_t(pl.n_gtiles) * kTileM, 1, rows);
+        pl.n_gtiles++;
+    }
+    // items: shrink passes, then main items banded for L2 reuse
+    const int32_t nk = int32_t(cdiv(p.K, kBK));
+    for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
+        const TileDesc& td = pl.tiles[ti];
+        for (int32_t c0 = 0; c0 < td.ext_k; c0 += kPassCols) {
+            WorkItem w{};
+            w.kind = kShrinkFwd;
+            w.tile = int32_t(ti);
+            w.n0 = c0;
+            w.nk = nk;
+            w.mma_n = std::min(kPassCols, td.ext_k - c0);
+            pl.items[0].push_back(w);
+        }
+    }
+    const int32_t n_nt = int32_t(cdiv(p.N, kBN));
+    for (size_t b0 = 0; b0 < pl.tiles.size(); b0 += kBandTiles) {
+        size_t b1 = std::min(pl.tiles.size(), b0 + kBandTiles);
+        for (int32_t nt = 0; nt < n_nt; ++nt)
+            for (size_t ti = b0; ti < b1; ++ti) {
+                WorkItem w{};
+                w.kind = kMainFwd;
+                w.tile = int32_t(ti);
+                w.n0 = nt * kBN;
+                w.nk = nk;
+                w.mma_n = kBN;
+                w.n_ext = int32_t(cdiv(pl.tiles[ti].ext_k, kBK));
+                pl.items[1].push_back(w);
+            }
+    }
+}
+
+void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out) {
+    Plan& pl = *out;
+    pl = Plan();
+    // fine-tuning segments in increasing start order, grouped by adapter
+    std::vector<int32_t> group_of_adapter(p.n_adapters, -1);
+    std::vector<std::vector<int32_t>> members;
+    std::vector<lora_segment_t> tr;
+    for (const auto& s : p.segs)
+        if (s.is_train) tr.push_back(s);
+    for (size_t i = 0; i < tr.size(); ++i) {
+        int32_t a = tr[i].adapter_id;
+        if (group_of_adapter[a] < 0) {
+            group_of_adapter[a] = int32_t(members.size());
+            members.emplace_back();
+        }
+        members[group_of_adapter[a]].push_back(int32_t(i));
+    }
+    // train-segment records ordered by group, then start (the fixed summation order of dA/dB)
+    int64_t tpos = 0, xo = 0;
+    std::vector<int32_t> tpos_of(tr.size()), xoff_of(tr.size());
+    for (size_t i = 0; i < tr.size(); ++i) {
+        tpos_of[i] = int32_t(tpos);
+        tpos += cdiv(tr[i].len, kTileM) * kTileM;
+        xoff_of[i] = int32_t(xo);
+        xo += (int64_t)tr[i].len * p.rank[tr[i].adapter_id];
+    }
+    pl.tcols = tpos;
+    for (size_t g = 0; g < members.size(); ++g) {
+        GradGroup gg{};
+        int32_t a = tr[members[g][0]].adapter_id;
+        gg.adapter = a;
+        gg.r = p.rank[a];
+        gg.seg0 = int32_t(pl.tsegs.size());
+        gg.nseg = int32_t(members[g].size());
+        gg.prow_a = int32_t(p.a_off[a] / p.K);
+        gg.prow_b = int32_t(p.b_off[a] / p.N);
+        gg.scale = p.scale[a];
+        for (int32_t i : members[g])
+            pl.tsegs.push_back(TrainSeg{tr[i].start, tr[i].len, tpos_of[i], int32_t(g), xoff_of[i], gg.r, 0, 0});
+        pl.groups.push_back(gg);
+    }
+    // one tile per 128 rows of each fine-tuning segment
+    for (size_t i = 0; i < tr.size(); ++i) {
+        for (int32_t b = 0; b < tr[i].len; b += kTileM) {
+            TileDesc td{};
+            td.a_row0 = tr[i].start + b;
+            td.a_src = 0;
+            td.tpos0 = tpos_of[i] + b;
+            int32_t row_ad[kTileM];
+            size_t base = pl.rowmap.size();
+            pl.rowmap.resize(base + kTileM);
+            pl.rowchunk.resize(base + kTileM);
+            pl.rowaux.resize(base + kTileM);
+            for (int k = 0; k < kTileM; ++k) {
+                bool v = b + k < tr[i].len;
+                pl.rowmap[base + k] = v ? tr[i].start + b + k : -1;
+                row_ad[k] = v ? tr[i].adapter_id : -1;
+                pl.rowaux[base + k] = -1;
+            }
+            make_chunks(p, row_ad, &pl, &td, &pl.rowchunk[base]);
+            pl.tiles.push_back(td);
+        }
+    }
+    const bool need_dyb = want_dx || want_da;
+    const bool need_xa = want_db && recompute;
+    for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
+        const TileDesc& td = pl.tiles[ti];
+        if (need_dyb) {
+            WorkItem w{};
+            w.kind = kShrinkDyb; w.tile = int32_t(ti); w.n0 = 0; w.nk = int32_t(cdiv(p.N, kBK)); w.mma_n = td.ext_k;
+            pl.items[0].push_back(w);
+        }
+        if (need_xa) {
+            WorkItem w{};
+            w.kind = kShrinkXa; w.tile = int32_t(ti); w.n0 = 0; w.nk = int32_t(cdiv(p.K, kBK)); w.mma_n = td.ext_k;
+            pl.items[0].push_back(w);
+        }
+    }
+    if (want_dx) {
+        const int32_t n_nt = int32_t(cdiv(p.K, kBN));
+        for (size_t b0 = 0; b0 < pl.tiles.size(); b0 += kBandTiles) {
+            size_t b1 = std::min(pl.tiles.size(), b0 + kBandTiles);
+            for (int32_t nt = 0; nt < n_nt; ++nt)
+                for (size_t ti = b0; ti < b1; ++ti) {
+                    WorkItem w{};
+                    w.kind = kMainDx; w.tile = int32_t(ti); w.n0 = nt * kBN; w.nk = int32_t(cdiv(p.N, kBK));
+                    w.mma_n = kBN; w.n_ext = int32_t(cdiv(pl.tiles[ti].ext_k, kBK));
+                    pl.items[1].push_back(w);
+                }
+        }
+    }
+    for (size_t g = 0; g < pl.groups.size(); ++g) {
+        int32_t kb = 0;
+        for (int32_t q = 0; q < pl.groups[g].nseg; ++q) kb += int32_t(cdiv(pl.tsegs[pl.groups[g].seg0 + q].len, kBK));
+        if (want_db)
+            for (int32_t m0 = 0; m0 < p.N; m0 += kTileM) {
+                WorkItem w{};
+                w.kind = kGradDb; w.tile = int32_t(g); w.n0 = m0; w.nk = kb; w.mma_n = pad16(pl.groups[g].r);
+                pl.items[1].push_back(w);
+            }
+        if (want_da)
+            for (int32_t m0 = 0; m0 < p.K; m0 += kTileM) {
+                WorkItem w{};
+                w.kind = kGradDa; w.tile = int32_t(g); w.n0 = m0; w.nk = kb; w.mma_n = pad16(pl.groups[g].r);
+                pl.items[1].push_back(w);
+            }
+    }
+}
+
+static int64_t item_cost(const WorkItem& w) {
+    // rough cycles: an MMA k-block costs ~2 cycles per N column; a stage load at least ~256 cycles
+    int64_t per = std::max<int64_t>(2 * w.mma_n, 256);
+    int64_t c = (int64_t)w.nk * per;
+    if (w.kind == kMainFwd || w.kind == kMainDx) c += (int64_t)w.n_ext * per;
+    return c + 2000;
+}
+
+void assign_items(const std::vector<WorkItem>& items, const Plan&, int G, std::vector<int32_t>* off,
+                  std::vector<int32_t>* list) {
+    std::vector<std::vector<int32_t>> per(G);
+    using E = std::pair<int64_t, int32_t>;
+    std::priority_queue<E, std::vector<E>, std::greater<E>> heap;
+    for (int c = 0; c < G; ++c) heap.push({0, c});
+    for (size_t i = 0; i < items.size(); ++i) {
+        E e = heap.top();
+        heap.pop();
+        per[e.second].push_back(int32_t(i));
+        heap.push({e.first + item_cost(items[i]), e.second});
+    }
+    off->assign(G + 1, 0);
+    list->clear();
+    for (int c = 0; c < G; ++c) {
+        (*off)[c] = int32_t(list->size());
+        list->insert(list->end(), per[c].begin(), per[c].end());
+    }
+    (*off)[G] = int32_t(list->size());
+}
+
+size_t simt_scratch_bytes(const Problem& p) {
+    // per-token adapter ids, adapter records, segment records, then xA and dY B^T scratch [T, 128] each
+    return align256(sizeof(int32_t) * (size_t)p.T) + align256(32 * (size_t)(p.n_adapters + 1)) +
+           align256(32 * (size_t)(p.segs.size() + 1)) + 2 * align256(sizeof(float) * (size_t)p.T * 128);
+}
+
+Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
+    Layout L;
+    size_t at = 0;
+    auto take = [&](size_t bytes) { size_t o = at; at = align256(at + bytes); return o; };
+    L.status = take(256);
+    L.tiles = take(sizeof(TileDesc) * pl.tiles.size());
+    L.chunks = take(sizeof(Chunk) * pl.chunks.size());
+    L.rowmap = take(sizeof(int32_t) * pl.rowmap.size());
+    L.rowchunk = take(sizeof(int32_t) * pl.rowchunk.size());
+    L.rowaux = take(sizeof(int32_t) * pl.rowaux.size());
+    L.groups = take(sizeof(GradGroup) * pl.groups.size());
+    L.tsegs = take(sizeof(TrainSeg) * pl.tsegs.size());
+    for (int k = 0; k < 2; ++k) {
+        L.items[k] = take(sizeof(WorkItem) * pl.items[k].size());
+        L.cta_off[k] = take(sizeof(int32_t) * (kMaxCtas + 1));
+        L.cta_list[k] = take(sizeof(int32_t) * pl.items[k].size());
+    }
+    L.plan_end = at;
+    if (p.dt == LORA_BF16) {
+        L.xg = take((size_t)pl.n_gtiles * kTileM * p.K * 2);
+        L.z = take((size_t)pl.z_blocks * kZBlockBytes);
+        if (backward) {
+            L.xat = take((size_t)LORA_MAX_RANK * pl.tcols * 2);
+            L.dybt = take((size_t)LORA_MAX_RANK * pl.tcols * 2);
+        }
+    } else {
+        L.simt = take(simt_scratch_bytes(p));
+    }
+    L.total = at;
+    return L;
+}
+
+}  // namespace lora

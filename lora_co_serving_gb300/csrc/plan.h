@@ -1,0 +1,77 @@
+// plan.h -- host-side validation and tile planning for the mixed-batch LoRA layer.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "common.h"
+#include "lora_mixed.h"
+
+namespace lora {
+
+// Segments shorter than this (and not fine-tuning) are decode-like: their rows are copied into a
+// gathered buffer sorted by adapter, so that a tile meets as few adapters as possible.
+constexpr int kShortSegment = 16;
+// Tiles per L2 band: main items sweep all output columns of a band of tiles before the next band.
+constexpr int kBandTiles = 16;
+
+struct Problem {
+    int32_t T = 0, K = 0, N = 0;
+    lora_dtype_t dt = LORA_BF16;
+    int32_t n_adapters = 0;
+    const int64_t* a_off = nullptr;
+    const int64_t* b_off = nullptr;
+    const int32_t* rank = nullptr;
+    const float* scale = nullptr;
+    std::vector<lora_segment_t> segs;   // non-empty segments, increasing start
+    int64_t rows_a = 0, rows_b = 0;     // row extents of the pools viewed as [rows, K] and [rows, N]
+    int64_t xa_elems = 0;               // elements of the saved-activation buffer
+    int32_t n_train = 0;
+};
+
+// Host validation of every argument that does not need the GPU.  Returns LORA_OK or a LORA_ERR_* code.
+int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool, const lora_segment_t* segs,
+             int32_t n_segs, Problem* out, std::string* err);
+
+struct Plan {
+    std::vector<TileDesc> tiles;
+    std::vector<Chunk> chunks;
+    std::vector<int32_t> rowmap;     // 128 per tile: token row or -1
+    std::vector<int32_t> rowchunk;   // 128 per tile: chunk index or -1
+    std::vector<int32_t> rowaux;     // 128 per tile: forward: xa_save element offset or -1; backward: -1
+    std::vector<WorkItem> items[2];  // first and second launch
+    std::vector<GradGroup> groups;
+    std::vector<TrainSeg> tsegs;
+    int32_t n_gtiles = 0;            // forward: tiles of the gathered buffer
+    int64_t z_blocks = 0;
+    int64_t tcols = 0;               // backward: columns of the transposed xA / dYB buffers
+};
+
+void plan_forward(const Problem& p, Plan* out);
+void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out);
+
+// Greedy list scheduling of the items (in order) onto G persistent CTAs by estimated cost.
+// off has G+1 entries; list holds item indices grouped by CTA, each CTA's in increasing order.
+void assign_items(const std::vector<WorkItem>& items, const Plan& plan, int G, std::vector<int32_t>* off,
+                  std::vector<int32_t>* list);
+
+// Byte offsets of everything a call keeps in the workspace.
+struct Layout {
+    size_t status = 0;
+    size_t tiles = 0, chunks = 0, rowmap = 0, rowchunk = 0, rowaux = 0, groups = 0, tsegs = 0;
+    size_t items[2] = {0, 0}, cta_off[2] = {0, 0}, cta_list[2] = {0, 0};
+    size_t plan_end = 0;
+    size_t xg = 0, z = 0, xat = 0, dybt = 0;
+    size_t simt = 0;                 // float32 path scratch
+    size_t total = 0;
+};
+
+constexpr int kMaxCtas = 1024;
+Layout layout_of(const Problem& p, const Plan& plan, bool backward);
+
+// The float32 path keeps per-token adapter ids and an xA scratch of [T, 128] floats.
+size_t simt_scratch_bytes(const Problem& p);
+
+}  // namespace lora

@@ -1,0 +1,224 @@
+// simt.cu -- CUDA-core kernels: row gathering, saved-xA transposition, and the float32 path.
+//
+// The float32 path (LORA_F32) evaluates the layer and its LoRA backward with one thread per output
+// element and float32 accumulation.  It serves the small float32 layers; bf16 layers take the
+// tcgen05 path in tc_kernel.cu.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.h"
+#include "simt.h"
+
+namespace lora {
+
+namespace {
+
+__global__ void gather_rows_kernel(const uint4* __restrict__ x, int32_t k8, const int32_t* __restrict__ rows,
+                                   uint4* __restrict__ out, int32_t n_rows) {
+    for (int32_t i = blockIdx.x; i < n_rows; i += gridDim.x) {
+        const int32_t t = rows[i];
+        uint4* dst = out + (size_t)i * k8;
+        if (t >= 0) {
+            const uint4* src = x + (size_t)t * k8;
+            for (int32_t v = threadIdx.x; v < k8; v += blockDim.x) dst[v] = src[v];
+        } else {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int32_t v = threadIdx.x; v < k8; v += blockDim.x) dst[v] = z;
+        }
+    }
+}
+
+// xat[j, tpos0 + t] = xa_saved[xoff + t*r + j] for t < len, 0 for len <= t < roundup(len, 128)
+__global__ void xat_from_saved_kernel(const __nv_bfloat16* __restrict__ xa_saved, const TrainSeg* __restrict__ tsegs,
+                                      int32_t n_tsegs, __nv_bfloat16* __restrict__ xat, int32_t P) {
+    const TrainSeg s = tsegs[blockIdx.y];
+    const int32_t span = (s.len + 127) / 128 * 128;
+    for (int32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < span; t += gridDim.x * blockDim.x) {
+        for (int32_t j = 0; j < s.r; ++j) {
+            __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+            if (t < s.len) v = xa_saved[(size_t)s.xoff + (size_t)t * s.r + j];
+            xat[(size_t)j * P + s.tpos0 + t] = v;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------- float32 path
+__global__ void f32_shrink_kernel(const float* __restrict__ x, const float* __restrict__ A,
+                                  const AdapterRec* __restrict__ ad, const int32_t* __restrict__ tok_ad,
+                                  const F32Seg* __restrict__ segs, int32_t n_segs, int32_t K,
+                                  float* __restrict__ xa, int32_t train_only) {
+    // one thread per (token, j) over the listed segments
+    int64_t total = 0;
+    for (int32_t s = 0; s < n_segs; ++s) total += (int64_t)segs[s].len * LORA_MAX_RANK;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        int64_t rem = i / LORA_MAX_RANK;
+        const int32_t j = (int32_t)(i % LORA_MAX_RANK);
+        int32_t s = 0;
+        while (rem >= segs[s].len) { rem -= segs[s].len; ++s; }
+        if (train_only && !segs[s].is_train) continue;
+        const int32_t t = segs[s].start + (int32_t)rem;
+        const int32_t a = tok_ad[t];
+        if (a < 0 || j >= ad[a].r) continue;
+        const float* xr = x + (size_t)t * K;
+        const float* Ar = A + ad[a].a_off + (size_t)j * K;
+        float acc = 0.f;
+        for (int32_t k = 0; k < K; ++k) acc = fmaf(xr[k], Ar[k], acc);
+        xa[(size_t)t * LORA_MAX_RANK + j] = acc;
+    }
+}
+
+__global__ void f32_forward_kernel(const float* __restrict__ x, const float* __restrict__ Wt,
+                                   const float* __restrict__ B, const AdapterRec* __restrict__ ad,
+                                   const int32_t* __restrict__ tok_ad, const float* __restrict__ xa, int32_t T,
+                                   int32_t K, int32_t N, float* __restrict__ y) {
+    const int64_t total = (int64_t)T * N;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t t = (int32_t)(i / N), n = (int32_t)(i % N);
+        const float* xr = x + (size_t)t * K;
+        const float* wr = Wt + (size_t)n * K;
+        float acc = 0.f;
+        for (int32_t k = 0; k < K; ++k) acc = fmaf(xr[k], wr[k], acc);
+        const int32_t a = tok_ad[t];
+        if (a >= 0) {
+            float lo = 0.f;
+            const float* Bb = B + ad[a].b_off + n;
+            for (int32_t j = 0; j < ad[a].r; ++j) lo = fmaf(xa[(size_t)t * LORA_MAX_RANK + j], Bb[(size_t)j * N], lo);
+            acc = fmaf(ad[a].scale, lo, acc);
+        }
+        y[i] = acc;
+    }
+}
+
+// copy xA of fine-tuning rows to / from the packed saved-activation layout
+__global__ void f32_xa_pack_kernel(float* __restrict__ xa, float* __restrict__ packed, const F32Seg* __restrict__ segs,
+                                   int32_t n_segs, const AdapterRec* __restrict__ ad, int32_t to_packed) {
+    for (int32_t s = 0; s < n_segs; ++s) {
+        if (!segs[s].is_train) continue;
+        const int32_t r = ad[segs[s].adapter].r;
+        const int64_t n = (int64_t)segs[s].len * r;
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+            const int32_t t = segs[s].start + (int32_t)(i / r), j = (int32_t)(i % r);
+            float* p = packed + segs[s].xoff + i;
+            float* q = xa + (size_t)t * LORA_MAX_RANK + j;
+            if (to_packed) *p = *q; else *q = *p;
+        }
+    }
+}
+
+__global__ void f32_dyb_kernel(const float* __restrict__ dY, const float* __restrict__ B,
+                               const AdapterRec* __restrict__ ad, const F32Seg* __restrict__ segs, int32_t n_segs,
+                               int32_t N, float* __restrict__ dyb) {
+    for (int32_t s = 0; s < n_segs; ++s) {
+        if (!segs[s].is_train) continue;
+        const AdapterRec rec = ad[segs[s].adapter];
+        const int64_t n = (int64_t)segs[s].len * rec.r;
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+            const int32_t t = segs[s].start + (int32_t)(i / rec.r), j = (int32_t)(i % rec.r);
+            const float* d = dY + (size_t)t * N;
+            const float* Bj = B + rec.b_off + (size_t)j * N;
+            float acc = 0.f;
+            for (int32_t c = 0; c < N; ++c) acc = fmaf(d[c], Bj[c], acc);
+            dyb[(size_t)t * LORA_MAX_RANK + j] = acc;
+        }
+    }
+}
+
+__global__ void f32_dx_kernel(const float* __restrict__ dY, const float* __restrict__ Wt, const float* __restrict__ A,
+                              const AdapterRec* __restrict__ ad, const F32Seg* __restrict__ segs, int32_t n_segs,
+                              const float* __restrict__ dyb, int32_t K, int32_t N, float* __restrict__ dX) {
+    for (int32_t s = 0; s < n_segs; ++s) {
+        if (!segs[s].is_train) continue;
+        const AdapterRec rec = ad[segs[s].adapter];
+        const int64_t n = (int64_t)segs[s].len * K;
+        for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+            const int32_t t = segs[s].start + (int32_t)(i / K), k = (int32_t)(i % K);
+            const float* d = dY + (size_t)t * N;
+            float acc = 0.f;
+            for (int32_t c = 0; c < N; ++c) acc = fmaf(d[c], Wt[(size_t)c * K + k], acc);
+            float lo = 0.f;
+            for (int32_t j = 0; j < rec.r; ++j)
+                lo = fmaf(dyb[(size_t)t * LORA_MAX_RANK + j], A[rec.a_off + (size_t)j * K + k], lo);
+            dX[(size_t)t * K + k] = fmaf(rec.scale, lo, acc);
+        }
+    }
+}
+
+// dB[j, n] (or dA[j, k]) of one adapter: sum over its fine-tuning segments in increasing start order
+__global__ void f32_grad_kernel(const float* __restrict__ act, const float* __restrict__ other, int32_t ld_other,
+                                const F32Seg* __restrict__ segs, int32_t n_segs, int32_t adapter, int32_t r,
+                                float scale, int32_t width, float* __restrict__ out, int32_t accumulate) {
+    // out[j*width + c] = s * sum_t act[t, j] * other[t, c]
+    const int64_t total = (int64_t)r * width;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t j = (int32_t)(i / width), c = (int32_t)(i % width);
+        float acc = 0.f;
+        for (int32_t s = 0; s < n_segs; ++s) {
+            if (!segs[s].is_train || segs[s].adapter != adapter) continue;
+            for (int32_t t = segs[s].start; t < segs[s].start + segs[s].len; ++t)
+                acc = fmaf(act[(size_t)t * LORA_MAX_RANK + j], other[(size_t)t * ld_other + c], acc);
+        }
+        out[i] = accumulate ? out[i] + scale * acc : scale * acc;
+    }
+}
+
+inline int grid_for(int64_t n) {
+    int64_t g = (n + 255) / 256;
+    return (int)(g < 1 ? 1 : (g > 4096 ? 4096 : g));
+}
+
+}  // namespace
+
+cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out, int32_t n_rows, cudaStream_t s) {
+    if (n_rows <= 0) return cudaSuccess;
+    gather_rows_kernel<<<n_rows < 65535 ? n_rows : 65535, 256, 0, s>>>(
+        static_cast<const uint4*>(x), K / 8, rows, static_cast<uint4*>(out), n_rows);
+    return cudaGetLastError();
+}
+
+cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len, void* xat,
+                           int32_t P, cudaStream_t s) {
+    if (n_tsegs <= 0) return cudaSuccess;
+    dim3 grid((max_len + 127) / 128, n_tsegs);
+    xat_from_saved_kernel<<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(xa_saved), tsegs, n_tsegs,
+                                               static_cast<__nv_bfloat16*>(xat), P);
+    return cudaGetLastError();
+}
+
+cudaError_t f32_forward(const F32Args& a, cudaStream_t s) {
+    f32_shrink_kernel<<<grid_for((int64_t)a.T * LORA_MAX_RANK), 256, 0, s>>>(a.x, a.A, a.ad, a.tok_ad, a.segs,
+                                                                               a.n_segs, a.K, a.xa, 0);
+    f32_forward_kernel<<<grid_for((int64_t)a.T * a.N), 256, 0, s>>>(a.x, a.Wt, a.B, a.ad, a.tok_ad, a.xa, a.T, a.K,
+                                                                     a.N, a.y);
+    if (a.xa_save)
+        f32_xa_pack_kernel<<<grid_for(a.xa_elems), 256, 0, s>>>(a.xa, a.xa_save, a.segs, a.n_segs, a.ad, 1);
+    return cudaGetLastError();
+}
+
+cudaError_t f32_backward(const F32Args& a, cudaStream_t s) {
+    if (a.xa_saved)
+        f32_xa_pack_kernel<<<grid_for(a.xa_elems), 256, 0, s>>>(a.xa, const_cast<float*>(a.xa_saved), a.segs, a.n_segs,
+                                                                a.ad, 0);
+    else
+        f32_shrink_kernel<<<grid_for((int64_t)a.T * LORA_MAX_RANK), 256, 0, s>>>(a.x, a.A, a.ad, a.tok_ad, a.segs,
+                                                                                   a.n_segs, a.K, a.xa, 1);
+    f32_dyb_kernel<<<grid_for((int64_t)a.train_tokens * LORA_MAX_RANK), 256, 0, s>>>(a.dY, a.B, a.ad, a.segs,
+                                                                                       a.n_segs, a.N, a.dyb);
+    if (a.dX)
+        f32_dx_kernel<<<grid_for((int64_t)a.train_tokens * a.K), 256, 0, s>>>(a.dY, a.Wt, a.A, a.ad, a.segs, a.n_segs,
+                                                                              a.dyb, a.K, a.N, a.dX);
+    for (int32_t g = 0; g < a.n_groups; ++g) {
+        const int32_t ad = a.group_adapter[g], r = a.group_r[g];
+        if (a.dB)
+            f32_grad_kernel<<<grid_for((int64_t)r * a.N), 256, 0, s>>>(a.xa, a.dY, a.N, a.segs, a.n_segs, ad, r,
+                                                                       a.group_scale[g], a.N,
+                                                                       a.dB + a.group_b_off[g], a.accumulate);
+        if (a.dA)
+            f32_grad_kernel<<<grid_for((int64_t)r * a.K), 256, 0, s>>>(a.dyb, a.x, a.K, a.segs, a.n_segs, ad, r,
+                                                                       a.group_scale[g], a.K,
+                                                                       a.dA + a.group_a_off[g], a.accumulate);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace lora

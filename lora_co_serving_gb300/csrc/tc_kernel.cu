@@ -1,0 +1,501 @@
+// tc_kernel.cu -- persistent tcgen05 / TMEM / TMA kernel for every dense contraction of the layer.
+//
+// One kernel body runs all work-item kinds of a launch (see common.h):
+//   shrink  : [128 tile rows] x [LoRA columns]  = x A^T  (or dY B^T)      -> Z / xa_save / transposed copies
+//   main    : [128 tile rows] x [256 outputs]   = x Wt^T + Z Bstack       -> y       (forward)
+//                                               = dY Wt  + Z Astack       -> dX      (backward)
+//   grad    : [128 of N or K] x [r]             = dY^T xA  or  x^T dYB    -> dB, dA  (fp32)
+// The expand of the LoRA layer ("DeltaServe: Host-Agnostic Co-Serving of Inference and Fine-Tuning for LLMs",
+// section 2.2: W_eff = W + BA) is carried out as extra K-steps of the main GEMM over the tile's Z matrix
+// (s_a * x A_a, masked to each row's own adapter) against the stacked rows of the tile's adapters, so the
+// LoRA term accumulates in the same TMEM accumulator as x W and y is written once.
+//
+// Roles (192 threads, one CTA per SM, persistent over a host-assigned item list):
+//   warp 0, lane 0 : TMA producer (cp.async.bulk.tensor into a 4-stage ring of 48 KB stages)
+//   warp 1         : TMEM allocation; lane 0 issues tcgen05.mma (M=128) and tcgen05.commit
+//   warps 2..5     : epilogue (tcgen05.ld from the double-buffered accumulator, conversion, stores)
+// Every wait is bounded: on timeout the CTA records LORA_ERR_TIMEOUT in the status word and all roles stop.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.h"
+#include "tc_kernel.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kABytes = kTileM * kBK * 2;            // 16 KB: 128 rows x 64 bf16
+constexpr int kBBytes = kBN * kBK * 2;               // 32 KB: 256 rows x 64 bf16
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;      // 1 s
+constexpr uint32_t kTmemCols = 512;                   // two 256-column fp32 accumulators
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t global_timer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting (this wait timed out, or
+// another role's did).
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((spin & 31u) == 0 && global_timer() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicCAS(status, 0, LORA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle, sm_100-family layout (version field = 1).
+//   K-major operand: rows of 128 B, 8-row groups SBO apart (LBO unused).
+//   MN-major operand: 64-element (128 B) MN atoms LBO apart, 8-row K groups SBO apart.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N, operand majors (0 = K, 1 = MN).
+__device__ __forceinline__ uint32_t instr_desc(int n, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Pool row that holds LoRA column `col` (a multiple of 8) of a tile.  Columns past a chunk's rank (its
+// padding to 16) repeat the chunk's last 8-row atom: they meet zero Z columns (main) or are discarded
+// (shrink), and repeating keeps every loaded value inside the adapter's own block.
+__device__ __forceinline__ int32_t atom_row(const Chunk* chunks, int32_t c0, int32_t nchunk, int32_t col, bool use_b,
+                                            int32_t* cursor) {
+    int32_t ci = *cursor;
+    while (ci + 1 < nchunk) {
+        const Chunk& ch = chunks[c0 + ci];
+        if (col < ch.zcol + ((ch.r + 15) & ~15)) break;
+        ++ci;
+    }
+    *cursor = ci;
+    const Chunk& ch = chunks[c0 + ci];
+    int32_t o = col - ch.zcol;
+    const int32_t last = ((ch.r + 7) / 8 - 1) * 8;
+    if (o > last) o = last;
+    return (use_b ? ch.prow_b : ch.prow_a) + o;
+}
+
+struct Ring {
+    int stage = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next() {
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+};
+
+// --------------------------------------------------------------------------------------------- producer
+__device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty, int i0, int i1,
+                             volatile int* abort_flag) {
+    Ring ring;
+    for (int ii = i0; ii < i1; ++ii) {
+        const WorkItem w = P.items[P.cta_list[ii]];
+        if (w.kind == kGradDb || w.kind == kGradDa) {
+            const GradGroup g = P.groups[w.tile];
+            const CUtensorMap* mb = (w.kind == kGradDb) ? &P.tm_xat : &P.tm_dybt;
+            const int natoms = w.mma_n / 8;
+            const uint32_t bytes = kABytes + natoms * 1024;
+            for (int q = 0; q < g.nseg; ++q) {
+                const TrainSeg s = P.tsegs[g.seg0 + q];
+                const CUtensorMap* ma = (w.kind == kGradDb) ? &P.tm_seg_dy[g.seg0 + q] : &P.tm_seg_x[g.seg0 + q];
+                for (int b = 0; b * kBK < s.len; ++b) {
+                    const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
+                    if (!wait_phase(empty, ring.phase ^ 1u, abort_flag, P.status)) return;
+                    const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
+                    mbar_expect_tx(full, bytes);
+                    tma_load_2d(sa, ma, w.n0, b * kBK, full);
+                    tma_load_2d(sa + 8192, ma, w.n0 + 64, b * kBK, full);
+                    for (int j = 0; j < natoms; ++j) tma_load_2d(sb + j * 1024, mb, s.tpos0 + b * kBK, j * 8, full);
+                    ring.next();
+                }
+            }
+            continue;
+        }
+        const TileDesc td = P.tiles[w.tile];
+        if (w.kind == kMainFwd || w.kind == kMainDx) {
+            const bool fwd = (w.kind == kMainFwd);
+            const CUtensorMap* ma = fwd ? (td.a_src ? &P.tm_xg : &P.tm_x) : &P.tm_dy;
+            for (int kb = 0; kb < w.nk; ++kb) {
+                const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
+                if (!wait_phase(empty, ring.phase ^ 1u, abort_flag, P.status)) return;
+                const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
+                mbar_expect_tx(full, kABytes + kBBytes);
+                tma_load_2d(sa, ma, kb * kBK, td.a_row0, full);
+                if (fwd) {
+                    tma_load_2d(sb, &P.tm_w, kb * kBK, w.n0, full);
+                } else {
+                    for (int m = 0; m < 4; ++m) tma_load_2d(sb + m * 8192, &P.tm_w, w.n0 + 64 * m, kb * kBK, full);
+                }
+                ring.next();
+            }
+            const CUtensorMap* mp = fwd ? &P.tm_pb : &P.tm_pa;
+            int32_t cursor = 0;
+            for (int e = 0; e < w.n_ext; ++e) {
+                const int atoms = min(8, (td.ext_k - e * kBK) / 8);
+                const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
+                if (!wait_phase(empty, ring.phase ^ 1u, abort_flag, P.status)) return;
+                const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
+                mbar_expect_tx(full, kZBlockBytes + atoms * 4096);
+                bulk_load(sa, P.zin + (size_t)(td.z_blk0 + e) * kZBlockBytes, kZBlockBytes, full);
+                for (int q = 0; q < atoms; ++q) {
+                    const int32_t prow = atom_row(P.chunks, td.chunk0, td.nchunk, e * kBK + q * 8, fwd, &cursor);
+                    for (int m = 0; m < 4; ++m) tma_load_2d(sb + m * 8192 + q * 1024, mp, w.n0 + 64 * m, prow, full);
+                }
+                ring.next();
+            }
+            continue;
+        }
+        // shrink
+        const CUtensorMap* ma = (w.kind == kShrinkFwd) ? (td.a_src ? &P.tm_xg : &P.tm_x)
+                                : (w.kind == kShrinkDyb) ? &P.tm_dy : &P.tm_x;
+        const bool use_b = (w.kind == kShrinkDyb);
+        const CUtensorMap* mp = use_b ? &P.tm_pb : &P.tm_pa;
+        const int natoms = w.mma_n / 8;
+        for (int kb = 0; kb < w.nk; ++kb) {
+            const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
+            if (!wait_phase(empty, ring.phase ^ 1u, abort_flag, P.status)) return;
+            const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
+            mbar_expect_tx(full, kABytes + natoms * 1024);
+            tma_load_2d(sa, ma, kb * kBK, td.a_row0, full);
+            int32_t cursor = 0;
+            for (int q = 0; q < natoms; ++q) {
+                const int32_t prow = atom_row(P.chunks, td.chunk0, td.nchunk, w.n0 + q * 8, use_b, &cursor);
+                tma_load_2d(sb + q * 1024, mp, kb * kBK, prow, full);
+            }
+            ring.next();
+        }
+    }
+}
+
+// --------------------------------------------------------------------------------------------- MMA issuer
+__device__ void run_mma(const KParams& P, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_tfull,
+                        uint32_t bar_tempty, uint32_t tmem, int i0, int i1, volatile int* abort_flag) {
+    Ring ring;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int ii = i0; ii < i1; ++ii) {
+        const WorkItem w = P.items[P.cta_list[ii]];
+        if (!wait_phase(bar_tempty + acc * 8, acc_phase ^ 1u, abort_flag, P.status)) return;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)acc * kBN;
+        uint32_t accumulate = 0;
+        // one k-block: wait for the stage, issue `steps` MMAs of K=16, release the stage
+        auto kblock = [&](int steps, uint32_t idesc, int a_mn, int b_mn) -> bool {
+            const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
+            if (!wait_phase(full, ring.phase, abort_flag, P.status)) return false;
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
+            for (int k = 0; k < steps; ++k) {
+                const uint64_t ad = a_mn ? smem_desc(sa + k * 2048, 8192, 1024) : smem_desc(sa + k * 32, 16, 1024);
+                const uint64_t bd = b_mn ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
+                mma_bf16(d, ad, bd, idesc, accumulate);
+                accumulate = 1;
+            }
+            mma_commit(empty);
+            ring.next();
+            return true;
+        };
+        bool ok = true;
+        if (w.kind == kMainFwd || w.kind == kMainDx) {
+            const int b_mn = (w.kind == kMainDx) ? 1 : 0;
+            const uint32_t id_main = instr_desc(kBN, 0, b_mn);
+            for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id_main, 0, b_mn);
+            const TileDesc td = P.tiles[w.tile];
+            const uint32_t id_ext = instr_desc(kBN, 0, 1);
+            for (int e = 0; e < w.n_ext && ok; ++e) ok = kblock(min(4, (td.ext_k - e * kBK) / 16), id_ext, 0, 1);
+        } else if (w.kind == kGradDb || w.kind == kGradDa) {
+            const uint32_t id = instr_desc(w.mma_n, 1, 0);
+            for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id, 1, 0);
+        } else {
+            const uint32_t id = instr_desc(w.mma_n, 0, 0);
+            for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id, 0, 0);
+        }
+        if (!ok) return;
+        mma_commit(bar_tfull + acc * 8);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+}
+
+// --------------------------------------------------------------------------------------------- epilogue
+__device__ __forceinline__ void ld32_cols(uint32_t taddr, float (&v)[32]) {
+    uint32_t a[16], b[16];
+    tmem_ld16(taddr, a);
+    tmem_ld16(taddr + 16, b);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v[i] = __uint_as_float(a[i]);
+        v[16 + i] = __uint_as_float(b[i]);
+    }
+}
+
+__device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t tmem, int i0, int i1,
+                             volatile int* abort_flag) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int quarter = warp & 3;                 // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;          // tile row = accumulator lane
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int ii = i0; ii < i1; ++ii) {
+        const WorkItem w = P.items[P.cta_list[ii]];
+        if (!wait_phase(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) return;
+        tc_fence_after();
+        const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);
+        if (w.kind == kMainFwd || w.kind == kMainDx) {
+            const int32_t t = P.rowmap[w.tile * kTileM + row];
+            for (int c = 0; c < kBN; c += 32) {
+                float v[32];
+                ld32_cols(taddr + c, v);
+                if (t >= 0) {
+                    __nv_bfloat16* dst = P.out + (size_t)t * P.out_ld + w.n0 + c;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (w.n0 + c + 8 * g + 8 <= P.out_cols) {
+                            uint4 q;
+                            q.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+                            q.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+                            q.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+                            q.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+                            *reinterpret_cast<uint4*>(dst + 8 * g) = q;
+                        }
+                    }
+                }
+            }
+        } else if (w.kind == kGradDb || w.kind == kGradDa) {
+            const GradGroup g = P.groups[w.tile];
+            const bool is_b = (w.kind == kGradDb);
+            const int32_t ld = is_b ? P.N : P.K;
+            const int32_t m = w.n0 + row;
+            float* base = is_b ? P.dB + (size_t)g.prow_b * P.N : P.dA + (size_t)g.prow_a * P.K;
+            for (int c = 0; c < w.mma_n; c += 16) {
+                uint32_t a[16];
+                tmem_ld16(taddr + c, a);
+                tmem_ld_wait();
+                if (m < ld) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int j = c + i;
+                        if (j < g.r) {
+                            float* p = base + (size_t)j * ld + m;
+                            const float val = g.scale * __uint_as_float(a[i]);
+                            *p = P.accumulate ? (*p + val) : val;
+                        }
+                    }
+                }
+            }
+        } else {
+            // shrink: mask each row to its own adapter's columns, then write Z / xa_save / transposed copies
+            const TileDesc td = P.tiles[w.tile];
+            const int32_t rc = P.rowchunk[w.tile * kTileM + row];
+            int32_t zc0 = 0, zr = 0;
+            float s = 0.f;
+            if (rc >= 0) {
+                const Chunk ch = P.chunks[rc];
+                zc0 = ch.zcol; zr = ch.r; s = ch.scale;
+            }
+            const bool write_z = (w.kind != kShrinkXa);
+            const int32_t save_off = (w.kind == kShrinkFwd) ? P.rowaux[w.tile * kTileM + row] : -1;
+            __nv_bfloat16* tdst = (w.kind == kShrinkDyb) ? P.dybt : (w.kind == kShrinkXa) ? P.xat : nullptr;
+            int32_t t_r = 0;
+            if (tdst) t_r = P.chunks[td.chunk0].r;    // backward tiles hold one adapter
+            for (int c = 0; c < w.mma_n; c += 16) {
+                uint32_t a[16];
+                tmem_ld16(taddr + c, a);
+                tmem_ld_wait();
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int zc = w.n0 + c + i;
+                    v[i] = (rc >= 0 && zc >= zc0 && zc < zc0 + zr) ? __uint_as_float(a[i]) : 0.f;
+                }
+                if (write_z) {
+                    const int zc = w.n0 + c;
+                    uint8_t* blk = P.zout + (size_t)(td.z_blk0 + zc / kBK) * kZBlockBytes + row * 128;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int chunk16 = ((zc % kBK) / 8 + h) ^ (row & 7);
+                        uint4 q;
+                        q.x = pack_bf16(s * v[8 * h + 0], s * v[8 * h + 1]);
+                        q.y = pack_bf16(s * v[8 * h + 2], s * v[8 * h + 3]);
+                        q.z = pack_bf16(s * v[8 * h + 4], s * v[8 * h + 5]);
+                        q.w = pack_bf16(s * v[8 * h + 6], s * v[8 * h + 7]);
+                        *reinterpret_cast<uint4*>(blk + chunk16 * 16) = q;
+                    }
+                }
+                if (save_off >= 0) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int j = w.n0 + c + i - zc0;
+                        if (j >= 0 && j < zr) P.xa_save[save_off + j] = __float2bfloat16_rn(v[i]);
+                    }
+                }
+                if (tdst) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int j = w.n0 + c + i;     // the tile's single chunk starts at column 0
+                        if (j < t_r) tdst[(size_t)j * P.t_ld + td.tpos0 + row] = __float2bfloat16_rn(v[i]);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_tempty + acc * 8);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) lora_tc_kernel(const __grid_constant__ KParams P) {
+    extern __shared__ uint8_t dsmem[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + kStages * 8;
+    const uint32_t bar_tfull = bar_empty + kStages * 8, bar_tempty = bar_tfull + 16;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_full + s * 8, 1);
+            mbar_init(bar_empty + s * 8, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_tfull + b * 8, 1);
+            mbar_init(bar_tempty + b * 8, 128);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int i0 = P.cta_off[blockIdx.x], i1 = P.cta_off[blockIdx.x + 1];
+
+    if (warp == 0) {
+        if (lane == 0) run_producer(P, smem, bar_full, bar_empty, i0, i1, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0) run_mma(P, smem, bar_full, bar_empty, bar_tfull, bar_tempty, tmem, i0, i1, abort_flag);
+    } else {
+        run_epilogue(P, bar_tfull, bar_tempty, tmem, i0, i1, abort_flag);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+}  // namespace
+
+size_t tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024 + 1024; }
+
+cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream) {
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(lora_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_bytes());
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    lora_tc_kernel<<<grid, kThreads, tc_smem_bytes(), stream>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,57 @@
+// tc_kernel.h -- launch interface of the persistent tcgen05 kernel.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.h"
+#include "lora_mixed.h"
+
+namespace lora {
+
+// Everything one launch needs.  Tensor maps live in the kernel's parameter space (__grid_constant__).
+struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA unit needs
+    CUtensorMap tm_x;      // x rows,  [T, K] bf16, box {64, 128}, 128B swizzle
+    CUtensorMap tm_xg;     // gathered rows buffer, [G*128, K], box {64, 128}
+    CUtensorMap tm_dy;     // dY rows, [T, N], box {64, 128}
+    CUtensorMap tm_w;      // Wt [N, K]: forward box {64, 256} (K-major B); backward box {64, 64} (MN-major B)
+    CUtensorMap tm_pa;     // A pool viewed as [rows, K], box {64, 8}
+    CUtensorMap tm_pb;     // B pool viewed as [rows, N], box {64, 8}
+    CUtensorMap tm_xat;    // xA^T  [128, P], box {64, 8}
+    CUtensorMap tm_dybt;   // dYB^T [128, P], box {64, 8}
+    CUtensorMap tm_seg_dy[kMaxTrainSegs];   // dY rows of fine-tuning segment q, [len, N], box {64, 64}
+    CUtensorMap tm_seg_x[kMaxTrainSegs];    // x rows of fine-tuning segment q,  [len, K], box {64, 64}
+
+    const TileDesc* tiles;
+    const Chunk* chunks;
+    const int32_t* rowmap;
+    const int32_t* rowchunk;
+    const int32_t* rowaux;
+    const GradGroup* groups;
+    const TrainSeg* tsegs;
+    const WorkItem* items;
+    const int32_t* cta_off;
+    const int32_t* cta_list;
+
+    const uint8_t* zin;     // Z blocks read by main items
+    uint8_t* zout;          // Z blocks written by shrink items
+    __nv_bfloat16* out;     // main items: y [T, N] or dX [T, K]
+    __nv_bfloat16* xa_save; // forward shrink: saved xA of fine-tuning rows
+    __nv_bfloat16* xat;     // backward shrink: xA^T  [128, P]
+    __nv_bfloat16* dybt;    // backward shrink: dYB^T [128, P]
+    float* dA;
+    float* dB;
+    int32_t* status;
+    int32_t out_ld;         // row stride of `out` in elements
+    int32_t out_cols;       // valid columns of `out`
+    int32_t t_ld;           // P
+    int32_t K, N;
+    int32_t accumulate;
+};
+
+size_t tc_smem_bytes();
+cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream);
+
+}  // namespace lora

@@ -1,0 +1,65 @@
+"""Helpers for the GPU tests: upload a seeded workload, call the library, compare with the oracle."""
+import numpy as np
+
+import lora_co_serving_gb300 as lm
+import workloads
+
+# Tolerance of the layer (bf16 inputs, fp32 accumulation): per output tensor
+MAX_ERR = 2e-2      # max |err| <= MAX_ERR * max |ref|
+FRO_ERR = 5e-3      # ||err||_F <= FRO_ERR * ||ref||_F
+
+
+def to_dev(a, dtype):
+    import torch
+    if dtype == "bf16":
+        bits = workloads.bf16_bits(a)
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def to_np(t):
+    import torch
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+class Dev:
+    """A workload on the device."""
+
+    def __init__(self, wl):
+        import torch
+        self.wl = wl
+        self.x = to_dev(wl.x, wl.dtype)
+        self.Wt = to_dev(wl.Wt, wl.dtype)
+        self.A = to_dev(wl.A, wl.dtype)
+        self.B = to_dev(wl.B, wl.dtype)
+        self.dY = to_dev(wl.dY, wl.dtype) if wl.dY is not None else None
+        self.pool = lm.Pool(self.A, self.B, wl.a_off, wl.b_off, wl.rank, wl.scale)
+        self.segs = wl.segs
+
+    def forward(self, **kw):
+        return lm.forward(self.x, self.Wt, self.pool, self.segs, **kw)
+
+    def backward(self, **kw):
+        return lm.backward(self.x, self.Wt, self.pool, self.segs, self.dY, **kw)
+
+
+def compare(got, ref, name, max_err=MAX_ERR, fro_err=FRO_ERR):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), name + ": non-finite values"
+    d = got - ref
+    mref = np.abs(ref).max() if ref.size else 0.0
+    mx = np.abs(d).max() if d.size else 0.0
+    fro = np.linalg.norm(d) / max(np.linalg.norm(ref), 1e-300)
+    assert mx <= max_err * max(mref, 1e-30), "%s: max|err| %.3g > %.3g * max|ref| %.3g" % (name, mx, max_err, mref)
+    assert fro <= fro_err, "%s: relative Frobenius error %.3g > %.3g" % (name, fro, fro_err)
+    return mx / max(mref, 1e-30), fro
+
+
+def train_blocks(wl):
+    """Pool index ranges of the A and B blocks of adapters with fine-tuning segments."""
+    ads = sorted(set(int(s[2]) for s in wl.segs.tolist() if s[3]))
+    ia = np.concatenate([np.arange(wl.a_off[a], wl.a_off[a] + wl.rank[a] * wl.K) for a in ads])
+    ib = np.concatenate([np.arange(wl.b_off[a], wl.b_off[a] + wl.rank[a] * wl.N) for a in ads])
+    return ia, ib

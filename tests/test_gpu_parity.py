@@ -1,0 +1,134 @@
+"""GPU parity: the CUDA library against the float64 oracle on the same seeded inputs.
+
+Every comparison uses the layer's tolerance (max |err| <= 2e-2 * max |ref|, relative Frobenius
+error <= 5e-3, per output tensor); routing and indexing checks are bit-exact (test_gpu_invariants.py).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_util import Dev, compare, to_np, train_blocks
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    import lora_co_serving_gb300 as lm
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lm.build()
+    lm.library()
+
+
+def check_forward(wl, save=False):
+    import lora_co_serving_gb300 as lm
+    d = Dev(wl)
+    ref, u = oracle.forward_wl(wl, want_u=True)
+    if save:
+        y, xs = d.forward(save_xa=True)
+    else:
+        y = d.forward()
+    import torch
+    torch.cuda.synchronize()
+    compare(to_np(y), ref, "y")
+    if save:
+        exp = []
+        for st, ln, a, tr in sorted(wl.segs.tolist()):
+            if tr and ln > 0:
+                exp.append(u[st:st + ln, :wl.rank[a]].reshape(-1))
+        exp = np.concatenate(exp)
+        compare(to_np(xs)[:exp.shape[0]], exp, "xa_save")
+    return d, y
+
+
+def check_backward(wl, d=None, xa_saved=None, recompute=True):
+    import torch
+    d = d or Dev(wl)
+    dX, dA, dB = d.backward(xa_saved=xa_saved, recompute=recompute)
+    torch.cuda.synchronize()
+    rX, rA, rB = oracle.backward_wl(wl)
+    rows = wl.train_rows()
+    compare(to_np(dX)[rows], rX, "dX")
+    ia, ib = train_blocks(wl)
+    compare(to_np(dA)[ia], rA[ia], "dA")
+    compare(to_np(dB)[ib], rB[ib], "dB")
+    # entries outside the fine-tuning adapters' blocks and dX rows outside fine-tuning segments stay zero
+    mA = np.ones(dA.numel(), bool)
+    mA[ia] = False
+    mB = np.ones(dB.numel(), bool)
+    mB[ib] = False
+    assert np.all(to_np(dA)[mA] == 0) and np.all(to_np(dB)[mB] == 0)
+    other = np.setdiff1d(np.arange(wl.T), rows)
+    assert np.all(to_np(dX)[other] == 0)
+
+
+def test_f32_config1():
+    wl = workloads.config1()
+    d, _ = check_forward(wl, save=True)
+    check_backward(wl, d)
+
+
+def test_bf16_base_only():
+    wl = workloads.custom(7, 256, 256, 512, [(0, 256, -1, 0)], [16])
+    check_forward(wl)
+
+
+def test_bf16_single_adapter_ragged():
+    # ragged T (3 tiles, last partial), ragged N (last 256-column tile half full), K not a multiple of 64
+    wl = workloads.custom(8, 300, 328, 384, [(0, 300, 0, 0)], [16])
+    check_forward(wl)
+
+
+def test_bf16_adapters_and_base_mixed():
+    segs = [(0, 100, 2, 0), (100, 60, -1, 0), (160, 90, 0, 0), (250, 50, 1, 0), (300, 33, 2, 0)]
+    wl = workloads.custom(9, 333, 256, 512, segs, [8, 24, 128])
+    check_forward(wl)
+
+
+def test_bf16_decode_small():
+    wl = workloads.config2(T=256, K=512, N=512, n_adapters=64)
+    check_forward(wl)
+
+
+def test_bf16_odd_ranks():
+    segs = [(0, 40, 0, 0), (40, 1, 1, 0), (41, 1, 2, 0), (42, 86, 3, 0), (128, 3, 4, 0), (131, 61, 1, 0)]
+    wl = workloads.custom(10, 192, 256, 256, segs, [1, 4, 13, 100, 127])
+    check_forward(wl)
+
+
+def test_bf16_mixed_small_forward_backward():
+    wl = workloads.config5(K=512, N=768, n_adapters=24, n_decode=150, prefill_tokens=500, len_lo=30, len_hi=250,
+                           train_len=100)
+    d, _ = check_forward(wl)
+    check_backward(wl, d)
+
+
+def test_bf16_config3_small_save_then_backward_from_saved():
+    wl = workloads.config3(K=512, N=1024, prefill_tokens=1000, train_len=200, len_lo=64, len_hi=400)
+    d, _ = check_forward(wl, save=True)
+    _, xs = d.forward(save_xa=True)
+    check_backward(wl, d, xa_saved=xs, recompute=False)
+    check_backward(wl, d, xa_saved=xs, recompute=True)
+
+
+@pytest.mark.parametrize("r,four", [(16, False), (64, False), (16, True), (64, True)])
+def test_bf16_config4_small(r, four):
+    wl = workloads.config4(K=640, N=640, n_samples=4, sample_len=160, r=r, four_adapters=four)
+    check_backward(wl)
+
+
+def test_bf16_backward_accumulate():
+    import torch
+    wl = workloads.config4(K=256, N=384, n_samples=3, sample_len=70, r=32, four_adapters=True)
+    d = Dev(wl)
+    _, dA, dB = d.backward()
+    dA0 = torch.randn_like(dA)
+    dB0 = torch.randn_like(dB)
+    _, aA, aB = d.backward(dA=dA0.clone(), dB=dB0.clone(), accumulate=True)
+    torch.cuda.synchronize()
+    ia, ib = train_blocks(wl)
+    compare(to_np(aA)[ia], to_np(dA0)[ia] + to_np(dA)[ia], "dA accumulate", max_err=1e-5, fro_err=1e-6)
+    compare(to_np(aB)[ib], to_np(dB0)[ib] + to_np(dB)[ib], "dB accumulate", max_err=1e-5, fro_err=1e-6)
