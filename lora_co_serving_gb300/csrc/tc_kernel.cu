@@ -378,7 +378,8 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 zc0 = ch.zcol; zr = ch.r; s = ch.scale;
             }
             const bool write_z = (w.kind != kShrinkXa);
-            const int32_t save_off = (w.kind == kShrinkFwd) ? P.rowaux[w.tile * kTileM + row] : -1;
+            const int32_t save_off =
+                (w.kind == kShrinkFwd && P.xa_save != nullptr) ? P.rowaux[w.tile * kTileM + row] : -1;
             __nv_bfloat16* tdst = (w.kind == kShrinkDyb) ? P.dybt : (w.kind == kShrinkXa) ? P.xat : nullptr;
             int32_t t_r = 0;
             if (tdst) t_r = P.chunks[td.chunk0].r;    // backward tiles hold one adapter
