@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark of the mixed-batch multi-adapter LoRA layer: one forward + backward step per iteration.
+
+Default workload (the large heterogeneous co-serving batch): Llama-70B-like MLP projection K=8192 -> N=28672, bf16,
+an adapter pool of 320 adapters with ranks drawn from {8,16,32,64,128}, a batch of 2048 decode tokens (one per
+segment, Zipf(1.1) adapter popularity) + 4096 prefill tokens (segments of 64..1024) + 2048 fine-tuning tokens
+(2 segments on one adapter).  A step is the forward over all 8192 tokens followed by the LoRA backward of the 2048
+fine-tuning tokens (xA recomputed), i.e. every step of the layer's hot path.
+
+Prints one JSON line (rank 0).  `value` is forward tokens per second over all ranks, timed with CUDA events on the
+launching stream after warm-up; the step's inputs (W 470 MB, the adapter pool, x, dY) exceed the 129 MB L2, so L2 is
+not flushed.  `--impl reference` times the float64 CPU oracle on a bounded sample of the same workload instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "mixed-batch multi-LoRA fwd+bwd tokens/s; TFLOP/s and HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=5, choices=[2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------------------------- workload accounting
+def make_workload(cfg, rank=0):
+    seed = 1000 + cfg + 7919 * rank      # each rank draws its own batch (weak scaling)
+    if cfg == 5:
+        return workloads.config5(seed=seed)
+    if cfg == 3:
+        return workloads.config3(seed=seed)
+    if cfg == 4:
+        return workloads.config4(seed=seed)
+    return workloads.config2(seed=seed)
+
+
+def accounting(wl):
+    """Algorithmic FLOPs and bytes of one step, split by launch group (no padding, no redundant work)."""
+    T, K, N = wl.T, wl.K, wl.N
+    segs = wl.segs.tolist()
+    r_of = lambda a: int(wl.rank[a]) if a >= 0 else 0
+    fwd = wl.forward
+    bwd = wl.backward
+    out = {}
+    if fwd:
+        shrink = sum(2 * ln * K * r_of(a) for _, ln, a, _ in segs)
+        expand = sum(2 * ln * N * r_of(a) for _, ln, a, _ in segs)
+        out["fwd_main_flops"] = 2 * T * K * N + expand
+        out["fwd_flops"] = 2 * T * K * N + expand + shrink
+        used = sorted(set(a for _, ln, a, _ in segs if a >= 0 and ln > 0))
+        save = sum(ln * r_of(a) for _, ln, a, tr in segs if tr) * 2 if wl.xa_mode == "save" else 0
+        out["fwd_bytes"] = 2 * (T * K + K * N + T * N) + sum(2 * r_of(a) * (K + N) for a in used) + save
+        # main launch: x, W, adapters' B blocks and y
+        out["fwd_main_bytes"] = 2 * (T * K + K * N + T * N) + sum(2 * r_of(a) * N for a in used)
+    if bwd:
+        tr = [(st, ln, a) for st, ln, a, t in segs if t and ln > 0]
+        Tt = sum(ln for _, ln, _ in tr)
+        lora = sum(2 * ln * r_of(a) * (2 * K + 2 * N) for _, ln, a in tr)
+        recompute = sum(2 * ln * K * r_of(a) for _, ln, a in tr) if wl.xa_mode != "save" else 0
+        out["bwd_flops"] = 2 * Tt * K * N + lora + recompute
+        tads = sorted(set(a for _, _, a in tr))
+        out["bwd_bytes"] = 2 * (Tt * N + K * N + 2 * Tt * K) + sum(6 * r_of(a) * (K + N) for a in tads)
+        out["train_tokens"] = Tt
+    out["flops"] = out.get("fwd_flops", 0) + out.get("bwd_flops", 0)
+    out["bytes"] = out.get("fwd_bytes", 0) + out.get("bwd_bytes", 0)
+    out["tokens"] = T if fwd else out.get("train_tokens", 0)
+    return out
+
+
+def launches_per_step(wl):
+    segs = wl.segs.tolist()
+    n = 0
+    if wl.forward:
+        n += 1 if any(ln < 16 and not tr and ln > 0 for _, ln, _, tr in segs) else 0    # row gather
+        n += 1 if any(a >= 0 for _, _, a, _ in segs) else 0                                # shrink pass
+        n += 1                                                                              # main pass
+    if wl.backward and any(tr for *_, tr in segs):
+        n += 2
+    return n
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in ("tc_kernel.cu", "tc_kernel.h", "common.h"):
+        h.update(open(os.path.join(ROOT, "lora_co_serving_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(cfg):
+    """DRAM bytes per launch of the forward main pass from a committed ncu summary, if it matches this kernel."""
+    p = os.path.join(ROOT, "profiles", "fwd_main_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_sha") != kernel_hash() or d.get("config") != cfg:
+        return None
+    return d.get("bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max([float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()] or [0])}
+
+
+# ----------------------------------------------------------------------------------------------- CPU oracle sample
+def oracle_sample(wl, fwd_rows=32, dx_rows=16, cols=32, seed=0):
+    """Time the float64 oracle on a bounded, stratified sample of one step and extrapolate to the full step.
+
+    Returns (seconds per full step, description, threads)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    T, K, N = wl.T, wl.K, wl.N
+    t_total = 0.0
+    desc = []
+    if wl.forward:
+        segs = sorted(wl.segs.tolist())
+        kinds = {"decode": [], "prefill": [], "train": []}
+        for st, ln, a, tr in segs:
+            kinds["train" if tr else ("decode" if ln < 16 else "prefill")].append((st, ln))
+        rows = []
+        per = max(1, fwd_rows // max(1, sum(1 for v in kinds.values() if v)))
+        for v in kinds.values():
+            if v:
+                for i in rng.integers(0, len(v), per):
+                    st, ln = v[i]
+                    rows.append(st + int(rng.integers(0, ln)))
+        rows = np.array(rows[:fwd_rows])
+        t0 = time.perf_counter()
+        oracle.forward_wl(wl, rows=rows)
+        dt = time.perf_counter() - t0
+        t_total += dt * T / rows.shape[0]
+        desc.append("%d forward rows (stratified over decode/prefill/fine-tuning) x %d/%d" % (rows.shape[0], T,
+                                                                                               rows.shape[0]))
+    if wl.backward:
+        trows = wl.train_rows()
+        pick = trows[rng.integers(0, trows.shape[0], dx_rows)]
+        t0 = time.perf_counter()
+        oracle.backward_wl(wl, dx_rows=pick, want_grads=False)
+        dt = time.perf_counter() - t0
+        t_total += dt * trows.shape[0] / dx_rows
+        cb1, ca1 = np.array([0]), np.array([0])
+        t0 = time.perf_counter()
+        oracle.backward_wl(wl, want_dx=False, cols_b=cb1, cols_a=ca1)
+        t1 = time.perf_counter() - t0
+        cb = rng.choice(N, cols, replace=False)
+        ca = rng.choice(K, cols, replace=False)
+        t0 = time.perf_counter()
+        oracle.backward_wl(wl, want_dx=False, cols_b=cb, cols_a=ca)
+        tc = time.perf_counter() - t0
+        per_col = max(0.0, (tc - t1) / (2 * (cols - 1)))
+        t_total += t1 + per_col * (N + K)
+        desc.append("%d dX rows x %d/%d; dA/dB: shrink of all fine-tuning rows + %d+%d gradient columns "
+                    "extrapolated to %d+%d" % (dx_rows, trows.shape[0], dx_rows, cols, cols, K, N))
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return t_total, "; ".join(desc) + "; linear extrapolation to one full step", threads
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = make_workload(args.config)
+    acc = accounting(wl)
+    times = []
+    desc = threads = None
+    for i in range(args.warmup + args.steps):
+        # each step a smaller sample so that the whole run stays within minutes
+        t, desc, threads = oracle_sample(wl, fwd_rows=8, dx_rows=4, cols=8, seed=i)
+        if i >= args.warmup:
+            times.append(t)
+    t = statistics.mean(times) if times else float("nan")
+    v = acc["tokens"] / t
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "K": wl.K, "N": wl.N},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------------------------- GPU arm
+def to_dev(a, torch):
+    return torch.from_numpy(workloads.bf16_bits(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def run_ours(args):
+    import torch
+    import lora_co_serving_gb300 as lm
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    lm.build()
+
+    wl = make_workload(args.config, rank)
+    acc = accounting(wl)
+    x, Wt, A, B = to_dev(wl.x, torch), to_dev(wl.Wt, torch), to_dev(wl.A, torch), to_dev(wl.B, torch)
+    dY = to_dev(wl.dY, torch) if wl.dY is not None else None
+    pool = lm.Pool(A, B, wl.a_off, wl.b_off, wl.rank, wl.scale)
+    segs = lm.segments(wl.segs)
+    T, K, N = wl.T, wl.K, wl.N
+    ws = torch.empty(lm.workspace_size(T, K, N, 0, pool, segs), dtype=torch.uint8, device="cuda")
+    y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    save = wl.xa_mode == "save"
+    xs = torch.empty(max(1, lm.xa_size(0, pool, segs) // 2), dtype=torch.bfloat16, device="cuda") if save else None
+    dX = torch.zeros((T, K), dtype=torch.bfloat16, device="cuda") if wl.backward else None
+    dA = torch.zeros(A.numel(), dtype=torch.float32, device="cuda") if wl.backward else None
+    dB = torch.zeros(B.numel(), dtype=torch.float32, device="cuda") if wl.backward else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if wl.forward:
+            lm.forward(x, Wt, pool, segs, y=y, xa_save=xs, save_xa=save, workspace=ws, stream=stream)
+        if wl.backward:
+            lm.backward(x, Wt, pool, segs, dY, dX=dX, dA=dA, dB=dB, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    lm.workspace_status(ws)
+
+    # ---- device-timed region: K steps, per-step trace events around each launch group
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device())
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    start.record(stream)
+    for i in range(args.steps):
+        lm.set_trace_events(ev[i])
+        step()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    lm.set_trace_events(None)
+    if dist:
+        dist.barrier()
+    lm.workspace_status(ws)
+    ms = start.elapsed_time(stop) / args.steps
+    group_ms = [statistics.mean(ev[i][2 * g].elapsed_time(ev[i][2 * g + 1]) for i in range(args.steps))
+                for g in range(4)]
+    t_max = torch.tensor([ms], device="cuda", dtype=torch.float64)
+    if dist:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    ms_max = float(t_max.item())
+    value = acc["tokens"] * world / (ms_max / 1e3)
+
+    # ---- end to end: pinned host inputs -> device, the two calls, results -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        x_h = torch.empty_like(x, device="cpu").pin_memory()
+        x_h.copy_(x)
+        trows = wl.train_rows() if wl.backward else np.zeros(0, np.int64)
+        tspans = sorted((s, l) for s, l, a, t in wl.segs.tolist() if t and l > 0) if wl.backward else []
+        dY_h = dY.cpu().pin_memory() if wl.backward else None
+        y_h = torch.empty_like(y, device="cpu").pin_memory()
+        dX_h = torch.empty_like(dX, device="cpu").pin_memory() if wl.backward else None
+        tads = sorted(set(int(a) for _, _, a, t in wl.segs.tolist() if t)) if wl.backward else []
+        dA_h = torch.empty_like(dA, device="cpu").pin_memory() if wl.backward else None
+        dB_h = torch.empty_like(dB, device="cpu").pin_memory() if wl.backward else None
+        h2d = x.numel() * 2 + int(trows.shape[0]) * N * 2
+        d2h = y.numel() * 2 + int(trows.shape[0]) * K * 2 + sum(int(wl.rank[a]) * (K + N) * 4 for a in tads)
+
+        def e2e_step():
+            x.copy_(x_h, non_blocking=True)
+            for s, l in tspans:
+                dY[s:s + l].copy_(dY_h[s:s + l], non_blocking=True)
+            step()
+            y_h.copy_(y, non_blocking=True)
+            for s, l in tspans:
+                dX_h[s:s + l].copy_(dX[s:s + l], non_blocking=True)
+            for a in tads:
+                ao, bo, r = int(wl.a_off[a]), int(wl.b_off[a]), int(wl.rank[a])
+                dA_h[ao:ao + r * K].copy_(dA[ao:ao + r * K], non_blocking=True)
+                dB_h[bo:bo + r * N].copy_(dB[bo:bo + r * N], non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 20))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = torch.tensor([e0.elapsed_time(e1) / n_e2e], device="cuda", dtype=torch.float64)
+        if dist:
+            dist.all_reduce(ems, op=dist.ReduceOp.MAX)
+        e2e = {"value": acc["tokens"] * world / (float(ems.item()) / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": float(ems.item()), "steps": n_e2e}
+
+    # ---- roofline of the dominant launch (the forward main pass) and of the whole step
+    pk = peaks()
+    line = None
+    if rank == 0:
+        if wl.forward:
+            main_ms = group_ms[1]
+            achieved = acc["fwd_main_flops"] / (main_ms / 1e3) / 1e12
+            tr = profiled_traffic(args.config)
+            roof = {"kernel": "lora_tc_kernel (forward main pass: x W + fused LoRA expand)", "bound": "tensor",
+                    "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                    "frac": achieved / pk["bf16_tflops_sustained"], "traffic": tr,
+                    "peak_source": pk["source"] + " (sustained bf16)", "ms_per_launch": main_ms,
+                    "algorithmic_flops_per_launch": acc["fwd_main_flops"]}
+        else:
+            main_ms = group_ms[3]
+            achieved = acc["bwd_flops"] / (main_ms / 1e3) / 1e12
+            roof = {"kernel": "lora_tc_kernel (backward main pass)", "bound": "tensor", "achieved": achieved,
+                    "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                    "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
+                    "peak_source": pk["source"] + " (sustained bf16)", "ms_per_launch": main_ms}
+        t_roof = max(acc["flops"] / (pk["bf16_tflops_sustained"] * 1e12), acc["bytes"] / (pk["hbm_gbs"] * 1e9))
+        step_stats = {"tflops": acc["flops"] / (ms / 1e3) / 1e12, "hbm_gbs": acc["bytes"] / (ms / 1e3) / 1e9,
+                      "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms,
+                      "algorithmic_flops": acc["flops"], "algorithmic_bytes": acc["bytes"],
+                      "group_ms": {"fwd_shrink": group_ms[0], "fwd_main": group_ms[1], "bwd_shrink": group_ms[2],
+                                   "bwd_main": group_ms[3]}}
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            t_cpu, desc, threads = oracle_sample(wl)
+            cpu = {"value": acc["tokens"] / t_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the pages' workloads)",
+                "config": {"workload": wl.name, "T": T, "K": K, "N": N, "adapters": wl.n_adapters,
+                           "train_tokens": acc.get("train_tokens", 0), "xa": wl.xa_mode,
+                           "l2": "inputs larger than L2 (W alone %.0f MB); no flush" % (2 * K * N / 1e6),
+                           "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
+                "roofline": roof, "step": step_stats, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+                "gpu_launches": launches_per_step(wl) * args.steps}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

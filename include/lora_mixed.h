@@ -41,9 +41,11 @@
  *     launches nothing, and lora_last_error() describes the problem.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without waiting for it.  Segment-table
- *     planning happens on the host; the plan is copied into `workspace` with
- *     an asynchronous copy from pageable host memory, so the host-side
- *     segment array may be reused as soon as the call returns.
+ *     planning happens on the host; the plan travels into `workspace` by an
+ *     asynchronous copy from a small library-owned ring of pinned host
+ *     buffers (allocated on first use, per device; a slot is reused only
+ *     after its previous copy has completed), so the host-side segment array
+ *     may be reused as soon as the call returns.
  *   - Two calls that share a workspace must not overlap on the GPU.
  *   - Kernels never wait without a bound.  If one gives up, it records a
  *     nonzero code in the workspace's status word; lora_workspace_status()
@@ -159,6 +161,19 @@ const char* lora_last_error(void);
  * that used `workspace`: LORA_OK, or LORA_ERR_TIMEOUT if a kernel gave up a
  * bounded wait (its outputs are then incomplete).  Blocking. */
 int lora_workspace_status(const void* workspace, void* stream);
+
+/* Tracing (per-step timing, cf. DeltaServe section 3.1: engine hooks record
+ * per-step execution time).  With `events` non-NULL, every later call on the
+ * calling thread records events[2*i] just before and events[2*i+1] just after
+ * its launch group i on the call's stream:
+ *   i = 0: forward shrink pass (row gather + x A of every tile)
+ *   i = 1: forward main pass   (x W plus the fused LoRA expand, writes y)
+ *   i = 2: backward shrink pass (dY B^T, and x A when recomputed)
+ *   i = 3: backward main pass   (dX, dA, dB)
+ * `events` points to 8 cudaEvent_t handles owned by the caller; the array is
+ * copied, the events must outlive the calls.  NULL switches tracing off.
+ * A call that has no work in group i still records both of its events. */
+int lora_set_trace_events(void* const* events);
 
 /* Diagnostic: the forward tile plan of a segment table, for host-side tests.
  *   n_tiles_out: number of 128-row tiles.

@@ -35,7 +35,7 @@ ERRORS = {0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_SEGMENTS", -3:
           -8: "LORA_ERR_CUDA", -9: "LORA_ERR_RANK", -10: "LORA_ERR_LIMIT", -11: "LORA_ERR_TIMEOUT"}
 
 EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_mixed_backward", "lora_last_error",
-            "lora_workspace_status", "lora_plan_describe"]
+            "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events"]
 
 
 class LoraError(RuntimeError):
@@ -92,6 +92,8 @@ def library(path=None):
     lib.lora_workspace_status.restype = ctypes.c_int
     lib.lora_plan_describe.argtypes = [I32, I32, I32, P, P, I32, P, P, P, I32]
     lib.lora_plan_describe.restype = ctypes.c_int
+    lib.lora_set_trace_events.argtypes = [P]
+    lib.lora_set_trace_events.restype = ctypes.c_int
     if path is None:
         _LIB = lib
     return lib
@@ -221,6 +223,16 @@ def backward(x, Wt, pool, segs, dY, xa_saved=None, dX=None, dA=None, dB=None, wa
 def workspace_status(workspace, stream=None):
     """Raise LoraError if a kernel of the last call on this workspace gave up a bounded wait."""
     _check(library().lora_workspace_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def set_trace_events(events):
+    """Record 8 torch.cuda.Event objects around the four launch groups of later calls (None: off)."""
+    if events is None:
+        _check(library().lora_set_trace_events(None))
+        return
+    assert len(events) == 8
+    arr = (ctypes.c_void_p * 8)(*[e.cuda_event for e in events])
+    _check(library().lora_set_trace_events(ctypes.cast(arr, ctypes.c_void_p)))
 
 
 def plan_describe(T, K, N, pool, segs, cap=None):

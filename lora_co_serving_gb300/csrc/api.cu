@@ -18,6 +18,14 @@ using namespace lora;
 namespace {
 
 thread_local std::string g_err;
+thread_local bool g_trace_on = false;
+thread_local cudaEvent_t g_trace[8];
+
+// Record the tracing event that opens (end = 0) or closes (end = 1) launch group `group`.
+cudaError_t trace(int group, int end, cudaStream_t stream) {
+    if (!g_trace_on) return cudaSuccess;
+    return cudaEventRecord(g_trace[2 * group + end], stream);
+}
 
 int fail(int code, const std::string& msg) {
     g_err = msg;
@@ -253,6 +261,19 @@ size_t lora_xa_size(lora_dtype_t dt, const lora_pool_t* pool, const lora_segment
     return elems * (dt == LORA_BF16 ? 2 : 4);
 }
 
+int lora_set_trace_events(void* const* events) {
+    if (!events) {
+        g_trace_on = false;
+        return LORA_OK;
+    }
+    for (int i = 0; i < 8; ++i) {
+        if (!events[i]) return fail(LORA_ERR_INVALID_ARG, "trace events must be non-NULL");
+        g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    g_trace_on = true;
+    return LORA_OK;
+}
+
 int lora_workspace_status(const void* workspace, void* stream) {
     if (!workspace) return fail(LORA_ERR_WORKSPACE, "workspace is NULL");
     CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
@@ -368,15 +389,19 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
 
     rc = begin_call(L, workspace, blob.size(), blob.data(), stream);
     if (rc) return rc;
+    CUDA_TRY(trace(0, 0, stream));
     if (pl.n_gtiles > 0) {
         const int32_t first = int32_t(pl.tiles.size()) - pl.n_gtiles;
         CUDA_TRY(gather_rows(x, K, reinterpret_cast<const int32_t*>(ws + L.rowmap) + (size_t)first * kTileM,
                              ws + L.xg, pl.n_gtiles * kTileM, stream));
     }
     for (int k = 0; k < 2; ++k) {
-        if (grid[k] == 0) continue;
-        fill_plan_pointers(&P, ws, L, k);
-        CUDA_TRY(tc_launch(P, grid[k], stream));
+        if (k == 1) CUDA_TRY(trace(1, 0, stream));
+        if (grid[k] > 0) {
+            fill_plan_pointers(&P, ws, L, k);
+            CUDA_TRY(tc_launch(P, grid[k], stream));
+        }
+        CUDA_TRY(trace(k, 1, stream));
     }
     return LORA_OK;
 }
@@ -509,13 +534,17 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
 
     rc = begin_call(L, workspace, blob.size(), blob.data(), stream);
     if (rc) return rc;
+    CUDA_TRY(trace(2, 0, stream));
     if (!recompute && dB)
         CUDA_TRY(xat_from_saved(xa_saved, reinterpret_cast<const TrainSeg*>(ws + L.tsegs), int32_t(pl.tsegs.size()),
                                 max_len, ws + L.xat, int32_t(Pcols), stream));
     for (int k = 0; k < 2; ++k) {
-        if (grid[k] == 0) continue;
-        fill_plan_pointers(&P, ws, L, k);
-        CUDA_TRY(tc_launch(P, grid[k], stream));
+        if (k == 1) CUDA_TRY(trace(3, 0, stream));
+        if (grid[k] > 0) {
+            fill_plan_pointers(&P, ws, L, k);
+            CUDA_TRY(tc_launch(P, grid[k], stream));
+        }
+        CUDA_TRY(trace(2 + k, 1, stream));
     }
     return LORA_OK;
 }

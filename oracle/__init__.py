@@ -36,7 +36,7 @@ def _lib():
         lib.oracle_forward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, I32, P, I32, P, I64, P, P]
         lib.oracle_forward.restype = ctypes.c_int
         lib.oracle_backward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, I32, P, I32, P, P, I64, P, P,
-                                        P, ctypes.c_int]
+                                        P, ctypes.c_int, P, I64, P, I64]
         lib.oracle_backward.restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -55,7 +55,7 @@ def load_library(path):
     lib.oracle_forward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, I32, P, I32, P, I64, P, P]
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_backward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, I32, P, I32, P, P, I64, P, P,
-                                    P, ctypes.c_int]
+                                    P, ctypes.c_int, P, I64, P, I64]
     lib.oracle_backward.restype = ctypes.c_int
     return lib
 
@@ -99,16 +99,20 @@ def forward(x, Wt, A, B, a_off, b_off, rank, scale, segs, rows=None, want_u=Fals
 
 
 def backward(x, Wt, A, B, a_off, b_off, rank, scale, segs, dY, dx_rows=None, want_dx=True, want_grads=True,
-             accumulate=False, dA_init=None, dB_init=None, lib=None):
+             accumulate=False, dA_init=None, dB_init=None, cols_b=None, cols_a=None, lib=None):
     """(dX, dA, dB) in float64.
 
     dX holds the rows listed in ``dx_rows`` (default: every training token in
     increasing segment-start order).  dA/dB are pool-shaped; adapters without
     training segments keep ``dA_init``/``dB_init`` (zeros by default).
+    ``cols_b`` / ``cols_a`` restrict dB to the listed columns n and dA to the
+    listed columns k (other entries keep their initial values).
     """
     g = _Args(x, Wt, A, B, a_off, b_off, rank, scale, segs)
     dYa = _f32(dY)
     rows_a = None if dx_rows is None else np.ascontiguousarray(dx_rows, dtype=np.int64)
+    cb = None if cols_b is None else np.ascontiguousarray(cols_b, dtype=np.int64)
+    ca = None if cols_a is None else np.ascontiguousarray(cols_a, dtype=np.int64)
     if want_dx:
         if rows_a is None:
             tr = g.segs[g.segs[:, 3] != 0]
@@ -126,7 +130,8 @@ def backward(x, Wt, A, B, a_off, b_off, rank, scale, segs, dY, dx_rows=None, wan
                                          _ptr(g.b_off), _ptr(g.rank), _ptr(g.scale), len(g.rank), _ptr(g.segs),
                                          g.segs.shape[0], _ptr(dYa), _ptr(rows_a),
                                          0 if rows_a is None else rows_a.shape[0], _ptr(dX), _ptr(dA), _ptr(dB),
-                                         1 if accumulate else 0)
+                                         1 if accumulate else 0, _ptr(cb), 0 if cb is None else cb.shape[0],
+                                         _ptr(ca), 0 if ca is None else ca.shape[0])
     if rc != 0:
         raise ValueError("oracle_backward: malformed segment table")
     return dX, dA, dB
@@ -139,7 +144,7 @@ def forward_wl(wl, rows=None, want_u=False, lib=None):
 
 
 def backward_wl(wl, dx_rows=None, want_dx=True, want_grads=True, accumulate=False, dA_init=None, dB_init=None,
-                lib=None):
+                cols_b=None, cols_a=None, lib=None):
     return backward(wl.x, wl.Wt, wl.A, wl.B, wl.a_off, wl.b_off, wl.rank, wl.scale, wl.segs, wl.dY,
                     dx_rows=dx_rows, want_dx=want_dx, want_grads=want_grads, accumulate=accumulate,
-                    dA_init=dA_init, dB_init=dB_init, lib=lib)
+                    dA_init=dA_init, dB_init=dB_init, cols_b=cols_b, cols_a=cols_a, lib=lib)

@@ -141,6 +141,9 @@ static int32_t train_segments_sorted(const int32_t* segs, int32_t n_segs, int32_
  *   dA,dB pool-shaped (same sizes and offsets as A and B).  For every adapter
  *         with a training segment, its block is overwritten (accumulate == 0)
  *         or added to (accumulate != 0); other blocks are left untouched.
+ *   cols_b / cols_a (optional): compute only the listed columns n of dB_a
+ *         (entries dB_a[j, n], all j) and columns k of dA_a; the other
+ *         entries keep their initial values.  NULL = every column.
  * Returns 0, or -1 on a malformed table (a training segment on id -1 or out
  * of range, or a dX row that is not a training token).
  */
@@ -148,7 +151,8 @@ int oracle_backward(int64_t T, int64_t K, int64_t N, const float* x, const float
                     const float* B, const int64_t* a_off, const int64_t* b_off, const int32_t* rank,
                     const double* scale, int32_t n_adapters, const int32_t* segs, int32_t n_segs,
                     const float* dY, const int64_t* dx_rows, int64_t n_dx_rows, double* dX, double* dA,
-                    double* dB, int accumulate) {
+                    double* dB, int accumulate, const int64_t* cols_b, int64_t n_cols_b, const int64_t* cols_a,
+                    int64_t n_cols_a) {
     int32_t* tsegs = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_segs > 0 ? n_segs : 1));
     int32_t n_train = train_segments_sorted(segs, n_segs, tsegs);
     for (int32_t q = 0; q < n_train; ++q) {
@@ -233,8 +237,10 @@ int oracle_backward(int64_t T, int64_t K, int64_t N, const float* x, const float
             double s = scale[a];
             if (dB) {
                 double* dBa = dB + b_off[a];
+                int64_t nn = cols_b ? n_cols_b : N;
 #pragma omp parallel for schedule(static)
-                for (int64_t n = 0; n < N; ++n) {
+                for (int64_t c = 0; c < nn; ++c) {
+                    int64_t n = cols_b ? cols_b[c] : c;
                     for (int32_t j = 0; j < r; ++j) {
                         double acc = 0.0;
                         for (int64_t i = 0; i < n_all; ++i)
@@ -245,8 +251,10 @@ int oracle_backward(int64_t T, int64_t K, int64_t N, const float* x, const float
             }
             if (dA) {
                 double* dAa = dA + a_off[a];
+                int64_t nk = cols_a ? n_cols_a : K;
 #pragma omp parallel for schedule(static)
-                for (int64_t k = 0; k < K; ++k) {
+                for (int64_t c = 0; c < nk; ++c) {
+                    int64_t k = cols_a ? cols_a[c] : c;
                     for (int32_t j = 0; j < r; ++j) {
                         double acc = 0.0;
                         for (int64_t i = 0; i < n_all; ++i)

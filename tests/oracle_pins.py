@@ -259,5 +259,32 @@ def pin_accumulate(lib=None):
     assert np.array_equal(aA[~mA], initA[~mA]) and np.array_equal(aB[~mB], initB[~mB]), "untouched blocks"
 
 
+def pin_sampled_columns(lib=None):
+    """Column-restricted gradients and row-restricted outputs equal the matching slices of the full ones."""
+    wl = workloads.config5(K=48, N=72, n_adapters=9, n_decode=12, prefill_tokens=40, len_lo=4, len_hi=20,
+                           train_len=16)
+    y = oracle.forward_wl(wl, lib=lib)
+    rows = np.array([0, 5, wl.T - 1, 17])
+    assert np.array_equal(oracle.forward_wl(wl, rows=rows, lib=lib), y[rows]), "row-sampled forward"
+    dX, dA, dB = oracle.backward_wl(wl, lib=lib)
+    cb = np.array([0, 3, wl.N - 1])
+    ca = np.array([1, wl.K - 2])
+    _, sA, sB = oracle.backward_wl(wl, want_dx=False, cols_b=cb, cols_a=ca, lib=lib)
+    a = int(wl.meta["train_adapter"])
+    r = int(wl.rank[a])
+    fB = dB[wl.b_off[a]:wl.b_off[a] + r * wl.N].reshape(r, wl.N)
+    gB = sB[wl.b_off[a]:wl.b_off[a] + r * wl.N].reshape(r, wl.N)
+    fA = dA[wl.a_off[a]:wl.a_off[a] + r * wl.K].reshape(r, wl.K)
+    gA = sA[wl.a_off[a]:wl.a_off[a] + r * wl.K].reshape(r, wl.K)
+    assert np.array_equal(gB[:, cb], fB[:, cb]) and np.array_equal(gA[:, ca], fA[:, ca]), "column-sampled grads"
+    others = np.setdiff1d(np.arange(wl.N), cb)
+    assert np.all(gB[:, others] == 0.0), "unsampled columns untouched"
+    trows = wl.train_rows()
+    pick = np.array([2, 20])
+    sX, _, _ = oracle.backward_wl(wl, dx_rows=trows[pick], want_grads=False, lib=lib)
+    assert np.array_equal(sX, dX[pick]), "row-sampled dX"
+
+
 ALL_PINS = [pin_brute_forward, pin_brute_backward, pin_merged_weight_config1, pin_zero_B, pin_finite_differences,
-            pin_segment_order, pin_pool_order, pin_routing, pin_trainable_count, pin_accumulate]
+            pin_segment_order, pin_pool_order, pin_routing, pin_trainable_count, pin_accumulate,
+            pin_sampled_columns]
