@@ -40,19 +40,19 @@ def parse():
     ap.add_argument("--config", type=int, default=5, choices=[2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
+                    help="override a workload parameter (e.g. N=4096) for profiling a reduced case")
     return ap.parse_args()
 
 
 # ----------------------------------------------------------------------------------------------- workload accounting
-def make_workload(cfg, rank=0):
+def make_workload(cfg, rank=0, overrides=()):
     seed = 1000 + cfg + 7919 * rank      # each rank draws its own batch (weak scaling)
-    if cfg == 5:
-        return workloads.config5(seed=seed)
-    if cfg == 3:
-        return workloads.config3(seed=seed)
-    if cfg == 4:
-        return workloads.config4(seed=seed)
-    return workloads.config2(seed=seed)
+    kw = {}
+    for item in overrides:
+        k, v = item.split("=", 1)
+        kw[k] = int(v)
+    return workloads.config(cfg, seed=seed, **kw)
 
 
 def accounting(wl):
@@ -129,7 +129,7 @@ def profiled_traffic(cfg):
 
 # ----------------------------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -146,12 +146,24 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        """Summary of the samples taken between host times t0 and t1 (the timed region)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
         rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if t0 is not None:
+            import datetime
+            keep = []
+            for r in rows:
+                try:
+                    ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if t0 - 0.05 <= ts <= t1 + 0.05:
+                    keep.append(r)
+            rows = keep
         sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
         reasons = set()
@@ -222,7 +234,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    wl = make_workload(args.config)
+    wl = make_workload(args.config, 0, args.set)
     acc = accounting(wl)
     times = []
     desc = threads = None
@@ -262,7 +274,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     lm.build()
 
-    wl = make_workload(args.config, rank)
+    wl = make_workload(args.config, rank, args.set)
     acc = accounting(wl)
     x, Wt, A, B = to_dev(wl.x, torch), to_dev(wl.Wt, torch), to_dev(wl.A, torch), to_dev(wl.B, torch)
     dY = to_dev(wl.dY, torch) if wl.dY is not None else None
@@ -291,19 +303,24 @@ def run_ours(args):
 
     # ---- device-timed region: K steps, per-step trace events around each launch group
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    for row in ev:          # torch creates the CUDA event on first record
+        for e in row:
+            e.record(stream)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device())
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
+    wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
         lm.set_trace_events(ev[i])
         step()
     stop.record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop()
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1)
     lm.set_trace_events(None)
     if dist:
         dist.barrier()

@@ -157,6 +157,9 @@ void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&of
     put(b, at(L.rowaux), pl.rowaux);
     put(b, at(L.groups), pl.groups);
     put(b, at(L.tsegs), pl.tsegs);
+    put(b, at(L.atoms_a), pl.atoms_a);
+    put(b, at(L.atoms_b), pl.atoms_b);
+    put(b, at(L.units), pl.units);
     for (int k = 0; k < 2; ++k) {
         put(b, at(L.items[k]), pl.items[k]);
         put(b, at(L.cta_off[k]), off[k]);
@@ -175,6 +178,9 @@ void fill_plan_pointers(KParams* P, uint8_t* ws, const Layout& L, int launch) {
     P->items = reinterpret_cast<const WorkItem*>(ws + L.items[launch]);
     P->cta_off = reinterpret_cast<const int32_t*>(ws + L.cta_off[launch]);
     P->cta_list = reinterpret_cast<const int32_t*>(ws + L.cta_list[launch]);
+    P->atoms_a = reinterpret_cast<const int32_t*>(ws + L.atoms_a);
+    P->atoms_b = reinterpret_cast<const int32_t*>(ws + L.atoms_b);
+    P->part = reinterpret_cast<float*>(ws + L.part);
     P->status = reinterpret_cast<int32_t*>(ws + L.status);
 }
 
@@ -221,6 +227,23 @@ void f32_layout(const Problem& p, size_t base, F32Blob* fb) {
     put(fb->bytes, fb->tok - base, tok);
     put(fb->bytes, fb->ad - base, ad);
     put(fb->bytes, fb->segs - base, segs);
+}
+
+cudaError_t finalize_shrink(const Plan& pl, const Layout& L, uint8_t* ws, const KParams& P, cudaStream_t stream) {
+    FinalizeArgs f{};
+    f.units = reinterpret_cast<const ShrinkUnit*>(ws + L.units);
+    f.n_units = int32_t(pl.units.size());
+    f.tiles = reinterpret_cast<const TileDesc*>(ws + L.tiles);
+    f.chunks = reinterpret_cast<const Chunk*>(ws + L.chunks);
+    f.rowchunk = reinterpret_cast<const int32_t*>(ws + L.rowchunk);
+    f.rowaux = reinterpret_cast<const int32_t*>(ws + L.rowaux);
+    f.part = reinterpret_cast<const float*>(ws + L.part);
+    f.z = ws + L.z;
+    f.xa_save = P.xa_save;
+    f.xat = P.xat;
+    f.dybt = P.dybt;
+    f.t_ld = P.t_ld;
+    return shrink_finalize(f, stream);
 }
 
 int begin_call(const Layout& L, void* ws, size_t bytes_plan, const void* blob, cudaStream_t stream) {
@@ -401,6 +424,7 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
             fill_plan_pointers(&P, ws, L, k);
             CUDA_TRY(tc_launch(P, grid[k], stream));
         }
+        if (k == 0) CUDA_TRY(finalize_shrink(pl, L, ws, P, stream));
         CUDA_TRY(trace(k, 1, stream));
     }
     return LORA_OK;
@@ -544,6 +568,7 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
             fill_plan_pointers(&P, ws, L, k);
             CUDA_TRY(tc_launch(P, grid[k], stream));
         }
+        if (k == 0) CUDA_TRY(finalize_shrink(pl, L, ws, P, stream));
         CUDA_TRY(trace(2 + k, 1, stream));
     }
     return LORA_OK;

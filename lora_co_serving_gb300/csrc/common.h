@@ -41,7 +41,7 @@ struct TileDesc {
     int32_t ext_k;    // LoRA columns: sum over chunks of roundup(r,16)
     int32_t z_blk0;   // first Z block of this tile
     int32_t tpos0;    // backward tiles: column of tile row 0 in the transposed buffers; -1 otherwise
-    int32_t pad;
+    int32_t atom0;    // first entry of this tile in the atom-row tables (one entry per 8 LoRA columns)
 };
 
 struct Chunk {
@@ -61,8 +61,25 @@ struct WorkItem {
     int32_t nk;       // main/shrink: k-blocks of the dense loop; grad: total token blocks
     int32_t mma_n;    // N of the MMA
     int32_t n_ext;    // main: LoRA k-blocks after the dense loop
+    int32_t kb0;      // shrink: first k-block of this split of the reduction
+    int32_t part;     // shrink: column offset of this split's fp32 partial [mma_n, 128] in the partial buffer
+};
+
+// One shrink pass of one tile: the finalize step sums its K-splits (in order) and writes Z and the saved or
+// transposed copies.
+struct ShrinkUnit {
+    int32_t kind;     // kShrinkFwd, kShrinkDyb or kShrinkXa
+    int32_t tile;
+    int32_t n0;       // first LoRA column of the pass
+    int32_t mma_n;
+    int32_t nsplit;
+    int32_t part0;    // column offset of split 0; split s sits at part0 + s * mma_n
     int32_t pad0, pad1;
 };
+
+// K-blocks per split of a shrink reduction.  Split boundaries depend on K alone, so a row's xA is summed in the
+// same order whatever the rest of its tile holds.
+constexpr int kShrinkSplitKb = 32;
 
 struct GradGroup {    // one fine-tuning adapter of a backward call
     int32_t adapter;

@@ -114,11 +114,40 @@ static void make_chunks(const Problem& p, const int32_t* row_adapter, Plan* pl, 
     td->ext_k = zcol;
     td->z_blk0 = int32_t(pl->z_blocks);
     pl->z_blocks += cdiv(zcol, kBK);
+    // pool row of every 8-column atom of the tile's LoRA columns; the padding of a chunk to 16 repeats the
+    // chunk's last atom, so every loaded row stays inside the adapter's own block
+    td->atom0 = int32_t(pl->atoms_a.size());
+    for (int c = 0; c < n; ++c) {
+        const Chunk& ch = pl->chunks[td->chunk0 + c];
+        const int32_t last = ((ch.r + 7) / 8 - 1) * 8;
+        for (int32_t o = 0; o < pad16(ch.r); o += 8) {
+            pl->atoms_a.push_back(ch.prow_a + std::min(o, last));
+            pl->atoms_b.push_back(ch.prow_b + std::min(o, last));
+        }
+    }
     for (int i = 0; i < kTileM; ++i) {
         rowchunk[i] = -1;
         if (row_adapter[i] >= 0)
             rowchunk[i] = td->chunk0 + int32_t(std::lower_bound(ids, ids + n, row_adapter[i]) - ids);
     }
+}
+
+// Shrink items of one pass, split along the reduction at boundaries that depend on the k-block count alone.
+static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t mma_n, int32_t nk) {
+    const int32_t nsplit = std::max<int32_t>(1, int32_t(cdiv(nk, kShrinkSplitKb)));
+    ShrinkUnit u{};
+    u.kind = kind; u.tile = tile; u.n0 = n0; u.mma_n = mma_n; u.nsplit = nsplit;
+    u.part0 = int32_t(pl->part_cols);
+    for (int32_t s = 0; s < nsplit; ++s) {
+        WorkItem w{};
+        w.kind = kind; w.tile = tile; w.n0 = n0; w.mma_n = mma_n;
+        w.kb0 = int32_t((int64_t)s * nk / nsplit);
+        w.nk = int32_t((int64_t)(s + 1) * nk / nsplit) - w.kb0;
+        w.part = u.part0 + s * mma_n;
+        pl->items[0].push_back(w);
+    }
+    pl->part_cols += (int64_t)nsplit * mma_n;
+    pl->units.push_back(u);
 }
 
 void plan_forward(const Problem& p, Plan* out) {
@@ -190,15 +219,8 @@ void plan_forward(const Problem& p, Plan* out) {
     const int32_t nk = int32_t(cdiv(p.K, kBK));
     for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
         const TileDesc& td = pl.tiles[ti];
-        for (int32_t c0 = 0; c0 < td.ext_k; c0 += kPassCols) {
-            WorkItem w{};
-            w.kind = kShrinkFwd;
-            w.tile = int32_t(ti);
-            w.n0 = c0;
-            w.nk = nk;
-            w.mma_n = std::min(kPassCols, td.ext_k - c0);
-            pl.items[0].push_back(w);
-        }
+        for (int32_t c0 = 0; c0 < td.ext_k; c0 += kPassCols)
+            add_shrink(&pl, kShrinkFwd, int32_t(ti), c0, std::min(kPassCols, td.ext_k - c0), nk);
     }
     const int32_t n_nt = int32_t(cdiv(p.N, kBN));
     for (size_t b0 = 0; b0 < pl.tiles.size(); b0 += kBandTiles) {
@@ -284,16 +306,8 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
     const bool need_xa = want_db && recompute;
     for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
         const TileDesc& td = pl.tiles[ti];
-        if (need_dyb) {
-            WorkItem w{};
-            w.kind = kShrinkDyb; w.tile = int32_t(ti); w.n0 = 0; w.nk = int32_t(cdiv(p.N, kBK)); w.mma_n = td.ext_k;
-            pl.items[0].push_back(w);
-        }
-        if (need_xa) {
-            WorkItem w{};
-            w.kind = kShrinkXa; w.tile = int32_t(ti); w.n0 = 0; w.nk = int32_t(cdiv(p.K, kBK)); w.mma_n = td.ext_k;
-            pl.items[0].push_back(w);
-        }
+        if (need_dyb) add_shrink(&pl, kShrinkDyb, int32_t(ti), 0, td.ext_k, int32_t(cdiv(p.N, kBK)));
+        if (need_xa) add_shrink(&pl, kShrinkXa, int32_t(ti), 0, td.ext_k, int32_t(cdiv(p.K, kBK)));
     }
     if (want_dx) {
         const int32_t n_nt = int32_t(cdiv(p.K, kBN));
@@ -327,8 +341,15 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
 }
 
 static int64_t item_cost(const WorkItem& w) {
-    // rough cycles: an MMA k-block costs ~2 cycles per N column; a stage load at least ~256 cycles
-    int64_t per = std::max<int64_t>(2 * w.mma_n, 256);
+    // rough cycles per k-block: the larger of its TMA bytes at ~64 B/cycle and its MMA time (~2.7 cycles per N
+    // column for M = 128, K = 64)
+    int64_t bytes = 0;
+    switch (w.kind) {
+        case kMainFwd:
+        case kMainDx: bytes = kTileM * kBK * 2 + kBN * kBK * 2; break;
+        default: bytes = kTileM * kBK * 2 + (int64_t)w.mma_n * kBK * 2; break;
+    }
+    const int64_t per = std::max<int64_t>(bytes / 64, (27 * (int64_t)w.mma_n) / 10);
     int64_t c = (int64_t)w.nk * per;
     if (w.kind == kMainFwd || w.kind == kMainDx) c += (int64_t)w.n_ext * per;
     return c + 2000;
@@ -373,6 +394,9 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     L.rowaux = take(sizeof(int32_t) * pl.rowaux.size());
     L.groups = take(sizeof(GradGroup) * pl.groups.size());
     L.tsegs = take(sizeof(TrainSeg) * pl.tsegs.size());
+    L.atoms_a = take(sizeof(int32_t) * pl.atoms_a.size());
+    L.atoms_b = take(sizeof(int32_t) * pl.atoms_b.size());
+    L.units = take(sizeof(ShrinkUnit) * pl.units.size());
     for (int k = 0; k < 2; ++k) {
         L.items[k] = take(sizeof(WorkItem) * pl.items[k].size());
         L.cta_off[k] = take(sizeof(int32_t) * (kMaxCtas + 1));
@@ -382,6 +406,7 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     if (p.dt == LORA_BF16) {
         L.xg = take((size_t)pl.n_gtiles * kTileM * p.K * 2);
         L.z = take((size_t)pl.z_blocks * kZBlockBytes);
+        L.part = take((size_t)pl.part_cols * kTileM * sizeof(float));
         if (backward) {
             L.xat = take((size_t)LORA_MAX_RANK * pl.tcols * 2);
             L.dybt = take((size_t)LORA_MAX_RANK * pl.tcols * 2);

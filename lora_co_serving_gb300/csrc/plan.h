@@ -41,12 +41,16 @@ struct Plan {
     std::vector<int32_t> rowmap;     // 128 per tile: token row or -1
     std::vector<int32_t> rowchunk;   // 128 per tile: chunk index or -1
     std::vector<int32_t> rowaux;     // 128 per tile: forward: xa_save element offset or -1; backward: -1
+    std::vector<int32_t> atoms_a;    // per tile, per 8 LoRA columns: first A-pool row of that 8-row atom
+    std::vector<int32_t> atoms_b;    // same for the B pool
     std::vector<WorkItem> items[2];  // first and second launch
+    std::vector<ShrinkUnit> units;   // shrink passes to finalize between the two launches
     std::vector<GradGroup> groups;
     std::vector<TrainSeg> tsegs;
     int32_t n_gtiles = 0;            // forward: tiles of the gathered buffer
     int64_t z_blocks = 0;
     int64_t tcols = 0;               // backward: columns of the transposed xA / dYB buffers
+    int64_t part_cols = 0;           // columns (of 128 fp32 each) of the shrink partial-sum buffer
 };
 
 void plan_forward(const Problem& p, Plan* out);
@@ -61,9 +65,10 @@ void assign_items(const std::vector<WorkItem>& items, const Plan& plan, int G, s
 struct Layout {
     size_t status = 0;
     size_t tiles = 0, chunks = 0, rowmap = 0, rowchunk = 0, rowaux = 0, groups = 0, tsegs = 0;
+    size_t atoms_a = 0, atoms_b = 0, units = 0;
     size_t items[2] = {0, 0}, cta_off[2] = {0, 0}, cta_list[2] = {0, 0};
     size_t plan_end = 0;
-    size_t xg = 0, z = 0, xat = 0, dybt = 0;
+    size_t xg = 0, z = 0, xat = 0, dybt = 0, part = 0;
     size_t simt = 0;                 // float32 path scratch
     size_t total = 0;
 };

@@ -140,25 +140,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Pool row that holds LoRA column `col` (a multiple of 8) of a tile.  Columns past a chunk's rank (its
-// padding to 16) repeat the chunk's last 8-row atom: they meet zero Z columns (main) or are discarded
-// (shrink), and repeating keeps every loaded value inside the adapter's own block.
-__device__ __forceinline__ int32_t atom_row(const Chunk* chunks, int32_t c0, int32_t nchunk, int32_t col, bool use_b,
-                                            int32_t* cursor) {
-    int32_t ci = *cursor;
-    while (ci + 1 < nchunk) {
-        const Chunk& ch = chunks[c0 + ci];
-        if (col < ch.zcol + ((ch.r + 15) & ~15)) break;
-        ++ci;
-    }
-    *cursor = ci;
-    const Chunk& ch = chunks[c0 + ci];
-    int32_t o = col - ch.zcol;
-    const int32_t last = ((ch.r + 7) / 8 - 1) * 8;
-    if (o > last) o = last;
-    return (use_b ? ch.prow_b : ch.prow_a) + o;
-}
-
 struct Ring {
     int stage = 0;
     uint32_t phase = 0;
@@ -167,13 +148,27 @@ struct Ring {
     }
 };
 
-// --------------------------------------------------------------------------------------------- producer
+// Lane 0 of the producer warp waits for the ring slot to be free and arms its barrier with the stage's byte
+// count; the result is shared with the warp, whose 32 lanes then issue the stage's loads in parallel.
+__device__ __forceinline__ bool acquire_stage(const Ring& ring, uint32_t bar_full, uint32_t bar_empty, uint32_t bytes,
+                                              int lane, volatile int* abort_flag, int32_t* status) {
+    int ok = 1;
+    if (lane == 0) {
+        ok = wait_phase(bar_empty + ring.stage * 8, ring.phase ^ 1u, abort_flag, status) ? 1 : 0;
+        if (ok) mbar_expect_tx(bar_full + ring.stage * 8, bytes);
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// --------------------------------------------------------------------------------------------- producer (warp 0)
 __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty, int i0, int i1,
                              volatile int* abort_flag) {
+    const int lane = threadIdx.x & 31;
     Ring ring;
     for (int ii = i0; ii < i1; ++ii) {
         const WorkItem w = P.items[P.cta_list[ii]];
         if (w.kind == kGradDb || w.kind == kGradDa) {
+            // A: [128 of N or K] x 64 tokens, MN-major (two 64-wide boxes); B: r_pad rows of xA^T / dYB^T
             const GradGroup g = P.groups[w.tile];
             const CUtensorMap* mb = (w.kind == kGradDb) ? &P.tm_xat : &P.tm_dybt;
             const int natoms = w.mma_n / 8;
@@ -182,13 +177,11 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
                 const TrainSeg s = P.tsegs[g.seg0 + q];
                 const CUtensorMap* ma = (w.kind == kGradDb) ? &P.tm_seg_dy[g.seg0 + q] : &P.tm_seg_x[g.seg0 + q];
                 for (int b = 0; b * kBK < s.len; ++b) {
-                    const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
-                    if (!wait_phase(empty, ring.phase ^ 1u, abort_flag, P.status)) return;
+                    if (!acquire_stage(ring, bar_full, bar_empty, bytes, lane, abort_flag, P.status)) return;
+                    const uint32_t full = bar_full + ring.stage * 8;
                     const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
-                    mbar_expect_tx(full, bytes);
-                    tma_load_2d(sa, ma, w.n0, b * kBK, full);
-                    tma_load_2d(sa + 8192, ma, w.n0 + 64, b * kBK, full);
-                    for (int j = 0; j < natoms; ++j) tma_load_2d(sb + j * 1024, mb, s.tpos0 + b * kBK, j * 8, full);
+                    if (lane < 2) tma_load_2d(sa + lane * 8192, ma, w.n0 + 64 * lane, b * kBK, full);
+                    if (lane < natoms) tma_load_2d(sb + lane * 1024, mb, s.tpos0 + b * kBK, lane * 8, full);
                     ring.next();
                 }
             }
@@ -199,52 +192,53 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
             const bool fwd = (w.kind == kMainFwd);
             const CUtensorMap* ma = fwd ? (td.a_src ? &P.tm_xg : &P.tm_x) : &P.tm_dy;
             for (int kb = 0; kb < w.nk; ++kb) {
-                const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
-                if (!wait_phase(empty, ring.phase ^ 1u, abort_flag, P.status)) return;
+                if (!acquire_stage(ring, bar_full, bar_empty, kABytes + kBBytes, lane, abort_flag, P.status)) return;
+                const uint32_t full = bar_full + ring.stage * 8;
                 const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
-                mbar_expect_tx(full, kABytes + kBBytes);
-                tma_load_2d(sa, ma, kb * kBK, td.a_row0, full);
+                if (lane == 0) tma_load_2d(sa, ma, kb * kBK, td.a_row0, full);
                 if (fwd) {
-                    tma_load_2d(sb, &P.tm_w, kb * kBK, w.n0, full);
-                } else {
-                    for (int m = 0; m < 4; ++m) tma_load_2d(sb + m * 8192, &P.tm_w, w.n0 + 64 * m, kb * kBK, full);
+                    if (lane == 1) tma_load_2d(sb, &P.tm_w, kb * kBK, w.n0, full);
+                } else if (lane >= 1 && lane <= 4) {
+                    const int m = lane - 1;
+                    tma_load_2d(sb + m * 8192, &P.tm_w, w.n0 + 64 * m, kb * kBK, full);
                 }
                 ring.next();
             }
+            // LoRA k-blocks: the tile's Z block (already in its shared-memory image) and, for each 8-row atom of
+            // stacked adapter rows, four 64-column MN-major boxes
             const CUtensorMap* mp = fwd ? &P.tm_pb : &P.tm_pa;
-            int32_t cursor = 0;
+            const int32_t* atoms = (fwd ? P.atoms_b : P.atoms_a) + td.atom0;
             for (int e = 0; e < w.n_ext; ++e) {
-                const int atoms = min(8, (td.ext_k - e * kBK) / 8);
-                const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
-                if (!wait_phase(empty, ring.phase ^ 1u, abort_flag, P.status)) return;
+                const int natoms = min(8, (td.ext_k - e * kBK) / 8);
+                if (!acquire_stage(ring, bar_full, bar_empty, kZBlockBytes + natoms * 4096, lane, abort_flag,
+                                   P.status))
+                    return;
+                const uint32_t full = bar_full + ring.stage * 8;
                 const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
-                mbar_expect_tx(full, kZBlockBytes + atoms * 4096);
-                bulk_load(sa, P.zin + (size_t)(td.z_blk0 + e) * kZBlockBytes, kZBlockBytes, full);
-                for (int q = 0; q < atoms; ++q) {
-                    const int32_t prow = atom_row(P.chunks, td.chunk0, td.nchunk, e * kBK + q * 8, fwd, &cursor);
-                    for (int m = 0; m < 4; ++m) tma_load_2d(sb + m * 8192 + q * 1024, mp, w.n0 + 64 * m, prow, full);
+                if (lane == 0) bulk_load(sa, P.zin + (size_t)(td.z_blk0 + e) * kZBlockBytes, kZBlockBytes, full);
+                if (lane < natoms * 4) {
+                    const int q = lane >> 2, m = lane & 3;
+                    const int32_t prow = atoms[e * 8 + q];
+                    tma_load_2d(sb + m * 8192 + q * 1024, mp, w.n0 + 64 * m, prow, full);
                 }
                 ring.next();
             }
             continue;
         }
-        // shrink
+        // shrink split: k-blocks [kb0, kb0 + nk) of the reduction; B = the pass's 8-row atoms of pool rows
         const CUtensorMap* ma = (w.kind == kShrinkFwd) ? (td.a_src ? &P.tm_xg : &P.tm_x)
                                 : (w.kind == kShrinkDyb) ? &P.tm_dy : &P.tm_x;
         const bool use_b = (w.kind == kShrinkDyb);
         const CUtensorMap* mp = use_b ? &P.tm_pb : &P.tm_pa;
         const int natoms = w.mma_n / 8;
-        for (int kb = 0; kb < w.nk; ++kb) {
-            const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
-            if (!wait_phase(empty, ring.phase ^ 1u, abort_flag, P.status)) return;
+        const int32_t my_row = (lane < natoms) ? (use_b ? P.atoms_b : P.atoms_a)[td.atom0 + w.n0 / 8 + lane] : 0;
+        for (int kb = w.kb0; kb < w.kb0 + w.nk; ++kb) {
+            if (!acquire_stage(ring, bar_full, bar_empty, kABytes + natoms * 1024, lane, abort_flag, P.status))
+                return;
+            const uint32_t full = bar_full + ring.stage * 8;
             const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
-            mbar_expect_tx(full, kABytes + natoms * 1024);
-            tma_load_2d(sa, ma, kb * kBK, td.a_row0, full);
-            int32_t cursor = 0;
-            for (int q = 0; q < natoms; ++q) {
-                const int32_t prow = atom_row(P.chunks, td.chunk0, td.nchunk, w.n0 + q * 8, use_b, &cursor);
-                tma_load_2d(sb + q * 1024, mp, kb * kBK, prow, full);
-            }
+            if (lane == 0) tma_load_2d(sa, ma, kb * kBK, td.a_row0, full);
+            if (lane < natoms) tma_load_2d(sb + lane * 1024, mp, kb * kBK, my_row, full);
             ring.next();
         }
     }
@@ -368,59 +362,15 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 }
             }
         } else {
-            // shrink: mask each row to its own adapter's columns, then write Z / xa_save / transposed copies
-            const TileDesc td = P.tiles[w.tile];
-            const int32_t rc = P.rowchunk[w.tile * kTileM + row];
-            int32_t zc0 = 0, zr = 0;
-            float s = 0.f;
-            if (rc >= 0) {
-                const Chunk ch = P.chunks[rc];
-                zc0 = ch.zcol; zr = ch.r; s = ch.scale;
-            }
-            const bool write_z = (w.kind != kShrinkXa);
-            const int32_t save_off =
-                (w.kind == kShrinkFwd && P.xa_save != nullptr) ? P.rowaux[w.tile * kTileM + row] : -1;
-            __nv_bfloat16* tdst = (w.kind == kShrinkDyb) ? P.dybt : (w.kind == kShrinkXa) ? P.xat : nullptr;
-            int32_t t_r = 0;
-            if (tdst) t_r = P.chunks[td.chunk0].r;    // backward tiles hold one adapter
+            // shrink split: raw fp32 partial sums, column-major [mma_n][128] (the finalize step masks, scales,
+            // sums the splits and writes Z and the saved / transposed copies)
+            float* dst = P.part + (size_t)w.part * kTileM + row;
             for (int c = 0; c < w.mma_n; c += 16) {
                 uint32_t a[16];
                 tmem_ld16(taddr + c, a);
                 tmem_ld_wait();
-                float v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int zc = w.n0 + c + i;
-                    v[i] = (rc >= 0 && zc >= zc0 && zc < zc0 + zr) ? __uint_as_float(a[i]) : 0.f;
-                }
-                if (write_z) {
-                    const int zc = w.n0 + c;
-                    uint8_t* blk = P.zout + (size_t)(td.z_blk0 + zc / kBK) * kZBlockBytes + row * 128;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int chunk16 = ((zc % kBK) / 8 + h) ^ (row & 7);
-                        uint4 q;
-                        q.x = pack_bf16(s * v[8 * h + 0], s * v[8 * h + 1]);
-                        q.y = pack_bf16(s * v[8 * h + 2], s * v[8 * h + 3]);
-                        q.z = pack_bf16(s * v[8 * h + 4], s * v[8 * h + 5]);
-                        q.w = pack_bf16(s * v[8 * h + 6], s * v[8 * h + 7]);
-                        *reinterpret_cast<uint4*>(blk + chunk16 * 16) = q;
-                    }
-                }
-                if (save_off >= 0) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int j = w.n0 + c + i - zc0;
-                        if (j >= 0 && j < zr) P.xa_save[save_off + j] = __float2bfloat16_rn(v[i]);
-                    }
-                }
-                if (tdst) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int j = w.n0 + c + i;     // the tile's single chunk starts at column 0
-                        if (j < t_r) tdst[(size_t)j * P.t_ld + td.tpos0 + row] = __float2bfloat16_rn(v[i]);
-                    }
-                }
+                for (int i = 0; i < 16; ++i) dst[(size_t)(c + i) * kTileM] = __uint_as_float(a[i]);
             }
         }
         tc_fence_before();
@@ -466,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_tc_kernel(const __grid_const
     const int i0 = P.cta_off[blockIdx.x], i1 = P.cta_off[blockIdx.x + 1];
 
     if (warp == 0) {
-        if (lane == 0) run_producer(P, smem, bar_full, bar_empty, i0, i1, abort_flag);
+        run_producer(P, smem, bar_full, bar_empty, i0, i1, abort_flag);
     } else if (warp == 1) {
         if (lane == 0) run_mma(P, smem, bar_full, bar_empty, bar_tfull, bar_tempty, tmem, i0, i1, abort_flag);
     } else {

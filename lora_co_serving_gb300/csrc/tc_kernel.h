@@ -34,6 +34,9 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     const WorkItem* items;
     const int32_t* cta_off;
     const int32_t* cta_list;
+    const int32_t* atoms_a;  // per tile, per 8 LoRA columns: A-pool row of the atom
+    const int32_t* atoms_b;  // same for the B pool
+    float* part;             // shrink items: fp32 partial sums, [columns][128 rows]
 
     const uint8_t* zin;     // Z blocks read by main items
     uint8_t* zout;          // Z blocks written by shrink items
