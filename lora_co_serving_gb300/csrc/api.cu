@@ -181,6 +181,8 @@ void fill_plan_pointers(KParams* P, uint8_t* ws, const Layout& L, int launch) {
     P->atoms_a = reinterpret_cast<const int32_t*>(ws + L.atoms_a);
     P->atoms_b = reinterpret_cast<const int32_t*>(ws + L.atoms_b);
     P->part = reinterpret_cast<float*>(ws + L.part);
+    P->units = reinterpret_cast<const ShrinkUnit*>(ws + L.units);
+    P->counters = reinterpret_cast<int32_t*>(ws + L.counters);
     P->status = reinterpret_cast<int32_t*>(ws + L.status);
 }
 
@@ -229,26 +231,9 @@ void f32_layout(const Problem& p, size_t base, F32Blob* fb) {
     put(fb->bytes, fb->segs - base, segs);
 }
 
-cudaError_t finalize_shrink(const Plan& pl, const Layout& L, uint8_t* ws, const KParams& P, cudaStream_t stream) {
-    FinalizeArgs f{};
-    f.units = reinterpret_cast<const ShrinkUnit*>(ws + L.units);
-    f.n_units = int32_t(pl.units.size());
-    f.tiles = reinterpret_cast<const TileDesc*>(ws + L.tiles);
-    f.chunks = reinterpret_cast<const Chunk*>(ws + L.chunks);
-    f.rowchunk = reinterpret_cast<const int32_t*>(ws + L.rowchunk);
-    f.rowaux = reinterpret_cast<const int32_t*>(ws + L.rowaux);
-    f.part = reinterpret_cast<const float*>(ws + L.part);
-    f.z = ws + L.z;
-    f.xa_save = P.xa_save;
-    f.xat = P.xat;
-    f.dybt = P.dybt;
-    f.t_ld = P.t_ld;
-    return shrink_finalize(f, stream);
-}
-
 int begin_call(const Layout& L, void* ws, size_t bytes_plan, const void* blob, cudaStream_t stream) {
     uint8_t* w = static_cast<uint8_t*>(ws);
-    CUDA_TRY(cudaMemsetAsync(w + L.status, 0, 256, stream));
+    CUDA_TRY(cudaMemsetAsync(w + L.status, 0, L.zero_end - L.status, stream));
     return stage_copy(w + L.tiles, blob, bytes_plan, stream);
 }
 
@@ -424,7 +409,6 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
             fill_plan_pointers(&P, ws, L, k);
             CUDA_TRY(tc_launch(P, grid[k], stream));
         }
-        if (k == 0) CUDA_TRY(finalize_shrink(pl, L, ws, P, stream));
         CUDA_TRY(trace(k, 1, stream));
     }
     return LORA_OK;
@@ -568,7 +552,6 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
             fill_plan_pointers(&P, ws, L, k);
             CUDA_TRY(tc_launch(P, grid[k], stream));
         }
-        if (k == 0) CUDA_TRY(finalize_shrink(pl, L, ws, P, stream));
         CUDA_TRY(trace(2 + k, 1, stream));
     }
     return LORA_OK;

@@ -65,8 +65,8 @@ struct WorkItem {
     int32_t part;     // shrink: column offset of this split's fp32 partial [mma_n, 128] in the partial buffer
 };
 
-// One shrink pass of one tile: the finalize step sums its K-splits (in order) and writes Z and the saved or
-// transposed copies.
+// One shrink pass of one tile.  Its K-splits write fp32 partial sums; the last split to finish (counted per row
+// quarter) sums them in split order and writes Z and the saved or transposed copies.
 struct ShrinkUnit {
     int32_t kind;     // kShrinkFwd, kShrinkDyb or kShrinkXa
     int32_t tile;

@@ -144,6 +144,7 @@ static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t
         w.kb0 = int32_t((int64_t)s * nk / nsplit);
         w.nk = int32_t((int64_t)(s + 1) * nk / nsplit) - w.kb0;
         w.part = u.part0 + s * mma_n;
+        w.n_ext = int32_t(pl->units.size());    // shrink items carry their unit index here
         pl->items[0].push_back(w);
     }
     pl->part_cols += (int64_t)nsplit * mma_n;
@@ -351,7 +352,7 @@ static int64_t item_cost(const WorkItem& w) {
     }
     const int64_t per = std::max<int64_t>(bytes / 64, (27 * (int64_t)w.mma_n) / 10);
     int64_t c = (int64_t)w.nk * per;
-    if (w.kind == kMainFwd || w.kind == kMainDx) c += (int64_t)w.n_ext * per;
+    if (w.kind == kMainFwd || w.kind == kMainDx) c += (int64_t)w.n_ext * per;   // (shrink items: n_ext = unit)
     return c + 2000;
 }
 
@@ -387,6 +388,8 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     size_t at = 0;
     auto take = [&](size_t bytes) { size_t o = at; at = align256(at + bytes); return o; };
     L.status = take(256);
+    L.counters = take(sizeof(int32_t) * 4 * pl.units.size());
+    L.zero_end = at;
     L.tiles = take(sizeof(TileDesc) * pl.tiles.size());
     L.chunks = take(sizeof(Chunk) * pl.chunks.size());
     L.rowmap = take(sizeof(int32_t) * pl.rowmap.size());

@@ -44,7 +44,7 @@ struct Plan {
     std::vector<int32_t> atoms_a;    // per tile, per 8 LoRA columns: first A-pool row of that 8-row atom
     std::vector<int32_t> atoms_b;    // same for the B pool
     std::vector<WorkItem> items[2];  // first and second launch
-    std::vector<ShrinkUnit> units;   // shrink passes to finalize between the two launches
+    std::vector<ShrinkUnit> units;   // shrink passes (each finalized by its last K-split)
     std::vector<GradGroup> groups;
     std::vector<TrainSeg> tsegs;
     int32_t n_gtiles = 0;            // forward: tiles of the gathered buffer
@@ -64,6 +64,7 @@ void assign_items(const std::vector<WorkItem>& items, const Plan& plan, int G, s
 // Byte offsets of everything a call keeps in the workspace.
 struct Layout {
     size_t status = 0;
+    size_t counters = 0, zero_end = 0;   // [status, zero_end) is zeroed at the start of every call
     size_t tiles = 0, chunks = 0, rowmap = 0, rowchunk = 0, rowaux = 0, groups = 0, tsegs = 0;
     size_t atoms_a = 0, atoms_b = 0, units = 0;
     size_t items[2] = {0, 0}, cta_off[2] = {0, 0}, cta_list[2] = {0, 0};

@@ -43,65 +43,6 @@ __global__ void xat_from_saved_kernel(const __nv_bfloat16* __restrict__ xa_saved
     }
 }
 
-// Sum the K-splits of one shrink pass (in split order), keep each row's own adapter columns, and write:
-//   Z (s_a * xA, bf16) in the 128x64 shared-memory image the main pass loads with one bulk copy;
-//   xa_save (forward, fine-tuning rows): unscaled xA in the packed [len, r] layout;
-//   the transposed copy (backward): xA^T or dYB^T, [128, P] bf16, zero for tile rows past the segment.
-__global__ void shrink_finalize_kernel(const ShrinkUnit* __restrict__ units, const TileDesc* __restrict__ tiles,
-                                       const Chunk* __restrict__ chunks, const int32_t* __restrict__ rowchunk,
-                                       const int32_t* __restrict__ rowaux, const float* __restrict__ part,
-                                       uint8_t* __restrict__ z, __nv_bfloat16* __restrict__ xa_save,
-                                       __nv_bfloat16* __restrict__ xat, __nv_bfloat16* __restrict__ dybt, int32_t t_ld) {
-    const ShrinkUnit u = units[blockIdx.x];
-    const int row = threadIdx.x;
-    const TileDesc td = tiles[u.tile];
-    const int32_t rc = rowchunk[u.tile * kTileM + row];
-    int32_t zc0 = 0, zr = 0;
-    float s = 0.f;
-    if (rc >= 0) {
-        const Chunk ch = chunks[rc];
-        zc0 = ch.zcol; zr = ch.r; s = ch.scale;
-    }
-    const bool write_z = (u.kind != kShrinkXa);
-    const int32_t save_off = (u.kind == kShrinkFwd && xa_save != nullptr) ? rowaux[u.tile * kTileM + row] : -1;
-    __nv_bfloat16* tdst = (u.kind == kShrinkDyb) ? dybt : (u.kind == kShrinkXa) ? xat : nullptr;
-    const int32_t t_r = tdst ? chunks[td.chunk0].r : 0;    // backward tiles hold one adapter, at column 0
-    const float* p0 = part + (size_t)u.part0 * kTileM + row;
-    for (int c0 = 0; c0 < u.mma_n; c0 += 8) {
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float acc = 0.f;
-            for (int sp = 0; sp < u.nsplit; ++sp) acc += p0[((size_t)sp * u.mma_n + c0 + i) * kTileM];
-            const int zc = u.n0 + c0 + i;
-            v[i] = (rc >= 0 && zc >= zc0 && zc < zc0 + zr) ? acc : 0.f;
-        }
-        if (write_z) {
-            const int zc = u.n0 + c0;
-            uint8_t* blk = z + (size_t)(td.z_blk0 + zc / kBK) * kZBlockBytes + row * 128;
-            const int chunk16 = ((zc % kBK) / 8) ^ (row & 7);
-            __align__(16) __nv_bfloat16 h[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) h[i] = __float2bfloat16_rn(s * v[i]);
-            *reinterpret_cast<uint4*>(blk + chunk16 * 16) = *reinterpret_cast<const uint4*>(h);
-        }
-        if (save_off >= 0) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = u.n0 + c0 + i - zc0;
-                if (j >= 0 && j < zr) xa_save[save_off + j] = __float2bfloat16_rn(v[i]);
-            }
-        }
-        if (tdst) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = u.n0 + c0 + i;
-                if (j < t_r) tdst[(size_t)j * t_ld + td.tpos0 + row] = __float2bfloat16_rn(v[i]);
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------------------------------- float32 path
 __global__ void f32_shrink_kernel(const float* __restrict__ x, const float* __restrict__ A,
                                   const AdapterRec* __restrict__ ad, const int32_t* __restrict__ tok_ad,
@@ -241,13 +182,6 @@ cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t 
     dim3 grid((max_len + 127) / 128, n_tsegs);
     xat_from_saved_kernel<<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(xa_saved), tsegs, n_tsegs,
                                                static_cast<__nv_bfloat16*>(xat), P);
-    return cudaGetLastError();
-}
-
-cudaError_t shrink_finalize(const FinalizeArgs& a, cudaStream_t s) {
-    if (a.n_units <= 0) return cudaSuccess;
-    shrink_finalize_kernel<<<a.n_units, kTileM, 0, s>>>(a.units, a.tiles, a.chunks, a.rowchunk, a.rowaux, a.part, a.z,
-                                                         a.xa_save, a.xat, a.dybt, a.t_ld);
     return cudaGetLastError();
 }
 

@@ -52,22 +52,6 @@ struct F32Args {
     const int64_t* group_b_off;
 };
 
-struct FinalizeArgs {
-    const ShrinkUnit* units;
-    int32_t n_units;
-    const TileDesc* tiles;
-    const Chunk* chunks;
-    const int32_t* rowchunk;
-    const int32_t* rowaux;
-    const float* part;
-    uint8_t* z;
-    __nv_bfloat16* xa_save;
-    __nv_bfloat16* xat;
-    __nv_bfloat16* dybt;
-    int32_t t_ld;
-};
-
-cudaError_t shrink_finalize(const FinalizeArgs& a, cudaStream_t s);
 cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out, int32_t n_rows, cudaStream_t s);
 cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len, void* xat,
                            int32_t P, cudaStream_t s);

@@ -307,6 +307,70 @@ __device__ __forceinline__ void ld32_cols(uint32_t taddr, float (&v)[32]) {
     }
 }
 
+// Finalize of one tile row of a shrink pass: keep the row's own adapter columns (everything else is zero) and
+// write Z = bf16(s_a * xA) into the 128x64 shared-memory image the main pass bulk-loads, the unscaled xA of a
+// fine-tuning row into xa_save (forward), and the transposed copy xA^T / dYB^T (backward; zero past the segment).
+struct ShrinkRowOut {
+    const KParams& P;
+    const ShrinkUnit& u;
+    int row;
+    TileDesc td;
+    int32_t rc, zc0, zr, save_off, t_r;
+    float s;
+    __nv_bfloat16* tdst;
+
+    __device__ ShrinkRowOut(const KParams& P_, const ShrinkUnit& u_, int row_) : P(P_), u(u_), row(row_) {
+        td = P.tiles[u.tile];
+        rc = P.rowchunk[u.tile * kTileM + row];
+        zc0 = 0; zr = 0; s = 0.f;
+        if (rc >= 0) {
+            const Chunk ch = P.chunks[rc];
+            zc0 = ch.zcol; zr = ch.r; s = ch.scale;
+        }
+        save_off = (u.kind == kShrinkFwd && P.xa_save != nullptr) ? P.rowaux[u.tile * kTileM + row] : -1;
+        tdst = (u.kind == kShrinkDyb) ? P.dybt : (u.kind == kShrinkXa) ? P.xat : nullptr;
+        t_r = tdst ? P.chunks[td.chunk0].r : 0;    // backward tiles hold one adapter, at column 0
+    }
+
+    // columns [c, c+16) of the pass
+    __device__ void put16(int c, const float (&acc)[16]) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int zc = u.n0 + c + i;
+            v[i] = (rc >= 0 && zc >= zc0 && zc < zc0 + zr) ? acc[i] : 0.f;
+        }
+        if (u.kind != kShrinkXa) {
+            const int zc = u.n0 + c;
+            uint8_t* blk = P.zout + (size_t)(td.z_blk0 + zc / kBK) * kZBlockBytes + row * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int chunk16 = ((zc % kBK) / 8 + h) ^ (row & 7);
+                uint4 q;
+                q.x = pack_bf16(s * v[8 * h + 0], s * v[8 * h + 1]);
+                q.y = pack_bf16(s * v[8 * h + 2], s * v[8 * h + 3]);
+                q.z = pack_bf16(s * v[8 * h + 4], s * v[8 * h + 5]);
+                q.w = pack_bf16(s * v[8 * h + 6], s * v[8 * h + 7]);
+                *reinterpret_cast<uint4*>(blk + chunk16 * 16) = q;
+            }
+        }
+        if (save_off >= 0) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int j = u.n0 + c + i - zc0;
+                if (j >= 0 && j < zr) P.xa_save[save_off + j] = __float2bfloat16_rn(v[i]);
+            }
+        }
+        if (tdst) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int j = u.n0 + c + i;
+                if (j < t_r) tdst[(size_t)j * P.t_ld + td.tpos0 + row] = __float2bfloat16_rn(v[i]);
+            }
+        }
+    }
+};
+
 __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t tmem, int i0, int i1,
                              volatile int* abort_flag) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -362,15 +426,59 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 }
             }
         } else {
-            // shrink split: raw fp32 partial sums, column-major [mma_n][128] (the finalize step masks, scales,
-            // sums the splits and writes Z and the saved / transposed copies)
-            float* dst = P.part + (size_t)w.part * kTileM + row;
-            for (int c = 0; c < w.mma_n; c += 16) {
-                uint32_t a[16];
-                tmem_ld16(taddr + c, a);
-                tmem_ld_wait();
+            // shrink split (the item's n_ext field holds its shrink-unit index)
+            const ShrinkUnit u = P.units[w.n_ext];
+            if (u.nsplit == 1) {
+                ShrinkRowOut out(P, u, row);
+                for (int c = 0; c < w.mma_n; c += 16) {
+                    uint32_t a[16];
+                    tmem_ld16(taddr + c, a);
+                    tmem_ld_wait();
+                    float v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) dst[(size_t)(c + i) * kTileM] = __uint_as_float(a[i]);
+                    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(a[i]);
+                    out.put16(c, v);
+                }
+            } else {
+                // raw fp32 partial sums, column-major [mma_n][128]; the last split to arrive (per row quarter)
+                // sums all splits in split order and finalizes those 32 rows
+                float* dst = P.part + (size_t)w.part * kTileM + row;
+                for (int c = 0; c < w.mma_n; c += 16) {
+                    uint32_t a[16];
+                    tmem_ld16(taddr + c, a);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dst[(size_t)(c + i) * kTileM] = __uint_as_float(a[i]);
+                }
+                tc_fence_before();
+                mbar_arrive(bar_tempty + acc * 8);       // the accumulator is free; the rest reads global memory
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                int32_t* cnt = P.counters + w.n_ext * 4 + quarter;
+                if (lane == 0) last = (atomicAdd(cnt, 1) == u.nsplit - 1) ? 1 : 0;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    ShrinkRowOut out(P, u, row);
+                    const float* p0 = P.part + (size_t)u.part0 * kTileM + row;
+                    for (int c = 0; c < w.mma_n; c += 16) {
+                        float v[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                        for (int sp = 0; sp < u.nsplit; ++sp) {
+                            const float* ps = p0 + ((size_t)sp * u.mma_n + c) * kTileM;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] += __ldcg(ps + (size_t)i * kTileM);
+                        }
+                        out.put16(c, v);
+                    }
+                    __syncwarp();
+                    if (lane == 0) *cnt = 0;              // ready for the next call on this workspace
+                }
+                continue;
             }
         }
         tc_fence_before();

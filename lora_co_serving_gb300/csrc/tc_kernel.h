@@ -37,6 +37,8 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     const int32_t* atoms_a;  // per tile, per 8 LoRA columns: A-pool row of the atom
     const int32_t* atoms_b;  // same for the B pool
     float* part;             // shrink items: fp32 partial sums, [columns][128 rows]
+    const ShrinkUnit* units; // shrink passes (splits of one pass share a unit)
+    int32_t* counters;       // per unit and row quarter: splits finished (zeroed at the start of every call)
 
     const uint8_t* zin;     // Z blocks read by main items
     uint8_t* zout;          // Z blocks written by shrink items
