@@ -96,7 +96,7 @@ def launches_per_step(wl):
         n += 1 if any(a >= 0 for _, _, a, _ in segs) else 0                                # shrink pass
         n += 1                                                                              # main pass
     if wl.backward and any(tr for *_, tr in segs):
-        n += 2
+        n += 3                                                                              # shrink, dX, dA/dB
     return n
 
 
@@ -389,7 +389,7 @@ def run_ours(args):
             main_ms = group_ms[1]
             achieved = acc["fwd_main_flops"] / (main_ms / 1e3) / 1e12
             tr = profiled_traffic(args.config)
-            roof = {"kernel": "lora_tc_kernel (forward main pass: x W + fused LoRA expand)", "bound": "tensor",
+            roof = {"kernel": "lora_main2_kernel (forward main pass: x W + fused LoRA expand, CTA pairs)", "bound": "tensor",
                     "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                     "frac": achieved / pk["bf16_tflops_sustained"], "traffic": tr,
                     "peak_source": pk["source"] + " (sustained bf16)", "ms_per_launch": main_ms,
@@ -397,7 +397,7 @@ def run_ours(args):
         else:
             main_ms = group_ms[3]
             achieved = acc["bwd_flops"] / (main_ms / 1e3) / 1e12
-            roof = {"kernel": "lora_tc_kernel (backward main pass)", "bound": "tensor", "achieved": achieved,
+            roof = {"kernel": "lora_main2_kernel (backward dX pass) + lora_tc_kernel (dA, dB)", "bound": "tensor", "achieved": achieved,
                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                     "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
                     "peak_source": pk["source"] + " (sustained bf16)", "ms_per_launch": main_ms}

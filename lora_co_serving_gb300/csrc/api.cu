@@ -39,6 +39,9 @@ int fail(int code, const std::string& msg) {
     } while (0)
 
 // ------------------------------------------------------------------------------------------------ tensor maps
+#ifndef LORA_L2_PROMOTION
+#define LORA_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_NONE
+#endif
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -59,7 +62,7 @@ EncodeTiledFn encode_fn() {
 
 // 2-D bf16 tensor [outer, inner] with row stride `ld` elements, 128-byte swizzled boxes {box_in, box_out}.
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_in,
-               uint32_t box_out, std::string* err) {
+               uint32_t box_out, std::string* err, bool swizzle = true) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) { *err = "cuTensorMapEncodeTiled is not available from the driver"; return false; }
     cuuint64_t dims[2] = {inner, outer};
@@ -67,7 +70,8 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
     cuuint32_t box[2] = {box_in, box_out};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    LORA_L2_PROMOTION,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ") for a [" + std::to_string(outer) +
@@ -145,8 +149,8 @@ void put(std::vector<uint8_t>& blob, size_t off, const std::vector<T>& v) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 // Write the plan (tiles ... per-CTA lists) into a host blob laid out exactly like the workspace prefix.
-void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&off)[2],
-                const std::vector<int32_t> (&lst)[2], std::vector<uint8_t>* blob) {
+void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&off)[3],
+                const std::vector<int32_t> (&lst)[3], std::vector<uint8_t>* blob) {
     blob->assign(L.plan_end - L.tiles, 0);
     auto at = [&](size_t o) { return o - L.tiles; };
     std::vector<uint8_t>& b = *blob;
@@ -160,7 +164,7 @@ void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&of
     put(b, at(L.atoms_a), pl.atoms_a);
     put(b, at(L.atoms_b), pl.atoms_b);
     put(b, at(L.units), pl.units);
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < 3; ++k) {
         put(b, at(L.items[k]), pl.items[k]);
         put(b, at(L.cta_off[k]), off[k]);
         put(b, at(L.cta_list[k]), lst[k]);
@@ -231,10 +235,27 @@ void f32_layout(const Problem& p, size_t base, F32Blob* fb) {
     put(fb->bytes, fb->segs - base, segs);
 }
 
-int begin_call(const Layout& L, void* ws, size_t bytes_plan, const void* blob, cudaStream_t stream) {
+int begin_call(const Layout& L, const Plan& pl, void* ws, size_t bytes_plan, const void* blob, cudaStream_t stream) {
     uint8_t* w = static_cast<uint8_t*>(ws);
     CUDA_TRY(cudaMemsetAsync(w + L.status, 0, L.zero_end - L.status, stream));
+    // Z columns outside a tile's own adapters must read as zero in the main pass
+    if (pl.z_blocks > 0) CUDA_TRY(cudaMemsetAsync(w + L.z, 0, (size_t)pl.z_blocks * kZBlockBytes, stream));
     return stage_copy(w + L.tiles, blob, bytes_plan, stream);
+}
+
+// Per-launch CTA assignment: shrink and grad items over single CTAs, main items over CTA pairs.
+void assign_all(const Plan& pl, int sms, std::vector<int32_t> (&off)[3], std::vector<int32_t> (&lst)[3], int (&grid)[3]) {
+    for (int k = 0; k < 3; ++k) {
+        const int units = (k == 1) ? sms / 2 : sms;
+        grid[k] = std::min<int>(std::min(units, kMaxCtas), (int)pl.items[k].size());
+        if (grid[k] > 0) assign_items(pl.items[k], pl, grid[k], &off[k], &lst[k]);
+    }
+}
+
+cudaError_t launch_group(int k, KParams* P, uint8_t* ws, const Layout& L, const int (&grid)[3], cudaStream_t stream) {
+    if (grid[k] == 0) return cudaSuccess;
+    fill_plan_pointers(P, ws, L, k);
+    return (k == 1) ? tc2_launch(*P, grid[k], stream) : tc_launch(*P, grid[k], stream);
 }
 
 }  // namespace
@@ -368,12 +389,9 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
     if (T == 0) return LORA_OK;
     const int sms = sm_count();
     if (sms <= 0) return fail(LORA_ERR_CUDA, "no CUDA device available");
-    std::vector<int32_t> off[2], lst[2];
-    int grid[2];
-    for (int k = 0; k < 2; ++k) {
-        grid[k] = std::min<int>(std::min(sms, kMaxCtas), (int)pl.items[k].size());
-        if (grid[k] > 0) assign_items(pl.items[k], pl, grid[k], &off[k], &lst[k]);
-    }
+    std::vector<int32_t> off[3], lst[3];
+    int grid[3];
+    assign_all(pl, sms, off, lst, grid);
     std::vector<uint8_t> blob;
     build_blob(pl, L, off, lst, &blob);
 
@@ -383,7 +401,10 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
     if (!encode_2d(&P.tm_x, x, K, T, K, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
     if (pl.n_gtiles > 0 && !encode_2d(&P.tm_xg, ws + L.xg, K, (uint64_t)pl.n_gtiles * kTileM, K, 64, 128, &err))
         return fail(LORA_ERR_CUDA, err);
-    if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 256, &err)) return fail(LORA_ERR_CUDA, err);
+    if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
+    if (pl.z_blocks > 0 &&
+        !encode_2d(&P.tm_z, ws + L.z, 64, (uint64_t)pl.z_blocks * kTileM, 64, 64, 128, &err, false))
+        return fail(LORA_ERR_CUDA, err);
     if (p.rows_a > 0 && !encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (p.rows_b > 0 && !encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     P.zin = ws + L.z;
@@ -395,7 +416,7 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
     P.K = K;
     P.N = N;
 
-    rc = begin_call(L, workspace, blob.size(), blob.data(), stream);
+    rc = begin_call(L, pl, workspace, blob.size(), blob.data(), stream);
     if (rc) return rc;
     CUDA_TRY(trace(0, 0, stream));
     if (pl.n_gtiles > 0) {
@@ -403,14 +424,11 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
         CUDA_TRY(gather_rows(x, K, reinterpret_cast<const int32_t*>(ws + L.rowmap) + (size_t)first * kTileM,
                              ws + L.xg, pl.n_gtiles * kTileM, stream));
     }
-    for (int k = 0; k < 2; ++k) {
-        if (k == 1) CUDA_TRY(trace(1, 0, stream));
-        if (grid[k] > 0) {
-            fill_plan_pointers(&P, ws, L, k);
-            CUDA_TRY(tc_launch(P, grid[k], stream));
-        }
-        CUDA_TRY(trace(k, 1, stream));
-    }
+    CUDA_TRY(launch_group(0, &P, ws, L, grid, stream));
+    CUDA_TRY(trace(0, 1, stream));
+    CUDA_TRY(trace(1, 0, stream));
+    CUDA_TRY(launch_group(1, &P, ws, L, grid, stream));
+    CUDA_TRY(trace(1, 1, stream));
     return LORA_OK;
 }
 
@@ -497,12 +515,9 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
     if (p.n_train == 0) return LORA_OK;
     const int sms = sm_count();
     if (sms <= 0) return fail(LORA_ERR_CUDA, "no CUDA device available");
-    std::vector<int32_t> off[2], lst[2];
-    int grid[2];
-    for (int k = 0; k < 2; ++k) {
-        grid[k] = std::min<int>(std::min(sms, kMaxCtas), (int)pl.items[k].size());
-        if (grid[k] > 0) assign_items(pl.items[k], pl, grid[k], &off[k], &lst[k]);
-    }
+    std::vector<int32_t> off[3], lst[3];
+    int grid[3];
+    assign_all(pl, sms, off, lst, grid);
     std::vector<uint8_t> blob;
     build_blob(pl, L, off, lst, &blob);
 
@@ -517,6 +532,9 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
     if (!encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_xat, ws + L.xat, Pcols, LORA_MAX_RANK, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_dybt, ws + L.dybt, Pcols, LORA_MAX_RANK, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    if (pl.z_blocks > 0 &&
+        !encode_2d(&P.tm_z, ws + L.z, 64, (uint64_t)pl.z_blocks * kTileM, 64, 64, 128, &err, false))
+        return fail(LORA_ERR_CUDA, err);
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
     const __nv_bfloat16* db = static_cast<const __nv_bfloat16*>(dY);
     int32_t max_len = 0;
@@ -540,20 +558,18 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
     P.N = N;
     P.accumulate = acc ? 1 : 0;
 
-    rc = begin_call(L, workspace, blob.size(), blob.data(), stream);
+    rc = begin_call(L, pl, workspace, blob.size(), blob.data(), stream);
     if (rc) return rc;
     CUDA_TRY(trace(2, 0, stream));
     if (!recompute && dB)
         CUDA_TRY(xat_from_saved(xa_saved, reinterpret_cast<const TrainSeg*>(ws + L.tsegs), int32_t(pl.tsegs.size()),
                                 max_len, ws + L.xat, int32_t(Pcols), stream));
-    for (int k = 0; k < 2; ++k) {
-        if (k == 1) CUDA_TRY(trace(3, 0, stream));
-        if (grid[k] > 0) {
-            fill_plan_pointers(&P, ws, L, k);
-            CUDA_TRY(tc_launch(P, grid[k], stream));
-        }
-        CUDA_TRY(trace(2 + k, 1, stream));
-    }
+    CUDA_TRY(launch_group(0, &P, ws, L, grid, stream));
+    CUDA_TRY(trace(2, 1, stream));
+    CUDA_TRY(trace(3, 0, stream));
+    CUDA_TRY(launch_group(1, &P, ws, L, grid, stream));
+    CUDA_TRY(launch_group(2, &P, ws, L, grid, stream));
+    CUDA_TRY(trace(3, 1, stream));
     return LORA_OK;
 }
 

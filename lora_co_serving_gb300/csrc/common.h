@@ -42,7 +42,12 @@ struct TileDesc {
     int32_t z_blk0;   // first Z block of this tile
     int32_t tpos0;    // backward tiles: column of tile row 0 in the transposed buffers; -1 otherwise
     int32_t atom0;    // first entry of this tile in the atom-row tables (one entry per 8 LoRA columns)
+    int32_t sh_c0;    // LoRA columns [sh_c0, sh_c1) hold this tile's own adapters (the shrink computes only
+    int32_t sh_c1;    //   these; the pair's other columns of this tile's Z stay zero)
 };
+// Tiles come in pairs (2p, 2p+1) that share one chunk list, ordered [adapters only in the first tile |
+// adapters in both | adapters only in the second], so that the M = 256 main pass runs one pair per CTA pair
+// and each tile's own adapters occupy one contiguous column range.
 
 struct Chunk {
     int32_t adapter;

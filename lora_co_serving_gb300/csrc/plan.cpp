@@ -3,6 +3,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <iterator>
 #include <queue>
 #include <utility>
 
@@ -88,19 +89,34 @@ int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t
     return LORA_OK;
 }
 
-// Build the chunk list of one tile from the adapters of its valid rows (increasing adapter id).
-static void make_chunks(const Problem& p, const int32_t* row_adapter, Plan* pl, TileDesc* td, int32_t* rowchunk) {
-    int32_t ids[kTileM];
-    int n = 0;
-    for (int i = 0; i < kTileM; ++i)
-        if (row_adapter[i] >= 0) ids[n++] = row_adapter[i];
-    std::sort(ids, ids + n);
-    n = int(std::unique(ids, ids + n) - ids);
-    td->chunk0 = int32_t(pl->chunks.size());
-    td->nchunk = n;
-    int32_t zcol = 0;
-    for (int c = 0; c < n; ++c) {
-        int32_t a = ids[c];
+// Append one pair of tiles.  rows / row_ad: 256 entries (token row and adapter per tile row, -1 = none);
+// t0, t1: the two tiles' descriptors with a_row0 / a_src / tpos0 filled in.
+static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int32_t* row_ad, const int32_t* row_aux,
+                     TileDesc t0, TileDesc t1) {
+    std::vector<int32_t> A, B;
+    for (int i = 0; i < kTileM; ++i) {
+        if (row_ad[i] >= 0) A.push_back(row_ad[i]);
+        if (row_ad[kTileM + i] >= 0) B.push_back(row_ad[kTileM + i]);
+    }
+    std::sort(A.begin(), A.end());
+    A.erase(std::unique(A.begin(), A.end()), A.end());
+    std::sort(B.begin(), B.end());
+    B.erase(std::unique(B.begin(), B.end()), B.end());
+    std::vector<int32_t> onlyA, both, onlyB;
+    std::set_difference(A.begin(), A.end(), B.begin(), B.end(), std::back_inserter(onlyA));
+    std::set_intersection(A.begin(), A.end(), B.begin(), B.end(), std::back_inserter(both));
+    std::set_difference(B.begin(), B.end(), A.begin(), A.end(), std::back_inserter(onlyB));
+    std::vector<int32_t> order;
+    order.insert(order.end(), onlyA.begin(), onlyA.end());
+    order.insert(order.end(), both.begin(), both.end());
+    order.insert(order.end(), onlyB.begin(), onlyB.end());
+
+    const int32_t chunk0 = int32_t(pl->chunks.size());
+    const int32_t atom0 = int32_t(pl->atoms_a.size());
+    int32_t zcol = 0, end_a = 0, start_b = 0;
+    for (size_t c = 0; c < order.size(); ++c) {
+        if (c == onlyA.size()) start_b = zcol;
+        const int32_t a = order[c];
         Chunk ch{};
         ch.adapter = a;
         ch.zcol = zcol;
@@ -109,27 +125,40 @@ static void make_chunks(const Problem& p, const int32_t* row_adapter, Plan* pl, 
         ch.prow_b = int32_t(p.b_off[a] / p.N);
         ch.scale = p.scale[a];
         pl->chunks.push_back(ch);
-        zcol += pad16(ch.r);
-    }
-    td->ext_k = zcol;
-    td->z_blk0 = int32_t(pl->z_blocks);
-    pl->z_blocks += cdiv(zcol, kBK);
-    // pool row of every 8-column atom of the tile's LoRA columns; the padding of a chunk to 16 repeats the
-    // chunk's last atom, so every loaded row stays inside the adapter's own block
-    td->atom0 = int32_t(pl->atoms_a.size());
-    for (int c = 0; c < n; ++c) {
-        const Chunk& ch = pl->chunks[td->chunk0 + c];
+        // pool row of every 8-column atom; the padding of a chunk to 16 repeats its last atom, so every loaded
+        // row stays inside the adapter's own block
         const int32_t last = ((ch.r + 7) / 8 - 1) * 8;
         for (int32_t o = 0; o < pad16(ch.r); o += 8) {
             pl->atoms_a.push_back(ch.prow_a + std::min(o, last));
             pl->atoms_b.push_back(ch.prow_b + std::min(o, last));
         }
+        zcol += pad16(ch.r);
+        if (c + 1 == onlyA.size() + both.size()) end_a = zcol;
     }
-    for (int i = 0; i < kTileM; ++i) {
-        rowchunk[i] = -1;
-        if (row_adapter[i] >= 0)
-            rowchunk[i] = td->chunk0 + int32_t(std::lower_bound(ids, ids + n, row_adapter[i]) - ids);
+    if (onlyA.size() == order.size()) start_b = zcol;
+    TileDesc* td[2] = {&t0, &t1};
+    for (int h = 0; h < 2; ++h) {
+        td[h]->chunk0 = chunk0;
+        td[h]->nchunk = int32_t(order.size());
+        td[h]->ext_k = zcol;
+        td[h]->atom0 = atom0;
+        td[h]->z_blk0 = int32_t(pl->z_blocks);
+        pl->z_blocks += cdiv(zcol, kBK);
     }
+    t0.sh_c0 = 0;
+    t0.sh_c1 = A.empty() ? 0 : end_a;
+    t1.sh_c0 = B.empty() ? zcol : start_b;
+    t1.sh_c1 = zcol;
+    for (int i = 0; i < 2 * kTileM; ++i) {
+        int32_t rc = -1;
+        if (row_ad[i] >= 0)
+            rc = chunk0 + int32_t(std::find(order.begin(), order.end(), row_ad[i]) - order.begin());
+        pl->rowmap.push_back(rows[i]);
+        pl->rowchunk.push_back(rc);
+        pl->rowaux.push_back(row_aux ? row_aux[i] : -1);
+    }
+    pl->tiles.push_back(t0);
+    pl->tiles.push_back(t1);
 }
 
 // Shrink items of one pass, split along the reduction at boundaries that depend on the k-block count alone.
@@ -149,6 +178,27 @@ static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t
     }
     pl->part_cols += (int64_t)nsplit * mma_n;
     pl->units.push_back(u);
+}
+
+// Main items of the M = 256 pass: one per (tile pair, 256 output columns), bands of kBandTiles tiles sweeping all
+// output columns before the next band (L2 reuse of the band's rows).
+static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk) {
+    const size_t n_pairs = pl->tiles.size() / 2;
+    const size_t band = kBandTiles / 2;
+    for (size_t b0 = 0; b0 < n_pairs; b0 += band) {
+        const size_t b1 = std::min(n_pairs, b0 + band);
+        for (int32_t nt = 0; nt < n_nt; ++nt)
+            for (size_t q = b0; q < b1; ++q) {
+                WorkItem w{};
+                w.kind = kind;
+                w.tile = int32_t(2 * q);
+                w.n0 = nt * kBN;
+                w.nk = nk;
+                w.mma_n = kBN;
+                w.n_ext = int32_t(cdiv(pl->tiles[2 * q].ext_k, kBK));
+                pl->items[1].push_back(w);
+            }
+    }
 }
 
 void plan_forward(const Problem& p, Plan* out) {
@@ -173,71 +223,53 @@ void plan_forward(const Problem& p, Plan* out) {
             else is_long[t] = 1;
         }
     }
-    auto add_tile = [&](int32_t a_row0, int32_t a_src, const int32_t* rows) {
-        TileDesc td{};
-        td.a_row0 = a_row0;
-        td.a_src = a_src;
-        td.tpos0 = -1;
-        int32_t row_ad[kTileM];
-        size_t base = pl.rowmap.size();
-        pl.rowmap.resize(base + kTileM);
-        pl.rowchunk.resize(base + kTileM);
-        pl.rowaux.resize(base + kTileM);
-        for (int i = 0; i < kTileM; ++i) {
-            int32_t t = rows[i];
-            pl.rowmap[base + i] = t;
-            row_ad[i] = -1;
-            pl.rowaux[base + i] = -1;
-            if (t >= 0) {
-                const auto& s = p.segs[row_seg[t]];
-                row_ad[i] = s.adapter_id;
-                if (s.is_train) pl.rowaux[base + i] = int32_t(seg_xoff[row_seg[t]] + (int64_t)(t - s.start) * p.rank[s.adapter_id]);
-            }
+    // per pair: token rows, their adapters and saved-activation offsets
+    int32_t rows[2 * kTileM], row_ad[2 * kTileM], row_aux[2 * kTileM];
+    auto fill = [&](int i, int32_t t) {
+        rows[i] = t;
+        row_ad[i] = -1;
+        row_aux[i] = -1;
+        if (t >= 0) {
+            const auto& s = p.segs[row_seg[t]];
+            row_ad[i] = s.adapter_id;
+            if (s.is_train)
+                row_aux[i] = int32_t(seg_xoff[row_seg[t]] + (int64_t)(t - s.start) * p.rank[s.adapter_id]);
         }
-        make_chunks(p, row_ad, &pl, &td, &pl.rowchunk[base]);
-        pl.tiles.push_back(td);
     };
-    // windows over the long rows
-    int32_t rows[kTileM];
+    // 256-row windows over the long rows
     for (int32_t t = 0; t < p.T;) {
         if (!is_long[t]) { ++t; continue; }
-        int32_t w0 = t;
-        for (int i = 0; i < kTileM; ++i) {
-            int32_t r = w0 + i;
-            rows[i] = (r < p.T && is_long[r]) ? r : -1;
+        const int32_t w0 = t;
+        for (int i = 0; i < 2 * kTileM; ++i) {
+            const int32_t r = w0 + i;
+            fill(i, (r < p.T && is_long[r]) ? r : -1);
         }
-        add_tile(w0, 0, rows);
-        t = w0 + kTileM;
+        TileDesc t0{}, t1{};
+        t0.a_row0 = w0; t1.a_row0 = w0 + kTileM;
+        t0.tpos0 = t1.tpos0 = -1;
+        add_pair(p, &pl, rows, row_ad, row_aux, t0, t1);
+        t = w0 + 2 * kTileM;
     }
-    // gathered tiles: short rows sorted by (adapter, row)
+    // gathered pairs: short rows sorted by (adapter, row)
     std::sort(gathered.begin(), gathered.end());
-    for (size_t g0 = 0; g0 < gathered.size(); g0 += kTileM) {
-        for (int i = 0; i < kTileM; ++i) rows[i] = (g0 + i < gathered.size()) ? gathered[g0 + i].second : -1;
-        add_tile(int32_t(pl.n_gtiles) * kTileM, 1, rows);
-        pl.n_gtiles++;
+    for (size_t g0 = 0; g0 < gathered.size(); g0 += 2 * kTileM) {
+        for (int i = 0; i < 2 * kTileM; ++i) fill(i, (g0 + i < gathered.size()) ? gathered[g0 + i].second : -1);
+        TileDesc t0{}, t1{};
+        t0.a_src = t1.a_src = 1;
+        t0.a_row0 = pl.n_gtiles * kTileM;
+        t1.a_row0 = (pl.n_gtiles + 1) * kTileM;
+        t0.tpos0 = t1.tpos0 = -1;
+        add_pair(p, &pl, rows, row_ad, row_aux, t0, t1);
+        pl.n_gtiles += 2;
     }
     // items: shrink passes, then main items banded for L2 reuse
     const int32_t nk = int32_t(cdiv(p.K, kBK));
     for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
         const TileDesc& td = pl.tiles[ti];
-        for (int32_t c0 = 0; c0 < td.ext_k; c0 += kPassCols)
-            add_shrink(&pl, kShrinkFwd, int32_t(ti), c0, std::min(kPassCols, td.ext_k - c0), nk);
+        for (int32_t c0 = td.sh_c0; c0 < td.sh_c1; c0 += kPassCols)
+            add_shrink(&pl, kShrinkFwd, int32_t(ti), c0, std::min(kPassCols, td.sh_c1 - c0), nk);
     }
-    const int32_t n_nt = int32_t(cdiv(p.N, kBN));
-    for (size_t b0 = 0; b0 < pl.tiles.size(); b0 += kBandTiles) {
-        size_t b1 = std::min(pl.tiles.size(), b0 + kBandTiles);
-        for (int32_t nt = 0; nt < n_nt; ++nt)
-            for (size_t ti = b0; ti < b1; ++ti) {
-                WorkItem w{};
-                w.kind = kMainFwd;
-                w.tile = int32_t(ti);
-                w.n0 = nt * kBN;
-                w.nk = nk;
-                w.mma_n = kBN;
-                w.n_ext = int32_t(cdiv(pl.tiles[ti].ext_k, kBK));
-                pl.items[1].push_back(w);
-            }
-    }
+    add_main_items(&pl, kMainFwd, int32_t(cdiv(p.N, kBN)), nk);
 }
 
 void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out) {
@@ -262,7 +294,7 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
     std::vector<int32_t> tpos_of(tr.size()), xoff_of(tr.size());
     for (size_t i = 0; i < tr.size(); ++i) {
         tpos_of[i] = int32_t(tpos);
-        tpos += cdiv(tr[i].len, kTileM) * kTileM;
+        tpos += cdiv(tr[i].len, 2 * kTileM) * 2 * kTileM;
         xoff_of[i] = int32_t(xo);
         xo += (int64_t)tr[i].len * p.rank[tr[i].adapter_id];
     }
@@ -281,48 +313,32 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
             pl.tsegs.push_back(TrainSeg{tr[i].start, tr[i].len, tpos_of[i], int32_t(g), xoff_of[i], gg.r, 0, 0});
         pl.groups.push_back(gg);
     }
-    // one tile per 128 rows of each fine-tuning segment
+    // one pair of tiles per 256 rows of each fine-tuning segment
     for (size_t i = 0; i < tr.size(); ++i) {
-        for (int32_t b = 0; b < tr[i].len; b += kTileM) {
-            TileDesc td{};
-            td.a_row0 = tr[i].start + b;
-            td.a_src = 0;
-            td.tpos0 = tpos_of[i] + b;
-            int32_t row_ad[kTileM];
-            size_t base = pl.rowmap.size();
-            pl.rowmap.resize(base + kTileM);
-            pl.rowchunk.resize(base + kTileM);
-            pl.rowaux.resize(base + kTileM);
-            for (int k = 0; k < kTileM; ++k) {
-                bool v = b + k < tr[i].len;
-                pl.rowmap[base + k] = v ? tr[i].start + b + k : -1;
+        for (int32_t b = 0; b < tr[i].len; b += 2 * kTileM) {
+            int32_t rows[2 * kTileM], row_ad[2 * kTileM];
+            for (int k = 0; k < 2 * kTileM; ++k) {
+                const bool v = b + k < tr[i].len;
+                rows[k] = v ? tr[i].start + b + k : -1;
                 row_ad[k] = v ? tr[i].adapter_id : -1;
-                pl.rowaux[base + k] = -1;
             }
-            make_chunks(p, row_ad, &pl, &td, &pl.rowchunk[base]);
-            pl.tiles.push_back(td);
+            TileDesc t0{}, t1{};
+            t0.a_row0 = tr[i].start + b;
+            t1.a_row0 = tr[i].start + b + kTileM;
+            t0.tpos0 = tpos_of[i] + b;
+            t1.tpos0 = tpos_of[i] + b + kTileM;
+            add_pair(p, &pl, rows, row_ad, nullptr, t0, t1);
         }
     }
     const bool need_dyb = want_dx || want_da;
     const bool need_xa = want_db && recompute;
     for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
         const TileDesc& td = pl.tiles[ti];
-        if (need_dyb) add_shrink(&pl, kShrinkDyb, int32_t(ti), 0, td.ext_k, int32_t(cdiv(p.N, kBK)));
-        if (need_xa) add_shrink(&pl, kShrinkXa, int32_t(ti), 0, td.ext_k, int32_t(cdiv(p.K, kBK)));
+        if (td.sh_c1 <= td.sh_c0) continue;      // the empty second tile of a short segment's pair
+        if (need_dyb) add_shrink(&pl, kShrinkDyb, int32_t(ti), td.sh_c0, td.sh_c1 - td.sh_c0, int32_t(cdiv(p.N, kBK)));
+        if (need_xa) add_shrink(&pl, kShrinkXa, int32_t(ti), td.sh_c0, td.sh_c1 - td.sh_c0, int32_t(cdiv(p.K, kBK)));
     }
-    if (want_dx) {
-        const int32_t n_nt = int32_t(cdiv(p.K, kBN));
-        for (size_t b0 = 0; b0 < pl.tiles.size(); b0 += kBandTiles) {
-            size_t b1 = std::min(pl.tiles.size(), b0 + kBandTiles);
-            for (int32_t nt = 0; nt < n_nt; ++nt)
-                for (size_t ti = b0; ti < b1; ++ti) {
-                    WorkItem w{};
-                    w.kind = kMainDx; w.tile = int32_t(ti); w.n0 = nt * kBN; w.nk = int32_t(cdiv(p.N, kBK));
-                    w.mma_n = kBN; w.n_ext = int32_t(cdiv(pl.tiles[ti].ext_k, kBK));
-                    pl.items[1].push_back(w);
-                }
-        }
-    }
+    if (want_dx) add_main_items(&pl, kMainDx, int32_t(cdiv(p.K, kBN)), int32_t(cdiv(p.N, kBK)));
     for (size_t g = 0; g < pl.groups.size(); ++g) {
         int32_t kb = 0;
         for (int32_t q = 0; q < pl.groups[g].nseg; ++q) kb += int32_t(cdiv(pl.tsegs[pl.groups[g].seg0 + q].len, kBK));
@@ -330,13 +346,13 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
             for (int32_t m0 = 0; m0 < p.N; m0 += kTileM) {
                 WorkItem w{};
                 w.kind = kGradDb; w.tile = int32_t(g); w.n0 = m0; w.nk = kb; w.mma_n = pad16(pl.groups[g].r);
-                pl.items[1].push_back(w);
+                pl.items[2].push_back(w);
             }
         if (want_da)
             for (int32_t m0 = 0; m0 < p.K; m0 += kTileM) {
                 WorkItem w{};
                 w.kind = kGradDa; w.tile = int32_t(g); w.n0 = m0; w.nk = kb; w.mma_n = pad16(pl.groups[g].r);
-                pl.items[1].push_back(w);
+                pl.items[2].push_back(w);
             }
     }
 }
@@ -400,7 +416,7 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     L.atoms_a = take(sizeof(int32_t) * pl.atoms_a.size());
     L.atoms_b = take(sizeof(int32_t) * pl.atoms_b.size());
     L.units = take(sizeof(ShrinkUnit) * pl.units.size());
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < 3; ++k) {
         L.items[k] = take(sizeof(WorkItem) * pl.items[k].size());
         L.cta_off[k] = take(sizeof(int32_t) * (kMaxCtas + 1));
         L.cta_list[k] = take(sizeof(int32_t) * pl.items[k].size());

@@ -15,7 +15,10 @@ namespace lora {
 // gathered buffer sorted by adapter, so that a tile meets as few adapters as possible.
 constexpr int kShortSegment = 16;
 // Tiles per L2 band: main items sweep all output columns of a band of tiles before the next band.
-constexpr int kBandTiles = 16;
+#ifndef LORA_BAND_TILES
+#define LORA_BAND_TILES 16
+#endif
+constexpr int kBandTiles = LORA_BAND_TILES;
 
 struct Problem {
     int32_t T = 0, K = 0, N = 0;
@@ -43,7 +46,7 @@ struct Plan {
     std::vector<int32_t> rowaux;     // 128 per tile: forward: xa_save element offset or -1; backward: -1
     std::vector<int32_t> atoms_a;    // per tile, per 8 LoRA columns: first A-pool row of that 8-row atom
     std::vector<int32_t> atoms_b;    // same for the B pool
-    std::vector<WorkItem> items[2];  // first and second launch
+    std::vector<WorkItem> items[3];  // shrink items (1-CTA kernel), main pair items (2-CTA kernel), grad items
     std::vector<ShrinkUnit> units;   // shrink passes (each finalized by its last K-split)
     std::vector<GradGroup> groups;
     std::vector<TrainSeg> tsegs;
@@ -67,7 +70,7 @@ struct Layout {
     size_t counters = 0, zero_end = 0;   // [status, zero_end) is zeroed at the start of every call
     size_t tiles = 0, chunks = 0, rowmap = 0, rowchunk = 0, rowaux = 0, groups = 0, tsegs = 0;
     size_t atoms_a = 0, atoms_b = 0, units = 0;
-    size_t items[2] = {0, 0}, cta_off[2] = {0, 0}, cta_list[2] = {0, 0};
+    size_t items[3] = {0, 0, 0}, cta_off[3] = {0, 0, 0}, cta_list[3] = {0, 0, 0};
     size_t plan_end = 0;
     size_t xg = 0, z = 0, xat = 0, dybt = 0, part = 0;
     size_t simt = 0;                 // float32 path scratch

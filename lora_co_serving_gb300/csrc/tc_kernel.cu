@@ -106,9 +106,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N, operand majors (0 = K, 1 = MN).
-__device__ __forceinline__ uint32_t instr_desc(int n, int a_mn, int b_mn) {
+__device__ __forceinline__ uint32_t instr_desc(int m, int n, int a_mn, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -188,43 +188,6 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
             continue;
         }
         const TileDesc td = P.tiles[w.tile];
-        if (w.kind == kMainFwd || w.kind == kMainDx) {
-            const bool fwd = (w.kind == kMainFwd);
-            const CUtensorMap* ma = fwd ? (td.a_src ? &P.tm_xg : &P.tm_x) : &P.tm_dy;
-            for (int kb = 0; kb < w.nk; ++kb) {
-                if (!acquire_stage(ring, bar_full, bar_empty, kABytes + kBBytes, lane, abort_flag, P.status)) return;
-                const uint32_t full = bar_full + ring.stage * 8;
-                const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
-                if (lane == 0) tma_load_2d(sa, ma, kb * kBK, td.a_row0, full);
-                if (fwd) {
-                    if (lane == 1) tma_load_2d(sb, &P.tm_w, kb * kBK, w.n0, full);
-                } else if (lane >= 1 && lane <= 4) {
-                    const int m = lane - 1;
-                    tma_load_2d(sb + m * 8192, &P.tm_w, w.n0 + 64 * m, kb * kBK, full);
-                }
-                ring.next();
-            }
-            // LoRA k-blocks: the tile's Z block (already in its shared-memory image) and, for each 8-row atom of
-            // stacked adapter rows, four 64-column MN-major boxes
-            const CUtensorMap* mp = fwd ? &P.tm_pb : &P.tm_pa;
-            const int32_t* atoms = (fwd ? P.atoms_b : P.atoms_a) + td.atom0;
-            for (int e = 0; e < w.n_ext; ++e) {
-                const int natoms = min(8, (td.ext_k - e * kBK) / 8);
-                if (!acquire_stage(ring, bar_full, bar_empty, kZBlockBytes + natoms * 4096, lane, abort_flag,
-                                   P.status))
-                    return;
-                const uint32_t full = bar_full + ring.stage * 8;
-                const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
-                if (lane == 0) bulk_load(sa, P.zin + (size_t)(td.z_blk0 + e) * kZBlockBytes, kZBlockBytes, full);
-                if (lane < natoms * 4) {
-                    const int q = lane >> 2, m = lane & 3;
-                    const int32_t prow = atoms[e * 8 + q];
-                    tma_load_2d(sb + m * 8192 + q * 1024, mp, w.n0 + 64 * m, prow, full);
-                }
-                ring.next();
-            }
-            continue;
-        }
         // shrink split: k-blocks [kb0, kb0 + nk) of the reduction; B = the pass's 8-row atoms of pool rows
         const CUtensorMap* ma = (w.kind == kShrinkFwd) ? (td.a_src ? &P.tm_xg : &P.tm_x)
                                 : (w.kind == kShrinkDyb) ? &P.tm_dy : &P.tm_x;
@@ -273,18 +236,11 @@ __device__ void run_mma(const KParams& P, uint8_t* smem, uint32_t bar_full, uint
             return true;
         };
         bool ok = true;
-        if (w.kind == kMainFwd || w.kind == kMainDx) {
-            const int b_mn = (w.kind == kMainDx) ? 1 : 0;
-            const uint32_t id_main = instr_desc(kBN, 0, b_mn);
-            for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id_main, 0, b_mn);
-            const TileDesc td = P.tiles[w.tile];
-            const uint32_t id_ext = instr_desc(kBN, 0, 1);
-            for (int e = 0; e < w.n_ext && ok; ++e) ok = kblock(min(4, (td.ext_k - e * kBK) / 16), id_ext, 0, 1);
-        } else if (w.kind == kGradDb || w.kind == kGradDa) {
-            const uint32_t id = instr_desc(w.mma_n, 1, 0);
+        if (w.kind == kGradDb || w.kind == kGradDa) {
+            const uint32_t id = instr_desc(kTileM, w.mma_n, 1, 0);
             for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id, 1, 0);
         } else {
-            const uint32_t id = instr_desc(w.mma_n, 0, 0);
+            const uint32_t id = instr_desc(kTileM, w.mma_n, 0, 0);
             for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id, 0, 0);
         }
         if (!ok) return;
@@ -383,27 +339,7 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
         if (!wait_phase(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) return;
         tc_fence_after();
         const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);
-        if (w.kind == kMainFwd || w.kind == kMainDx) {
-            const int32_t t = P.rowmap[w.tile * kTileM + row];
-            for (int c = 0; c < kBN; c += 32) {
-                float v[32];
-                ld32_cols(taddr + c, v);
-                if (t >= 0) {
-                    __nv_bfloat16* dst = P.out + (size_t)t * P.out_ld + w.n0 + c;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (w.n0 + c + 8 * g + 8 <= P.out_cols) {
-                            uint4 q;
-                            q.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
-                            q.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
-                            q.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
-                            q.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
-                            *reinterpret_cast<uint4*>(dst + 8 * g) = q;
-                        }
-                    }
-                }
-            }
-        } else if (w.kind == kGradDb || w.kind == kGradDa) {
+        if (w.kind == kGradDb || w.kind == kGradDa) {
             const GradGroup g = P.groups[w.tile];
             const bool is_b = (w.kind == kGradDb);
             const int32_t ld = is_b ? P.N : P.K;
@@ -539,9 +475,323 @@ __global__ void __launch_bounds__(kThreads, 1) lora_tc_kernel(const __grid_const
     }
 }
 
+// =============================================================================================================
+// Main pass on CTA pairs: tcgen05.mma.cta_group::2, M = 256 (one tile pair), N = 256 output columns.
+//
+// A cluster of two CTAs works on one item at a time.  CTA rank r holds the 128 rows of tile (2p + r) as the A
+// operand and the 128-column half [n0 + 128 r, n0 + 128 r + 128) of the B operand; the leader (rank 0) issues
+// the MMAs, which read both CTAs' shared memory and write each CTA's 128 accumulator lanes.  Each CTA moves
+// only its own 32 KB per k-block (half of what one CTA needs for a 128x256 tile), so six stages fit.
+// Both CTAs' TMA loads complete on the leader's "full" barrier; the leader's commits arrive on both CTAs'
+// "empty" and "accumulator full" barriers; both CTAs' epilogue warps release the accumulator on the leader.
+// =============================================================================================================
+#ifndef LORA_MAIN_STAGES
+#define LORA_MAIN_STAGES 7
+#endif
+// L2 eviction priority of the main pass's TMA loads of the row operand (x / dY) and of W:
+// 0 = normal, 1 = evict_first, 2 = evict_last.  Keeping the rows of the current band of tiles resident while W
+// streams through measured +21 % on an 8192 x 8192 x 28672 product; seven 32-KB stages another +12 %.
+#ifndef LORA_HINT_ROWS
+#define LORA_HINT_ROWS 2
+#endif
+#ifndef LORA_HINT_W
+#define LORA_HINT_W 0
+#endif
+constexpr int kStages2 = LORA_MAIN_STAGES;
+constexpr int kHalfN = kBN / 2;
+constexpr int kA2Bytes = kTileM * kBK * 2;        // 16 KB
+constexpr int kB2Bytes = kHalfN * kBK * 2;        // 16 KB
+constexpr int kStage2Bytes = kA2Bytes + kB2Bytes;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// TMA load into this CTA's shared memory whose completion is signalled on an mbarrier of either CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+// Same, with an L2 cache-eviction policy (createpolicy) attached to the load
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                      uint32_t bar_cluster, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+        "[%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster), "l"(policy)
+        : "memory");
+}
+template <int HINT>
+__device__ __forceinline__ void tma_load_hinted(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                uint32_t bar_cluster) {
+    if constexpr (HINT == 0) {
+        tma_load_2d_pair(dst, map, c0, c1, bar_cluster);
+    } else {
+        uint64_t policy;
+        if constexpr (HINT == 1)
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+        else
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
+        tma_load_2d_pair_hint(dst, map, c0, c1, bar_cluster, policy);
+    }
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive (when the issued MMAs complete) on the barrier at this offset in both CTAs of the pair
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+struct Ring2 {
+    int stage = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next() {
+        if (++stage == kStages2) { stage = 0; phase ^= 1u; }
+    }
+};
+
+// Lane 0 waits for this CTA's ring slot; the leader also arms its "full" barrier with the bytes of both CTAs.
+__device__ __forceinline__ bool acquire_stage2(const Ring2& ring, uint32_t bar_full, uint32_t bar_empty,
+                                               uint32_t bytes_per_cta, bool leader, int lane, volatile int* abort_flag,
+                                               int32_t* status) {
+    int ok = 1;
+    if (lane == 0) {
+        ok = wait_phase(bar_empty + ring.stage * 8, ring.phase ^ 1u, abort_flag, status) ? 1 : 0;
+        if (ok && leader) mbar_expect_tx(bar_full + ring.stage * 8, 2 * bytes_per_cta);
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty, uint32_t rank,
+                              int i0, int i1, volatile int* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    const bool leader = (rank == 0);
+    const uint32_t full_leader = mapa_shared(bar_full, 0);
+    Ring2 ring;
+    for (int ii = i0; ii < i1; ++ii) {
+        const WorkItem w = P.items[P.cta_list[ii]];
+        const TileDesc td = P.tiles[w.tile + rank];
+        const bool fwd = (w.kind == kMainFwd);
+        const CUtensorMap* ma = fwd ? (td.a_src ? &P.tm_xg : &P.tm_x) : &P.tm_dy;
+        const int32_t nb = w.n0 + kHalfN * (int32_t)rank;     // first B column of this CTA's half
+        for (int kb = 0; kb < w.nk; ++kb) {
+            if (!acquire_stage2(ring, bar_full, bar_empty, kStage2Bytes, leader, lane, abort_flag, P.status)) return;
+            const uint32_t full = full_leader + ring.stage * 8;
+            const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
+            if (lane == 0) tma_load_hinted<LORA_HINT_ROWS>(sa, ma, kb * kBK, td.a_row0, full);
+            if (fwd) {
+                if (lane == 1) tma_load_hinted<LORA_HINT_W>(sb, &P.tm_w, kb * kBK, nb, full);     // Wt rows, K-major
+            } else if (lane == 1 || lane == 2) {
+                const int m = lane - 1;
+                tma_load_hinted<LORA_HINT_W>(sb + m * 8192, &P.tm_w, nb + 64 * m, kb * kBK, full);  // Wt, MN-major
+            }
+            ring.next();
+        }
+        // LoRA k-blocks: this tile's Z block and, per 8-row atom of stacked adapter rows, two 64-column MN boxes
+        const CUtensorMap* mp = fwd ? &P.tm_pb : &P.tm_pa;
+        const int32_t* atoms = (fwd ? P.atoms_b : P.atoms_a) + td.atom0;
+        for (int e = 0; e < w.n_ext; ++e) {
+            const int natoms = min(8, (td.ext_k - e * kBK) / 8);
+            if (!acquire_stage2(ring, bar_full, bar_empty, kZBlockBytes + natoms * 2048, leader, lane, abort_flag,
+                                P.status))
+                return;
+            const uint32_t full = full_leader + ring.stage * 8;
+            const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
+            if (lane == 0) tma_load_2d_pair(sa, &P.tm_z, 0, (td.z_blk0 + e) * kTileM, full);
+            if (lane < natoms * 2) {
+                const int q = lane >> 1, m = lane & 1;
+                tma_load_2d_pair(sb + m * 8192 + q * 1024, mp, nb + 64 * m, atoms[e * 8 + q], full);
+            }
+            ring.next();
+        }
+    }
+}
+
+__device__ void run_mma2(const KParams& P, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_tfull,
+                         uint32_t bar_tempty, uint32_t tmem, int i0, int i1, volatile int* abort_flag) {
+    Ring2 ring;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int ii = i0; ii < i1; ++ii) {
+        const WorkItem w = P.items[P.cta_list[ii]];
+        if (!wait_phase(bar_tempty + acc * 8, acc_phase ^ 1u, abort_flag, P.status)) return;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)acc * kBN;
+        uint32_t accumulate = 0;
+        auto kblock = [&](int steps, uint32_t idesc, int b_mn) -> bool {
+            const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
+            if (!wait_phase(full, ring.phase, abort_flag, P.status)) return false;
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
+            for (int k = 0; k < steps; ++k) {
+                const uint64_t ad = smem_desc(sa + k * 32, 16, 1024);
+                const uint64_t bd = b_mn ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
+                mma_bf16_pair(d, ad, bd, idesc, accumulate);
+                accumulate = 1;
+            }
+            mma_commit_pair(empty);
+            ring.next();
+            return true;
+        };
+        const int b_mn = (w.kind == kMainDx) ? 1 : 0;
+        const uint32_t id_main = instr_desc(2 * kTileM, kBN, 0, b_mn);
+        bool ok = true;
+        for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id_main, b_mn);
+        const TileDesc td = P.tiles[w.tile];
+        const uint32_t id_ext = instr_desc(2 * kTileM, kBN, 0, 1);
+        for (int e = 0; e < w.n_ext && ok; ++e) ok = kblock(min(4, (td.ext_k - e * kBK) / 16), id_ext, 1);
+        if (!ok) return;
+        mma_commit_pair(bar_tfull + acc * 8);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+}
+
+__device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t tmem, uint32_t rank,
+                              int i0, int i1, volatile int* abort_flag) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int ii = i0; ii < i1; ++ii) {
+        const WorkItem w = P.items[P.cta_list[ii]];
+        if (!wait_phase(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) return;
+        tc_fence_after();
+        const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);
+        const int32_t t = P.rowmap[(w.tile + rank) * kTileM + row];
+        for (int c = 0; c < kBN; c += 32) {
+            float v[32];
+            ld32_cols(taddr + c, v);
+            if (c + 32 == kBN) {
+                // the accumulator has been read: hand it back to the leader's MMA before the last stores
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
+            }
+            if (t >= 0) {
+                __nv_bfloat16* dst = P.out + (size_t)t * P.out_ld + w.n0 + c;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (w.n0 + c + 8 * g + 8 <= P.out_cols) {
+                        uint4 q;
+                        q.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+                        q.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+                        q.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+                        q.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+                        *reinterpret_cast<uint4*>(dst + 8 * g) = q;
+                    }
+                }
+            }
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    lora_main2_kernel(const __grid_constant__ KParams P) {
+    extern __shared__ uint8_t dsmem[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages2 * kStage2Bytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages2 + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + kStages2 * 8;
+    const uint32_t bar_tfull = bar_empty + kStages2 * 8, bar_tempty = bar_tfull + 16;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages2; ++s) {
+            mbar_init(bar_full + s * 8, 1);      // used in the leader: its arm + both CTAs' TMA bytes
+            mbar_init(bar_empty + s * 8, 1);     // the leader's commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_tfull + b * 8, 1);     // the leader's commit
+            mbar_init(bar_tempty + b * 8, 8);    // used in the leader: the 4 epilogue warps of each CTA
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int pair = blockIdx.x >> 1;
+    const int i0 = P.cta_off[pair], i1 = P.cta_off[pair + 1];
+
+    if (warp == 0) {
+        run_producer2(P, smem, bar_full, bar_empty, rank, i0, i1, abort_flag);
+    } else if (warp == 1) {
+        if (rank == 0 && lane == 0)
+            run_mma2(P, smem, bar_full, bar_empty, bar_tfull, bar_tempty, tmem, i0, i1, abort_flag);
+    } else {
+        run_epilogue2(P, bar_tfull, bar_tempty, tmem, rank, i0, i1, abort_flag);
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
 }  // namespace
 
 size_t tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024 + 1024; }
+size_t tc2_smem_bytes() { return (size_t)kStages2 * kStage2Bytes + 1024 + 1024; }
+
+cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream) {
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(lora_main2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc2_smem_bytes());
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    lora_main2_kernel<<<2 * pairs, kThreads, tc2_smem_bytes(), stream>>>(P);
+    return cudaGetLastError();
+}
 
 cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream) {
     static int configured[64] = {0};

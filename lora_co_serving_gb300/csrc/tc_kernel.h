@@ -16,11 +16,13 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     CUtensorMap tm_x;      // x rows,  [T, K] bf16, box {64, 128}, 128B swizzle
     CUtensorMap tm_xg;     // gathered rows buffer, [G*128, K], box {64, 128}
     CUtensorMap tm_dy;     // dY rows, [T, N], box {64, 128}
-    CUtensorMap tm_w;      // Wt [N, K]: forward box {64, 256} (K-major B); backward box {64, 64} (MN-major B)
+    CUtensorMap tm_w;      // Wt [N, K]: forward box {64, 128} (K-major B half); backward box {64, 64} (MN-major)
     CUtensorMap tm_pa;     // A pool viewed as [rows, K], box {64, 8}
     CUtensorMap tm_pb;     // B pool viewed as [rows, N], box {64, 8}
     CUtensorMap tm_xat;    // xA^T  [128, P], box {64, 8}
     CUtensorMap tm_dybt;   // dYB^T [128, P], box {64, 8}
+    CUtensorMap tm_z;      // Z blocks as [blocks*128, 64] bf16 rows of 128 B, box {64, 128}, no swizzle (the blocks
+                           // already hold the swizzled shared-memory image)
     CUtensorMap tm_seg_dy[kMaxTrainSegs];   // dY rows of fine-tuning segment q, [len, N], box {64, 64}
     CUtensorMap tm_seg_x[kMaxTrainSegs];    // x rows of fine-tuning segment q,  [len, K], box {64, 64}
 
@@ -57,6 +59,8 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
 };
 
 size_t tc_smem_bytes();
-cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream);
+cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream);      // shrink and grad items, 1 CTA each
+size_t tc2_smem_bytes();
+cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream);    // main items, clusters of 2 CTAs
 
 }  // namespace lora

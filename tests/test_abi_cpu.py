@@ -136,10 +136,13 @@ def test_plan_covers_every_token_once(lib, cfg):
     seg_of = np.empty(wl.T, np.int64)
     for i, (st, ln, a, tr) in enumerate(wl.segs.tolist()):
         seg_of[st:st + ln] = i
+    assert rows.shape[0] % 2 == 0, "tiles come in pairs"
     for ti in range(rows.shape[0]):
         r = rows[ti]
         v = r[r >= 0]
-        ads = sorted(set(int(wl.segs[seg_of[t], 2]) for t in v) - {-1})
+        pr = rows[ti - ti % 2: ti - ti % 2 + 2]      # the tile pair shares one adapter list
+        pv = pr[pr >= 0]
+        ads = sorted(set(int(wl.segs[seg_of[t], 2]) for t in pv) - {-1})
         assert info[ti, 1] == len(ads)
         assert info[ti, 2] == sum((int(wl.rank[a]) + 15) // 16 * 16 for a in ads)
         if info[ti, 0] == 0:   # window tile: rows are x rows [row0, row0+128) or -1
