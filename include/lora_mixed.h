@@ -154,6 +154,19 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
                         const void* dY, const void* xa_saved, void* dX, float* dA, float* dB, uint32_t flags,
                         void* workspace, size_t ws_bytes, void* stream);
 
+/* Forward pass for callers that cannot allocate device memory (no counterpart on the pages: this is a
+ * deployment concern of this library, not part of the method).  Same arguments and results as
+ * lora_mixed_forward, but its scratch lives in a fixed library-owned device array of
+ * LORA_STATIC_WORKSPACE_BYTES, held by every GPU that loads the library until the process exits; the call
+ * allocates nothing.  A batch whose scratch would exceed the array is rejected with LORA_ERR_LIMIT before
+ * any launch.  All calls share the array: two calls that overlap on the GPU race and must be ordered by the
+ * caller.  The first call on a device looks up the array's address for that device; make it before
+ * capturing a stream into a graph.  Its status word is not reachable through lora_workspace_status. */
+#define LORA_STATIC_WORKSPACE_BYTES (64u << 20)
+int lora_mixed_forward_static(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                              const lora_pool_t* pool, const lora_segment_t* segs /* HOST */, int32_t n_segs,
+                              void* y, void* xa_save, uint32_t flags, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* lora_last_error(void);
 

@@ -35,7 +35,7 @@ ERRORS = {0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_SEGMENTS", -3:
           -8: "LORA_ERR_CUDA", -9: "LORA_ERR_RANK", -10: "LORA_ERR_LIMIT", -11: "LORA_ERR_TIMEOUT"}
 
 EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_mixed_backward", "lora_last_error",
-            "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events"]
+            "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events", "lora_mixed_forward_static"]
 
 
 class LoraError(RuntimeError):
@@ -94,6 +94,8 @@ def library(path=None):
     lib.lora_plan_describe.restype = ctypes.c_int
     lib.lora_set_trace_events.argtypes = [P]
     lib.lora_set_trace_events.restype = ctypes.c_int
+    lib.lora_mixed_forward_static.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, I32, P, P, ctypes.c_uint32, P]
+    lib.lora_mixed_forward_static.restype = ctypes.c_int
     if path is None:
         _LIB = lib
     return lib
@@ -194,6 +196,25 @@ def forward(x, Wt, pool, segs, y=None, xa_save=None, save_xa=False, workspace=No
     flags = SAVE_XA if save_xa else 0
     _check(library().lora_mixed_forward(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), _ptr(s), s.shape[0], _ptr(y),
                                         _ptr(xa_save), flags, _ptr(ws), ws.numel(), _stream_ptr(stream)))
+    return (y, xa_save) if save_xa else y
+
+
+def forward_static(x, Wt, pool, segs, y=None, xa_save=None, save_xa=False, stream=None):
+    """forward() with the library's fixed device scratch instead of a caller workspace (allocates nothing in
+    the library; see lora_mixed_forward_static).  Returns y, or (y, xa_save) when save_xa is set."""
+    import torch
+    T, K = x.shape
+    N = Wt.shape[0]
+    code = _dtype_code(x)
+    s = segments(segs)
+    if y is None:
+        y = torch.empty((T, N), dtype=x.dtype, device=x.device)
+    if save_xa and xa_save is None:
+        n = xa_size(code, pool, s) // x.element_size()
+        xa_save = torch.empty(max(n, 1), dtype=x.dtype, device=x.device)
+    flags = SAVE_XA if save_xa else 0
+    _check(library().lora_mixed_forward_static(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), _ptr(s), s.shape[0],
+                                               _ptr(y), _ptr(xa_save), flags, _stream_ptr(stream)))
     return (y, xa_save) if save_xa else y
 
 

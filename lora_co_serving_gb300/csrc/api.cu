@@ -110,8 +110,16 @@ struct StagingRing {
 };
 StagingRing g_rings[64];
 
+// Set for the duration of a call made by an entry point that must not allocate: the plan is then copied
+// straight from the (pageable) host blob instead of through the pinned ring, which allocates on first use.
+thread_local bool g_direct_upload = false;
+
 int stage_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
     if (bytes == 0) return LORA_OK;
+    if (g_direct_upload) {
+        CUDA_TRY(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, stream));
+        return LORA_OK;
+    }
     int dev = 0;
     CUDA_TRY(cudaGetDevice(&dev));
     if (dev >= 64) {   // unusual device index: fall back to a pageable copy
@@ -259,6 +267,13 @@ cudaError_t launch_group(int k, KParams* P, uint8_t* ws, const Layout& L, const 
 }
 
 }  // namespace
+
+namespace lora {
+// Scoped switch to direct (non-staged) plan uploads for the calling thread; see g_direct_upload.
+DirectUpload::DirectUpload() : prev_(g_direct_upload) { g_direct_upload = true; }
+DirectUpload::~DirectUpload() { g_direct_upload = prev_; }
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace lora
 
 // ================================================================================================== C ABI
 extern "C" {

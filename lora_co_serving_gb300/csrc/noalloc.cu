@@ -1,0 +1,74 @@
+// noalloc.cu -- lora_mixed_forward_static: the forward pass with library-owned scratch, for callers that
+// cannot allocate device memory.
+//
+// Some callers of this layer cannot call cudaMalloc or any allocating routine while they run a batch: a
+// serving engine whose memory pool owns every byte of the device (allocations outside it would break its
+// accounting or fail once the pool has reserved the free memory), or a code path that must not allocate
+// because it runs inside a timing-critical step or while another component holds the allocator.  For them
+// the forward pass's scratch (segment plan, gathered decode rows, the per-tile LoRA operand Z, shrink partial
+// sums, status word and split counters) lives in one fixed array in device memory, declared below.
+//
+// Costs and limits:
+//   * every GPU that loads the library holds the array (LORA_STATIC_WORKSPACE_BYTES) until the process exits;
+//   * a batch whose scratch would exceed it is rejected with LORA_ERR_LIMIT before anything is launched;
+//   * all calls share the array, which keeps whatever the last call left in it; each call zeroes the parts
+//     that must start at zero (status word, split counters, Z) itself, but two calls that overlap on the GPU
+//     (different streams, or different host threads without ordering) race on it;
+//   * the first call on a device looks up the array's device address (cudaGetSymbolAddress) for that device;
+//     make that first call before capturing any stream into a graph.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "lora_mixed.h"
+#include "plan.h"
+
+namespace {
+
+// The scratch.  In host code this name is only a stand-in for the device array: its device address comes
+// from cudaGetSymbolAddress, per device.
+static __device__ __align__(256) unsigned char g_static_ws[LORA_STATIC_WORKSPACE_BYTES];
+
+std::mutex g_mu;
+void* g_addr[64] = {nullptr};
+
+}  // namespace
+
+extern "C" int lora_mixed_forward_static(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x,
+                                         const void* Wt, const lora_pool_t* pool, const lora_segment_t* segs,
+                                         int32_t n_segs, void* y, void* xa_save, uint32_t flags, void* stream) {
+    const size_t need = lora_workspace_size(T, K, N, dt, pool, segs, n_segs);
+    if (need == 0) return LORA_ERR_INVALID_ARG;            // lora_last_error() already describes the problem
+    if (need > (size_t)LORA_STATIC_WORKSPACE_BYTES) {
+        const std::string msg = "lora_mixed_forward_static: this batch needs " + std::to_string(need) +
+                                " bytes of scratch, more than the fixed " +
+                                std::to_string((size_t)LORA_STATIC_WORKSPACE_BYTES) +
+                                " bytes; split the batch or use lora_mixed_forward with a caller workspace";
+        lora::set_last_error(msg.c_str());
+        return LORA_ERR_LIMIT;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        lora::set_last_error(e != cudaSuccess ? cudaGetErrorString(e) : "device index beyond 63");
+        return LORA_ERR_CUDA;
+    }
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_addr[dev]) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_static_ws);       // with device `dev` current
+            if (e != cudaSuccess) {
+                lora::set_last_error((std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e)).c_str());
+                return LORA_ERR_CUDA;
+            }
+            g_addr[dev] = p;
+        }
+        ws = g_addr[dev];
+    }
+    lora::DirectUpload direct;                              // no pinned staging ring: nothing is allocated
+    return lora_mixed_forward(T, K, N, dt, x, Wt, pool, segs, n_segs, y, xa_save, flags, ws,
+                              (size_t)LORA_STATIC_WORKSPACE_BYTES, stream);
+}

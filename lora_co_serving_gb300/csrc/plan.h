@@ -80,6 +80,16 @@ struct Layout {
 constexpr int kMaxCtas = 1024;
 Layout layout_of(const Problem& p, const Plan& plan, bool backward);
 
+// While alive, calls on this thread copy their plan straight from host memory (no pinned staging ring).
+class DirectUpload {
+  public:
+    DirectUpload();
+    ~DirectUpload();
+  private:
+    bool prev_;
+};
+void set_last_error(const char* msg);
+
 // The float32 path keeps per-token adapter ids and an xA scratch of [T, 128] floats.
 size_t simt_scratch_bytes(const Problem& p);
 
