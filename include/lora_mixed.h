@@ -188,6 +188,13 @@ int lora_workspace_status(const void* workspace, void* stream);
  * A call that has no work in group i still records both of its events. */
 int lora_set_trace_events(void* const* events);
 
+/* Diagnostic of the failure path (no counterpart on the pages): launches one thread that waits, with the
+ * same bounded wait as every kernel of the library, on a barrier that nothing ever completes.  After the
+ * wait's limit (about one second) it records LORA_ERR_TIMEOUT in the workspace status word and returns, so
+ * lora_workspace_status() then reports LORA_ERR_TIMEOUT and the CUDA context stays usable.  Needs the first
+ * 256 bytes of a 256-byte aligned workspace. */
+int lora_selftest_wait_timeout(void* workspace, size_t ws_bytes, void* stream);
+
 /* Diagnostic: the forward tile plan of a segment table, for host-side tests.
  *   n_tiles_out: number of 128-row tiles.
  *   rows_out [cap*128]: token row held by each tile row, -1 for none.

@@ -35,7 +35,8 @@ ERRORS = {0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_SEGMENTS", -3:
           -8: "LORA_ERR_CUDA", -9: "LORA_ERR_RANK", -10: "LORA_ERR_LIMIT", -11: "LORA_ERR_TIMEOUT"}
 
 EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_mixed_backward", "lora_last_error",
-            "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events", "lora_mixed_forward_static"]
+            "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events", "lora_mixed_forward_static",
+            "lora_selftest_wait_timeout"]
 
 
 class LoraError(RuntimeError):
@@ -96,6 +97,8 @@ def library(path=None):
     lib.lora_set_trace_events.restype = ctypes.c_int
     lib.lora_mixed_forward_static.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, I32, P, P, ctypes.c_uint32, P]
     lib.lora_mixed_forward_static.restype = ctypes.c_int
+    lib.lora_selftest_wait_timeout.argtypes = [P, SZ, P]
+    lib.lora_selftest_wait_timeout.restype = ctypes.c_int
     if path is None:
         _LIB = lib
     return lib

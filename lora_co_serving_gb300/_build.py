@@ -40,25 +40,26 @@ def _run(cmd):
     return res.stdout + res.stderr
 
 
-def build(force=False, verbose=False, extra_flags=(), out=None, objdir=None):
+def build(force=False, verbose=False, extra_flags=(), out=None, objdir=None, csrc=None):
     """Compile and link the library if any source is newer than it; return its path.
 
     ``extra_flags``/``out``/``objdir`` build a variant (e.g. other -D tuning values) into another file.
     """
     lib_path = out or LIB
     objdir = objdir or OBJDIR
+    src_dir = csrc or CSRC
     if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _deps():
         return lib_path
     os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
-    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC, "-Xcompiler", "-fPIC"]
+    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", src_dir, "-Xcompiler", "-fPIC"]
     jobs = []
     for src in CUDA_SOURCES:
         obj = os.path.join(objdir, src + ".o")
-        jobs.append([nvcc, *ARCH, "-lineinfo", *common, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj])
+        jobs.append([nvcc, *ARCH, "-lineinfo", *common, *extra_flags, "-c", os.path.join(src_dir, src), "-o", obj])
     for src in CXX_SOURCES:
         obj = os.path.join(objdir, src + ".o")
-        jobs.append([nvcc, *common, *extra_flags, "-x", "c++", "-c", os.path.join(CSRC, src), "-o", obj])
+        jobs.append([nvcc, *common, *extra_flags, "-x", "c++", "-c", os.path.join(src_dir, src), "-o", obj])
     with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         outs = list(ex.map(_run, jobs))
     objs = [os.path.join(objdir, s + ".o") for s in CUDA_SOURCES + CXX_SOURCES]

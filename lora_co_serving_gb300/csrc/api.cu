@@ -251,11 +251,24 @@ int begin_call(const Layout& L, const Plan& pl, void* ws, size_t bytes_plan, con
     return stage_copy(w + L.tiles, blob, bytes_plan, stream);
 }
 
+#ifndef LORA_MAIN_PERSISTENT
+#define LORA_MAIN_PERSISTENT 1
+#endif
 // Per-launch CTA assignment: shrink and grad items over single CTAs, main items over CTA pairs.
 void assign_all(const Plan& pl, int sms, std::vector<int32_t> (&off)[3], std::vector<int32_t> (&lst)[3], int (&grid)[3]) {
     for (int k = 0; k < 3; ++k) {
+        const int n = (int)pl.items[k].size();
+        if (k == 1 && !LORA_MAIN_PERSISTENT) {
+            // one CTA pair per item, dispatched by the hardware in item order
+            grid[k] = n;
+            off[k].resize(n + 1);
+            lst[k].resize(n);
+            for (int i = 0; i <= n; ++i) off[k][i] = i;
+            for (int i = 0; i < n; ++i) lst[k][i] = i;
+            continue;
+        }
         const int units = (k == 1) ? sms / 2 : sms;
-        grid[k] = std::min<int>(std::min(units, kMaxCtas), (int)pl.items[k].size());
+        grid[k] = std::min<int>(std::min(units, kMaxCtas), n);
         if (grid[k] > 0) assign_items(pl.items[k], pl, grid[k], &off[k], &lst[k]);
     }
 }
@@ -315,6 +328,15 @@ int lora_set_trace_events(void* const* events) {
         g_trace[i] = static_cast<cudaEvent_t>(events[i]);
     }
     g_trace_on = true;
+    return LORA_OK;
+}
+
+int lora_selftest_wait_timeout(void* workspace, size_t ws_bytes, void* stream_) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 || ws_bytes < 256)
+        return fail(LORA_ERR_WORKSPACE, "workspace must be non-NULL, 256-byte aligned and at least 256 bytes");
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    CUDA_TRY(cudaMemsetAsync(workspace, 0, 256, stream));
+    CUDA_TRY(selftest_timeout_launch(static_cast<int32_t*>(workspace), stream));
     return LORA_OK;
 }
 

@@ -768,10 +768,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
+// Failure-path self-test: one thread waits, with the kernels' bounded wait, on an mbarrier that nothing ever
+// arrives on.  The wait gives up after its time limit and records LORA_ERR_TIMEOUT in the status word; the
+// kernel then returns normally, leaving the context usable.
+__global__ void selftest_timeout_kernel(int32_t* status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) wait_phase(smem_u32(&bar), 0, reinterpret_cast<volatile int*>(&abort_flag), status);
+}
+
 }  // namespace
 
 size_t tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024 + 1024; }
 size_t tc2_smem_bytes() { return (size_t)kStages2 * kStage2Bytes + 1024 + 1024; }
+
+cudaError_t selftest_timeout_launch(int32_t* status, cudaStream_t stream) {
+    selftest_timeout_kernel<<<1, 32, 0, stream>>>(status);
+    return cudaGetLastError();
+}
 
 cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream) {
     static int configured[64] = {0};

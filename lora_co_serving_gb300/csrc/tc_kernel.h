@@ -62,5 +62,6 @@ size_t tc_smem_bytes();
 cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream);      // shrink and grad items, 1 CTA each
 size_t tc2_smem_bytes();
 cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream);    // main items, clusters of 2 CTAs
+cudaError_t selftest_timeout_launch(int32_t* status, cudaStream_t stream);
 
 }  // namespace lora
