@@ -193,6 +193,7 @@ void fill_plan_pointers(KParams* P, uint8_t* ws, const Layout& L, int launch) {
     P->atoms_a = reinterpret_cast<const int32_t*>(ws + L.atoms_a);
     P->atoms_b = reinterpret_cast<const int32_t*>(ws + L.atoms_b);
     P->part = reinterpret_cast<float*>(ws + L.part);
+    P->part_main = reinterpret_cast<float*>(ws + L.part_main);
     P->units = reinterpret_cast<const ShrinkUnit*>(ws + L.units);
     P->counters = reinterpret_cast<int32_t*>(ws + L.counters);
     P->status = reinterpret_cast<int32_t*>(ws + L.status);

@@ -66,8 +66,13 @@ struct WorkItem {
     int32_t nk;       // main/shrink: k-blocks of the dense loop; grad: total token blocks
     int32_t mma_n;    // N of the MMA
     int32_t n_ext;    // main: LoRA k-blocks after the dense loop
-    int32_t kb0;      // shrink: first k-block of this split of the reduction
-    int32_t part;     // shrink: column offset of this split's fp32 partial [mma_n, 128] in the partial buffer
+    int32_t kb0;      // shrink and split main items: first k-block of this split of the reduction
+    int32_t part;     // shrink: column offset of this split's fp32 partial [mma_n, 128] in the partial buffer;
+                      // main: first partial slot of the output tile (split s writes slot part + s)
+    int32_t nsplit;   // main: number of K-splits of the output tile (1 = no split)
+    int32_t split;    // main: index of this split
+    int32_t counter;  // main, split: first of the 8 counters (2 CTAs x 4 row quarters) of the output tile
+    int32_t pad;
 };
 
 // One shrink pass of one tile.  Its K-splits write fp32 partial sums; the last split to finish (counted per row
@@ -82,9 +87,18 @@ struct ShrinkUnit {
     int32_t pad0, pad1;
 };
 
-// K-blocks per split of a shrink reduction.  Split boundaries depend on K alone, so a row's xA is summed in the
-// same order whatever the rest of its tile holds.
-constexpr int kShrinkSplitKb = 32;
+// K-blocks per split of a shrink reduction.  Split boundaries depend on the batch size and K alone, so a row's
+// xA is summed in the same order whatever the rest of its tile holds; small batches split finer so that their
+// few tiles still spread over every SM.
+inline int shrink_split_kb(int64_t T) { return T <= 1024 ? 8 : (T <= 4096 ? 16 : 32); }
+
+// Main pass K-splits: when a backward launch has fewer output tiles than ~1.5 waves of CTA pairs, each tile's
+// dense K loop is split and the last split to finish sums the fp32 partials in split order.  The forward keeps
+// one split: a decode tile's LoRA K-steps (which dominate small decode batches) would have to stay in a single
+// split for its rows to be summed in an order independent of the pool order (measured: splitting only the
+// dense loop made a 256-token decode batch slower, 64 -> 78 us).
+constexpr int kMainTargetItems = 114;
+constexpr int kMainPartialFloats = kBN * kTileM;   // one CTA's fp32 partial of a 128 x 256 output tile
 
 struct GradGroup {    // one fine-tuning adapter of a backward call
     int32_t adapter;

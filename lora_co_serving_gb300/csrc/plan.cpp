@@ -163,7 +163,7 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
 
 // Shrink items of one pass, split along the reduction at boundaries that depend on the k-block count alone.
 static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t mma_n, int32_t nk) {
-    const int32_t nsplit = std::max<int32_t>(1, int32_t(cdiv(nk, kShrinkSplitKb)));
+    const int32_t nsplit = std::max<int32_t>(1, int32_t(cdiv(nk, shrink_split_kb(pl->T))));
     ShrinkUnit u{};
     u.kind = kind; u.tile = tile; u.n0 = n0; u.mma_n = mma_n; u.nsplit = nsplit;
     u.part0 = int32_t(pl->part_cols);
@@ -185,18 +185,38 @@ static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t
 static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk) {
     const size_t n_pairs = pl->tiles.size() / 2;
     const size_t band = kBandTiles / 2;
+    // Few output tiles: split their dense K loop (the LoRA K-steps go with the last split).  Backward only:
+    // a fine-tuning tile holds one adapter at LoRA column 0, so the split leaves every row's summation order
+    // independent of the pool order; forward decode tiles would not be (see kMainTargetItems).
+    const int64_t tiles_out = (int64_t)n_pairs * n_nt;
+    int32_t nsplit = 1;
+    if (kind == kMainDx && tiles_out > 0 && tiles_out < kMainTargetItems)
+        nsplit = int32_t(std::max<int64_t>(1, std::min<int64_t>({cdiv(kMainTargetItems, tiles_out), nk / 4, 16})));
     for (size_t b0 = 0; b0 < n_pairs; b0 += band) {
         const size_t b1 = std::min(n_pairs, b0 + band);
         for (int32_t nt = 0; nt < n_nt; ++nt)
             for (size_t q = b0; q < b1; ++q) {
-                WorkItem w{};
-                w.kind = kind;
-                w.tile = int32_t(2 * q);
-                w.n0 = nt * kBN;
-                w.nk = nk;
-                w.mma_n = kBN;
-                w.n_ext = int32_t(cdiv(pl->tiles[2 * q].ext_k, kBK));
-                pl->items[1].push_back(w);
+                const int32_t slot0 = int32_t(pl->main_slots);
+                const int32_t cnt0 = int32_t(4 * pl->units.size() + pl->main_counters);   // after the shrink counters
+                for (int32_t sp = 0; sp < nsplit; ++sp) {
+                    WorkItem w{};
+                    w.kind = kind;
+                    w.tile = int32_t(2 * q);
+                    w.n0 = nt * kBN;
+                    w.kb0 = int32_t((int64_t)sp * nk / nsplit);
+                    w.nk = int32_t((int64_t)(sp + 1) * nk / nsplit) - w.kb0;
+                    w.mma_n = kBN;
+                    w.n_ext = (sp == nsplit - 1) ? int32_t(cdiv(pl->tiles[2 * q].ext_k, kBK)) : 0;
+                    w.nsplit = nsplit;
+                    w.split = sp;
+                    w.part = slot0;
+                    w.counter = cnt0;
+                    pl->items[1].push_back(w);
+                }
+                if (nsplit > 1) {
+                    pl->main_slots += nsplit;
+                    pl->main_counters += 8;
+                }
             }
     }
 }
@@ -204,6 +224,7 @@ static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk) {
 void plan_forward(const Problem& p, Plan* out) {
     Plan& pl = *out;
     pl = Plan();
+    pl.T = p.T;
     // xa_save offsets of fine-tuning segments (increasing start)
     std::vector<int64_t> seg_xoff(p.segs.size(), -1);
     int64_t xo = 0;
@@ -275,6 +296,7 @@ void plan_forward(const Problem& p, Plan* out) {
 void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out) {
     Plan& pl = *out;
     pl = Plan();
+    pl.T = p.T;
     // fine-tuning segments in increasing start order, grouped by adapter
     std::vector<int32_t> group_of_adapter(p.n_adapters, -1);
     std::vector<std::vector<int32_t>> members;
@@ -404,7 +426,7 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     size_t at = 0;
     auto take = [&](size_t bytes) { size_t o = at; at = align256(at + bytes); return o; };
     L.status = take(256);
-    L.counters = take(sizeof(int32_t) * 4 * pl.units.size());
+    L.counters = take(sizeof(int32_t) * (4 * pl.units.size() + pl.main_counters));
     L.zero_end = at;
     L.tiles = take(sizeof(TileDesc) * pl.tiles.size());
     L.chunks = take(sizeof(Chunk) * pl.chunks.size());
@@ -426,6 +448,7 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
         L.xg = take((size_t)pl.n_gtiles * kTileM * p.K * 2);
         L.z = take((size_t)pl.z_blocks * kZBlockBytes);
         L.part = take((size_t)pl.part_cols * kTileM * sizeof(float));
+        L.part_main = take((size_t)pl.main_slots * 2 * kMainPartialFloats * sizeof(float));
         if (backward) {
             L.xat = take((size_t)LORA_MAX_RANK * pl.tcols * 2);
             L.dybt = take((size_t)LORA_MAX_RANK * pl.tcols * 2);

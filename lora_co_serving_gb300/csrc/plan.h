@@ -54,6 +54,9 @@ struct Plan {
     int64_t z_blocks = 0;
     int64_t tcols = 0;               // backward: columns of the transposed xA / dYB buffers
     int64_t part_cols = 0;           // columns (of 128 fp32 each) of the shrink partial-sum buffer
+    int64_t main_slots = 0;          // K-split partial slots of the main pass (each 2 CTAs x 128 x 256 fp32)
+    int64_t main_counters = 0;       // counters of split main tiles (8 per tile), after the shrink counters
+    int64_t T = 0;                   // tokens of the batch (sets the shrink split size)
 };
 
 void plan_forward(const Problem& p, Plan* out);
@@ -72,7 +75,7 @@ struct Layout {
     size_t atoms_a = 0, atoms_b = 0, units = 0;
     size_t items[3] = {0, 0, 0}, cta_off[3] = {0, 0, 0}, cta_list[3] = {0, 0, 0};
     size_t plan_end = 0;
-    size_t xg = 0, z = 0, xat = 0, dybt = 0, part = 0;
+    size_t xg = 0, z = 0, xat = 0, dybt = 0, part = 0, part_main = 0;
     size_t simt = 0;                 // float32 path scratch
     size_t total = 0;
 };

@@ -597,7 +597,7 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
         const bool fwd = (w.kind == kMainFwd);
         const CUtensorMap* ma = fwd ? (td.a_src ? &P.tm_xg : &P.tm_x) : &P.tm_dy;
         const int32_t nb = w.n0 + kHalfN * (int32_t)rank;     // first B column of this CTA's half
-        for (int kb = 0; kb < w.nk; ++kb) {
+        for (int kb = w.kb0; kb < w.kb0 + w.nk; ++kb) {
             if (!acquire_stage2(ring, bar_full, bar_empty, kStage2Bytes, leader, lane, abort_flag, P.status)) return;
             const uint32_t full = full_leader + ring.stage * 8;
             const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
@@ -670,6 +670,21 @@ __device__ void run_mma2(const KParams& P, uint8_t* smem, uint32_t bar_full, uin
     }
 }
 
+__device__ __forceinline__ void store_row_bf16(const KParams& P, int32_t t, int32_t col0, const float (&v)[32]) {
+    __nv_bfloat16* dst = P.out + (size_t)t * P.out_ld + col0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (col0 + 8 * g + 8 <= P.out_cols) {
+            uint4 q;
+            q.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+            q.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+            q.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+            q.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+            *reinterpret_cast<uint4*>(dst + 8 * g) = q;
+        }
+    }
+}
+
 __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t tmem, uint32_t rank,
                               int i0, int i1, volatile int* abort_flag) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -684,6 +699,10 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
         tc_fence_after();
         const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);
         const int32_t t = P.rowmap[(w.tile + rank) * kTileM + row];
+        // K-split tiles: this split's fp32 partial goes to its slot, column-major [256][128] per CTA
+        float* part = (w.nsplit > 1)
+                          ? P.part_main + ((size_t)(w.part + w.split) * 2 + rank) * kMainPartialFloats + row
+                          : nullptr;
         for (int c = 0; c < kBN; c += 32) {
             float v[32];
             ld32_cols(taddr + c, v);
@@ -693,23 +712,41 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
             }
-            if (t >= 0) {
-                __nv_bfloat16* dst = P.out + (size_t)t * P.out_ld + w.n0 + c;
+            if (part) {
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    if (w.n0 + c + 8 * g + 8 <= P.out_cols) {
-                        uint4 q;
-                        q.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
-                        q.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
-                        q.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
-                        q.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
-                        *reinterpret_cast<uint4*>(dst + 8 * g) = q;
-                    }
-                }
+                for (int i = 0; i < 32; ++i) part[(size_t)(c + i) * kTileM] = v[i];
+            } else if (t >= 0) {
+                store_row_bf16(P, t, w.n0 + c, v);
             }
         }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
+        if (part) {
+            // the last split to finish this row quarter sums the splits in split order and writes y
+            __threadfence();
+            __syncwarp();
+            int32_t* cnt = P.counters + w.counter + rank * 4 + quarter;
+            int last = 0;
+            if (lane == 0) last = (atomicAdd(cnt, 1) == w.nsplit - 1) ? 1 : 0;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                const float* p0 = P.part_main + ((size_t)w.part * 2 + rank) * kMainPartialFloats + row;
+                for (int c = 0; c < kBN; c += 32) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    for (int sp = 0; sp < w.nsplit; ++sp) {
+                        const float* ps = p0 + (size_t)sp * 2 * kMainPartialFloats + (size_t)c * kTileM;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] += __ldcg(ps + (size_t)i * kTileM);
+                    }
+                    if (t >= 0) store_row_bf16(P, t, w.n0 + c, v);
+                }
+                __syncwarp();
+                if (lane == 0) *cnt = 0;                   // ready for the next call on this workspace
+            }
+        }
     }
 }
 

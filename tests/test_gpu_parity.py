@@ -132,3 +132,13 @@ def test_bf16_backward_accumulate():
     ia, ib = train_blocks(wl)
     compare(to_np(aA)[ia], to_np(dA0)[ia] + to_np(dA)[ia], "dA accumulate", max_err=1e-5, fro_err=1e-6)
     compare(to_np(aB)[ib], to_np(dB0)[ib] + to_np(dB)[ib], "dB accumulate", max_err=1e-5, fro_err=1e-6)
+
+
+def test_bf16_backward_small_batch_split_k():
+    # one 200-token fine-tuning segment on a 1024x1024 layer: 4 output tiles of dX, so the dX loop over N is
+    # split four ways and the last split of each tile reduces the partials
+    wl = workloads.config4(K=1024, N=1024, n_samples=1, sample_len=200, r=64)
+    check_backward(wl)
+    # and again with a second segment on another adapter, so two tile pairs share the launch
+    wl2 = workloads.config4(K=1024, N=1024, n_samples=2, sample_len=150, r=32, four_adapters=True)
+    check_backward(wl2)
