@@ -334,6 +334,33 @@ def run_ours(args):
     ms_max = float(t_max.item())
     value = acc["tokens"] * world / (ms_max / 1e3)
 
+    # ---- the optimizer step that follows (AdamW on the fine-tuning adapters, fp32 masters + bf16 pool), timed
+    # on its own: it is not part of the forward+backward step the metric is about
+    adamw_stats = None
+    if wl.backward:
+        tads_u = sorted(set(int(a) for _, _, a, t in wl.segs.tolist() if t))
+        masterA, masterB = A.float(), B.float()
+        mA, vA = torch.zeros_like(masterA), torch.zeros_like(masterA)
+        mB, vB = torch.zeros_like(masterB), torch.zeros_like(masterB)
+        for i in range(3):
+            lm.adamw_step(pool, K, N, dA, dB, mA, vA, mB, vB, tads_u, step=1 + i, A_master=masterA, B_master=masterB,
+                          stream=stream)
+        n_ad = max(3, min(args.steps, 50))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a0.record(stream)
+        for i in range(n_ad):
+            lm.adamw_step(pool, K, N, dA, dB, mA, vA, mB, vB, tads_u, step=4 + i, A_master=masterA,
+                          B_master=masterB, stream=stream)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ams = a0.elapsed_time(a1) / n_ad
+        elems = sum(int(wl.rank[a]) * (K + N) for a in tads_u)
+        abytes = elems * (4 * 4 + 3 * 4 + 2)      # read g, m, v, master; write m, v, master, bf16 weight
+        adamw_stats = {"ms": ams, "elements": elems, "algorithmic_bytes": abytes,
+                       "hbm_gbs": abytes / (ams / 1e3) / 1e9, "launches_per_call": 1}
+        del masterA, masterB, mA, vA, mB, vB
+
     # ---- end to end: every step's inputs come from pinned host memory and its results go back to pinned host
     # memory.  Two device buffer sets let the inputs of step i+1 and the results of step i-1 move on two copy
     # streams (the copy engines) while step i computes, as a serving loop would run it.
@@ -448,6 +475,7 @@ def run_ours(args):
                            "l2": "inputs larger than L2 (W alone %.0f MB); no flush" % (2 * K * N / 1e6),
                            "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
                 "roofline": roof, "step": step_stats, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+                "adamw": adamw_stats,
                 "gpu_launches": launches_per_step(wl) * args.steps}
         print(json.dumps(line), flush=True)
     if dist:

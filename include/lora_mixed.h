@@ -167,6 +167,34 @@ int lora_mixed_forward_static(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, 
                               const lora_pool_t* pool, const lora_segment_t* segs /* HOST */, int32_t n_segs,
                               void* y, void* xa_save, uint32_t flags, void* stream);
 
+/* AdamW hyperparameters for lora_adamw_step (DeltaServe section 4.1 trains with lr 1e-3, weight decay
+ * 0.01; betas and eps are the usual 0.9, 0.999, 1e-8).  step is the 1-based update count. */
+typedef struct lora_adamw {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;
+    int32_t step;
+} lora_adamw_t;
+
+/* The fine-tuning step after the backward: AdamW, in place, on the blocks of the listed adapters
+ * (DeltaServe section 3.2, "Backward subprocess": optimizer updates applied directly to the shared adapter
+ * weights):
+ *     m <- b1 m + (1-b1) g;   v <- b2 v + (1-b2) g^2
+ *     w <- w (1 - lr wd) - lr/(1-b1^step) * m / (sqrt(v)/sqrt(1-b2^step) + eps)
+ *   A, B:       the pool's weights (device, element type dt), updated in place.
+ *   A_master, B_master: optional fp32 master weights shaped like the pools (NULL: update A/B directly).
+ *               With masters, AdamW runs on the masters and A/B receive them rounded to dt.
+ *   dA, dB:     fp32 gradients shaped like the pools (lora_mixed_backward's outputs).
+ *   mA, vA, mB, vB: fp32 first and second moments shaped like the pools, updated in place (zero before
+ *               the first step).
+ *   adapters:   HOST [n_upd] distinct adapter ids (at most 48); only their blocks are read or written.
+ * Validated on the host; one launch on `stream`. */
+int lora_adamw_step(lora_dtype_t dt, const lora_pool_t* pool, int32_t K, int32_t N, void* A, void* B, float* A_master,
+                    float* B_master, const float* dA, const float* dB, float* mA, float* vA, float* mB, float* vB,
+                    const int32_t* adapters /* HOST */, int32_t n_upd, const lora_adamw_t* hp, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* lora_last_error(void);
 

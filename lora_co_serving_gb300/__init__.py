@@ -36,7 +36,7 @@ ERRORS = {0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_SEGMENTS", -3:
 
 EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_mixed_backward", "lora_last_error",
             "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events", "lora_mixed_forward_static",
-            "lora_selftest_wait_timeout"]
+            "lora_selftest_wait_timeout", "lora_adamw_step"]
 
 
 class LoraError(RuntimeError):
@@ -99,6 +99,8 @@ def library(path=None):
     lib.lora_mixed_forward_static.restype = ctypes.c_int
     lib.lora_selftest_wait_timeout.argtypes = [P, SZ, P]
     lib.lora_selftest_wait_timeout.restype = ctypes.c_int
+    lib.lora_adamw_step.argtypes = [ctypes.c_int, P, I32, I32, P, P, P, P, P, P, P, P, P, P, P, I32, P, P]
+    lib.lora_adamw_step.restype = ctypes.c_int
     if path is None:
         _LIB = lib
     return lib
@@ -138,6 +140,23 @@ def segments(segs):
     """Segment table as a contiguous int32 [n, 4] numpy array."""
     a = np.ascontiguousarray(np.asarray(segs, dtype=np.int32).reshape(-1, 4))
     return a
+
+
+class AdamW(ctypes.Structure):
+    """lora_adamw_t: AdamW hyperparameters (step is 1-based)."""
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int32)]
+
+
+def adamw_step(pool, K, N, dA, dB, mA, vA, mB, vB, adapters, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+               weight_decay=0.01, A_master=None, B_master=None, stream=None):
+    """AdamW on the listed adapters' blocks of pool.A / pool.B (and fp32 masters if given), in place."""
+    code = _dtype_code(pool.A)
+    ids = np.ascontiguousarray(adapters, dtype=np.int32)
+    hp = AdamW(lr, beta1, beta2, eps, weight_decay, step)
+    _check(library().lora_adamw_step(code, pool.cptr(), K, N, _ptr(pool.A), _ptr(pool.B), _ptr(A_master),
+                                     _ptr(B_master), _ptr(dA), _ptr(dB), _ptr(mA), _ptr(vA), _ptr(mB), _ptr(vB),
+                                     _ptr(ids), ids.shape[0], ctypes.addressof(hp), _stream_ptr(stream)))
 
 
 class Pool:

@@ -16,7 +16,7 @@ OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblora_mixed.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ["api.cu", "tc_kernel.cu", "simt.cu", "noalloc.cu"]
+CUDA_SOURCES = ["api.cu", "tc_kernel.cu", "simt.cu", "noalloc.cu", "adamw.cu"]
 CXX_SOURCES = ["plan.cpp"]
 
 
