@@ -195,6 +195,20 @@ int lora_adamw_step(lora_dtype_t dt, const lora_pool_t* pool, int32_t K, int32_t
                     float* B_master, const float* dA, const float* dB, float* mA, float* vA, float* mB, float* vB,
                     const int32_t* adapters /* HOST */, int32_t n_upd, const lora_adamw_t* hp, void* stream);
 
+/* lora_mixed_backward with the save/recompute choice made per fine-tuning segment on the device, from a
+ * flag table that another stream or process may rewrite between calls (in the spirit of MOLT section 4.3,
+ * "flexible activation checkpointing": whether an activation's slot is still backed is known only when the
+ * backward is dispatched, and unbacked activations are recomputed).
+ *   xa_valid: device int32 [number of fine-tuning segments], in increasing segment-start order; nonzero =
+ *             the segment's block of xa_saved holds its x A, zero = recompute it.  The call copies the table
+ *             on its stream when it starts on the GPU; all its kernels use that copy.
+ *   xa_saved: required (read only for flagged segments); LORA_RECOMPUTE_XA is not allowed.
+ * Everything else as lora_mixed_backward. */
+int lora_mixed_backward_flagged(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                                const lora_pool_t* pool, const lora_segment_t* segs /* HOST */, int32_t n_segs,
+                                const void* dY, const void* xa_saved, const int32_t* xa_valid, void* dX, float* dA,
+                                float* dB, uint32_t flags, void* workspace, size_t ws_bytes, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* lora_last_error(void);
 

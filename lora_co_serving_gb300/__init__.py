@@ -36,7 +36,7 @@ ERRORS = {0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_SEGMENTS", -3:
 
 EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_mixed_backward", "lora_last_error",
             "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events", "lora_mixed_forward_static",
-            "lora_selftest_wait_timeout", "lora_adamw_step"]
+            "lora_selftest_wait_timeout", "lora_adamw_step", "lora_mixed_backward_flagged"]
 
 
 class LoraError(RuntimeError):
@@ -101,6 +101,9 @@ def library(path=None):
     lib.lora_selftest_wait_timeout.restype = ctypes.c_int
     lib.lora_adamw_step.argtypes = [ctypes.c_int, P, I32, I32, P, P, P, P, P, P, P, P, P, P, P, I32, P, P]
     lib.lora_adamw_step.restype = ctypes.c_int
+    lib.lora_mixed_backward_flagged.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, I32, P, P, P, P, P, P,
+                                                ctypes.c_uint32, P, SZ, P]
+    lib.lora_mixed_backward_flagged.restype = ctypes.c_int
     if path is None:
         _LIB = lib
     return lib
@@ -260,6 +263,29 @@ def backward(x, Wt, pool, segs, dY, xa_saved=None, dX=None, dA=None, dB=None, wa
                                          _ptr(dY), _ptr(xa_saved), _ptr(dX) if want_dx else None,
                                          _ptr(dA) if want_grads else None, _ptr(dB) if want_grads else None, flags,
                                          _ptr(ws), ws.numel(), _stream_ptr(stream)))
+    return dX, dA, dB
+
+
+def backward_flagged(x, Wt, pool, segs, dY, xa_saved, xa_valid, dX=None, dA=None, dB=None, accumulate=False,
+                     workspace=None, stream=None):
+    """backward() with a device flag table choosing, per fine-tuning segment (increasing start order), the saved
+    xA (nonzero) or a recompute (zero)."""
+    import torch
+    T, K = x.shape
+    N = Wt.shape[0]
+    code = _dtype_code(x)
+    s = segments(segs)
+    if dX is None:
+        dX = torch.zeros((T, K), dtype=x.dtype, device=x.device)
+    if dA is None:
+        dA = torch.zeros(pool.A.numel(), dtype=torch.float32, device=x.device)
+    if dB is None:
+        dB = torch.zeros(pool.B.numel(), dtype=torch.float32, device=x.device)
+    ws = _workspace(T, K, N, code, pool, s, workspace, x.device)
+    flags = ACCUMULATE_GRAD if accumulate else 0
+    _check(library().lora_mixed_backward_flagged(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), _ptr(s), s.shape[0],
+                                                 _ptr(dY), _ptr(xa_saved), _ptr(xa_valid), _ptr(dX), _ptr(dA),
+                                                 _ptr(dB), flags, _ptr(ws), ws.numel(), _stream_ptr(stream)))
     return dX, dA, dB
 
 

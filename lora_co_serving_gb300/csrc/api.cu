@@ -226,13 +226,19 @@ void f32_layout(const Problem& p, size_t base, F32Blob* fb) {
     std::vector<int32_t> tok(p.T, -1);
     std::vector<F32Seg> segs(p.segs.size());
     int64_t xo = 0;
+    int32_t n_train_seen = 0;
     for (size_t i = 0; i < p.segs.size(); ++i) {
         const auto& s = p.segs[i];
         for (int32_t t = s.start; t < s.start + s.len; ++t) tok[t] = s.adapter_id;
         F32Seg f{};
         f.start = s.start; f.len = s.len; f.adapter = s.adapter_id; f.is_train = s.is_train;
         f.xoff = -1;
-        if (s.is_train) { f.xoff = int32_t(xo); xo += (int64_t)s.len * p.rank[s.adapter_id]; }
+        f.order = -1;
+        if (s.is_train) {
+            f.xoff = int32_t(xo);
+            xo += (int64_t)s.len * p.rank[s.adapter_id];
+            f.order = n_train_seen++;
+        }
         segs[i] = f;
     }
     std::vector<AdapterRec> ad(p.n_adapters);
@@ -470,18 +476,25 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
     return LORA_OK;
 }
 
-int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
-                        const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, const void* dY,
-                        const void* xa_saved, void* dX, float* dA, float* dB, uint32_t flags, void* workspace,
-                        size_t ws_bytes, void* stream_) {
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+}  // extern "C"
+
+namespace {
+
+// The backward of lora_mixed_backward and lora_mixed_backward_flagged (xa_valid: device flag table or null).
+int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                  const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, const void* dY,
+                  const void* xa_saved, const int32_t* xa_valid, void* dX, float* dA, float* dB, uint32_t flags,
+                  void* workspace, size_t ws_bytes, cudaStream_t stream) {
     Problem p;
     std::string err;
     int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err);
     if (rc != LORA_OK) return fail(rc, err);
     if (flags & ~uint32_t(LORA_SAVE_XA | LORA_RECOMPUTE_XA | LORA_ACCUMULATE_GRAD | LORA_DEBUG_CHECKS))
         return fail(LORA_ERR_INVALID_ARG, "unknown flag bits");
-    const bool recompute = (xa_saved == nullptr) || (flags & LORA_RECOMPUTE_XA);
+    const bool per_segment = (xa_valid != nullptr);
+    if (per_segment && (xa_saved == nullptr || (flags & LORA_RECOMPUTE_XA)))
+        return fail(LORA_ERR_INVALID_ARG, "a flag table needs xa_saved and excludes LORA_RECOMPUTE_XA");
+    const bool recompute = !per_segment && ((xa_saved == nullptr) || (flags & LORA_RECOMPUTE_XA));
     const bool acc = (flags & LORA_ACCUMULATE_GRAD) != 0;
     if (p.n_train > 0) {
         if (!x || !Wt || !dY) return fail(LORA_ERR_INVALID_ARG, "x, Wt and dY must be non-NULL");
@@ -505,6 +518,9 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
         CUDA_TRY(cudaMemsetAsync(w + L.status, 0, 256, stream));
         rc = stage_copy(w + fb.tok, fb.bytes.data(), fb.bytes.size(), stream);
         if (rc) return rc;
+        if (per_segment)        // the call's view of the flag table, taken when the call reaches the GPU
+            CUDA_TRY(cudaMemcpyAsync(w + L.seg_flags, xa_valid, sizeof(int32_t) * p.n_train,
+                                     cudaMemcpyDeviceToDevice, stream));
         // adapter groups in order of first appearance by start (host arrays)
         std::vector<int32_t> g_ad, g_r;
         std::vector<float> g_s;
@@ -532,6 +548,7 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
         a.xa = reinterpret_cast<float*>(w + fb.xa);
         a.dyb = reinterpret_cast<float*>(w + fb.dyb);
         a.xa_saved = recompute ? nullptr : static_cast<const float*>(xa_saved);
+        a.seg_flags = per_segment ? reinterpret_cast<const int32_t*>(w + L.seg_flags) : nullptr;
         a.xa_elems = p.xa_elems;
         a.dY = static_cast<const float*>(dY);
         a.dX = static_cast<float*>(dX);
@@ -546,7 +563,7 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
     }
 
     Plan pl;
-    plan_backward(p, dX != nullptr, dA != nullptr, dB != nullptr, recompute, &pl);
+    plan_backward(p, dX != nullptr, dA != nullptr, dB != nullptr, recompute, &pl, per_segment);
     Layout L = layout_of(p, pl, true);
     rc = check_workspace(workspace, ws_bytes, L.total);
     if (rc) return rc;
@@ -595,13 +612,17 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
     P.K = K;
     P.N = N;
     P.accumulate = acc ? 1 : 0;
+    P.seg_flags = per_segment ? reinterpret_cast<const int32_t*>(ws + L.seg_flags) : nullptr;
 
     rc = begin_call(L, pl, workspace, blob.size(), blob.data(), stream);
     if (rc) return rc;
+    if (per_segment)            // the call's view of the flag table, taken when the call reaches the GPU
+        CUDA_TRY(cudaMemcpyAsync(ws + L.seg_flags, xa_valid, sizeof(int32_t) * p.n_train, cudaMemcpyDeviceToDevice,
+                                 stream));
     CUDA_TRY(trace(2, 0, stream));
     if (!recompute && dB)
         CUDA_TRY(xat_from_saved(xa_saved, reinterpret_cast<const TrainSeg*>(ws + L.tsegs), int32_t(pl.tsegs.size()),
-                                max_len, ws + L.xat, int32_t(Pcols), stream));
+                                max_len, ws + L.xat, int32_t(Pcols), P.seg_flags, stream));
     CUDA_TRY(launch_group(0, &P, ws, L, grid, stream));
     CUDA_TRY(trace(2, 1, stream));
     CUDA_TRY(trace(3, 0, stream));
@@ -609,6 +630,27 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
     CUDA_TRY(launch_group(2, &P, ws, L, grid, stream));
     CUDA_TRY(trace(3, 1, stream));
     return LORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                        const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, const void* dY,
+                        const void* xa_saved, void* dX, float* dA, float* dB, uint32_t flags, void* workspace,
+                        size_t ws_bytes, void* stream) {
+    return backward_impl(T, K, N, dt, x, Wt, pool, segs, n_segs, dY, xa_saved, nullptr, dX, dA, dB, flags, workspace,
+                         ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int lora_mixed_backward_flagged(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                                const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, const void* dY,
+                                const void* xa_saved, const int32_t* xa_valid, void* dX, float* dA, float* dB,
+                                uint32_t flags, void* workspace, size_t ws_bytes, void* stream) {
+    if (!xa_valid) return fail(LORA_ERR_INVALID_ARG, "xa_valid (device flag table) is NULL");
+    return backward_impl(T, K, N, dt, x, Wt, pool, segs, n_segs, dY, xa_saved, xa_valid, dX, dA, dB, flags,
+                         workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

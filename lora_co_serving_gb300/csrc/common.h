@@ -44,6 +44,8 @@ struct TileDesc {
     int32_t atom0;    // first entry of this tile in the atom-row tables (one entry per 8 LoRA columns)
     int32_t sh_c0;    // LoRA columns [sh_c0, sh_c1) hold this tile's own adapters (the shrink computes only
     int32_t sh_c1;    //   these; the pair's other columns of this tile's Z stay zero)
+    int32_t seg;      // backward tiles: fine-tuning segment (index in increasing start order); -1 otherwise
+    int32_t pad;
 };
 // Tiles come in pairs (2p, 2p+1) that share one chunk list, ordered [adapters only in the first tile |
 // adapters in both | adapters only in the second], so that the M = 256 main pass runs one pair per CTA pair
@@ -117,7 +119,8 @@ struct TrainSeg {     // fine-tuning segment; grouped by adapter, increasing sta
     int32_t group;
     int32_t xoff;     // element offset of the segment's [len, r] block in the saved-activation buffer
     int32_t r;
-    int32_t pad0, pad1;
+    int32_t order;    // index among the fine-tuning segments in increasing start order
+    int32_t pad1;
 };
 
 }  // namespace lora

@@ -268,6 +268,7 @@ void plan_forward(const Problem& p, Plan* out) {
         TileDesc t0{}, t1{};
         t0.a_row0 = w0; t1.a_row0 = w0 + kTileM;
         t0.tpos0 = t1.tpos0 = -1;
+        t0.seg = t1.seg = -1;
         add_pair(p, &pl, rows, row_ad, row_aux, t0, t1);
         t = w0 + 2 * kTileM;
     }
@@ -280,6 +281,7 @@ void plan_forward(const Problem& p, Plan* out) {
         t0.a_row0 = pl.n_gtiles * kTileM;
         t1.a_row0 = (pl.n_gtiles + 1) * kTileM;
         t0.tpos0 = t1.tpos0 = -1;
+        t0.seg = t1.seg = -1;
         add_pair(p, &pl, rows, row_ad, row_aux, t0, t1);
         pl.n_gtiles += 2;
     }
@@ -293,7 +295,8 @@ void plan_forward(const Problem& p, Plan* out) {
     add_main_items(&pl, kMainFwd, int32_t(cdiv(p.N, kBN)), nk);
 }
 
-void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out) {
+void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out,
+                   bool per_segment) {
     Plan& pl = *out;
     pl = Plan();
     pl.T = p.T;
@@ -332,7 +335,7 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
         gg.prow_b = int32_t(p.b_off[a] / p.N);
         gg.scale = p.scale[a];
         for (int32_t i : members[g])
-            pl.tsegs.push_back(TrainSeg{tr[i].start, tr[i].len, tpos_of[i], int32_t(g), xoff_of[i], gg.r, 0, 0});
+            pl.tsegs.push_back(TrainSeg{tr[i].start, tr[i].len, tpos_of[i], int32_t(g), xoff_of[i], gg.r, i, 0});
         pl.groups.push_back(gg);
     }
     // one pair of tiles per 256 rows of each fine-tuning segment
@@ -349,11 +352,12 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
             t1.a_row0 = tr[i].start + b + kTileM;
             t0.tpos0 = tpos_of[i] + b;
             t1.tpos0 = tpos_of[i] + b + kTileM;
+            t0.seg = t1.seg = int32_t(i);
             add_pair(p, &pl, rows, row_ad, nullptr, t0, t1);
         }
     }
     const bool need_dyb = want_dx || want_da;
-    const bool need_xa = want_db && recompute;
+    const bool need_xa = want_db && (recompute || per_segment);
     for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
         const TileDesc& td = pl.tiles[ti];
         if (td.sh_c1 <= td.sh_c0) continue;      // the empty second tile of a short segment's pair
@@ -438,6 +442,7 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     L.atoms_a = take(sizeof(int32_t) * pl.atoms_a.size());
     L.atoms_b = take(sizeof(int32_t) * pl.atoms_b.size());
     L.units = take(sizeof(ShrinkUnit) * pl.units.size());
+    L.seg_flags = take(sizeof(int32_t) * ((size_t)p.n_train + 1));
     for (int k = 0; k < 3; ++k) {
         L.items[k] = take(sizeof(WorkItem) * pl.items[k].size());
         L.cta_off[k] = take(sizeof(int32_t) * (std::max<size_t>(kMaxCtas, pl.items[k].size()) + 1));

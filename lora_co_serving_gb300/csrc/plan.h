@@ -60,7 +60,10 @@ struct Plan {
 };
 
 void plan_forward(const Problem& p, Plan* out);
-void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out);
+// recompute: x A of every fine-tuning tile is recomputed.  per_segment: the caller's device flag table decides
+// per segment (recompute items exist for every tile and are skipped on the device for segments flagged saved).
+void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out,
+                   bool per_segment = false);
 
 // Greedy list scheduling of the items (in order) onto G persistent CTAs by estimated cost.
 // off has G+1 entries; list holds item indices grouped by CTA, each CTA's in increasing order.
@@ -72,7 +75,7 @@ struct Layout {
     size_t status = 0;
     size_t counters = 0, zero_end = 0;   // [status, zero_end) is zeroed at the start of every call
     size_t tiles = 0, chunks = 0, rowmap = 0, rowchunk = 0, rowaux = 0, groups = 0, tsegs = 0;
-    size_t atoms_a = 0, atoms_b = 0, units = 0;
+    size_t atoms_a = 0, atoms_b = 0, units = 0, seg_flags = 0;
     size_t items[3] = {0, 0, 0}, cta_off[3] = {0, 0, 0}, cta_list[3] = {0, 0, 0};
     size_t plan_end = 0;
     size_t xg = 0, z = 0, xat = 0, dybt = 0, part = 0, part_main = 0;

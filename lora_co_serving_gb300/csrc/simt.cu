@@ -29,10 +29,13 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, int32_t k8, cons
     }
 }
 
-// xat[j, tpos0 + t] = xa_saved[xoff + t*r + j] for t < len, 0 for len <= t < roundup(len, 128)
+// xat[j, tpos0 + t] = xa_saved[xoff + t*r + j] for t < len, 0 for len <= t < roundup(len, 128); with a flag
+// table, only for the segments it marks as saved (the others are recomputed by the shrink)
 __global__ void xat_from_saved_kernel(const __nv_bfloat16* __restrict__ xa_saved, const TrainSeg* __restrict__ tsegs,
-                                      int32_t n_tsegs, __nv_bfloat16* __restrict__ xat, int32_t P) {
+                                      int32_t n_tsegs, __nv_bfloat16* __restrict__ xat, int32_t P,
+                                      const int32_t* __restrict__ seg_flags) {
     const TrainSeg s = tsegs[blockIdx.y];
+    if (seg_flags != nullptr && seg_flags[s.order] == 0) return;
     const int32_t span = (s.len + 127) / 128 * 128;
     for (int32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < span; t += gridDim.x * blockDim.x) {
         for (int32_t j = 0; j < s.r; ++j) {
@@ -92,9 +95,11 @@ __global__ void f32_forward_kernel(const float* __restrict__ x, const float* __r
 
 // copy xA of fine-tuning rows to / from the packed saved-activation layout
 __global__ void f32_xa_pack_kernel(float* __restrict__ xa, float* __restrict__ packed, const F32Seg* __restrict__ segs,
-                                   int32_t n_segs, const AdapterRec* __restrict__ ad, int32_t to_packed) {
+                                   int32_t n_segs, const AdapterRec* __restrict__ ad, int32_t to_packed,
+                                   const int32_t* __restrict__ seg_flags) {
     for (int32_t s = 0; s < n_segs; ++s) {
         if (!segs[s].is_train) continue;
+        if (seg_flags != nullptr && seg_flags[segs[s].order] == 0) continue;
         const int32_t r = ad[segs[s].adapter].r;
         const int64_t n = (int64_t)segs[s].len * r;
         for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -177,11 +182,11 @@ cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out
 }
 
 cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len, void* xat,
-                           int32_t P, cudaStream_t s) {
+                           int32_t P, const int32_t* seg_flags, cudaStream_t s) {
     if (n_tsegs <= 0) return cudaSuccess;
     dim3 grid((max_len + 127) / 128, n_tsegs);
     xat_from_saved_kernel<<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(xa_saved), tsegs, n_tsegs,
-                                               static_cast<__nv_bfloat16*>(xat), P);
+                                               static_cast<__nv_bfloat16*>(xat), P, seg_flags);
     return cudaGetLastError();
 }
 
@@ -191,17 +196,19 @@ cudaError_t f32_forward(const F32Args& a, cudaStream_t s) {
     f32_forward_kernel<<<grid_for((int64_t)a.T * a.N), 256, 0, s>>>(a.x, a.Wt, a.B, a.ad, a.tok_ad, a.xa, a.T, a.K,
                                                                      a.N, a.y);
     if (a.xa_save)
-        f32_xa_pack_kernel<<<grid_for(a.xa_elems), 256, 0, s>>>(a.xa, a.xa_save, a.segs, a.n_segs, a.ad, 1);
+        f32_xa_pack_kernel<<<grid_for(a.xa_elems), 256, 0, s>>>(a.xa, a.xa_save, a.segs, a.n_segs, a.ad, 1, nullptr);
     return cudaGetLastError();
 }
 
 cudaError_t f32_backward(const F32Args& a, cudaStream_t s) {
-    if (a.xa_saved)
-        f32_xa_pack_kernel<<<grid_for(a.xa_elems), 256, 0, s>>>(a.xa, const_cast<float*>(a.xa_saved), a.segs, a.n_segs,
-                                                                a.ad, 0);
-    else
+    // xA of the fine-tuning rows: recomputed, then (all, or the segments the flag table marks) taken from the
+    // saved copy instead
+    if (!a.xa_saved || a.seg_flags)
         f32_shrink_kernel<<<grid_for((int64_t)a.T * LORA_MAX_RANK), 256, 0, s>>>(a.x, a.A, a.ad, a.tok_ad, a.segs,
                                                                                    a.n_segs, a.K, a.xa, 1);
+    if (a.xa_saved)
+        f32_xa_pack_kernel<<<grid_for(a.xa_elems), 256, 0, s>>>(a.xa, const_cast<float*>(a.xa_saved), a.segs, a.n_segs,
+                                                                a.ad, 0, a.seg_flags);
     f32_dyb_kernel<<<grid_for((int64_t)a.train_tokens * LORA_MAX_RANK), 256, 0, s>>>(a.dY, a.B, a.ad, a.segs,
                                                                                        a.n_segs, a.N, a.dyb);
     if (a.dX)

@@ -19,7 +19,8 @@ struct AdapterRec {     // float32 path: one pool entry
 struct F32Seg {         // float32 path: one segment, increasing start
     int32_t start, len, adapter, is_train;
     int32_t xoff;       // fine-tuning segments: offset of the [len, r] block in the saved-activation buffer
-    int32_t pad0, pad1, pad2;
+    int32_t order;      // fine-tuning segments: index among them in increasing start order
+    int32_t pad1, pad2;
 };
 
 struct F32Args {
@@ -37,6 +38,7 @@ struct F32Args {
     float* y;
     float* xa_save;
     const float* xa_saved;
+    const int32_t* seg_flags;       // device snapshot of the per-segment flag table, or null
     int64_t xa_elems;
     const float* dY;
     float* dX;
@@ -54,7 +56,7 @@ struct F32Args {
 
 cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out, int32_t n_rows, cudaStream_t s);
 cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len, void* xat,
-                           int32_t P, cudaStream_t s);
+                           int32_t P, const int32_t* seg_flags, cudaStream_t s);
 cudaError_t f32_forward(const F32Args& a, cudaStream_t s);
 cudaError_t f32_backward(const F32Args& a, cudaStream_t s);
 

@@ -154,6 +154,12 @@ __device__ __forceinline__ bool acquire_stage(const Ring& ring, uint32_t bar_ful
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// An x A recompute item of a fine-tuning segment whose saved xA the flag table marks as usable: every role skips
+// it (no stage, no accumulator), so the three roles stay in step.
+__device__ __forceinline__ bool skipped_item(const KParams& P, const WorkItem& w) {
+    return w.kind == kShrinkXa && P.seg_flags != nullptr && P.seg_flags[P.tiles[w.tile].seg] != 0;
+}
+
 // --------------------------------------------------------------------------------------------- producer (warp 0)
 __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full, uint32_t bar_empty, int i0, int i1,
                              volatile int* abort_flag) {
@@ -161,6 +167,7 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
     Ring ring;
     for (int ii = i0; ii < i1; ++ii) {
         const WorkItem w = P.items[P.cta_list[ii]];
+        if (skipped_item(P, w)) continue;
         if (w.kind == kGradDb || w.kind == kGradDa) {
             // A: [128 of N or K] x 64 tokens, MN-major (two 64-wide boxes); B: r_pad rows of xA^T / dYB^T
             const GradGroup g = P.groups[w.tile];
@@ -209,6 +216,7 @@ __device__ void run_mma(const KParams& P, uint8_t* smem, uint32_t bar_full, uint
     uint32_t acc_phase = 0;
     for (int ii = i0; ii < i1; ++ii) {
         const WorkItem w = P.items[P.cta_list[ii]];
+        if (skipped_item(P, w)) continue;
         if (!wait_phase(bar_tempty + acc * 8, acc_phase ^ 1u, abort_flag, P.status)) return;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)acc * kBN;
@@ -330,6 +338,7 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
     uint32_t acc_phase = 0;
     for (int ii = i0; ii < i1; ++ii) {
         const WorkItem w = P.items[P.cta_list[ii]];
+        if (skipped_item(P, w)) continue;
         if (!wait_phase(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) return;
         tc_fence_after();
         const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);

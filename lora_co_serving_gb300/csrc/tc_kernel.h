@@ -40,6 +40,8 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     const int32_t* atoms_b;  // same for the B pool
     float* part;             // shrink items: fp32 partial sums, [columns][128 rows]
     float* part_main;        // split main items: fp32 partial tiles, [slot][CTA][256 columns][128 rows]
+    const int32_t* seg_flags;  // backward with a per-segment flag table: snapshot, nonzero = saved xA is used
+                               // (the segment's x A recompute items are skipped); null otherwise
     const ShrinkUnit* units; // shrink passes (splits of one pass share a unit)
     int32_t* counters;       // per unit and row quarter: splits finished (zeroed at the start of every call)
 
