@@ -14,6 +14,7 @@ import numpy as np
 
 import oracle
 from oracle import brute
+from oracle import sliced
 import workloads
 
 
@@ -285,6 +286,141 @@ def pin_sampled_columns(lib=None):
     assert np.array_equal(sX, dX[pick]), "row-sampled dX"
 
 
+def _tiny_sliced(seed):
+    """A tiny fp32 sliced projection: 2-3 slices of random widths, 1-3 adapters of rank 1-3."""
+    rng = np.random.default_rng(seed)
+    S = int(rng.integers(2, 4))
+    bounds = np.concatenate([[0], np.cumsum([int(rng.integers(2, 7)) for _ in range(S)])])
+    T = int(rng.integers(3, 8))
+    K = int(rng.integers(4, 10))
+    n_ad = int(rng.integers(1, 4))
+    rank = [int(rng.integers(1, 4)) for _ in range(n_ad)]
+    cuts = sorted(set([0, T] + list(rng.integers(1, T, size=int(rng.integers(0, 3))))))
+    segs = []
+    for i in range(len(cuts) - 1):
+        a = int(rng.integers(-1, n_ad))
+        segs.append((cuts[i], cuts[i + 1] - cuts[i], a, 1 if (a >= 0 and rng.random() < 0.6) else 0))
+    if not any(q[3] for q in segs):
+        segs[0] = (segs[0][0], segs[0][1], 0, 1)
+    scale = [float(rng.choice([0.5, 1.0, 2.0])) for _ in range(n_ad)]
+    return workloads.sliced(seed + 91, T, K, bounds, segs, rank, scale=scale, dtype="f32")
+
+
+def _block_diagonal(wl):
+    """The sliced pool restated as a plain pool of rank S*r_a: the same stacked A, and an up factor with slice i's
+    columns in rows [i r_a, (i+1) r_a) and zeros elsewhere (so x A_cat B_cat = sum over slices, each on its own
+    columns)."""
+    S = wl.n_slices
+    rank = wl.rank.astype(np.int64) * S
+    blocks, b_off, at = [], [], 0
+    for a in range(wl.n_adapters):
+        r = int(wl.rank[a])
+        brow = int(wl.b_off[a]) // wl.N
+        Bc = np.zeros((S * r, wl.N), np.float32)
+        for i in range(S):
+            c0, c1 = int(wl.bounds[i]), int(wl.bounds[i + 1])
+            Bc[i * r:(i + 1) * r, c0:c1] = wl.B.reshape(-1, wl.N)[brow:brow + r, c0:c1]
+        blocks.append(Bc.reshape(-1))
+        b_off.append(at)
+        at += S * r * wl.N
+    return rank.astype(np.int32), np.concatenate(blocks), np.asarray(b_off, np.int64)
+
+
+def pin_sliced_block_diagonal(lib=None, seeds=range(6)):
+    """A sliced projection equals one LoRA layer of rank S*r with a block-diagonal up factor."""
+    for sd in seeds:
+        wl = _tiny_sliced(sd)
+        rank_c, B_c, b_off_c = _block_diagonal(wl)
+        y = sliced.forward_wl(wl, lib=lib)
+        yc = oracle.forward(wl.x, wl.Wt, wl.A, B_c, wl.a_off, b_off_c, rank_c, wl.scale, wl.segs, lib=lib)
+        assert _rel(y, yc) <= 1e-12, ("sliced forward vs block diagonal", sd)
+        dX, dA, dB = sliced.backward_wl(wl, lib=lib)
+        cX, cA, cB = oracle.backward(wl.x, wl.Wt, wl.A, B_c, wl.a_off, b_off_c, rank_c, wl.scale, wl.segs, wl.dY,
+                                     lib=lib)
+        assert _rel(dX, cX) <= 1e-12, ("sliced dX", sd)
+        assert _rel(dA, cA) <= 1e-12, ("sliced dA", sd)
+        for a in range(wl.n_adapters):
+            r = int(wl.rank[a])
+            got = dB.reshape(-1, wl.N)[int(wl.b_off[a]) // wl.N:int(wl.b_off[a]) // wl.N + r]
+            full = cB[b_off_c[a]:b_off_c[a] + wl.n_slices * r * wl.N].reshape(wl.n_slices * r, wl.N)
+            for i in range(wl.n_slices):
+                c0, c1 = int(wl.bounds[i]), int(wl.bounds[i + 1])
+                assert _rel(got[:, c0:c1], full[i * r:(i + 1) * r, c0:c1]) <= 1e-12 or \
+                    (np.abs(full[i * r:(i + 1) * r, c0:c1]).max() == 0 and np.abs(got[:, c0:c1]).max() == 0), \
+                    ("sliced dB", sd, a, i)
+
+
+def pin_sliced_merged_weight(lib=None, seeds=range(6)):
+    """Per output column n of slice i, the token's merged weight is W[:, n] + s A_{a,i}^T B_a[:, n]."""
+    for sd in seeds:
+        wl = _tiny_sliced(sd + 50)
+        y = sliced.forward_wl(wl, lib=lib)
+        x = wl.x.astype(np.float64)
+        A2 = wl.A.reshape(-1, wl.K).astype(np.float64)
+        B2 = wl.B.reshape(-1, wl.N).astype(np.float64)
+        for st, ln, a, _ in wl.segs.tolist():
+            W = wl.Wt.astype(np.float64).T.copy()
+            if a >= 0:
+                r = int(wl.rank[a])
+                arow = int(wl.a_off[a]) // wl.K
+                brow = int(wl.b_off[a]) // wl.N
+                for n in range(wl.N):
+                    i = int(np.searchsorted(wl.bounds, n, side="right")) - 1
+                    for k in range(wl.K):
+                        W[k, n] += float(wl.scale[a]) * sum(A2[arow + i * r + j, k] * B2[brow + j, n]
+                                                            for j in range(r))
+            ref = x[st:st + ln] @ W
+            assert _rel(y[st:st + ln], ref) <= 1e-12, ("sliced merged weight", sd, st)
+
+
+def pin_sliced_finite_differences(lib=None, seeds=range(3)):
+    """Central differences of L = sum over training rows of dY*y for the sliced layer (exact: L is linear in every
+    single entry of x, A and B)."""
+    for sd in seeds:
+        wl = _tiny_sliced(sd + 200)
+        rows = wl.train_rows()
+        dX, dA, dB = sliced.backward_wl(wl, lib=lib)
+
+        def loss():
+            y = sliced.forward_wl(wl, lib=lib)
+            return float((y[rows] * wl.dY[rows].astype(np.float64)).sum())
+
+        def fd(arr, idx):
+            old = arr[idx]
+            arr[idx] = old + np.float32(1.0)
+            hp = float(arr[idx]) - float(old)
+            lp = loss()
+            arr[idx] = old - np.float32(1.0)
+            hm = float(old) - float(arr[idx])
+            lm = loss()
+            arr[idx] = old
+            return (lp - lm) / (hp + hm)
+
+        for i in range(wl.A.shape[0]):
+            g = fd(wl.A, i)
+            assert abs(g - dA[i]) <= 1e-9 * max(1.0, abs(dA[i])), ("sliced dA fd", sd, i, g, dA[i])
+        for i in range(wl.B.shape[0]):
+            g = fd(wl.B, i)
+            assert abs(g - dB[i]) <= 1e-9 * max(1.0, abs(dB[i])), ("sliced dB fd", sd, i, g, dB[i])
+        for p in range(rows.shape[0]):
+            for k in range(wl.K):
+                g = fd(wl.x, (int(rows[p]), k))
+                assert abs(g - dX[p, k]) <= 1e-9 * max(1.0, abs(dX[p, k])), ("sliced dX fd", sd, p, k)
+
+
+def pin_sliced_one_slice(lib=None):
+    """One slice covering every column is the plain layer."""
+    wl = workloads.config5(K=48, N=64, n_adapters=7, n_decode=10, prefill_tokens=30, len_lo=4, len_hi=20,
+                           train_len=12)
+    b = np.array([0, wl.N], np.int32)
+    y = sliced.forward(wl.x, wl.Wt, wl.A, wl.B, wl.a_off, wl.b_off, wl.rank, wl.scale, wl.segs, b, lib=lib)
+    assert np.array_equal(y, oracle.forward_wl(wl, lib=lib)), "one-slice forward"
+    g = sliced.backward(wl.x, wl.Wt, wl.A, wl.B, wl.a_off, wl.b_off, wl.rank, wl.scale, wl.segs, b, wl.dY, lib=lib)
+    for u, v in zip(g, oracle.backward_wl(wl, lib=lib)):
+        assert np.array_equal(u, v), "one-slice backward"
+
+
 ALL_PINS = [pin_brute_forward, pin_brute_backward, pin_merged_weight_config1, pin_zero_B, pin_finite_differences,
             pin_segment_order, pin_pool_order, pin_routing, pin_trainable_count, pin_accumulate,
-            pin_sampled_columns]
+            pin_sampled_columns, pin_sliced_block_diagonal, pin_sliced_merged_weight, pin_sliced_finite_differences,
+            pin_sliced_one_slice]

@@ -50,3 +50,37 @@ def test_mutant_is_caught(tmp_path, name, orig, bad):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, "no pin caught mutant " + name
+
+
+# Mistakes planted in the sliced-projection layer of the oracle (``oracle/sliced.py``), loaded as a separate module
+# from an edited copy; each must fail one of the sliced pins.
+SLICED_SRC = os.path.join(os.path.dirname(obuild.__file__), "sliced.py")
+SLICED_MUTANTS = [
+    ("slice_down_factor_fixed", "[base + i * r:base + (i + 1) * r]", "[base:base + r]"),
+    ("slice_up_columns_shifted", "reshape(-1, N)[brow:brow + r, c0:c1]", "reshape(-1, N)[brow:brow + r, 0:c1 - c0]"),
+    ("dx_last_slice_only", "dX = dXi if dX is None else dX + dXi", "dX = dXi"),
+    ("dA_into_slice_zero", "dA[base + i * r * K:base + (i + 1) * r * K] = dAi[ao[a]:ao[a] + r * K]",
+     "dA[base:base + r * K] += dAi[ao[a]:ao[a] + r * K]"),
+]
+SLICED_PINS = [P.pin_sliced_block_diagonal, P.pin_sliced_merged_weight, P.pin_sliced_finite_differences]
+
+
+@pytest.mark.parametrize("name,orig,bad", SLICED_MUTANTS, ids=[m[0] for m in SLICED_MUTANTS])
+def test_sliced_mutant_is_caught(tmp_path, monkeypatch, name, orig, bad):
+    import importlib.util
+    text = open(SLICED_SRC).read()
+    assert text.count(orig) == 1, "mutation anchor not unique: " + orig
+    path = tmp_path / "sliced_mutant.py"
+    path.write_text(text.replace(orig, bad))
+    spec = importlib.util.spec_from_file_location("oracle.sliced_mutant", str(path))
+    mod = importlib.util.module_from_spec(spec)
+    mod.__package__ = "oracle"
+    spec.loader.exec_module(mod)
+    monkeypatch.setattr(P, "sliced", mod)
+    caught = []
+    for pin in SLICED_PINS:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, "no pin caught sliced mutant " + name

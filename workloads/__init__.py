@@ -64,6 +64,11 @@ class Workload:
     backward: bool = False
     xa_mode: str = "recompute"     # "save" (forward keeps xA) or "recompute"
     meta: dict = field(default_factory=dict)
+    bounds: Optional[np.ndarray] = None   # sliced layers: [S+1] int32 output-column bounds of the slices
+
+    @property
+    def n_slices(self):
+        return 1 if self.bounds is None else int(self.bounds.shape[0]) - 1
 
     @property
     def n_adapters(self):
@@ -88,31 +93,33 @@ def _uniform(rng, shape, bound, dtype):
     return bf16_round(v) if dtype == "bf16" else v
 
 
-def _pool_offsets(rank, K, N):
+def _pool_offsets(rank, K, N, n_slices=1):
+    """Adapters back to back: adapter a holds n_slices * r_a rows of K in A and r_a rows of N in B."""
     rank = np.asarray(rank, dtype=np.int64)
     a_off = np.zeros(rank.shape[0], np.int64)
     b_off = np.zeros(rank.shape[0], np.int64)
     if rank.shape[0]:
-        a_off[1:] = np.cumsum(rank[:-1] * K)
+        a_off[1:] = np.cumsum(n_slices * rank[:-1] * K)
         b_off[1:] = np.cumsum(rank[:-1] * N)
     return a_off, b_off
 
 
 def _fill(name, rng, T, K, N, dtype, segs, rank, scale, *, want_dy, w_var=None, a_bound=None, b_var=0.02,
-          **kw):
+          bounds=None, **kw):
     """Draw W, A, B, x, dY in that order and assemble the workload."""
     rank = np.asarray(rank, dtype=np.int32)
-    a_off, b_off = _pool_offsets(rank, K, N)
+    S = 1 if bounds is None else len(bounds) - 1
+    a_off, b_off = _pool_offsets(rank, K, N, S)
     w_std = np.sqrt(1.0 / K if w_var is None else w_var)
     a_bound = 1.0 / np.sqrt(K) if a_bound is None else a_bound
     Wt = _normal(rng, (N, K), w_std, dtype)
-    A = _uniform(rng, (int(rank.sum()) * K,), a_bound, dtype)
+    A = _uniform(rng, (S * int(rank.sum()) * K,), a_bound, dtype)
     B = _normal(rng, (int(rank.sum()) * N,), np.sqrt(b_var), dtype)
     x = _normal(rng, (T, K), 1.0, dtype)
     dY = _normal(rng, (T, N), 1.0, dtype) if want_dy else None
     return Workload(name=name, T=T, K=K, N=N, dtype=dtype, segs=np.asarray(segs, np.int32).reshape(-1, 4),
                     rank=rank, scale=np.asarray(scale, np.float32), a_off=a_off, b_off=b_off, x=x, Wt=Wt, A=A,
-                    B=B, dY=dY, **kw)
+                    B=B, dY=dY, bounds=None if bounds is None else np.asarray(bounds, np.int32), **kw)
 
 
 def _draw_lengths(rng, total, lo, hi):
@@ -220,6 +227,18 @@ def custom(seed, T, K, N, segs, rank, scale=None, dtype="bf16", want_dy=True, **
     rank = list(rank)
     scale = [2.0] * len(rank) if scale is None else scale
     return _fill("custom_%dx%d_T%d" % (K, N, T), rng, T, K, N, dtype, segs, rank, scale, want_dy=want_dy, **kw)
+
+
+def sliced(seed, T, K, bounds, segs, rank, scale=None, dtype="bf16", want_dy=True, **kw):
+    """A fused projection of several slices (e.g. q|k|v over one input): output columns [bounds[i], bounds[i+1])
+    form slice i.  Adapter a holds one [r_a, K] down factor per slice, stacked in slice order in A, and one
+    [r_a, N] up factor in B whose columns of slice i are that slice's up factor."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rank = list(rank)
+    scale = [2.0] * len(rank) if scale is None else scale
+    N = int(bounds[-1])
+    return _fill("sliced_%dx%d_S%d_T%d" % (K, N, len(bounds) - 1, T), rng, T, K, N, dtype, segs, rank, scale,
+                 want_dy=want_dy, bounds=bounds, **kw)
 
 
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
