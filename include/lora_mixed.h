@@ -209,6 +209,48 @@ int lora_mixed_backward_flagged(int32_t T, int32_t K, int32_t N, lora_dtype_t dt
                                 const void* dY, const void* xa_saved, const int32_t* xa_valid, void* dX, float* dA,
                                 float* dB, uint32_t flags, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- Sliced (fused) projections ----
+ * A decoder layer applies one adapter to several projections of the same input: DeltaServe section 4.1 puts
+ * its fine-tuning adapter on every attention projection of Llama 3-8B, whose q, k and v projections all read
+ * the layer's normalised hidden state (and an MLP's gate and up projections share theirs).  A sliced call
+ * runs such projections as one layer over the concatenated weight: output columns [b_i, b_{i+1}) form slice
+ * i, and each slice is an ordinary LoRA linear layer on the shared x:
+ *
+ *     y[:, b_i:b_{i+1}] = x W_i + s_a (x A_{a,i}) B_{a,i}
+ *     dX = sum over slices of (dY_i W_i^T + s_a (dY_i B_{a,i}^T) A_{a,i}^T)       (dY_i = dY[:, b_i:b_{i+1}])
+ *
+ * Pool layout of a sliced call: adapter a's block in A stacks its down factors, slice i's [r_a, K] factor at
+ * rows [i r_a, (i+1) r_a) (n_slices * r_a rows from a_off[a]); its block in B is [r_a, N], whose columns
+ * [b_i, b_{i+1}) are slice i's up factor.  dA and dB are shaped like these pools.  The saved-activation
+ * buffer holds, per fine-tuning segment in increasing start order, a [len, n_slices * r_a] block: slice i's
+ * x A_{a,i} in columns [i r_a, (i+1) r_a).
+ * Limits: bf16 only; 1 <= n_slices <= LORA_MAX_SLICES; col_bounds[0] = 0 < col_bounds[1] < ... <
+ * col_bounds[n_slices] = N with the interior bounds multiples of 256.  A one-slice call is exactly the
+ * corresponding lora_mixed_* call; slices = NULL means one slice. */
+#define LORA_MAX_SLICES 4
+typedef struct lora_slices {
+    int32_t n_slices;
+    const int32_t* col_bounds;   /* HOST [n_slices + 1] */
+} lora_slices_t;
+
+/* lora_workspace_size / lora_xa_size for a sliced layer. */
+size_t lora_sliced_workspace_size(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool,
+                                  const lora_slices_t* slices, const lora_segment_t* segs /* HOST */,
+                                  int32_t n_segs);
+size_t lora_sliced_xa_size(lora_dtype_t dt, const lora_pool_t* pool, const lora_slices_t* slices,
+                           const lora_segment_t* segs /* HOST */, int32_t n_segs);
+
+/* lora_mixed_forward / lora_mixed_backward of a sliced layer (same arguments otherwise; validation errors
+ * for bad slices: LORA_ERR_INVALID_ARG, or LORA_ERR_DTYPE for a float32 call with more than one slice). */
+int lora_sliced_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                        const lora_pool_t* pool, const lora_slices_t* slices, const lora_segment_t* segs /* HOST */,
+                        int32_t n_segs, void* y, void* xa_save, uint32_t flags, void* workspace, size_t ws_bytes,
+                        void* stream);
+int lora_sliced_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                         const lora_pool_t* pool, const lora_slices_t* slices, const lora_segment_t* segs /* HOST */,
+                         int32_t n_segs, const void* dY, const void* xa_saved, void* dX, float* dA, float* dB,
+                         uint32_t flags, void* workspace, size_t ws_bytes, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* lora_last_error(void);
 

@@ -6,6 +6,8 @@ kernels.  PyTorch supplies device memory and streams.  The entry points mirror
 
     forward(x, Wt, pool, segs, ...)         -> y   (and the saved xA when asked)
     backward(x, Wt, pool, segs, dY, ...)    -> dX, dA, dB
+    sliced_forward / sliced_backward        -> the same for a fused projection of several slices
+                                               (q|k|v, gate|up) over one input
 
 ``segs`` is an int32 array (or list) of rows {start, len, adapter_id, is_train};
 ``Pool`` holds the stacked adapter factors (A blocks [r_a, K], B blocks [r_a, N])
@@ -21,7 +23,8 @@ import numpy as np
 
 from . import _build
 
-__all__ = ["Pool", "forward", "backward", "workspace_size", "xa_size", "workspace_status", "plan_describe",
+__all__ = ["Pool", "forward", "backward", "sliced_forward", "sliced_backward", "sliced_workspace_size",
+           "sliced_xa_size", "workspace_size", "xa_size", "workspace_status", "plan_describe",
            "LoraError", "LibraryNotBuilt", "library", "build", "SAVE_XA", "RECOMPUTE_XA", "ACCUMULATE_GRAD"]
 
 SAVE_XA = 1
@@ -36,7 +39,8 @@ ERRORS = {0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_SEGMENTS", -3:
 
 EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_mixed_backward", "lora_last_error",
             "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events", "lora_mixed_forward_static",
-            "lora_selftest_wait_timeout", "lora_adamw_step", "lora_mixed_backward_flagged"]
+            "lora_selftest_wait_timeout", "lora_adamw_step", "lora_mixed_backward_flagged",
+            "lora_sliced_workspace_size", "lora_sliced_xa_size", "lora_sliced_forward", "lora_sliced_backward"]
 
 
 class LoraError(RuntimeError):
@@ -58,6 +62,10 @@ class _Pool(ctypes.Structure):
     _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("a_off", ctypes.c_void_p),
                 ("b_off", ctypes.c_void_p), ("rank", ctypes.c_void_p), ("scale", ctypes.c_void_p),
                 ("n_adapters", ctypes.c_int32)]
+
+
+class _Slices(ctypes.Structure):
+    _fields_ = [("n_slices", ctypes.c_int32), ("col_bounds", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -104,6 +112,16 @@ def library(path=None):
     lib.lora_mixed_backward_flagged.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, I32, P, P, P, P, P, P,
                                                 ctypes.c_uint32, P, SZ, P]
     lib.lora_mixed_backward_flagged.restype = ctypes.c_int
+    lib.lora_sliced_workspace_size.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, I32]
+    lib.lora_sliced_workspace_size.restype = SZ
+    lib.lora_sliced_xa_size.argtypes = [ctypes.c_int, P, P, P, I32]
+    lib.lora_sliced_xa_size.restype = SZ
+    lib.lora_sliced_forward.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, P, I32, P, P, ctypes.c_uint32, P, SZ,
+                                        P]
+    lib.lora_sliced_forward.restype = ctypes.c_int
+    lib.lora_sliced_backward.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, P, I32, P, P, P, P, P,
+                                         ctypes.c_uint32, P, SZ, P]
+    lib.lora_sliced_backward.restype = ctypes.c_int
     if path is None:
         _LIB = lib
     return lib
@@ -314,3 +332,84 @@ def plan_describe(T, K, N, pool, segs, cap=None):
     _check(library().lora_plan_describe(T, K, N, pool.cptr(), _ptr(s), s.shape[0], ctypes.addressof(nt), _ptr(rows),
                                         _ptr(info), cap))
     return rows[:nt.value], info[:nt.value]
+
+
+class Slices:
+    """Output-column bounds of a sliced (fused) projection: slice i = columns [bounds[i], bounds[i+1])."""
+
+    def __init__(self, bounds):
+        self.bounds = np.ascontiguousarray(bounds, dtype=np.int32)
+        self._c = _Slices(self.bounds.shape[0] - 1, _ptr(self.bounds))
+
+    @property
+    def n_slices(self):
+        return int(self.bounds.shape[0]) - 1
+
+    def cptr(self):
+        return ctypes.addressof(self._c)
+
+
+def _slices(bounds):
+    return bounds if isinstance(bounds, Slices) else Slices(bounds)
+
+
+def sliced_workspace_size(T, K, N, dtype_code, pool, bounds, segs):
+    s = segments(segs)
+    sl = _slices(bounds)
+    n = library().lora_sliced_workspace_size(T, K, N, dtype_code, pool.cptr(), sl.cptr(), _ptr(s), s.shape[0])
+    if n == 0:
+        raise LoraError(-1, library().lora_last_error().decode())
+    return int(n)
+
+
+def sliced_xa_size(dtype_code, pool, bounds, segs):
+    s = segments(segs)
+    return int(library().lora_sliced_xa_size(dtype_code, pool.cptr(), _slices(bounds).cptr(), _ptr(s), s.shape[0]))
+
+
+def sliced_forward(x, Wt, pool, bounds, segs, y=None, xa_save=None, save_xa=False, workspace=None, stream=None):
+    """Forward of a sliced projection (Wt [N, K] = the slices' weights stacked; pool laid out per
+    lora_sliced_forward).  Returns y, or (y, xa_save) when save_xa is set."""
+    import torch
+    T, K = x.shape
+    N = Wt.shape[0]
+    code = _dtype_code(x)
+    s = segments(segs)
+    sl = _slices(bounds)
+    if y is None:
+        y = torch.empty((T, N), dtype=x.dtype, device=x.device)
+    if save_xa and xa_save is None:
+        n = sliced_xa_size(code, pool, sl, s) // x.element_size()
+        xa_save = torch.empty(max(n, 1), dtype=x.dtype, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(sliced_workspace_size(T, K, N, code, pool, sl, s), dtype=torch.uint8, device=x.device)
+    flags = SAVE_XA if save_xa else 0
+    _check(library().lora_sliced_forward(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), sl.cptr(), _ptr(s),
+                                         s.shape[0], _ptr(y), _ptr(xa_save), flags, _ptr(workspace),
+                                         workspace.numel(), _stream_ptr(stream)))
+    return (y, xa_save) if save_xa else y
+
+
+def sliced_backward(x, Wt, pool, bounds, segs, dY, xa_saved=None, dX=None, dA=None, dB=None, want_dx=True,
+                    want_grads=True, recompute=False, accumulate=False, workspace=None, stream=None):
+    """LoRA backward of a sliced projection; dX sums every slice's contribution.  Returns (dX, dA, dB)."""
+    import torch
+    T, K = x.shape
+    N = Wt.shape[0]
+    code = _dtype_code(x)
+    s = segments(segs)
+    sl = _slices(bounds)
+    if want_dx and dX is None:
+        dX = torch.zeros((T, K), dtype=x.dtype, device=x.device)
+    if want_grads and dA is None:
+        dA = torch.zeros(pool.A.numel(), dtype=torch.float32, device=x.device)
+    if want_grads and dB is None:
+        dB = torch.zeros(pool.B.numel(), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(sliced_workspace_size(T, K, N, code, pool, sl, s), dtype=torch.uint8, device=x.device)
+    flags = (RECOMPUTE_XA if recompute else 0) | (ACCUMULATE_GRAD if accumulate else 0)
+    _check(library().lora_sliced_backward(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), sl.cptr(), _ptr(s),
+                                          s.shape[0], _ptr(dY), _ptr(xa_saved), _ptr(dX) if want_dx else None,
+                                          _ptr(dA) if want_grads else None, _ptr(dB) if want_grads else None, flags,
+                                          _ptr(workspace), workspace.numel(), _stream_ptr(stream)))
+    return dX, dA, dB

@@ -300,11 +300,11 @@ extern "C" {
 
 const char* lora_last_error(void) { return g_err.c_str(); }
 
-size_t lora_workspace_size(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool,
-                           const lora_segment_t* segs, int32_t n_segs) {
+size_t lora_sliced_workspace_size(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool,
+                                  const lora_slices_t* slices, const lora_segment_t* segs, int32_t n_segs) {
     Problem p;
     std::string err;
-    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err);
+    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err, slices);
     if (rc != LORA_OK) { g_err = err; return 0; }
     Plan f, b;
     plan_forward(p, &f);
@@ -312,17 +312,32 @@ size_t lora_workspace_size(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, con
     return std::max(layout_of(p, f, false).total, layout_of(p, b, true).total);
 }
 
-size_t lora_xa_size(lora_dtype_t dt, const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs) {
+size_t lora_workspace_size(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool,
+                           const lora_segment_t* segs, int32_t n_segs) {
+    return lora_sliced_workspace_size(T, K, N, dt, pool, nullptr, segs, n_segs);
+}
+
+size_t lora_sliced_xa_size(lora_dtype_t dt, const lora_pool_t* pool, const lora_slices_t* slices,
+                           const lora_segment_t* segs, int32_t n_segs) {
     if (dt != LORA_BF16 && dt != LORA_F32) { g_err = "unknown dtype"; return 0; }
     if (!pool || (n_segs > 0 && !segs) || n_segs < 0) { g_err = "NULL pool or segments"; return 0; }
+    int32_t S = 1;
+    if (slices) {
+        if (slices->n_slices < 1 || slices->n_slices > LORA_MAX_SLICES) { g_err = "n_slices outside [1, 4]"; return 0; }
+        S = slices->n_slices;
+    }
     size_t elems = 0;
     for (int32_t i = 0; i < n_segs; ++i) {
         const lora_segment_t& s = segs[i];
         if (!s.is_train || s.len <= 0) continue;
         if (s.adapter_id < 0 || s.adapter_id >= pool->n_adapters || !pool->rank) { g_err = "bad adapter id"; return 0; }
-        elems += (size_t)s.len * (size_t)pool->rank[s.adapter_id];
+        elems += (size_t)s.len * (size_t)S * (size_t)pool->rank[s.adapter_id];
     }
     return elems * (dt == LORA_BF16 ? 2 : 4);
+}
+
+size_t lora_xa_size(lora_dtype_t dt, const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs) {
+    return lora_sliced_xa_size(dt, pool, nullptr, segs, n_segs);
 }
 
 int lora_set_trace_events(void* const* events) {
@@ -379,13 +394,17 @@ int lora_plan_describe(int32_t T, int32_t K, int32_t N, const lora_pool_t* pool,
     return LORA_OK;
 }
 
-int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
-                       const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, void* y, void* xa_save,
-                       uint32_t flags, void* workspace, size_t ws_bytes, void* stream_) {
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+}  // extern "C"
+
+namespace {
+
+// The forward of lora_mixed_forward and lora_sliced_forward (slices: NULL = one slice).
+int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                 const lora_pool_t* pool, const lora_slices_t* slices, const lora_segment_t* segs, int32_t n_segs,
+                 void* y, void* xa_save, uint32_t flags, void* workspace, size_t ws_bytes, cudaStream_t stream) {
     Problem p;
     std::string err;
-    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err);
+    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err, slices);
     if (rc != LORA_OK) return fail(rc, err);
     if (flags & ~uint32_t(LORA_SAVE_XA | LORA_RECOMPUTE_XA | LORA_ACCUMULATE_GRAD | LORA_DEBUG_CHECKS))
         return fail(LORA_ERR_INVALID_ARG, "unknown flag bits");
@@ -463,11 +482,9 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
     rc = begin_call(L, pl, workspace, blob.size(), blob.data(), stream);
     if (rc) return rc;
     CUDA_TRY(trace(0, 0, stream));
-    if (pl.n_gtiles > 0) {
-        const int32_t first = int32_t(pl.tiles.size()) - pl.n_gtiles;
-        CUDA_TRY(gather_rows(x, K, reinterpret_cast<const int32_t*>(ws + L.rowmap) + (size_t)first * kTileM,
+    if (pl.n_gtiles > 0)
+        CUDA_TRY(gather_rows(x, K, reinterpret_cast<const int32_t*>(ws + L.rowmap) + (size_t)pl.g_tile0 * kTileM,
                              ws + L.xg, pl.n_gtiles * kTileM, stream));
-    }
     CUDA_TRY(launch_group(0, &P, ws, L, grid, stream));
     CUDA_TRY(trace(0, 1, stream));
     CUDA_TRY(trace(1, 0, stream));
@@ -476,18 +493,14 @@ int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const v
     return LORA_OK;
 }
 
-}  // extern "C"
-
-namespace {
-
 // The backward of lora_mixed_backward and lora_mixed_backward_flagged (xa_valid: device flag table or null).
 int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
-                  const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, const void* dY,
-                  const void* xa_saved, const int32_t* xa_valid, void* dX, float* dA, float* dB, uint32_t flags,
-                  void* workspace, size_t ws_bytes, cudaStream_t stream) {
+                  const lora_pool_t* pool, const lora_slices_t* slices, const lora_segment_t* segs, int32_t n_segs,
+                  const void* dY, const void* xa_saved, const int32_t* xa_valid, void* dX, float* dA, float* dB,
+                  uint32_t flags, void* workspace, size_t ws_bytes, cudaStream_t stream) {
     Problem p;
     std::string err;
-    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err);
+    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err, slices);
     if (rc != LORA_OK) return fail(rc, err);
     if (flags & ~uint32_t(LORA_SAVE_XA | LORA_RECOMPUTE_XA | LORA_ACCUMULATE_GRAD | LORA_DEBUG_CHECKS))
         return fail(LORA_ERR_INVALID_ARG, "unknown flag bits");
@@ -585,8 +598,9 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
     if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    if (!encode_2d(&P.tm_xat, ws + L.xat, Pcols, LORA_MAX_RANK, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    if (!encode_2d(&P.tm_dybt, ws + L.dybt, Pcols, LORA_MAX_RANK, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    const uint64_t trows = (uint64_t)p.S * LORA_MAX_RANK;
+    if (!encode_2d(&P.tm_xat, ws + L.xat, Pcols, trows, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    if (!encode_2d(&P.tm_dybt, ws + L.dybt, Pcols, trows, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (pl.z_blocks > 0 &&
         !encode_2d(&P.tm_z, ws + L.z, 64, (uint64_t)pl.z_blocks * kTileM, 64, 64, 128, &err, false))
         return fail(LORA_ERR_CUDA, err);
@@ -636,12 +650,37 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
 
 extern "C" {
 
+int lora_mixed_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                       const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, void* y, void* xa_save,
+                       uint32_t flags, void* workspace, size_t ws_bytes, void* stream) {
+    return forward_impl(T, K, N, dt, x, Wt, pool, nullptr, segs, n_segs, y, xa_save, flags, workspace, ws_bytes,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int lora_sliced_forward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                        const lora_pool_t* pool, const lora_slices_t* slices, const lora_segment_t* segs,
+                        int32_t n_segs, void* y, void* xa_save, uint32_t flags, void* workspace, size_t ws_bytes,
+                        void* stream) {
+    if (!slices) return fail(LORA_ERR_INVALID_ARG, "slices is NULL");
+    return forward_impl(T, K, N, dt, x, Wt, pool, slices, segs, n_segs, y, xa_save, flags, workspace, ws_bytes,
+                        static_cast<cudaStream_t>(stream));
+}
+
 int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
                         const lora_pool_t* pool, const lora_segment_t* segs, int32_t n_segs, const void* dY,
                         const void* xa_saved, void* dX, float* dA, float* dB, uint32_t flags, void* workspace,
                         size_t ws_bytes, void* stream) {
-    return backward_impl(T, K, N, dt, x, Wt, pool, segs, n_segs, dY, xa_saved, nullptr, dX, dA, dB, flags, workspace,
-                         ws_bytes, static_cast<cudaStream_t>(stream));
+    return backward_impl(T, K, N, dt, x, Wt, pool, nullptr, segs, n_segs, dY, xa_saved, nullptr, dX, dA, dB, flags,
+                         workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int lora_sliced_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
+                         const lora_pool_t* pool, const lora_slices_t* slices, const lora_segment_t* segs,
+                         int32_t n_segs, const void* dY, const void* xa_saved, void* dX, float* dA, float* dB,
+                         uint32_t flags, void* workspace, size_t ws_bytes, void* stream) {
+    if (!slices) return fail(LORA_ERR_INVALID_ARG, "slices is NULL");
+    return backward_impl(T, K, N, dt, x, Wt, pool, slices, segs, n_segs, dY, xa_saved, nullptr, dX, dA, dB, flags,
+                         workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int lora_mixed_backward_flagged(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
@@ -649,7 +688,7 @@ int lora_mixed_backward_flagged(int32_t T, int32_t K, int32_t N, lora_dtype_t dt
                                 const void* xa_saved, const int32_t* xa_valid, void* dX, float* dA, float* dB,
                                 uint32_t flags, void* workspace, size_t ws_bytes, void* stream) {
     if (!xa_valid) return fail(LORA_ERR_INVALID_ARG, "xa_valid (device flag table) is NULL");
-    return backward_impl(T, K, N, dt, x, Wt, pool, segs, n_segs, dY, xa_saved, xa_valid, dX, dA, dB, flags,
+    return backward_impl(T, K, N, dt, x, Wt, pool, nullptr, segs, n_segs, dY, xa_saved, xa_valid, dX, dA, dB, flags,
                          workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 

@@ -45,11 +45,18 @@ struct TileDesc {
     int32_t sh_c0;    // LoRA columns [sh_c0, sh_c1) hold this tile's own adapters (the shrink computes only
     int32_t sh_c1;    //   these; the pair's other columns of this tile's Z stay zero)
     int32_t seg;      // backward tiles: fine-tuning segment (index in increasing start order); -1 otherwise
-    int32_t pad;
+    int32_t zstride;  // sliced layers: LoRA-column stride between the slices' copies of a chunk (0: one slice).
+                      //   A row keeps columns zcol + i*zstride + [0, r) of its chunk for every slice i.
 };
 // Tiles come in pairs (2p, 2p+1) that share one chunk list, ordered [adapters only in the first tile |
 // adapters in both | adapters only in the second], so that the M = 256 main pass runs one pair per CTA pair
 // and each tile's own adapters occupy one contiguous column range.
+//
+// Sliced layers (several projections of one input fused along N, e.g. q|k|v): slice i of adapter a has its own
+// down factor (rows [i r, (i+1) r) of a's A block) and the up factor is a's B block restricted to the slice's
+// output columns.  Forward tiles hold one region of LoRA columns per slice (stride zstride, a multiple of 64);
+// the main items of slice i's output columns use a copy of the tile whose Z starts at region i.  Backward tiles
+// (one adapter) hold the slices side by side, each padded to 16 columns.
 
 struct Chunk {
     int32_t adapter;
@@ -74,7 +81,7 @@ struct WorkItem {
     int32_t nsplit;   // main: number of K-splits of the output tile (1 = no split)
     int32_t split;    // main: index of this split
     int32_t counter;  // main, split: first of the 8 counters (2 CTAs x 4 row quarters) of the output tile
-    int32_t pad;
+    int32_t j0;       // grad: first row of the transposed xA / dYB buffer this item reads (the slice's rows)
 };
 
 // One shrink pass of one tile.  Its K-splits write fp32 partial sums; the last split to finish (counted per row
@@ -109,7 +116,7 @@ struct GradGroup {    // one fine-tuning adapter of a backward call
     int32_t nseg;
     int32_t prow_a, prow_b;
     float scale;
-    int32_t pad;
+    int32_t nslice;   // slices of the layer: the adapter's A block has nslice * r rows
 };
 
 struct TrainSeg {     // fine-tuning segment; grouped by adapter, increasing start within a group
@@ -118,7 +125,7 @@ struct TrainSeg {     // fine-tuning segment; grouped by adapter, increasing sta
     int32_t tpos0;    // first column in the transposed buffers (multiple of 128)
     int32_t group;
     int32_t xoff;     // element offset of the segment's [len, r] block in the saved-activation buffer
-    int32_t r;
+    int32_t r;        // width of that block (rank x slices)
     int32_t order;    // index among the fine-tuning segments in increasing start order
     int32_t pad1;
 };

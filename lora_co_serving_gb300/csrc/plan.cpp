@@ -14,7 +14,7 @@ static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool, const lora_segment_t* segs,
-             int32_t n_segs, Problem* out, std::string* err) {
+             int32_t n_segs, Problem* out, std::string* err, const lora_slices_t* slices) {
     if (dt != LORA_BF16 && dt != LORA_F32) { *err = "unknown dtype"; return LORA_ERR_DTYPE; }
     if (T < 0 || K <= 0 || N <= 0 || n_segs < 0) { *err = "T must be >= 0, K and N > 0, n_segs >= 0"; return LORA_ERR_INVALID_ARG; }
     if (dt == LORA_BF16 && ((K % 8) != 0 || (N % 8) != 0)) {
@@ -31,6 +31,25 @@ int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t
     Problem& p = *out;
     p = Problem();
     p.T = T; p.K = K; p.N = N; p.dt = dt;
+    p.bounds[0] = 0;
+    p.bounds[1] = N;
+    if (slices != nullptr) {
+        const int32_t S = slices->n_slices;
+        if (S < 1 || S > LORA_MAX_SLICES) { *err = "n_slices outside [1, 4]"; return LORA_ERR_INVALID_ARG; }
+        if (!slices->col_bounds) { *err = "slices->col_bounds is NULL"; return LORA_ERR_INVALID_ARG; }
+        const int32_t* b = slices->col_bounds;
+        if (b[0] != 0 || b[S] != N) { *err = "slice bounds must start at 0 and end at N"; return LORA_ERR_INVALID_ARG; }
+        for (int32_t i = 0; i < S; ++i) {
+            if (b[i + 1] <= b[i]) { *err = "slice bounds must increase strictly"; return LORA_ERR_INVALID_ARG; }
+            if (i > 0 && b[i] % kBN != 0) {
+                *err = "interior slice bounds must be multiples of 256";
+                return LORA_ERR_INVALID_ARG;
+            }
+        }
+        if (S > 1 && dt != LORA_BF16) { *err = "sliced layers need the bf16 path"; return LORA_ERR_DTYPE; }
+        p.S = S;
+        for (int32_t i = 0; i <= S; ++i) p.bounds[i] = b[i];
+    }
     p.n_adapters = pool->n_adapters;
     p.a_off = pool->a_off; p.b_off = pool->b_off; p.rank = pool->rank; p.scale = pool->scale;
     for (int32_t a = 0; a < pool->n_adapters; ++a) {
@@ -41,7 +60,7 @@ int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t
             *err = "adapter " + std::to_string(a) + ": a_off must be a non-negative multiple of K and b_off of N";
             return LORA_ERR_ADAPTER;
         }
-        p.rows_a = std::max<int64_t>(p.rows_a, ao / K + r);
+        p.rows_a = std::max<int64_t>(p.rows_a, ao / K + (int64_t)p.S * r);
         p.rows_b = std::max<int64_t>(p.rows_b, bo / N + r);
         if (p.rows_a > INT32_MAX || p.rows_b > INT32_MAX) { *err = "pool too large"; return LORA_ERR_LIMIT; }
     }
@@ -81,7 +100,7 @@ int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t
     for (const auto& s : p.segs) {
         if (s.is_train) {
             p.n_train++;
-            p.xa_elems += (int64_t)s.len * p.rank[s.adapter_id];
+            p.xa_elems += (int64_t)s.len * p.S * p.rank[s.adapter_id];
         }
     }
     if (p.n_train > kMaxTrainSegs) { *err = "more than 48 fine-tuning segments in one call"; return LORA_ERR_LIMIT; }
@@ -91,8 +110,14 @@ int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t
 
 // Append one pair of tiles.  rows / row_ad: 256 entries (token row and adapter per tile row, -1 = none);
 // t0, t1: the two tiles' descriptors with a_row0 / a_src / tpos0 filled in.
+//
+// LoRA-column layouts (chunks 16-aligned, one 8-row pool atom per 8 columns):
+//   one slice:           [chunk 0 | chunk 1 | ...]
+//   sliced, forward:     S regions of stride W = roundup(chunk columns, 64), region i = the chunks' slice-i
+//                        columns (down-factor rows of slice i; the up-factor rows are the same in every region)
+//   sliced, backward:    one adapter; its slices side by side, slice i at [i rp, i rp + r), rp = roundup(r, 16)
 static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int32_t* row_ad, const int32_t* row_aux,
-                     TileDesc t0, TileDesc t1) {
+                     TileDesc t0, TileDesc t1, bool backward) {
     std::vector<int32_t> A, B;
     for (int i = 0; i < kTileM; ++i) {
         if (row_ad[i] >= 0) A.push_back(row_ad[i]);
@@ -111,8 +136,9 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
     order.insert(order.end(), both.begin(), both.end());
     order.insert(order.end(), onlyB.begin(), onlyB.end());
 
+    const int32_t S = p.S;
+    const bool side_by_side = backward && S > 1;     // backward tiles hold one adapter
     const int32_t chunk0 = int32_t(pl->chunks.size());
-    const int32_t atom0 = int32_t(pl->atoms_a.size());
     int32_t zcol = 0, end_a = 0, start_b = 0;
     for (size_t c = 0; c < order.size(); ++c) {
         if (c == onlyA.size()) start_b = zcol;
@@ -125,17 +151,35 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
         ch.prow_b = int32_t(p.b_off[a] / p.N);
         ch.scale = p.scale[a];
         pl->chunks.push_back(ch);
-        // pool row of every 8-column atom; the padding of a chunk to 16 repeats its last atom, so every loaded
-        // row stays inside the adapter's own block
-        const int32_t last = ((ch.r + 7) / 8 - 1) * 8;
-        for (int32_t o = 0; o < pad16(ch.r); o += 8) {
-            pl->atoms_a.push_back(ch.prow_a + std::min(o, last));
-            pl->atoms_b.push_back(ch.prow_b + std::min(o, last));
-        }
-        zcol += pad16(ch.r);
+        zcol += side_by_side ? S * pad16(ch.r) : pad16(ch.r);
         if (c + 1 == onlyA.size() + both.size()) end_a = zcol;
     }
     if (onlyA.size() == order.size()) start_b = zcol;
+    // pool row of every 8-column atom; the padding of a chunk to 16 repeats its last atom, so every loaded row
+    // stays inside the adapter's own block (sliced: the slice's own rows or the next slice's)
+    const int32_t atom0 = int32_t(pl->atoms_a.size());
+    const int32_t n_reg = (S > 1 && !side_by_side) ? S : 1;
+    const int32_t W = (n_reg > 1) ? int32_t(cdiv(zcol, kBK) * kBK) : zcol;
+    for (int32_t reg = 0; reg < n_reg; ++reg) {
+        for (size_t c = 0; c < order.size(); ++c) {
+            const Chunk& ch = pl->chunks[chunk0 + c];
+            const int32_t last = ((ch.r + 7) / 8 - 1) * 8;
+            const int32_t nsl = side_by_side ? S : 1;
+            for (int32_t i = 0; i < nsl; ++i) {
+                const int32_t sl = side_by_side ? i : reg;      // slice whose down-factor rows these columns hold
+                for (int32_t o = 0; o < pad16(ch.r); o += 8) {
+                    pl->atoms_a.push_back(ch.prow_a + sl * ch.r + std::min(o, last));
+                    pl->atoms_b.push_back(ch.prow_b + std::min(o, last));
+                }
+            }
+        }
+        for (int32_t o = zcol; o < W; o += 8) {     // region padding: any in-pool row (its columns are masked)
+            pl->atoms_a.push_back(pl->atoms_a.back());
+            pl->atoms_b.push_back(pl->atoms_b.back());
+        }
+    }
+    const int32_t zstride = (S == 1) ? 0 : (side_by_side ? 0 : W);
+    const int32_t z_cols = n_reg * W;
     TileDesc* td[2] = {&t0, &t1};
     for (int h = 0; h < 2; ++h) {
         td[h]->chunk0 = chunk0;
@@ -143,8 +187,14 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
         td[h]->ext_k = zcol;
         td[h]->atom0 = atom0;
         td[h]->z_blk0 = int32_t(pl->z_blocks);
-        pl->z_blocks += cdiv(zcol, kBK);
+        td[h]->zstride = zstride;
+        pl->z_blocks += cdiv(z_cols, kBK);
     }
+    if (side_by_side) {
+        // the mask of a backward sliced tile: slice i of the chunk at columns [i rp, i rp + r)
+        t0.zstride = t1.zstride = order.empty() ? 0 : pad16(pl->chunks[chunk0].r);
+    }
+    // the shrink columns of each tile (region 0's; a forward sliced tile repeats them in every region)
     t0.sh_c0 = 0;
     t0.sh_c1 = A.empty() ? 0 : end_a;
     t1.sh_c0 = B.empty() ? zcol : start_b;
@@ -162,7 +212,9 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
 }
 
 // Shrink items of one pass, split along the reduction at boundaries that depend on the k-block count alone.
-static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t mma_n, int32_t nk) {
+// kb_first: first k-block of the reduction (a slice's output columns, for the backward shrink over N).
+static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t mma_n, int32_t nk,
+                       int32_t kb_first = 0) {
     const int32_t nsplit = std::max<int32_t>(1, int32_t(cdiv(nk, shrink_split_kb(pl->T))));
     ShrinkUnit u{};
     u.kind = kind; u.tile = tile; u.n0 = n0; u.mma_n = mma_n; u.nsplit = nsplit;
@@ -172,6 +224,7 @@ static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t
         w.kind = kind; w.tile = tile; w.n0 = n0; w.mma_n = mma_n;
         w.kb0 = int32_t((int64_t)s * nk / nsplit);
         w.nk = int32_t((int64_t)(s + 1) * nk / nsplit) - w.kb0;
+        w.kb0 += kb_first;
         w.part = u.part0 + s * mma_n;
         w.n_ext = int32_t(pl->units.size());    // shrink items carry their unit index here
         pl->items[0].push_back(w);
@@ -181,9 +234,10 @@ static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t
 }
 
 // Main items of the M = 256 pass: one per (tile pair, 256 output columns), bands of kBandTiles tiles sweeping all
-// output columns before the next band (L2 reuse of the band's rows).
-static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk) {
-    const size_t n_pairs = pl->tiles.size() / 2;
+// output columns before the next band (L2 reuse of the band's rows).  tile_of(q, nt): first tile of the pair
+// that output tile (pair q, column tile nt) reads (a sliced forward reads the copy of its slice).
+template <class TileOf>
+static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk, size_t n_pairs, TileOf tile_of) {
     const size_t band = kBandTiles / 2;
     // Few output tiles: split their dense K loop (the LoRA K-steps go with the last split).  Backward only:
     // a fine-tuning tile holds one adapter at LoRA column 0, so the split leaves every row's summation order
@@ -201,12 +255,12 @@ static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk) {
                 for (int32_t sp = 0; sp < nsplit; ++sp) {
                     WorkItem w{};
                     w.kind = kind;
-                    w.tile = int32_t(2 * q);
+                    w.tile = tile_of(q, nt);
                     w.n0 = nt * kBN;
                     w.kb0 = int32_t((int64_t)sp * nk / nsplit);
                     w.nk = int32_t((int64_t)(sp + 1) * nk / nsplit) - w.kb0;
                     w.mma_n = kBN;
-                    w.n_ext = (sp == nsplit - 1) ? int32_t(cdiv(pl->tiles[2 * q].ext_k, kBK)) : 0;
+                    w.n_ext = (sp == nsplit - 1) ? int32_t(cdiv(pl->tiles[w.tile].ext_k, kBK)) : 0;
                     w.nsplit = nsplit;
                     w.split = sp;
                     w.part = slot0;
@@ -229,7 +283,7 @@ void plan_forward(const Problem& p, Plan* out) {
     std::vector<int64_t> seg_xoff(p.segs.size(), -1);
     int64_t xo = 0;
     for (size_t i = 0; i < p.segs.size(); ++i)
-        if (p.segs[i].is_train) { seg_xoff[i] = xo; xo += (int64_t)p.segs[i].len * p.rank[p.segs[i].adapter_id]; }
+        if (p.segs[i].is_train) { seg_xoff[i] = xo; xo += (int64_t)p.segs[i].len * p.S * p.rank[p.segs[i].adapter_id]; }
 
     // classify rows: long (windowed) or short (gathered)
     std::vector<int32_t> row_seg(p.T);
@@ -254,7 +308,7 @@ void plan_forward(const Problem& p, Plan* out) {
             const auto& s = p.segs[row_seg[t]];
             row_ad[i] = s.adapter_id;
             if (s.is_train)
-                row_aux[i] = int32_t(seg_xoff[row_seg[t]] + (int64_t)(t - s.start) * p.rank[s.adapter_id]);
+                row_aux[i] = int32_t(seg_xoff[row_seg[t]] + (int64_t)(t - s.start) * p.S * p.rank[s.adapter_id]);
         }
     };
     // 256-row windows over the long rows
@@ -269,11 +323,12 @@ void plan_forward(const Problem& p, Plan* out) {
         t0.a_row0 = w0; t1.a_row0 = w0 + kTileM;
         t0.tpos0 = t1.tpos0 = -1;
         t0.seg = t1.seg = -1;
-        add_pair(p, &pl, rows, row_ad, row_aux, t0, t1);
+        add_pair(p, &pl, rows, row_ad, row_aux, t0, t1, false);
         t = w0 + 2 * kTileM;
     }
     // gathered pairs: short rows sorted by (adapter, row)
     std::sort(gathered.begin(), gathered.end());
+    pl.g_tile0 = int32_t(pl.tiles.size());
     for (size_t g0 = 0; g0 < gathered.size(); g0 += 2 * kTileM) {
         for (int i = 0; i < 2 * kTileM; ++i) fill(i, (g0 + i < gathered.size()) ? gathered[g0 + i].second : -1);
         TileDesc t0{}, t1{};
@@ -282,17 +337,37 @@ void plan_forward(const Problem& p, Plan* out) {
         t1.a_row0 = (pl.n_gtiles + 1) * kTileM;
         t0.tpos0 = t1.tpos0 = -1;
         t0.seg = t1.seg = -1;
-        add_pair(p, &pl, rows, row_ad, row_aux, t0, t1);
+        add_pair(p, &pl, rows, row_ad, row_aux, t0, t1, false);
         pl.n_gtiles += 2;
     }
-    // items: shrink passes, then main items banded for L2 reuse
+    // items: shrink passes (per slice region), then main items banded for L2 reuse
     const int32_t nk = int32_t(cdiv(p.K, kBK));
-    for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
+    const size_t n_orig = pl.tiles.size();
+    for (size_t ti = 0; ti < n_orig; ++ti) {
         const TileDesc& td = pl.tiles[ti];
-        for (int32_t c0 = td.sh_c0; c0 < td.sh_c1; c0 += kPassCols)
-            add_shrink(&pl, kShrinkFwd, int32_t(ti), c0, std::min(kPassCols, td.sh_c1 - c0), nk);
+        for (int32_t reg = 0; reg < p.S; ++reg) {
+            const int32_t base = reg * td.zstride;
+            for (int32_t c0 = base + td.sh_c0; c0 < base + td.sh_c1; c0 += kPassCols)
+                add_shrink(&pl, kShrinkFwd, int32_t(ti), c0, std::min(kPassCols, base + td.sh_c1 - c0), nk);
+        }
     }
-    add_main_items(&pl, kMainFwd, int32_t(cdiv(p.N, kBN)), nk);
+    // sliced: one copy of every tile per further slice, its Z starting at that slice's region
+    for (int32_t reg = 1; reg < p.S; ++reg)
+        for (size_t ti = 0; ti < n_orig; ++ti) {
+            TileDesc c = pl.tiles[ti];
+            c.z_blk0 += reg * (c.zstride / kBK);
+            c.sh_c0 = c.sh_c1 = 0;
+            pl.tiles.push_back(c);
+            for (int i = 0; i < kTileM; ++i) {
+                pl.rowmap.push_back(pl.rowmap[ti * kTileM + i]);
+                pl.rowchunk.push_back(pl.rowchunk[ti * kTileM + i]);
+                pl.rowaux.push_back(pl.rowaux[ti * kTileM + i]);
+            }
+        }
+    add_main_items(&pl, kMainFwd, int32_t(cdiv(p.N, kBN)), nk, n_orig / 2, [&](size_t q, int32_t nt) {
+        const int32_t reg = p.slice_of_col(nt * kBN);
+        return int32_t(reg * n_orig + 2 * q);
+    });
 }
 
 void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out,
@@ -321,7 +396,7 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
         tpos_of[i] = int32_t(tpos);
         tpos += cdiv(tr[i].len, 2 * kTileM) * 2 * kTileM;
         xoff_of[i] = int32_t(xo);
-        xo += (int64_t)tr[i].len * p.rank[tr[i].adapter_id];
+        xo += (int64_t)tr[i].len * p.S * p.rank[tr[i].adapter_id];
     }
     pl.tcols = tpos;
     for (size_t g = 0; g < members.size(); ++g) {
@@ -334,8 +409,9 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
         gg.prow_a = int32_t(p.a_off[a] / p.K);
         gg.prow_b = int32_t(p.b_off[a] / p.N);
         gg.scale = p.scale[a];
+        gg.nslice = p.S;
         for (int32_t i : members[g])
-            pl.tsegs.push_back(TrainSeg{tr[i].start, tr[i].len, tpos_of[i], int32_t(g), xoff_of[i], gg.r, i, 0});
+            pl.tsegs.push_back(TrainSeg{tr[i].start, tr[i].len, tpos_of[i], int32_t(g), xoff_of[i], p.S * gg.r, i, 0});
         pl.groups.push_back(gg);
     }
     // one pair of tiles per 256 rows of each fine-tuning segment
@@ -353,7 +429,7 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
             t0.tpos0 = tpos_of[i] + b;
             t1.tpos0 = tpos_of[i] + b + kTileM;
             t0.seg = t1.seg = int32_t(i);
-            add_pair(p, &pl, rows, row_ad, nullptr, t0, t1);
+            add_pair(p, &pl, rows, row_ad, nullptr, t0, t1, true);
         }
     }
     const bool need_dyb = want_dx || want_da;
@@ -361,25 +437,46 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
     for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
         const TileDesc& td = pl.tiles[ti];
         if (td.sh_c1 <= td.sh_c0) continue;      // the empty second tile of a short segment's pair
-        if (need_dyb) add_shrink(&pl, kShrinkDyb, int32_t(ti), td.sh_c0, td.sh_c1 - td.sh_c0, int32_t(cdiv(p.N, kBK)));
-        if (need_xa) add_shrink(&pl, kShrinkXa, int32_t(ti), td.sh_c0, td.sh_c1 - td.sh_c0, int32_t(cdiv(p.K, kBK)));
+        if (need_dyb) {
+            if (p.S == 1) {
+                add_shrink(&pl, kShrinkDyb, int32_t(ti), td.sh_c0, td.sh_c1 - td.sh_c0, int32_t(cdiv(p.N, kBK)));
+            } else {
+                // slice i: dY's slice-i columns against the up factor's slice-i columns, into LoRA columns
+                // [i rp, (i+1) rp)
+                for (int32_t i = 0; i < p.S; ++i) {
+                    const int32_t kb_a = p.bounds[i] / kBK, kb_b = int32_t(cdiv(p.bounds[i + 1], kBK));
+                    add_shrink(&pl, kShrinkDyb, int32_t(ti), i * td.zstride, td.zstride, kb_b - kb_a, kb_a);
+                }
+            }
+        }
+        if (need_xa)
+            for (int32_t c0 = td.sh_c0; c0 < td.sh_c1; c0 += kPassCols)
+                add_shrink(&pl, kShrinkXa, int32_t(ti), c0, std::min(kPassCols, td.sh_c1 - c0), int32_t(cdiv(p.K, kBK)));
     }
-    if (want_dx) add_main_items(&pl, kMainDx, int32_t(cdiv(p.K, kBN)), int32_t(cdiv(p.N, kBK)));
+    if (want_dx)
+        add_main_items(&pl, kMainDx, int32_t(cdiv(p.K, kBN)), int32_t(cdiv(p.N, kBK)), pl.tiles.size() / 2,
+                       [](size_t q, int32_t) { return int32_t(2 * q); });
     for (size_t g = 0; g < pl.groups.size(); ++g) {
+        const GradGroup& gg = pl.groups[g];
         int32_t kb = 0;
-        for (int32_t q = 0; q < pl.groups[g].nseg; ++q) kb += int32_t(cdiv(pl.tsegs[pl.groups[g].seg0 + q].len, kBK));
+        for (int32_t q = 0; q < gg.nseg; ++q) kb += int32_t(cdiv(pl.tsegs[gg.seg0 + q].len, kBK));
         if (want_db)
-            for (int32_t m0 = 0; m0 < p.N; m0 += kTileM) {
-                WorkItem w{};
-                w.kind = kGradDb; w.tile = int32_t(g); w.n0 = m0; w.nk = kb; w.mma_n = pad16(pl.groups[g].r);
-                pl.items[2].push_back(w);
-            }
+            for (int32_t i = 0; i < p.S; ++i)              // slice i's columns of dB read slice i's rows of xA^T
+                for (int32_t m0 = p.bounds[i]; m0 < p.bounds[i + 1]; m0 += kTileM) {
+                    WorkItem w{};
+                    w.kind = kGradDb; w.tile = int32_t(g); w.n0 = m0; w.nk = kb; w.mma_n = pad16(gg.r);
+                    w.j0 = i * gg.r;
+                    pl.items[2].push_back(w);
+                }
         if (want_da)
-            for (int32_t m0 = 0; m0 < p.K; m0 += kTileM) {
-                WorkItem w{};
-                w.kind = kGradDa; w.tile = int32_t(g); w.n0 = m0; w.nk = kb; w.mma_n = pad16(pl.groups[g].r);
-                pl.items[2].push_back(w);
-            }
+            for (int32_t m0 = 0; m0 < p.K; m0 += kTileM)
+                for (int32_t j0 = 0; j0 < p.S * gg.r; j0 += kPassCols) {   // all slices' rows of the A block
+                    WorkItem w{};
+                    w.kind = kGradDa; w.tile = int32_t(g); w.n0 = m0; w.nk = kb;
+                    w.mma_n = std::min(kPassCols, pad16(p.S * gg.r - j0));
+                    w.j0 = j0;
+                    pl.items[2].push_back(w);
+                }
     }
 }
 
@@ -455,8 +552,8 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
         L.part = take((size_t)pl.part_cols * kTileM * sizeof(float));
         L.part_main = take((size_t)pl.main_slots * 2 * kMainPartialFloats * sizeof(float));
         if (backward) {
-            L.xat = take((size_t)LORA_MAX_RANK * pl.tcols * 2);
-            L.dybt = take((size_t)LORA_MAX_RANK * pl.tcols * 2);
+            L.xat = take((size_t)p.S * LORA_MAX_RANK * pl.tcols * 2);
+            L.dybt = take((size_t)p.S * LORA_MAX_RANK * pl.tcols * 2);
         }
     } else {
         L.simt = take(simt_scratch_bytes(p));

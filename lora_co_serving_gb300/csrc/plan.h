@@ -32,11 +32,19 @@ struct Problem {
     int64_t rows_a = 0, rows_b = 0;     // row extents of the pools viewed as [rows, K] and [rows, N]
     int64_t xa_elems = 0;               // elements of the saved-activation buffer
     int32_t n_train = 0;
+    int32_t S = 1;                      // slices of a fused layer; slice i = output columns [bounds[i], bounds[i+1])
+    int32_t bounds[LORA_MAX_SLICES + 1] = {0, 0, 0, 0, 0};
+    int32_t slice_of_col(int32_t n) const {
+        int32_t i = 0;
+        while (i + 1 < S && n >= bounds[i + 1]) ++i;
+        return i;
+    }
 };
 
 // Host validation of every argument that does not need the GPU.  Returns LORA_OK or a LORA_ERR_* code.
+// slices may be NULL (one slice).
 int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool, const lora_segment_t* segs,
-             int32_t n_segs, Problem* out, std::string* err);
+             int32_t n_segs, Problem* out, std::string* err, const lora_slices_t* slices = nullptr);
 
 struct Plan {
     std::vector<TileDesc> tiles;
@@ -51,6 +59,7 @@ struct Plan {
     std::vector<GradGroup> groups;
     std::vector<TrainSeg> tsegs;
     int32_t n_gtiles = 0;            // forward: tiles of the gathered buffer
+    int32_t g_tile0 = 0;             // forward: index of the first gathered tile (they are consecutive)
     int64_t z_blocks = 0;
     int64_t tcols = 0;               // backward: columns of the transposed xA / dYB buffers
     int64_t part_cols = 0;           // columns (of 128 fp32 each) of the shrink partial-sum buffer

@@ -182,7 +182,7 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
                     const uint32_t full = bar_full + ring.stage * 8;
                     const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
                     if (lane < 2) tma_load_2d(sa + lane * 8192, ma, w.n0 + 64 * lane, b * kBK, full);
-                    if (lane < natoms) tma_load_2d(sb + lane * 1024, mb, s.tpos0 + b * kBK, lane * 8, full);
+                    if (lane < natoms) tma_load_2d(sb + lane * 1024, mb, s.tpos0 + b * kBK, w.j0 + lane * 8, full);
                     ring.next();
                 }
             }
@@ -268,36 +268,42 @@ __device__ __forceinline__ void ld32_cols(uint32_t taddr, float (&v)[32]) {
 // Finalize of one tile row of a shrink pass: keep the row's own adapter columns (everything else is zero) and
 // write Z = bf16(s_a * xA) into the 128x64 shared-memory image the main pass bulk-loads, the unscaled xA of a
 // fine-tuning row into xa_save (forward), and the transposed copy xA^T / dYB^T (backward; zero past the segment).
+// Sliced layers: the chunk repeats every td.zstride columns, once per slice; its copy in region i holds slice
+// i's values, which land at columns [i r, (i+1) r) of the saved / transposed layouts.
 struct ShrinkRowOut {
     const KParams& P;
     const ShrinkUnit& u;
     int row;
     TileDesc td;
-    int32_t rc, zc0, zr, save_off, t_r;
+    int32_t rc, zc0, zr, save_off;
     float s;
+    bool live;
     __nv_bfloat16* tdst;
 
     __device__ ShrinkRowOut(const KParams& P_, const ShrinkUnit& u_, int row_) : P(P_), u(u_), row(row_) {
         td = P.tiles[u.tile];
         rc = P.rowchunk[u.tile * kTileM + row];
+        tdst = (u.kind == kShrinkDyb) ? P.dybt : (u.kind == kShrinkXa) ? P.xat : nullptr;
+        live = rc >= 0;
+        // backward tiles hold one adapter (at column 0): its columns are written for every row of the tile
+        const int32_t ci = tdst ? td.chunk0 : rc;
         zc0 = 0; zr = 0; s = 0.f;
-        if (rc >= 0) {
-            const Chunk ch = P.chunks[rc];
+        if (ci >= 0 && (!tdst || td.nchunk > 0)) {
+            const Chunk ch = P.chunks[ci];
             zc0 = ch.zcol; zr = ch.r; s = ch.scale;
         }
         save_off = (u.kind == kShrinkFwd && P.xa_save != nullptr) ? P.rowaux[u.tile * kTileM + row] : -1;
-        tdst = (u.kind == kShrinkDyb) ? P.dybt : (u.kind == kShrinkXa) ? P.xat : nullptr;
-        t_r = tdst ? P.chunks[td.chunk0].r : 0;    // backward tiles hold one adapter, at column 0
     }
 
-    // columns [c, c+16) of the pass
+    // columns [c, c+16) of the pass (all in one slice region: regions and chunks are 16-aligned)
     __device__ void put16(int c, const float (&acc)[16]) {
+        const int d0 = u.n0 + c - zc0;
+        const int reg = (td.zstride > 0 && d0 >= 0) ? d0 / td.zstride : 0;
+        const int j0 = d0 - reg * td.zstride;        // column within the chunk's copy in region `reg`
+        const int p0 = reg * zr + j0;                // the same column in the saved / transposed layouts
         float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int zc = u.n0 + c + i;
-            v[i] = (rc >= 0 && zc >= zc0 && zc < zc0 + zr) ? acc[i] : 0.f;
-        }
+        for (int i = 0; i < 16; ++i) v[i] = (live && d0 >= 0 && j0 + i < zr) ? acc[i] : 0.f;
         if (u.kind != kShrinkXa) {
             const int zc = u.n0 + c;
             uint8_t* blk = P.zout + (size_t)(td.z_blk0 + zc / kBK) * kZBlockBytes + row * 128;
@@ -312,19 +318,16 @@ struct ShrinkRowOut {
                 *reinterpret_cast<uint4*>(blk + chunk16 * 16) = q;
             }
         }
+        if (d0 < 0) return;
         if (save_off >= 0) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int j = u.n0 + c + i - zc0;
-                if (j >= 0 && j < zr) P.xa_save[save_off + j] = __float2bfloat16_rn(v[i]);
-            }
+            for (int i = 0; i < 16; ++i)
+                if (j0 + i < zr) P.xa_save[save_off + p0 + i] = __float2bfloat16_rn(v[i]);
         }
         if (tdst) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int j = u.n0 + c + i;
-                if (j < t_r) tdst[(size_t)j * P.t_ld + td.tpos0 + row] = __float2bfloat16_rn(v[i]);
-            }
+            for (int i = 0; i < 16; ++i)
+                if (j0 + i < zr) tdst[(size_t)(p0 + i) * P.t_ld + td.tpos0 + row] = __float2bfloat16_rn(v[i]);
         }
     }
 };
@@ -347,7 +350,11 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
             const bool is_b = (w.kind == kGradDb);
             const int32_t ld = is_b ? P.N : P.K;
             const int32_t m = w.n0 + row;
-            float* base = is_b ? P.dB + (size_t)g.prow_b * P.N : P.dA + (size_t)g.prow_a * P.K;
+            // dB: accumulator column j is row j of the up factor (this item's slice columns); dA: row j0 + j of
+            // the stacked down factors
+            const int32_t jbase = is_b ? 0 : w.j0;
+            const int32_t jend = is_b ? g.r : g.r * g.nslice;
+            float* base = (is_b ? P.dB + (size_t)g.prow_b * P.N : P.dA + (size_t)g.prow_a * P.K) + (size_t)jbase * ld;
             for (int c = 0; c < w.mma_n; c += 16) {
                 uint32_t a[16];
                 tmem_ld16(taddr + c, a);
@@ -356,7 +363,7 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int j = c + i;
-                        if (j < g.r) {
+                        if (jbase + j < jend) {
                             float* p = base + (size_t)j * ld + m;
                             const float val = g.scale * __uint_as_float(a[i]);
                             *p = P.accumulate ? (*p + val) : val;

@@ -163,3 +163,45 @@ def test_plan_segment_order_does_not_matter(lib):
     wl.segs = wl.segs[rng.permutation(wl.segs.shape[0])]
     r1, i1 = _plan(wl)
     assert np.array_equal(r0, r1) and np.array_equal(i0, i1)
+
+
+def call_sliced_fwd(lib, T, K, N, pool, bounds, segs, dt=0, ws=None, wsb=0):
+    s = lm.segments(segs)
+    sl = lm.Slices(bounds)
+    return lib.lora_sliced_forward(T, K, N, dt, 0x30000000, 0x40000000, pool.cptr(), sl.cptr(), s.ctypes.data,
+                                   s.shape[0], 0x50000000, None, 0, ws, wsb, None)
+
+
+def test_sliced_validation(lib):
+    K, N = 256, 1024
+    pool = FakePool([8, 16], K, N)
+    segs = [(0, 10, 0, 0), (10, 6, 1, 1)]
+    # bounds must start at 0, end at N, increase, and have interior bounds on 256-column tiles
+    assert call_sliced_fwd(lib, 16, K, N, pool, [0, 512, 1000], segs) == -1
+    assert call_sliced_fwd(lib, 16, K, N, pool, [8, 512, 1024], segs) == -1
+    assert call_sliced_fwd(lib, 16, K, N, pool, [0, 520, 1024], segs) == -1
+    assert call_sliced_fwd(lib, 16, K, N, pool, [0, 512, 512, 1024], segs) == -1
+    assert call_sliced_fwd(lib, 16, K, N, pool, [0, 256, 512, 768, 896, 1024], segs) == -1   # 5 slices
+    # float32 layers take one slice only
+    assert call_sliced_fwd(lib, 16, K, N, pool, [0, 512, 1024], segs, dt=1) == -7
+    # a NULL slices argument is rejected by the sliced entry point
+    s = lm.segments(segs)
+    assert lib.lora_sliced_forward(16, K, N, 0, 0x30000000, 0x40000000, pool.cptr(), None, s.ctypes.data, 2,
+                                   0x50000000, None, 0, None, 0, None) == -1
+    # valid slices, missing workspace: the workspace check is the first failure
+    assert call_sliced_fwd(lib, 16, K, N, pool, [0, 512, 768, 1024], segs) == -6
+
+
+def test_sliced_sizes(lib):
+    K, N = 256, 1024
+    pool = FakePool([8, 16], K, N)
+    segs = lm.segments([(0, 10, 0, 0), (10, 6, 1, 1), (16, 20, 0, 1)])
+    for S, b in ((1, [0, 1024]), (3, [0, 512, 768, 1024]), (4, [0, 256, 512, 768, 1024])):
+        sl = lm.Slices(b)
+        xa = lib.lora_sliced_xa_size(0, pool.cptr(), sl.cptr(), segs.ctypes.data, segs.shape[0])
+        assert xa == 2 * S * (6 * 16 + 20 * 8)
+        ws = lib.lora_sliced_workspace_size(36, K, N, 0, pool.cptr(), sl.cptr(), segs.ctypes.data, segs.shape[0])
+        assert ws > 0
+    sl1 = lm.Slices([0, 1024])
+    one = lib.lora_sliced_workspace_size(36, K, N, 0, pool.cptr(), sl1.cptr(), segs.ctypes.data, 3)
+    assert one == lib.lora_workspace_size(36, K, N, 0, pool.cptr(), segs.ctypes.data, 3)
