@@ -38,6 +38,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, choices=[2, 3, 4, 5])
+    ap.add_argument("--workload", choices=["config", "layer"], default="config",
+                    help="layer: the LoRA projections of one Llama-3-8B decoder layer (q|k|v, o, gate|up, down) "
+                         "on a co-serving batch, chained on one stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
@@ -58,29 +61,30 @@ def make_workload(cfg, rank=0, overrides=()):
 def accounting(wl):
     """Algorithmic FLOPs and bytes of one step, split by launch group (no padding, no redundant work)."""
     T, K, N = wl.T, wl.K, wl.N
+    S = wl.n_slices                      # a sliced layer: S down factors per adapter, one up factor over N
     segs = wl.segs.tolist()
     r_of = lambda a: int(wl.rank[a]) if a >= 0 else 0
     fwd = wl.forward
     bwd = wl.backward
     out = {}
     if fwd:
-        shrink = sum(2 * ln * K * r_of(a) for _, ln, a, _ in segs)
+        shrink = sum(2 * ln * S * K * r_of(a) for _, ln, a, _ in segs)
         expand = sum(2 * ln * N * r_of(a) for _, ln, a, _ in segs)
         out["fwd_main_flops"] = 2 * T * K * N + expand
         out["fwd_flops"] = 2 * T * K * N + expand + shrink
         used = sorted(set(a for _, ln, a, _ in segs if a >= 0 and ln > 0))
-        save = sum(ln * r_of(a) for _, ln, a, tr in segs if tr) * 2 if wl.xa_mode == "save" else 0
-        out["fwd_bytes"] = 2 * (T * K + K * N + T * N) + sum(2 * r_of(a) * (K + N) for a in used) + save
+        save = sum(ln * S * r_of(a) for _, ln, a, tr in segs if tr) * 2 if wl.xa_mode == "save" else 0
+        out["fwd_bytes"] = 2 * (T * K + K * N + T * N) + sum(2 * r_of(a) * (S * K + N) for a in used) + save
         # main launch: x, W, adapters' B blocks and y
         out["fwd_main_bytes"] = 2 * (T * K + K * N + T * N) + sum(2 * r_of(a) * N for a in used)
     if bwd:
         tr = [(st, ln, a) for st, ln, a, t in segs if t and ln > 0]
         Tt = sum(ln for _, ln, _ in tr)
-        lora = sum(2 * ln * r_of(a) * (2 * K + 2 * N) for _, ln, a in tr)
-        recompute = sum(2 * ln * K * r_of(a) for _, ln, a in tr) if wl.xa_mode != "save" else 0
+        lora = sum(2 * ln * r_of(a) * (2 * S * K + 2 * N) for _, ln, a in tr)
+        recompute = sum(2 * ln * S * K * r_of(a) for _, ln, a in tr) if wl.xa_mode != "save" else 0
         out["bwd_flops"] = 2 * Tt * K * N + lora + recompute
         tads = sorted(set(a for _, _, a in tr))
-        out["bwd_bytes"] = 2 * (Tt * N + K * N + 2 * Tt * K) + sum(6 * r_of(a) * (K + N) for a in tads)
+        out["bwd_bytes"] = 2 * (Tt * N + K * N + 2 * Tt * K) + sum(6 * r_of(a) * (S * K + N) for a in tads)
         out["train_tokens"] = Tt
     out["flops"] = out.get("fwd_flops", 0) + out.get("bwd_flops", 0)
     out["bytes"] = out.get("fwd_bytes", 0) + out.get("bwd_bytes", 0)
@@ -230,9 +234,58 @@ def oracle_sample(wl, fwd_rows=32, dx_rows=16, cols=32, seed=0):
     return t_total, "; ".join(desc) + "; linear extrapolation to one full step", threads
 
 
+LAYER_ORDER = ["qkv", "o", "gate_up", "down"]
+
+
+def make_layer(rank=0, overrides=()):
+    kw = {}
+    for item in overrides:
+        k, v = item.split("=", 1)
+        kw[k] = int(v)
+    return workloads.llama_layer(seed=1006 + 7919 * rank, **kw)
+
+
+def layer_oracle_sample(L, seed=0, fwd_rows=8, dx_rows=4, cols=8):
+    """The oracle on a bounded sample of one layer step: every projection, a sliced one slice by slice (each slice
+    is a plain LoRA layer on the shared input)."""
+    t = 0.0
+    desc = threads = None
+    for n in LAYER_ORDER:
+        wl = L[n]
+        parts = [workloads.slice_of(wl, i) for i in range(wl.n_slices)] if wl.bounds is not None else [wl]
+        for part in parts:
+            dt, desc, threads = oracle_sample(part, fwd_rows=fwd_rows, dx_rows=dx_rows, cols=cols, seed=seed)
+            t += dt
+    return t, "per projection (a sliced one per slice): " + desc, threads
+
+
+def layer_name(L):
+    q = L["qkv"]
+    return "llama3_8b_layer_h%d_kv%d_i%d_T%d_P%d" % (q.K, (q.N - q.K) // 2, L["down"].K, q.T, q.n_adapters)
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
+        return 0
+    if args.workload == "layer":
+        L = make_layer(0, args.set)
+        tokens = L["qkv"].T
+        times = []
+        desc = threads = None
+        for i in range(args.warmup + args.steps):
+            t, desc, threads = layer_oracle_sample(L, seed=i)
+            if i >= args.warmup:
+                times.append(t)
+        t = statistics.mean(times) if times else float("nan")
+        v = tokens / t
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": layer_name(L), "T": tokens},
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
         return 0
     wl = make_workload(args.config, 0, args.set)
     acc = accounting(wl)
@@ -484,10 +537,157 @@ def run_ours(args):
     return 0
 
 
+def run_layer(args):
+    """One decoder layer's LoRA projections per step: forward q|k|v -> o -> gate|up -> down over every token, then
+    the LoRA backward of the fine-tuning tokens in reverse order, all on one stream with one shared workspace."""
+    import torch
+    import lora_co_serving_gb300 as lm
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    lm.build()
+    L = make_layer(rank, args.set)
+    T = L["qkv"].T
+    acc = {n: accounting(L[n]) for n in LAYER_ORDER}
+    dev = {}
+    need = 0
+    for n in LAYER_ORDER:
+        wl = L[n]
+        d = {"x": to_dev(wl.x, torch), "Wt": to_dev(wl.Wt, torch), "A": to_dev(wl.A, torch),
+             "B": to_dev(wl.B, torch), "dY": to_dev(wl.dY, torch)}
+        d["pool"] = lm.Pool(d["A"], d["B"], wl.a_off, wl.b_off, wl.rank, wl.scale)
+        d["segs"] = lm.segments(wl.segs)
+        d["sl"] = lm.Slices(wl.bounds) if wl.bounds is not None else None
+        d["y"] = torch.empty((T, wl.N), dtype=torch.bfloat16, device="cuda")
+        d["dX"] = torch.zeros((T, wl.K), dtype=torch.bfloat16, device="cuda")
+        d["dA"] = torch.zeros(d["A"].numel(), dtype=torch.float32, device="cuda")
+        d["dB"] = torch.zeros(d["B"].numel(), dtype=torch.float32, device="cuda")
+        if d["sl"] is not None:
+            need = max(need, lm.sliced_workspace_size(T, wl.K, wl.N, 0, d["pool"], d["sl"], d["segs"]))
+        else:
+            need = max(need, lm.workspace_size(T, wl.K, wl.N, 0, d["pool"], d["segs"]))
+        dev[n] = d
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def fwd(n):
+        d = dev[n]
+        if d["sl"] is not None:
+            lm.sliced_forward(d["x"], d["Wt"], d["pool"], d["sl"], d["segs"], y=d["y"], workspace=ws, stream=stream)
+        else:
+            lm.forward(d["x"], d["Wt"], d["pool"], d["segs"], y=d["y"], workspace=ws, stream=stream)
+
+    def bwd(n):
+        d = dev[n]
+        kw = dict(dX=d["dX"], dA=d["dA"], dB=d["dB"], recompute=True, workspace=ws, stream=stream)
+        if d["sl"] is not None:
+            lm.sliced_backward(d["x"], d["Wt"], d["pool"], d["sl"], d["segs"], d["dY"], **kw)
+        else:
+            lm.backward(d["x"], d["Wt"], d["pool"], d["segs"], d["dY"], **kw)
+
+    calls = [("fwd", n) for n in LAYER_ORDER] + [("bwd", n) for n in reversed(LAYER_ORDER)]
+
+    def step(evs=None):
+        for j, (kind, n) in enumerate(calls):
+            if evs is not None:
+                evs[j].record(stream)
+            (fwd if kind == "fwd" else bwd)(n)
+        if evs is not None:
+            evs[len(calls)].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    lm.workspace_status(ws)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    tev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    for row in tev:
+        for e in row:
+            e.record(stream)
+    sampler = ClockSampler(torch.cuda.current_device())
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.time()
+    for i in range(args.steps):
+        # trace the launch groups of the gate|up forward (the layer's largest launch)
+        for j, (kind, n) in enumerate(calls):
+            evs[i][j].record(stream)
+            if kind == "fwd" and n == "gate_up":
+                lm.set_trace_events(tev[i])
+            (fwd if kind == "fwd" else bwd)(n)
+            if kind == "fwd" and n == "gate_up":
+                lm.set_trace_events(None)
+        evs[i][len(calls)].record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1)
+    lm.workspace_status(ws)
+    ms_steps = [evs[i][0].elapsed_time(evs[i][len(calls)]) for i in range(args.steps)]
+    ms = statistics.mean(ms_steps)
+    per_call = {"%s_%s" % c: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                for j, c in enumerate(calls)}
+    gu_main_ms = statistics.mean(tev[i][2].elapsed_time(tev[i][3]) for i in range(args.steps))
+    t_max = torch.tensor([ms], device="cuda", dtype=torch.float64)
+    if dist:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    ms_max = float(t_max.item())
+    value = T * world / (ms_max / 1e3)
+    pk = peaks()
+    if rank == 0:
+        flops = sum(a["flops"] for a in acc.values())
+        nbytes = sum(a["bytes"] for a in acc.values())
+        t_roof = max(flops / (pk["bf16_tflops_sustained"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
+        achieved = acc["gate_up"]["fwd_main_flops"] / (gu_main_ms / 1e3) / 1e12
+        roof = {"kernel": "lora_main2_kernel (gate|up forward main pass: x W + fused LoRA expand, 2 slices)",
+                "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
+                "peak_source": pk["source"] + " (sustained bf16)", "ms_per_launch": gu_main_ms,
+                "algorithmic_flops_per_launch": acc["gate_up"]["fwd_main_flops"]}
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            t_cpu, desc, threads = layer_oracle_sample(L, fwd_rows=16, dx_rows=8, cols=16)
+            cpu = {"value": T / t_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+        q = L["qkv"]
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the pages' workloads)",
+                "config": {"workload": layer_name(L), "T": T, "hidden": q.K, "kv": (q.N - q.K) // 2,
+                           "intermediate": L["down"].K, "adapters": q.n_adapters,
+                           "train_tokens": acc["qkv"].get("train_tokens", 0), "xa": "recompute",
+                           "projections": "q|k|v (3 slices), o, gate|up (2 slices), down",
+                           "l2": "inputs larger than L2 (weights %.0f MB); no flush"
+                                 % (sum(2 * L[n].K * L[n].N for n in LAYER_ORDER) / 1e6),
+                           "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
+                "roofline": roof,
+                "step": {"tflops": flops / (ms / 1e3) / 1e12, "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
+                         "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms,
+                         "algorithmic_flops": flops, "algorithmic_bytes": nbytes, "call_ms": per_call},
+                "cpu_baseline": cpu, "clocks": clocks, "e2e": None,
+                "gpu_launches": sum(launches_per_step(L[n]) for n in LAYER_ORDER) * args.steps}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "layer":
+        return run_layer(args)
     return run_ours(args)
 
 

@@ -5,8 +5,6 @@ the slice), so besides the float64 oracle of ``oracle/sliced.py`` every slice of
 BITWISE against a plain call of that slice alone: the sliced plan keeps each row's shrink and expand summation
 order, so fusing the slices must not change a single bit of y, dA or dB.
 """
-import dataclasses
-
 import numpy as np
 import pytest
 
@@ -35,28 +33,6 @@ def mixed(bounds, K=512, seed=21, n_adapters=24, ranks=(8, 16, 32, 64), n_decode
     wl = workloads.sliced(seed, base.T, K, bounds, base.segs, base.rank)
     wl.meta["train_adapter"] = base.meta["train_adapter"]
     return wl
-
-
-def slice_of(wl, i):
-    """Slice i of a sliced workload as a plain workload (its weight rows, down factors and up-factor columns)."""
-    c0, c1 = int(wl.bounds[i]), int(wl.bounds[i + 1])
-    Ni = c1 - c0
-    A2 = wl.A.reshape(-1, wl.K)
-    B2 = wl.B.reshape(-1, wl.N)
-    As, Bs, ao, bo = [], [], [], []
-    for a in range(wl.n_adapters):
-        r = int(wl.rank[a])
-        row = int(wl.a_off[a]) // wl.K
-        As.append(A2[row + i * r:row + (i + 1) * r])
-        brow = int(wl.b_off[a]) // wl.N
-        Bs.append(B2[brow:brow + r, c0:c1])
-        ao.append(sum(int(wl.rank[b]) * wl.K for b in range(a)))
-        bo.append(sum(int(wl.rank[b]) * Ni for b in range(a)))
-    return dataclasses.replace(wl, N=Ni, Wt=np.ascontiguousarray(wl.Wt[c0:c1]),
-                               A=np.ascontiguousarray(np.concatenate(As).reshape(-1)),
-                               B=np.ascontiguousarray(np.concatenate(Bs).reshape(-1)),
-                               a_off=np.asarray(ao, np.int64), b_off=np.asarray(bo, np.int64),
-                               dY=None if wl.dY is None else np.ascontiguousarray(wl.dY[:, c0:c1]), bounds=None)
 
 
 def sliced_train_blocks(wl):
@@ -136,7 +112,7 @@ def test_sliced_slices_equal_plain_calls_bitwise():
     B_s = dB.cpu().numpy().reshape(-1, wl.N)
     for i in range(wl.n_slices):
         c0, c1 = int(wl.bounds[i]), int(wl.bounds[i + 1])
-        sw = slice_of(wl, i)
+        sw = workloads.slice_of(wl, i)
         ds = Dev(sw)
         yi = ds.forward()
         _, gA, gB = ds.backward(recompute=True)

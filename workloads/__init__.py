@@ -241,6 +241,74 @@ def sliced(seed, T, K, bounds, segs, rank, scale=None, dtype="bf16", want_dy=Tru
                  want_dy=want_dy, bounds=bounds, **kw)
 
 
+def llama_layer(seed=1006, hidden=4096, kv=1024, inter=14336, n_adapters=320, n_decode=2048, prefill_tokens=4096,
+                len_lo=64, len_hi=1024, n_train=2, train_len=1024, zipf_s=1.1, ranks=(8, 16, 32), train_rank=16):
+    """The LoRA projections of one Llama-3-8B decoder layer on a co-serving batch.
+
+    Shapes: q|k|v fused (hidden -> hidden + 2 kv, three slices), o (hidden -> hidden), gate|up fused
+    (hidden -> 2 inter, two slices), down (inter -> hidden).  Every projection has its own adapter pool; the
+    segment table and the adapters' ranks are shared (one adapter = one rank on every projection).  The
+    batch: Zipf(zipf_s) decode tokens over the pool, prefill segments of U{len_lo..len_hi} tokens, and
+    n_train fine-tuning sequences on a reserved adapter of rank train_rank (scale 2, the pages' r = 16,
+    alpha = 32).  Inference adapters draw their rank from ``ranks``.  Generation order: table -> ranks ->
+    then each projection in the order qkv, o, gate_up, down (W, A, B, x, dY each)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n_inf = n_adapters - 1
+    dec = _zipf_ids(rng, n_decode, n_inf, zipf_s)
+    lens = _draw_lengths(rng, prefill_tokens, len_lo, len_hi)
+    pre_ids = rng.integers(0, n_inf, size=len(lens))
+    segs, t = [], 0
+    for a in dec:
+        segs.append((t, 1, int(a), 0))
+        t += 1
+    for ln, a in zip(lens, pre_ids):
+        segs.append((t, ln, int(a), 0))
+        t += ln
+    for _ in range(n_train):
+        segs.append((t, train_len, n_inf, 1))
+        t += train_len
+    rank = np.concatenate([rng.choice(np.array(ranks), size=n_inf), [train_rank]]).astype(np.int32)
+    scale = [2.0] * n_adapters
+    shapes = [("qkv", hidden, [0, hidden, hidden + kv, hidden + 2 * kv]), ("o", hidden, [0, hidden]),
+              ("gate_up", hidden, [0, inter, 2 * inter]), ("down", inter, [0, hidden])]
+    out = {}
+    for name, K, bounds in shapes:
+        N = bounds[-1]
+        b = bounds if len(bounds) > 2 else None
+        wl = _fill("llama_layer_%s_%dx%d_T%d" % (name, K, N, t), rng, t, K, N, "bf16", segs, rank, scale,
+                   want_dy=True, forward=True, backward=True, xa_mode="recompute", bounds=b,
+                   meta={"n_decode": n_decode, "train_adapter": n_inf, "projection": name})
+        out[name] = wl
+    return out
+
+
+def slice_of(wl, i):
+    """Slice i of a sliced workload as a plain workload: that slice's weight rows, down factors and up-factor
+    columns, with the same segment table and inputs (plain indexing of the drawn arrays)."""
+    import dataclasses
+    c0, c1 = int(wl.bounds[i]), int(wl.bounds[i + 1])
+    Ni = c1 - c0
+    A2 = wl.A.reshape(-1, wl.K)
+    B2 = wl.B.reshape(-1, wl.N)
+    As, Bs, ao, bo = [], [], [], []
+    at_a = at_b = 0
+    for a in range(wl.n_adapters):
+        r = int(wl.rank[a])
+        row = int(wl.a_off[a]) // wl.K
+        As.append(A2[row + i * r:row + (i + 1) * r])
+        brow = int(wl.b_off[a]) // wl.N
+        Bs.append(B2[brow:brow + r, c0:c1])
+        ao.append(at_a)
+        bo.append(at_b)
+        at_a += r * wl.K
+        at_b += r * Ni
+    return dataclasses.replace(wl, N=Ni, Wt=np.ascontiguousarray(wl.Wt[c0:c1]),
+                               A=np.ascontiguousarray(np.concatenate(As).reshape(-1)),
+                               B=np.ascontiguousarray(np.concatenate(Bs).reshape(-1)),
+                               a_off=np.asarray(ao, np.int64), b_off=np.asarray(bo, np.int64),
+                               dY=None if wl.dY is None else np.ascontiguousarray(wl.dY[:, c0:c1]), bounds=None)
+
+
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
 
 
