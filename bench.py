@@ -38,9 +38,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, choices=[2, 3, 4, 5])
-    ap.add_argument("--workload", choices=["config", "layer"], default="config",
+    ap.add_argument("--workload", choices=["config", "layer", "sweep"], default="config",
                     help="layer: the LoRA projections of one Llama-3-8B decoder layer (q|k|v, o, gate|up, down) "
-                         "on a co-serving batch, chained on one stream")
+                         "on a co-serving batch, chained on one stream; sweep: that layer step over a grid of batch "
+                         "compositions, with the step-latency model (Eq. I / II) fitted to the timings")
+    ap.add_argument("--out", default=None, help="sweep: also write the fitted coefficients to this JSON file")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
@@ -682,12 +684,159 @@ def run_layer(args):
     return 0
 
 
+def sweep_tables(L, seed=77):
+    """Segment tables of the sweep: decode-only batches (Eq. II) and mixed batches of decode, prefill and
+    fine-tuning tokens (Eq. I), adapters drawn like the layer workload's."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    wl = L["qkv"]
+    n_inf = wl.n_adapters - 1
+    train_ad = int(wl.meta["train_adapter"])
+
+    def table(b_d, t_in, t_ft):
+        segs, t = [], 0
+        for a in workloads._zipf_ids(rng, b_d, n_inf, 1.1):
+            segs.append((t, 1, int(a), 0))
+            t += 1
+        for ln in (workloads._draw_lengths(rng, t_in, 64, 1024) if t_in else []):
+            if ln == 1:                               # a 1-token remainder would read as a decode request
+                ln, segs[-1] = ln, (segs[-1][0], segs[-1][1] + 1, segs[-1][2], 0)
+                t += 1
+                continue
+            segs.append((t, ln, int(rng.integers(0, n_inf)), 0))
+            t += ln
+        left = t_ft
+        while left > 0:
+            ln = min(1024, left)
+            segs.append((t, ln, train_ad, 1))
+            t += ln
+            left -= ln
+        return np.asarray(segs, np.int32), t
+
+    decode = [table(b, 0, 0) for b in (16, 32, 64, 128, 256, 512, 768, 1024, 1536, 2048)]
+    mixed = []
+    for b_d in (0, 256, 1024, 2048):
+        for t_in in (0, 1024, 2048, 4096):
+            for t_ft in (0, 1024, 2048):
+                if t_in == 0 and t_ft == 0:
+                    continue
+                mixed.append(table(b_d, t_in, t_ft))
+    return decode, mixed
+
+
+def run_sweep(args):
+    """Time the layer step over the sweep's batch compositions and fit Eq. I (mixed) and Eq. II (decode-only)."""
+    import torch
+    import lora_co_serving_gb300 as lm
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    lm.build()
+    L = make_layer(0, args.set)
+    decode, mixed = sweep_tables(L)
+    dev = {}
+    need = 0
+    for n in LAYER_ORDER:
+        wl = L[n]
+        d = {"x": to_dev(wl.x, torch), "Wt": to_dev(wl.Wt, torch), "A": to_dev(wl.A, torch),
+             "B": to_dev(wl.B, torch), "dY": to_dev(wl.dY, torch)}
+        d["pool"] = lm.Pool(d["A"], d["B"], wl.a_off, wl.b_off, wl.rank, wl.scale)
+        d["sl"] = lm.Slices(wl.bounds) if wl.bounds is not None else None
+        d["y"] = torch.empty((wl.T, wl.N), dtype=torch.bfloat16, device="cuda")
+        d["dX"] = torch.zeros((wl.T, wl.K), dtype=torch.bfloat16, device="cuda")
+        d["dA"] = torch.zeros(d["A"].numel(), dtype=torch.float32, device="cuda")
+        d["dB"] = torch.zeros(d["B"].numel(), dtype=torch.float32, device="cuda")
+        for segs, T in decode + mixed:
+            if d["sl"] is not None:
+                need = max(need, lm.sliced_workspace_size(T, wl.K, wl.N, 0, d["pool"], d["sl"], segs))
+            else:
+                need = max(need, lm.workspace_size(T, wl.K, wl.N, 0, d["pool"], segs))
+        dev[n] = d
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(segs, T):
+        train = bool((segs[:, 3] != 0).any())
+        for n in LAYER_ORDER:
+            d = dev[n]
+            if d["sl"] is not None:
+                lm.sliced_forward(d["x"][:T], d["Wt"], d["pool"], d["sl"], segs, y=d["y"][:T], workspace=ws,
+                                  stream=stream)
+            else:
+                lm.forward(d["x"][:T], d["Wt"], d["pool"], segs, y=d["y"][:T], workspace=ws, stream=stream)
+        if train:
+            for n in reversed(LAYER_ORDER):
+                d = dev[n]
+                kw = dict(dX=d["dX"][:T], dA=d["dA"], dB=d["dB"], recompute=True, workspace=ws, stream=stream)
+                if d["sl"] is not None:
+                    lm.sliced_backward(d["x"][:T], d["Wt"], d["pool"], d["sl"], segs, d["dY"][:T], **kw)
+                else:
+                    lm.backward(d["x"][:T], d["Wt"], d["pool"], segs, d["dY"][:T], **kw)
+
+    reps = max(3, min(args.steps, 10))
+
+    def time_point(segs, T):
+        for _ in range(max(3, args.warmup)):
+            step(segs, T)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0.record(stream)
+            step(segs, T)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    wall0 = time.time()
+    res = {}
+    for name, pts, model in (("decode", decode, lm.EQ_II), ("mixed", mixed, lm.EQ_I)):
+        F = np.array([lm.latency_features(model, segs) for segs, _ in pts])
+        t = np.array([time_point(segs, T) for segs, T in pts])
+        coef = lm.latency_fit(model, F, t)
+        pred = F @ coef
+        rel = np.abs(pred - t) / t
+        r2 = 1.0 - float(((t - pred) ** 2).sum() / max(1e-300, ((t - t.mean()) ** 2).sum()))
+        # 5-fold cross-validation: relative error of each point when it is left out of the fit
+        folds = np.arange(len(pts)) % 5
+        cv = np.zeros(len(pts))
+        for k in range(5):
+            tr, te = folds != k, folds == k
+            ck = lm.latency_fit(model, F[tr], t[tr])
+            cv[te] = np.abs(F[te] @ ck - t[te]) / t[te]
+        names = ["alpha", "beta", "gamma", "eps", "c"] if model == lm.EQ_I else ["beta'", "eps'", "c'"]
+        res[name] = {"equation": "I" if model == lm.EQ_I else "II", "points": len(pts),
+                     "coefficients_ms": dict(zip(names, coef.tolist())), "r2": r2,
+                     "median_rel_err": float(np.median(rel)), "max_rel_err": float(rel.max()),
+                     "cv_median_rel_err": float(np.median(cv)), "cv_max_rel_err": float(cv.max()),
+                     "samples": [{"features": f.tolist(), "ms": float(x)} for f, x in zip(F, t)]}
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1)
+    line = {"metric": "step-latency model fit (DeltaServe Eq. I / II) over the layer step", "unit": "ms",
+            "n_gpus": 1, "data": "synthetic (seeded; shapes of the pages' workloads)",
+            "config": {"workload": layer_name(L) + "_sweep", "reps_per_point": reps,
+                       "step": "forward of q|k|v, o, gate|up, down over every token + LoRA backward of the "
+                               "fine-tuning tokens (xA recomputed)",
+                       "features": "Eq. I {sum (n_i+B_d)^2, T_in+B_d, T_ft, K=0, 1}; Eq. II {B_d, K=0, 1}"},
+            "fit": res, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    if args.out:
+        json.dump({k: {"equation": v["equation"], "coefficients_ms": v["coefficients_ms"], "r2": v["r2"],
+                       "cv_median_rel_err": v["cv_median_rel_err"], "cv_max_rel_err": v["cv_max_rel_err"],
+                       "points": v["points"]} for k, v in res.items()},
+                  open(args.out, "w"), indent=1)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "layer":
         return run_layer(args)
+    if args.workload == "sweep":
+        return run_sweep(args)
     return run_ours(args)
 
 

@@ -40,7 +40,8 @@ ERRORS = {0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_SEGMENTS", -3:
 EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_mixed_backward", "lora_last_error",
             "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events", "lora_mixed_forward_static",
             "lora_selftest_wait_timeout", "lora_adamw_step", "lora_mixed_backward_flagged",
-            "lora_sliced_workspace_size", "lora_sliced_xa_size", "lora_sliced_forward", "lora_sliced_backward"]
+            "lora_sliced_workspace_size", "lora_sliced_xa_size", "lora_sliced_forward", "lora_sliced_backward",
+            "lora_latency_terms", "lora_latency_features", "lora_latency_fit", "lora_latency_predict"]
 
 
 class LoraError(RuntimeError):
@@ -122,6 +123,14 @@ def library(path=None):
     lib.lora_sliced_backward.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, P, I32, P, P, P, P, P,
                                          ctypes.c_uint32, P, SZ, P]
     lib.lora_sliced_backward.restype = ctypes.c_int
+    lib.lora_latency_terms.argtypes = [I32]
+    lib.lora_latency_terms.restype = I32
+    lib.lora_latency_features.argtypes = [I32, P, I32, ctypes.c_double, P]
+    lib.lora_latency_features.restype = ctypes.c_int
+    lib.lora_latency_fit.argtypes = [I32, P, P, I32, P]
+    lib.lora_latency_fit.restype = ctypes.c_int
+    lib.lora_latency_predict.argtypes = [I32, P, P]
+    lib.lora_latency_predict.restype = ctypes.c_double
     if path is None:
         _LIB = lib
     return lib
@@ -413,3 +422,33 @@ def sliced_backward(x, Wt, pool, bounds, segs, dY, xa_saved=None, dX=None, dA=No
                                           _ptr(dA) if want_grads else None, _ptr(dB) if want_grads else None, flags,
                                           _ptr(workspace), workspace.numel(), _stream_ptr(stream)))
     return dX, dA, dB
+
+
+# ----------------------------------------------------------------------------------------------- latency model
+EQ_I = 1
+EQ_II = 2
+
+
+def latency_features(model, segs, kv_size=0.0):
+    """Feature vector of one step (Eq. I: {sum (n_i+B_d)^2, T_in+B_d, T_ft, K, 1}; Eq. II: {B_d, K, 1})."""
+    s = segments(segs)
+    p = library().lora_latency_terms(model)
+    out = np.zeros(p, np.float64)
+    _check(library().lora_latency_features(model, _ptr(s), s.shape[0], float(kv_size), _ptr(out)))
+    return out
+
+
+def latency_fit(model, feats, times):
+    """Least-squares coefficients of the model over measured steps (feats [n, terms], times [n])."""
+    f = np.ascontiguousarray(feats, dtype=np.float64)
+    t = np.ascontiguousarray(times, dtype=np.float64)
+    p = library().lora_latency_terms(model)
+    coef = np.zeros(p, np.float64)
+    _check(library().lora_latency_fit(model, _ptr(f), _ptr(t), t.shape[0], _ptr(coef)))
+    return coef
+
+
+def latency_predict(model, coef, feat):
+    c = np.ascontiguousarray(coef, dtype=np.float64)
+    f = np.ascontiguousarray(feat, dtype=np.float64)
+    return float(library().lora_latency_predict(model, _ptr(c), _ptr(f)))

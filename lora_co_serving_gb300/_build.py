@@ -17,7 +17,7 @@ LIB = os.path.join(PKG, "liblora_mixed.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_SOURCES = ["api.cu", "tc_kernel.cu", "simt.cu", "noalloc.cu", "adamw.cu"]
-CXX_SOURCES = ["plan.cpp"]
+CXX_SOURCES = ["plan.cpp", "latency.cpp"]
 
 
 def _nvcc():
@@ -28,7 +28,7 @@ def _nvcc():
 
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "lora_mixed.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 
