@@ -94,15 +94,23 @@ def accounting(wl):
     return out
 
 
-def launches_per_step(wl):
+def launches_per_step(wl, fwd_tiles=None):
+    """Kernel launches of one step.  fwd_tiles: tiles of the forward plan (from lora_plan_describe) when known; a
+    main pass with fewer output tiles than kMainTargetItems (114) is split and adds a reduce launch."""
     segs = wl.segs.tolist()
+    n_nt = lambda cols: -(-cols // 256)
     n = 0
     if wl.forward:
         n += 1 if any(ln < 16 and not tr and ln > 0 for _, ln, _, tr in segs) else 0    # row gather
         n += 1 if any(a >= 0 for _, _, a, _ in segs) else 0                                # shrink pass
         n += 1                                                                              # main pass
+        if fwd_tiles is not None and 0 < (fwd_tiles // 2) * n_nt(wl.N) < 114:
+            n += 1                                                                          # split reduce
     if wl.backward and any(tr for *_, tr in segs):
         n += 3                                                                              # shrink, dX, dA/dB
+        pairs = sum(-(-ln // 256) for _, ln, _, tr in segs if tr and ln > 0)
+        if pairs * n_nt(wl.K) < 114 and -(-wl.N // 64) // 4 >= 2:
+            n += 1                                                                          # split reduce
     return n
 
 
@@ -337,6 +345,7 @@ def run_ours(args):
     segs = lm.segments(wl.segs)
     T, K, N = wl.T, wl.K, wl.N
     ws = torch.empty(lm.workspace_size(T, K, N, 0, pool, segs), dtype=torch.uint8, device="cuda")
+    fwd_tiles = lm.plan_describe(T, K, N, pool, segs)[0].shape[0] if wl.forward else None
     y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
     save = wl.xa_mode == "save"
     xs = torch.empty(max(1, lm.xa_size(0, pool, segs) // 2), dtype=torch.bfloat16, device="cuda") if save else None
@@ -531,7 +540,7 @@ def run_ours(args):
                            "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
                 "roofline": roof, "step": step_stats, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
                 "adamw": adamw_stats,
-                "gpu_launches": launches_per_step(wl) * args.steps}
+                "gpu_launches": launches_per_step(wl, fwd_tiles) * args.steps}
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

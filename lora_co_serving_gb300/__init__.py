@@ -225,10 +225,10 @@ def xa_size(dtype_code, pool, segs):
 
 
 def _workspace(T, K, N, code, pool, s, workspace, device):
+    """The caller's workspace, or a new one of the size this call needs (the library checks a given one)."""
     import torch
-    need = workspace_size(T, K, N, code, pool, s)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+        workspace = torch.empty(workspace_size(T, K, N, code, pool, s), dtype=torch.uint8, device=device)
     return workspace
 
 

@@ -4,6 +4,8 @@
 
 #include <algorithm>
 #include <cstring>
+#include <list>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -172,6 +174,7 @@ void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&of
     put(b, at(L.atoms_a), pl.atoms_a);
     put(b, at(L.atoms_b), pl.atoms_b);
     put(b, at(L.units), pl.units);
+    put(b, at(L.splits), pl.splits);
     for (int k = 0; k < 3; ++k) {
         put(b, at(L.items[k]), pl.items[k]);
         put(b, at(L.cta_off[k]), off[k]);
@@ -286,6 +289,103 @@ cudaError_t launch_group(int k, KParams* P, uint8_t* ws, const Layout& L, const 
     return (k == 1) ? tc2_launch(*P, grid[k], stream) : tc_launch(*P, grid[k], stream);
 }
 
+// The reduce of the main pass's split output tiles (after the main launch, on the same stream).
+cudaError_t launch_reduce(const Plan& pl, const KParams& P, uint8_t* ws, const Layout& L, cudaStream_t stream) {
+    if (pl.splits.empty()) return cudaSuccess;
+    return main_reduce_launch(reinterpret_cast<const SplitTile*>(ws + L.splits), int32_t(pl.splits.size()),
+                              reinterpret_cast<const int32_t*>(ws + L.rowmap), reinterpret_cast<const float*>(ws + L.part_main),
+                              P.out, P.out_ld, P.out_cols, stream);
+}
+
+
+// ------------------------------------------------------------------------------------------------ plan cache
+// Validation, the tile plan, the workspace layout, the per-CTA item lists and the plan blob depend only on the
+// call's shape, segment table and pool description (host arrays), not on any device pointer.  A serving step
+// reuses one segment table for every projection of every layer, so each thread keeps its last few plans and a
+// call whose inputs are byte-for-byte those of a kept plan reuses it (compared in full, no hashing).
+struct Prepared {
+    int32_t kind = 0, T = 0, K = 0, N = 0, S = 1, opts = 0;
+    int32_t bounds[LORA_MAX_SLICES + 1] = {0, 0, 0, 0, 0};
+    std::vector<lora_segment_t> segs;
+    std::vector<int64_t> a_off, b_off;
+    std::vector<int32_t> rank;
+    std::vector<float> scale;
+    Problem p;
+    Plan pl;
+    Layout L;
+    int sms = 0;                         // the CTA lists below were made for this many SMs
+    std::vector<int32_t> off[3], lst[3];
+    int grid[3] = {0, 0, 0};
+    std::vector<uint8_t> blob;
+};
+constexpr size_t kPlanCacheEntries = 8;
+thread_local std::list<std::unique_ptr<Prepared>> g_plans;
+
+template <class T>
+bool same(const std::vector<T>& v, const T* a, size_t n) {
+    return v.size() == n && (n == 0 || std::memcmp(v.data(), a, sizeof(T) * n) == 0);
+}
+
+bool matches(const Prepared& e, int32_t kind, int32_t T, int32_t K, int32_t N, const lora_pool_t* pool,
+             const lora_slices_t* slices, const lora_segment_t* segs, int32_t n_segs, int32_t opts) {
+    const int32_t S = slices ? slices->n_slices : 1;
+    if (e.kind != kind || e.T != T || e.K != K || e.N != N || e.S != S || e.opts != opts) return false;
+    if (slices && (S < 1 || S > LORA_MAX_SLICES || !slices->col_bounds ||
+                   std::memcmp(e.bounds, slices->col_bounds, sizeof(int32_t) * (S + 1)) != 0))
+        return false;
+    const size_t P = pool->n_adapters > 0 ? size_t(pool->n_adapters) : 0;
+    if (e.rank.size() != P || (P > 0 && (!pool->a_off || !pool->b_off || !pool->rank || !pool->scale))) return false;
+    return same(e.segs, segs, n_segs > 0 ? size_t(n_segs) : 0) && same(e.rank, pool->rank, P) &&
+           same(e.a_off, pool->a_off, P) && same(e.b_off, pool->b_off, P) && same(e.scale, pool->scale, P);
+}
+
+// The bf16 plan of a call: from the cache, or validated and planned now (kind 0: forward; 1: backward with
+// opts = want_dx | want_da << 1 | want_db << 2 | recompute << 3 | per_segment << 4).
+int prepare(int32_t kind, int32_t T, int32_t K, int32_t N, const lora_pool_t* pool, const lora_slices_t* slices,
+            const lora_segment_t* segs, int32_t n_segs, int32_t opts, Prepared** out) {
+    if (pool && n_segs >= 0 && (n_segs == 0 || segs)) {
+        for (auto it = g_plans.begin(); it != g_plans.end(); ++it) {
+            if (matches(**it, kind, T, K, N, pool, slices, segs, n_segs, opts)) {
+                g_plans.splice(g_plans.begin(), g_plans, it);
+                *out = g_plans.front().get();
+                return LORA_OK;
+            }
+        }
+    }
+    auto e = std::make_unique<Prepared>();
+    std::string err;
+    int rc = validate(T, K, N, LORA_BF16, pool, segs, n_segs, &e->p, &err, slices);
+    if (rc != LORA_OK) return fail(rc, err);
+    e->kind = kind; e->T = T; e->K = K; e->N = N; e->opts = opts;
+    e->S = e->p.S;
+    std::memcpy(e->bounds, e->p.bounds, sizeof(e->bounds));
+    e->segs.assign(segs, segs + n_segs);
+    const size_t P = size_t(pool->n_adapters);
+    if (P > 0) {
+        e->a_off.assign(pool->a_off, pool->a_off + P);
+        e->b_off.assign(pool->b_off, pool->b_off + P);
+        e->rank.assign(pool->rank, pool->rank + P);
+        e->scale.assign(pool->scale, pool->scale + P);
+    }
+    // the cached problem reads the entry's own copies of the pool arrays
+    e->p.a_off = e->a_off.data(); e->p.b_off = e->b_off.data();
+    e->p.rank = e->rank.data(); e->p.scale = e->scale.data();
+    if (kind == 0) plan_forward(e->p, &e->pl);
+    else plan_backward(e->p, opts & 1, opts & 2, opts & 4, opts & 8, &e->pl, opts & 16);
+    e->L = layout_of(e->p, e->pl, kind == 1);
+    g_plans.push_front(std::move(e));
+    if (g_plans.size() > kPlanCacheEntries) g_plans.pop_back();
+    *out = g_plans.front().get();
+    return LORA_OK;
+}
+
+// The per-CTA item lists and the plan blob of a prepared call for this device's SM count.
+void assign_for(Prepared* e, int sms) {
+    if (e->sms == sms) return;
+    assign_all(e->pl, sms, e->off, e->lst, e->grid);
+    build_blob(e->pl, e->L, e->off, e->lst, &e->blob);
+    e->sms = sms;
+}
 }  // namespace
 
 namespace lora {
@@ -402,10 +502,18 @@ namespace {
 int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
                  const lora_pool_t* pool, const lora_slices_t* slices, const lora_segment_t* segs, int32_t n_segs,
                  void* y, void* xa_save, uint32_t flags, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-    Problem p;
+    Problem pv;
+    Prepared* pr = nullptr;
     std::string err;
-    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err, slices);
-    if (rc != LORA_OK) return fail(rc, err);
+    int rc;
+    if (dt == LORA_BF16) {
+        rc = prepare(0, T, K, N, pool, slices, segs, n_segs, 0, &pr);
+        if (rc != LORA_OK) return rc;
+    } else {
+        rc = validate(T, K, N, dt, pool, segs, n_segs, &pv, &err, slices);
+        if (rc != LORA_OK) return fail(rc, err);
+    }
+    const Problem& p = pr ? pr->p : pv;
     if (flags & ~uint32_t(LORA_SAVE_XA | LORA_RECOMPUTE_XA | LORA_ACCUMULATE_GRAD | LORA_DEBUG_CHECKS))
         return fail(LORA_ERR_INVALID_ARG, "unknown flag bits");
     const bool save = (flags & LORA_SAVE_XA) && p.xa_elems > 0;
@@ -444,19 +552,16 @@ int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x
         return LORA_OK;
     }
 
-    Plan pl;
-    plan_forward(p, &pl);
-    Layout L = layout_of(p, pl, false);
+    const Plan& pl = pr->pl;
+    const Layout& L = pr->L;
     rc = check_workspace(workspace, ws_bytes, L.total);
     if (rc) return rc;
     if (T == 0) return LORA_OK;
     const int sms = sm_count();
     if (sms <= 0) return fail(LORA_ERR_CUDA, "no CUDA device available");
-    std::vector<int32_t> off[3], lst[3];
-    int grid[3];
-    assign_all(pl, sms, off, lst, grid);
-    std::vector<uint8_t> blob;
-    build_blob(pl, L, off, lst, &blob);
+    assign_for(pr, sms);
+    const int(&grid)[3] = pr->grid;
+    const std::vector<uint8_t>& blob = pr->blob;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     KParams P;
@@ -489,6 +594,7 @@ int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x
     CUDA_TRY(trace(0, 1, stream));
     CUDA_TRY(trace(1, 0, stream));
     CUDA_TRY(launch_group(1, &P, ws, L, grid, stream));
+    CUDA_TRY(launch_reduce(pl, P, ws, L, stream));
     CUDA_TRY(trace(1, 1, stream));
     return LORA_OK;
 }
@@ -498,16 +604,26 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
                   const lora_pool_t* pool, const lora_slices_t* slices, const lora_segment_t* segs, int32_t n_segs,
                   const void* dY, const void* xa_saved, const int32_t* xa_valid, void* dX, float* dA, float* dB,
                   uint32_t flags, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-    Problem p;
+    const bool per_segment = (xa_valid != nullptr);
+    const bool recompute = !per_segment && ((xa_saved == nullptr) || (flags & LORA_RECOMPUTE_XA));
+    Problem pv;
+    Prepared* pr = nullptr;
     std::string err;
-    int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err, slices);
-    if (rc != LORA_OK) return fail(rc, err);
+    int rc;
+    if (dt == LORA_BF16) {
+        const int32_t opts = (dX != nullptr) | (dA != nullptr) << 1 | (dB != nullptr) << 2 | int32_t(recompute) << 3 |
+                             int32_t(per_segment) << 4;
+        rc = prepare(1, T, K, N, pool, slices, segs, n_segs, opts, &pr);
+        if (rc != LORA_OK) return rc;
+    } else {
+        rc = validate(T, K, N, dt, pool, segs, n_segs, &pv, &err, slices);
+        if (rc != LORA_OK) return fail(rc, err);
+    }
+    const Problem& p = pr ? pr->p : pv;
     if (flags & ~uint32_t(LORA_SAVE_XA | LORA_RECOMPUTE_XA | LORA_ACCUMULATE_GRAD | LORA_DEBUG_CHECKS))
         return fail(LORA_ERR_INVALID_ARG, "unknown flag bits");
-    const bool per_segment = (xa_valid != nullptr);
     if (per_segment && (xa_saved == nullptr || (flags & LORA_RECOMPUTE_XA)))
         return fail(LORA_ERR_INVALID_ARG, "a flag table needs xa_saved and excludes LORA_RECOMPUTE_XA");
-    const bool recompute = !per_segment && ((xa_saved == nullptr) || (flags & LORA_RECOMPUTE_XA));
     const bool acc = (flags & LORA_ACCUMULATE_GRAD) != 0;
     if (p.n_train > 0) {
         if (!x || !Wt || !dY) return fail(LORA_ERR_INVALID_ARG, "x, Wt and dY must be non-NULL");
@@ -575,19 +691,16 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
         return LORA_OK;
     }
 
-    Plan pl;
-    plan_backward(p, dX != nullptr, dA != nullptr, dB != nullptr, recompute, &pl, per_segment);
-    Layout L = layout_of(p, pl, true);
+    const Plan& pl = pr->pl;
+    const Layout& L = pr->L;
     rc = check_workspace(workspace, ws_bytes, L.total);
     if (rc) return rc;
     if (p.n_train == 0) return LORA_OK;
     const int sms = sm_count();
     if (sms <= 0) return fail(LORA_ERR_CUDA, "no CUDA device available");
-    std::vector<int32_t> off[3], lst[3];
-    int grid[3];
-    assign_all(pl, sms, off, lst, grid);
-    std::vector<uint8_t> blob;
-    build_blob(pl, L, off, lst, &blob);
+    assign_for(pr, sms);
+    const int(&grid)[3] = pr->grid;
+    const std::vector<uint8_t>& blob = pr->blob;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     KParams P;
@@ -641,6 +754,7 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
     CUDA_TRY(trace(2, 1, stream));
     CUDA_TRY(trace(3, 0, stream));
     CUDA_TRY(launch_group(1, &P, ws, L, grid, stream));
+    CUDA_TRY(launch_reduce(pl, P, ws, L, stream));
     CUDA_TRY(launch_group(2, &P, ws, L, grid, stream));
     CUDA_TRY(trace(3, 1, stream));
     return LORA_OK;

@@ -74,14 +74,25 @@ struct WorkItem {
     int32_t n0;       // main: first output column; shrink: first LoRA column of the pass; grad: first row m0
     int32_t nk;       // main/shrink: k-blocks of the dense loop; grad: total token blocks
     int32_t mma_n;    // N of the MMA
-    int32_t n_ext;    // main: LoRA k-blocks after the dense loop
+    int32_t n_ext;    // main: LoRA k-blocks of this item (Z blocks it touches); shrink: its shrink-unit index
     int32_t kb0;      // shrink and split main items: first k-block of this split of the reduction
     int32_t part;     // shrink: column offset of this split's fp32 partial [mma_n, 128] in the partial buffer;
                       // main: first partial slot of the output tile (split s writes slot part + s)
     int32_t nsplit;   // main: number of K-splits of the output tile (1 = no split)
     int32_t split;    // main: index of this split
-    int32_t counter;  // main, split: first of the 8 counters (2 CTAs x 4 row quarters) of the output tile
+    int32_t ext_c0;   // main: LoRA columns [ext_c0, ext_c1) of the tile's Z that this item multiplies (16-aligned)
+    int32_t ext_c1;
     int32_t j0;       // grad: first row of the transposed xA / dYB buffer this item reads (the slice's rows)
+    int32_t pad0, pad1, pad2;
+};
+
+// An output tile of the main pass whose K loop is split: its splits write fp32 partials
+// (slot part + s, each 2 CTAs x [256 columns][128 rows]) and a reduce launch sums them in split order.
+struct SplitTile {
+    int32_t tile;     // first tile of the pair (its rows)
+    int32_t n0;       // first output column
+    int32_t part;     // first partial slot
+    int32_t nsplit;
 };
 
 // One shrink pass of one tile.  Its K-splits write fp32 partial sums; the last split to finish (counted per row
@@ -100,13 +111,21 @@ struct ShrinkUnit {
 // xA is summed in the same order whatever the rest of its tile holds; small batches split finer so that their
 // few tiles still spread over every SM.
 inline int shrink_split_kb(int64_t T) { return T <= 1024 ? 8 : (T <= 4096 ? 16 : 32); }
+// Forward shrink passes are kPassCols wide, narrowed (down to 64 columns) while a launch would have fewer items
+// than about one per SM: a decode batch's few tiles carry many adapters' columns, and narrower passes spread them
+// over more SMs and shrink each unit's partial sums.  A column's sum does not depend on the pass width.
+constexpr int kShrinkTargetItems = 148;
 
-// Main pass K-splits: when a backward launch has fewer output tiles than ~1.5 waves of CTA pairs, each tile's
-// dense K loop is split and the last split to finish sums the fp32 partials in split order.  The forward keeps
-// one split: a decode tile's LoRA K-steps (which dominate small decode batches) would have to stay in a single
-// split for its rows to be summed in an order independent of the pool order (measured: splitting only the
-// dense loop made a 256-token decode batch slower, 64 -> 78 us).
-constexpr int kMainTargetItems = 114;
+// Main pass K-splits: when a launch has fewer output tiles than ~1.5 waves of CTA pairs, each tile's K loop is
+// split, the splits write fp32 partials, and a reduce launch sums them in split order.  Forward tiles keep their
+// LoRA K-steps out of the dense splits and cut them only at chunk boundaries, so every row's own adapter columns
+// sit in one split: a row's sum is (dense splits, in K order) + (its LoRA term) + exact zeros, whatever the other
+// rows of its tile, and stays independent of the segment and pool order.  Backward tiles hold one adapter; their
+// LoRA K-steps go with the last dense split.
+#ifndef LORA_MAIN_TARGET_ITEMS
+#define LORA_MAIN_TARGET_ITEMS 114
+#endif
+constexpr int kMainTargetItems = LORA_MAIN_TARGET_ITEMS;
 constexpr int kMainPartialFloats = kBN * kTileM;   // one CTA's fp32 partial of a 128 x 256 output tile
 
 struct GradGroup {    // one fine-tuning adapter of a backward call

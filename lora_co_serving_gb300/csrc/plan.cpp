@@ -4,7 +4,6 @@
 #include <algorithm>
 #include <cstring>
 #include <iterator>
-#include <queue>
 #include <utility>
 
 namespace lora {
@@ -236,40 +235,66 @@ static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t
 // Main items of the M = 256 pass: one per (tile pair, 256 output columns), bands of kBandTiles tiles sweeping all
 // output columns before the next band (L2 reuse of the band's rows).  tile_of(q, nt): first tile of the pair
 // that output tile (pair q, column tile nt) reads (a sliced forward reads the copy of its slice).
+//
+// Few output tiles (less than ~1.5 waves of CTA pairs): the K loop of every output tile is split (see
+// kMainTargetItems).  The number of dense splits is the same for every tile of the call; forward LoRA splits are
+// cut at chunk boundaries and hold about as many k-blocks as a dense split.
 template <class TileOf>
 static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk, size_t n_pairs, TileOf tile_of) {
     const size_t band = kBandTiles / 2;
-    // Few output tiles: split their dense K loop (the LoRA K-steps go with the last split).  Backward only:
-    // a fine-tuning tile holds one adapter at LoRA column 0, so the split leaves every row's summation order
-    // independent of the pool order; forward decode tiles would not be (see kMainTargetItems).
     const int64_t tiles_out = (int64_t)n_pairs * n_nt;
-    int32_t nsplit = 1;
-    if (kind == kMainDx && tiles_out > 0 && tiles_out < kMainTargetItems)
-        nsplit = int32_t(std::max<int64_t>(1, std::min<int64_t>({cdiv(kMainTargetItems, tiles_out), nk / 4, 16})));
+    int32_t nsb = 1;
+    if (tiles_out > 0 && tiles_out < kMainTargetItems)
+        nsb = int32_t(std::max<int64_t>(1, std::min<int64_t>({cdiv(kMainTargetItems, tiles_out), nk / 4, 16})));
+    const bool fwd = (kind == kMainFwd);
+    const bool split = nsb > 1 || (fwd && tiles_out > 0 && tiles_out < kMainTargetItems);
+    std::vector<int32_t> cuts;       // LoRA split bounds (Z columns) of the current pair
     for (size_t b0 = 0; b0 < n_pairs; b0 += band) {
         const size_t b1 = std::min(n_pairs, b0 + band);
         for (int32_t nt = 0; nt < n_nt; ++nt)
             for (size_t q = b0; q < b1; ++q) {
+                const int32_t tile = tile_of(q, nt);
+                const TileDesc& td = pl->tiles[tile];
+                cuts.assign(1, 0);
+                if (split && fwd && td.ext_k > 0) {
+                    // chunk-aligned LoRA splits of about one dense split's k-blocks each
+                    const int32_t target = std::max<int32_t>(kBK, int32_t(cdiv(nk, nsb)) * kBK);
+                    for (int32_t c = 0; c < td.nchunk; ++c) {
+                        const Chunk& ch = pl->chunks[td.chunk0 + c];
+                        const int32_t end = (c + 1 < td.nchunk) ? pl->chunks[td.chunk0 + c + 1].zcol : td.ext_k;
+                        if (end - cuts.back() >= target || c + 1 == td.nchunk) cuts.push_back(end);
+                        (void)ch;
+                    }
+                }
+                const int32_t n_lora = split && fwd ? int32_t(cuts.size()) - 1 : 0;
+                const int32_t nsplit = split ? nsb + n_lora : 1;
                 const int32_t slot0 = int32_t(pl->main_slots);
-                const int32_t cnt0 = int32_t(4 * pl->units.size() + pl->main_counters);   // after the shrink counters
                 for (int32_t sp = 0; sp < nsplit; ++sp) {
                     WorkItem w{};
                     w.kind = kind;
-                    w.tile = tile_of(q, nt);
+                    w.tile = tile;
                     w.n0 = nt * kBN;
-                    w.kb0 = int32_t((int64_t)sp * nk / nsplit);
-                    w.nk = int32_t((int64_t)(sp + 1) * nk / nsplit) - w.kb0;
                     w.mma_n = kBN;
-                    w.n_ext = (sp == nsplit - 1) ? int32_t(cdiv(pl->tiles[w.tile].ext_k, kBK)) : 0;
                     w.nsplit = nsplit;
                     w.split = sp;
                     w.part = slot0;
-                    w.counter = cnt0;
+                    if (sp < nsb) {                       // dense k-blocks [kb0, kb0 + nk)
+                        w.kb0 = int32_t((int64_t)sp * nk / nsb);
+                        w.nk = int32_t((int64_t)(sp + 1) * nk / nsb) - w.kb0;
+                    }
+                    if (!split || (!fwd && sp == nsb - 1)) {   // the whole LoRA range
+                        w.ext_c0 = 0;
+                        w.ext_c1 = td.ext_k;
+                    } else if (sp >= nsb) {               // a forward LoRA split
+                        w.ext_c0 = cuts[sp - nsb];
+                        w.ext_c1 = cuts[sp - nsb + 1];
+                    }
+                    w.n_ext = (w.ext_c1 > w.ext_c0) ? int32_t(cdiv(w.ext_c1, kBK) - w.ext_c0 / kBK) : 0;
                     pl->items[1].push_back(w);
                 }
                 if (nsplit > 1) {
+                    pl->splits.push_back(SplitTile{tile, nt * kBN, slot0, nsplit});
                     pl->main_slots += nsplit;
-                    pl->main_counters += 8;
                 }
             }
     }
@@ -343,12 +368,21 @@ void plan_forward(const Problem& p, Plan* out) {
     // items: shrink passes (per slice region), then main items banded for L2 reuse
     const int32_t nk = int32_t(cdiv(p.K, kBK));
     const size_t n_orig = pl.tiles.size();
+    const int64_t nsplit = std::max<int64_t>(1, cdiv(nk, shrink_split_kb(p.T)));
+    auto shrink_items = [&](int32_t width) {
+        int64_t n = 0;
+        for (size_t ti = 0; ti < n_orig; ++ti)
+            n += p.S * cdiv(std::max(0, pl.tiles[ti].sh_c1 - pl.tiles[ti].sh_c0), width);
+        return n * nsplit;
+    };
+    int32_t width = kPassCols;
+    while (width > 64 && shrink_items(width) < kShrinkTargetItems) width /= 2;
     for (size_t ti = 0; ti < n_orig; ++ti) {
         const TileDesc& td = pl.tiles[ti];
         for (int32_t reg = 0; reg < p.S; ++reg) {
             const int32_t base = reg * td.zstride;
-            for (int32_t c0 = base + td.sh_c0; c0 < base + td.sh_c1; c0 += kPassCols)
-                add_shrink(&pl, kShrinkFwd, int32_t(ti), c0, std::min(kPassCols, base + td.sh_c1 - c0), nk);
+            for (int32_t c0 = base + td.sh_c0; c0 < base + td.sh_c1; c0 += width)
+                add_shrink(&pl, kShrinkFwd, int32_t(ti), c0, std::min(width, base + td.sh_c1 - c0), nk);
         }
     }
     // sliced: one copy of every tile per further slice, its Z starting at that slice's region
@@ -497,23 +531,40 @@ static int64_t item_cost(const WorkItem& w) {
 
 void assign_items(const std::vector<WorkItem>& items, const Plan&, int G, std::vector<int32_t>* off,
                   std::vector<int32_t>* list) {
-    std::vector<std::vector<int32_t>> per(G);
-    using E = std::pair<int64_t, int32_t>;
-    std::priority_queue<E, std::vector<E>, std::greater<E>> heap;
-    for (int c = 0; c < G; ++c) heap.push({0, c});
+    // min-heap of (load, CTA) in a flat array: each item goes to the least-loaded CTA (ties: lowest index)
+    struct Slot {
+        int64_t load;
+        int32_t cta;
+    };
+    auto less = [](const Slot& a, const Slot& b) { return a.load < b.load || (a.load == b.load && a.cta < b.cta); };
+    std::vector<Slot> heap(G);
+    for (int c = 0; c < G; ++c) heap[c] = Slot{0, c};
+    std::vector<int32_t> owner(items.size());
+    std::vector<int32_t> count(G + 1, 0);
     for (size_t i = 0; i < items.size(); ++i) {
-        E e = heap.top();
-        heap.pop();
-        per[e.second].push_back(int32_t(i));
-        heap.push({e.first + item_cost(items[i]), e.second});
+        Slot top = heap[0];
+        owner[i] = top.cta;
+        count[top.cta + 1]++;
+        top.load += item_cost(items[i]);
+        // sift the grown root down
+        size_t j = 0;
+        for (;;) {
+            const size_t l = 2 * j + 1, r = l + 1;
+            size_t best = j;
+            const Slot* bs = &top;
+            if (l < heap.size() && less(heap[l], *bs)) { best = l; bs = &heap[l]; }
+            if (r < heap.size() && less(heap[r], *bs)) { best = r; bs = &heap[r]; }
+            if (best == j) break;
+            heap[j] = heap[best];
+            j = best;
+        }
+        heap[j] = top;
     }
     off->assign(G + 1, 0);
-    list->clear();
-    for (int c = 0; c < G; ++c) {
-        (*off)[c] = int32_t(list->size());
-        list->insert(list->end(), per[c].begin(), per[c].end());
-    }
-    (*off)[G] = int32_t(list->size());
+    for (int c = 0; c < G; ++c) (*off)[c + 1] = (*off)[c] + count[c + 1];
+    list->assign(items.size(), 0);
+    std::vector<int32_t> at(off->begin(), off->end() - 1);
+    for (size_t i = 0; i < items.size(); ++i) (*list)[at[owner[i]]++] = int32_t(i);
 }
 
 size_t simt_scratch_bytes(const Problem& p) {
@@ -527,7 +578,7 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     size_t at = 0;
     auto take = [&](size_t bytes) { size_t o = at; at = align256(at + bytes); return o; };
     L.status = take(256);
-    L.counters = take(sizeof(int32_t) * (4 * pl.units.size() + pl.main_counters));
+    L.counters = take(sizeof(int32_t) * 4 * pl.units.size());
     L.zero_end = at;
     L.tiles = take(sizeof(TileDesc) * pl.tiles.size());
     L.chunks = take(sizeof(Chunk) * pl.chunks.size());
@@ -540,6 +591,7 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     L.atoms_b = take(sizeof(int32_t) * pl.atoms_b.size());
     L.units = take(sizeof(ShrinkUnit) * pl.units.size());
     L.seg_flags = take(sizeof(int32_t) * ((size_t)p.n_train + 1));
+    L.splits = take(sizeof(SplitTile) * pl.splits.size());
     for (int k = 0; k < 3; ++k) {
         L.items[k] = take(sizeof(WorkItem) * pl.items[k].size());
         L.cta_off[k] = take(sizeof(int32_t) * (std::max<size_t>(kMaxCtas, pl.items[k].size()) + 1));

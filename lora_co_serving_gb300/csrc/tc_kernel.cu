@@ -626,19 +626,22 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
             }
             ring.next();
         }
-        // LoRA k-blocks: this tile's Z block and, per 8-row atom of stacked adapter rows, two 64-column MN boxes
+        // LoRA k-blocks: this tile's Z block and, per 8-row atom of stacked adapter rows, two 64-column MN boxes;
+        // only the atoms of the item's LoRA columns [ext_c0, ext_c1)
         const CUtensorMap* mp = fwd ? &P.tm_pb : &P.tm_pa;
         const int32_t* atoms = (fwd ? P.atoms_b : P.atoms_a) + td.atom0;
-        for (int e = 0; e < w.n_ext; ++e) {
-            const int natoms = min(8, (td.ext_k - e * kBK) / 8);
-            if (!acquire_stage2(ring, bar_full, bar_empty, kZBlockBytes + natoms * 2048, leader, lane, abort_flag,
+        const int e0 = w.ext_c0 / kBK;
+        for (int e = e0; e < e0 + w.n_ext; ++e) {
+            const int q0 = (max(w.ext_c0, e * kBK) - e * kBK) / 8;
+            const int q1 = (min(w.ext_c1, e * kBK + kBK) - e * kBK) / 8;
+            if (!acquire_stage2(ring, bar_full, bar_empty, kZBlockBytes + (q1 - q0) * 2048, leader, lane, abort_flag,
                                 P.status))
                 return;
             const uint32_t full = full_leader + ring.stage * 8;
             const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
             if (lane == 0) tma_load_2d_pair(sa, &P.tm_z, 0, (td.z_blk0 + e) * kTileM, full);
-            if (lane < natoms * 2) {
-                const int q = lane >> 1, m = lane & 1;
+            if (lane < (q1 - q0) * 2) {
+                const int q = q0 + (lane >> 1), m = lane & 1;
                 tma_load_2d_pair(sb + m * 8192 + q * 1024, mp, nb + 64 * m, atoms[e * 8 + q], full);
             }
             ring.next();
@@ -657,12 +660,12 @@ __device__ void run_mma2(const KParams& P, uint8_t* smem, uint32_t bar_full, uin
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)acc * kBN;
         uint32_t accumulate = 0;
-        auto kblock = [&](int steps, uint32_t idesc, int b_mn) -> bool {
+        auto kblock = [&](int k0, int k1, uint32_t idesc, int b_mn) -> bool {
             const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
             if (!wait_phase(full, ring.phase, abort_flag, P.status)) return false;
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
-            for (int k = 0; k < steps; ++k) {
+            for (int k = k0; k < k1; ++k) {
                 const uint64_t ad = smem_desc(sa + k * 32, 16, 1024);
                 const uint64_t bd = b_mn ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
                 mma_bf16_pair(d, ad, bd, idesc, accumulate);
@@ -675,10 +678,12 @@ __device__ void run_mma2(const KParams& P, uint8_t* smem, uint32_t bar_full, uin
         const int b_mn = (w.kind == kMainDx) ? 1 : 0;
         const uint32_t id_main = instr_desc(2 * kTileM, kBN, 0, b_mn);
         bool ok = true;
-        for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id_main, b_mn);
-        const TileDesc td = P.tiles[w.tile];
+        for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(0, 4, id_main, b_mn);
         const uint32_t id_ext = instr_desc(2 * kTileM, kBN, 0, 1);
-        for (int e = 0; e < w.n_ext && ok; ++e) ok = kblock(min(4, (td.ext_k - e * kBK) / 16), id_ext, 1);
+        const int e0 = w.ext_c0 / kBK;
+        for (int e = e0; e < e0 + w.n_ext && ok; ++e)
+            ok = kblock((max(w.ext_c0, e * kBK) - e * kBK) / 16, (min(w.ext_c1, e * kBK + kBK) - e * kBK) / 16,
+                        id_ext, 1);
         if (!ok) return;
         mma_commit_pair(bar_tfull + acc * 8);
         acc ^= 1;
@@ -715,7 +720,8 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
         tc_fence_after();
         const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);
         const int32_t t = P.rowmap[(w.tile + rank) * kTileM + row];
-        // K-split tiles: this split's fp32 partial goes to its slot, column-major [256][128] per CTA
+        // K-split tiles: this split's fp32 partial goes to its slot, column-major [256][128] per CTA (coalesced
+        // across the warp's rows; rows without a token are skipped); the reduce launch sums the slots
         float* part = (w.nsplit > 1)
                           ? P.part_main + ((size_t)(w.part + w.split) * 2 + rank) * kMainPartialFloats + row
                           : nullptr;
@@ -728,41 +734,16 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
             }
+            if (t < 0) continue;
             if (part) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) part[(size_t)(c + i) * kTileM] = v[i];
-            } else if (t >= 0) {
+                for (int i = 0; i < 32; ++i) __stcg(part + (size_t)(c + i) * kTileM, v[i]);
+            } else {
                 store_row_bf16(P, t, w.n0 + c, v);
             }
         }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
-        if (part) {
-            // the last split to finish this row quarter sums the splits in split order and writes y
-            __threadfence();
-            __syncwarp();
-            int32_t* cnt = P.counters + w.counter + rank * 4 + quarter;
-            int last = 0;
-            if (lane == 0) last = (atomicAdd(cnt, 1) == w.nsplit - 1) ? 1 : 0;
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-                __threadfence();
-                const float* p0 = P.part_main + ((size_t)w.part * 2 + rank) * kMainPartialFloats + row;
-                for (int c = 0; c < kBN; c += 32) {
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                    for (int sp = 0; sp < w.nsplit; ++sp) {
-                        const float* ps = p0 + (size_t)sp * 2 * kMainPartialFloats + (size_t)c * kTileM;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] += __ldcg(ps + (size_t)i * kTileM);
-                    }
-                    if (t >= 0) store_row_bf16(P, t, w.n0 + c, v);
-                }
-                __syncwarp();
-                if (lane == 0) *cnt = 0;                   // ready for the next call on this workspace
-            }
-        }
     }
 }
 
@@ -821,6 +802,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
+// --------------------------------------------------------------------------------------------- split reduce
+// Sums the fp32 partials of every split output tile in split order and writes the tile's rows of the output.
+// One block per (split tile, CTA half, row quarter, 64-column group); warp w sums 8 columns, lane = tile row, so
+// every partial load is one coalesced 128-byte row of the column-major partial.
+__global__ void __launch_bounds__(256) main_reduce_kernel(const SplitTile* __restrict__ splits,
+                                                          const int32_t* __restrict__ rowmap,
+                                                          const float* __restrict__ part, __nv_bfloat16* out,
+                                                          int32_t out_ld, int32_t out_cols) {
+    const int b = blockIdx.x;
+    const SplitTile st = splits[b / 32];
+    const int half = (b / 16) & 1, quarter = (b / 4) & 3, cgrp = b & 3;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int r = quarter * 32 + lane;
+    const int c0 = cgrp * 64 + warp * 8;
+    const int32_t t = rowmap[(st.tile + half) * kTileM + r];
+    const int32_t col = st.n0 + c0;
+    if (t < 0 || col + 8 > out_cols) return;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const float* p = part + ((size_t)st.part * 2 + half) * kMainPartialFloats + (size_t)c0 * kTileM + r;
+#pragma unroll 2
+    for (int sp = 0; sp < st.nsplit; ++sp) {
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = __ldcg(p + (size_t)i * kTileM);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] += a[i];
+        p += (size_t)2 * kMainPartialFloats;
+    }
+    uint4 q;
+    q.x = pack_bf16(v[0], v[1]);
+    q.y = pack_bf16(v[2], v[3]);
+    q.z = pack_bf16(v[4], v[5]);
+    q.w = pack_bf16(v[6], v[7]);
+    *reinterpret_cast<uint4*>(out + (size_t)t * out_ld + col) = q;
+}
+
 // Failure-path self-test: one thread waits, with the kernels' bounded wait, on an mbarrier that nothing ever
 // arrives on.  The wait gives up after its time limit and records LORA_ERR_TIMEOUT in the status word; the
 // kernel then returns normally, leaving the context usable.
@@ -857,6 +874,13 @@ cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream) {
         configured[dev] = 1;
     }
     lora_main2_kernel<<<2 * pairs, kThreads, tc2_smem_bytes(), stream>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t main_reduce_launch(const SplitTile* splits, int32_t n_splits, const int32_t* rowmap, const float* part,
+                               __nv_bfloat16* out, int32_t out_ld, int32_t out_cols, cudaStream_t stream) {
+    if (n_splits <= 0) return cudaSuccess;
+    main_reduce_kernel<<<n_splits * 32, 256, 0, stream>>>(splits, rowmap, part, out, out_ld, out_cols);
     return cudaGetLastError();
 }
 

@@ -64,6 +64,9 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
 size_t tc_smem_bytes();
 cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream);      // shrink and grad items, 1 CTA each
 size_t tc2_smem_bytes();
+// Sums the partials of the split output tiles (device array of n_splits records) and writes their output rows.
+cudaError_t main_reduce_launch(const SplitTile* splits, int32_t n_splits, const int32_t* rowmap, const float* part,
+                               __nv_bfloat16* out, int32_t out_ld, int32_t out_cols, cudaStream_t stream);
 cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream);    // main items, clusters of 2 CTAs
 cudaError_t selftest_timeout_launch(int32_t* status, cudaStream_t stream);
 
