@@ -65,8 +65,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting (this wait timed out, or
 // another role's did).
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
     const uint64_t t0 = global_timer();
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -77,6 +76,12 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
             return false;
         }
     }
+}
+// The first test of the phase is inlined, so a wait that is already satisfied costs no call (a call would also
+// make every load still in flight complete first).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_phase_slow(bar, parity, abort_flag, status);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
@@ -628,10 +633,18 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
         }
         // LoRA k-blocks: this tile's Z block and, per 8-row atom of stacked adapter rows, two 64-column MN boxes;
         // only the atoms of the item's LoRA columns [ext_c0, ext_c1)
+        // (lane L < 16 loads half L & 1 of 8-row atom L >> 1; its pool row is read one block ahead)
         const CUtensorMap* mp = fwd ? &P.tm_pb : &P.tm_pa;
         const int32_t* atoms = (fwd ? P.atoms_b : P.atoms_a) + td.atom0;
+        const int n_atoms = td.ext_k / 8;
         const int e0 = w.ext_c0 / kBK;
+        auto atom_row = [&](int e) -> int32_t {
+            const int i = e * 8 + (lane >> 1);
+            return (lane < 16 && i < n_atoms) ? atoms[i] : 0;
+        };
+        int32_t cur = (w.n_ext > 0) ? atom_row(e0) : 0;
         for (int e = e0; e < e0 + w.n_ext; ++e) {
+            const int32_t nxt = (e + 1 < e0 + w.n_ext) ? atom_row(e + 1) : 0;
             const int q0 = (max(w.ext_c0, e * kBK) - e * kBK) / 8;
             const int q1 = (min(w.ext_c1, e * kBK + kBK) - e * kBK) / 8;
             if (!acquire_stage2(ring, bar_full, bar_empty, kZBlockBytes + (q1 - q0) * 2048, leader, lane, abort_flag,
@@ -640,11 +653,10 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
             const uint32_t full = full_leader + ring.stage * 8;
             const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
             if (lane == 0) tma_load_2d_pair(sa, &P.tm_z, 0, (td.z_blk0 + e) * kTileM, full);
-            if (lane < (q1 - q0) * 2) {
-                const int q = q0 + (lane >> 1), m = lane & 1;
-                tma_load_2d_pair(sb + m * 8192 + q * 1024, mp, nb + 64 * m, atoms[e * 8 + q], full);
-            }
+            const int q = lane >> 1, m = lane & 1;
+            if (lane < 16 && q >= q0 && q < q1) tma_load_2d_pair(sb + m * 8192 + q * 1024, mp, nb + 64 * m, cur, full);
             ring.next();
+            cur = nxt;
         }
     }
 }
