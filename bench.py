@@ -109,7 +109,8 @@ def launches_per_step(wl, fwd_tiles=None):
     if wl.backward and any(tr for *_, tr in segs):
         n += 3                                                                              # shrink, dX, dA/dB
         pairs = sum(-(-ln // 256) for _, ln, _, tr in segs if tr and ln > 0)
-        if pairs * n_nt(wl.K) < 114 and -(-wl.N // 64) // 4 >= 2:
+        tiles, nk = pairs * n_nt(wl.K), -(-wl.N // 64)
+        if (tiles < 114 and nk // 4 >= 2) or (tiles >= 114 and 0 < tiles % 76 <= 38 and nk // 4 >= 2):
             n += 1                                                                          # split reduce
     return n
 

@@ -126,6 +126,8 @@ constexpr int kShrinkTargetItems = 148;
 #define LORA_MAIN_TARGET_ITEMS 114
 #endif
 constexpr int kMainTargetItems = LORA_MAIN_TARGET_ITEMS;
+// CTA pairs the planner sizes waves for (76 on a 152-SM GB300; plans stay valid on any device).
+constexpr int kPairsPlanned = 76;
 constexpr int kMainPartialFloats = kBN * kTileM;   // one CTA's fp32 partial of a 128 x 256 output tile
 
 struct GradGroup {    // one fine-tuning adapter of a backward call

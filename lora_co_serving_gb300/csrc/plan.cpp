@@ -243,27 +243,41 @@ template <class TileOf>
 static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk, size_t n_pairs, TileOf tile_of) {
     const size_t band = kBandTiles / 2;
     const int64_t tiles_out = (int64_t)n_pairs * n_nt;
-    int32_t nsb = 1;
+    int32_t nsb_all = 1;
     if (tiles_out > 0 && tiles_out < kMainTargetItems)
-        nsb = int32_t(std::max<int64_t>(1, std::min<int64_t>({cdiv(kMainTargetItems, tiles_out), nk / 4, 16})));
+        nsb_all = int32_t(std::max<int64_t>(1, std::min<int64_t>({cdiv(kMainTargetItems, tiles_out), nk / 4, 16})));
+    const int32_t nsb_fwd = nsb_all;
     const bool fwd = (kind == kMainFwd);
-    const bool split = nsb > 1 || (fwd && tiles_out > 0 && tiles_out < kMainTargetItems);
+    const bool split_all = nsb_all > 1 || (fwd && tiles_out > 0 && tiles_out < kMainTargetItems);
+    // dX: when the output tiles leave a last, partly filled wave of CTA pairs, the last ones in item order are
+    // split so that the last wave runs short items (backward tiles follow the fine-tuning segments in start order,
+    // so which rows are split does not depend on the segment or pool order)
+    int64_t tail_from = tiles_out;
+    int32_t nsb_tail = 1;
+    if (!split_all && kind == kMainDx) {
+        const int64_t rem = tiles_out % kPairsPlanned;
+        if (rem > 0 && kPairsPlanned / rem >= 2) {
+            nsb_tail = int32_t(std::min<int64_t>({kPairsPlanned / rem, nk / 4, 8}));
+            if (nsb_tail > 1) tail_from = tiles_out - rem;
+        }
+    }
+    int64_t o = 0;                   // output tiles emitted so far
     std::vector<int32_t> cuts;       // LoRA split bounds (Z columns) of the current pair
     for (size_t b0 = 0; b0 < n_pairs; b0 += band) {
         const size_t b1 = std::min(n_pairs, b0 + band);
         for (int32_t nt = 0; nt < n_nt; ++nt)
-            for (size_t q = b0; q < b1; ++q) {
+            for (size_t q = b0; q < b1; ++q, ++o) {
                 const int32_t tile = tile_of(q, nt);
                 const TileDesc& td = pl->tiles[tile];
+                const bool split = split_all || o >= tail_from;
+                const int32_t nsb = split_all ? nsb_all : (o >= tail_from ? nsb_tail : 1);
                 cuts.assign(1, 0);
                 if (split && fwd && td.ext_k > 0) {
                     // chunk-aligned LoRA splits of about one dense split's k-blocks each
-                    const int32_t target = std::max<int32_t>(kBK, int32_t(cdiv(nk, nsb)) * kBK);
+                    const int32_t target = std::max<int32_t>(kBK, int32_t(cdiv(nk, nsb_fwd)) * kBK);
                     for (int32_t c = 0; c < td.nchunk; ++c) {
-                        const Chunk& ch = pl->chunks[td.chunk0 + c];
                         const int32_t end = (c + 1 < td.nchunk) ? pl->chunks[td.chunk0 + c + 1].zcol : td.ext_k;
                         if (end - cuts.back() >= target || c + 1 == td.nchunk) cuts.push_back(end);
-                        (void)ch;
                     }
                 }
                 const int32_t n_lora = split && fwd ? int32_t(cuts.size()) - 1 : 0;
