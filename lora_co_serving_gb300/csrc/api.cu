@@ -173,6 +173,8 @@ void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&of
     put(b, at(L.tsegs), pl.tsegs);
     put(b, at(L.atoms_a), pl.atoms_a);
     put(b, at(L.atoms_b), pl.atoms_b);
+    put(b, at(L.boxes_a), pl.boxes_a);
+    put(b, at(L.boxes_b), pl.boxes_b);
     put(b, at(L.units), pl.units);
     put(b, at(L.splits), pl.splits);
     for (int k = 0; k < 3; ++k) {
@@ -195,6 +197,8 @@ void fill_plan_pointers(KParams* P, uint8_t* ws, const Layout& L, int launch) {
     P->cta_list = reinterpret_cast<const int32_t*>(ws + L.cta_list[launch]);
     P->atoms_a = reinterpret_cast<const int32_t*>(ws + L.atoms_a);
     P->atoms_b = reinterpret_cast<const int32_t*>(ws + L.atoms_b);
+    P->boxes_a = reinterpret_cast<const int32_t*>(ws + L.boxes_a);
+    P->boxes_b = reinterpret_cast<const int32_t*>(ws + L.boxes_b);
     P->part = reinterpret_cast<float*>(ws + L.part);
     P->part_main = reinterpret_cast<float*>(ws + L.part_main);
     P->units = reinterpret_cast<const ShrinkUnit*>(ws + L.units);
@@ -575,6 +579,8 @@ int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x
         return fail(LORA_ERR_CUDA, err);
     if (p.rows_a > 0 && !encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (p.rows_b > 0 && !encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    for (int h = 0; h < 3 && p.rows_b > 0; ++h)        // taller boxes for runs of consecutive atoms (main pass)
+        if (!encode_2d(&P.tm_pb_h[h], pool->B, N, p.rows_b, N, 64, 16u << h, &err)) return fail(LORA_ERR_CUDA, err);
     P.zin = ws + L.z;
     P.zout = ws + L.z;
     P.out = static_cast<__nv_bfloat16*>(y);
@@ -711,6 +717,8 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
     if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
+    for (int h = 0; h < 3; ++h)                         // taller boxes for runs of consecutive atoms (dX pass)
+        if (!encode_2d(&P.tm_pa_h[h], pool->A, K, p.rows_a, K, 64, 16u << h, &err)) return fail(LORA_ERR_CUDA, err);
     const uint64_t trows = (uint64_t)p.S * LORA_MAX_RANK;
     if (!encode_2d(&P.tm_xat, ws + L.xat, Pcols, trows, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_dybt, ws + L.dybt, Pcols, trows, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);

@@ -157,6 +157,7 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
     // pool row of every 8-column atom; the padding of a chunk to 16 repeats its last atom, so every loaded row
     // stays inside the adapter's own block (sliced: the slice's own rows or the next slice's)
     const int32_t atom0 = int32_t(pl->atoms_a.size());
+    std::vector<uint8_t> brk;        // per atom: starts a chunk's (or a slice's, or a region padding's) columns
     const int32_t n_reg = (S > 1 && !side_by_side) ? S : 1;
     const int32_t W = (n_reg > 1) ? int32_t(cdiv(zcol, kBK) * kBK) : zcol;
     for (int32_t reg = 0; reg < n_reg; ++reg) {
@@ -169,14 +170,36 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
                 for (int32_t o = 0; o < pad16(ch.r); o += 8) {
                     pl->atoms_a.push_back(ch.prow_a + sl * ch.r + std::min(o, last));
                     pl->atoms_b.push_back(ch.prow_b + std::min(o, last));
+                    brk.push_back(o == 0 ? 1 : 0);
                 }
             }
         }
         for (int32_t o = zcol; o < W; o += 8) {     // region padding: any in-pool row (its columns are masked)
             pl->atoms_a.push_back(pl->atoms_a.back());
             pl->atoms_b.push_back(pl->atoms_b.back());
+            brk.push_back(1);
         }
     }
+    // TMA boxes: runs of atoms whose pool rows follow one another, cut at chunk starts and at 64-column blocks
+    // (relative to the tile's first LoRA column), split greedily into 8-, 4-, 2- and 1-atom boxes
+    auto boxes_of = [&](const std::vector<int32_t>& rows, std::vector<int32_t>* out) {
+        const size_t n = brk.size();
+        for (size_t i = 0; i < n;) {
+            size_t j = i + 1;
+            while (j < n && (j % 8) != 0 && !brk[j] && rows[atom0 + j] == rows[atom0 + j - 1] + 8) ++j;
+            size_t k = i;
+            while (k < j) {
+                int32_t h = 8;
+                while (size_t(h) > j - k) h >>= 1;
+                out->push_back(h);
+                for (int32_t t = 1; t < h; ++t) out->push_back(0);
+                k += size_t(h);
+            }
+            i = j;
+        }
+    };
+    boxes_of(pl->atoms_a, &pl->boxes_a);
+    boxes_of(pl->atoms_b, &pl->boxes_b);
     const int32_t zstride = (S == 1) ? 0 : (side_by_side ? 0 : W);
     const int32_t z_cols = n_reg * W;
     TileDesc* td[2] = {&t0, &t1};
@@ -603,6 +626,8 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     L.tsegs = take(sizeof(TrainSeg) * pl.tsegs.size());
     L.atoms_a = take(sizeof(int32_t) * pl.atoms_a.size());
     L.atoms_b = take(sizeof(int32_t) * pl.atoms_b.size());
+    L.boxes_a = take(sizeof(int32_t) * pl.boxes_a.size());
+    L.boxes_b = take(sizeof(int32_t) * pl.boxes_b.size());
     L.units = take(sizeof(ShrinkUnit) * pl.units.size());
     L.seg_flags = take(sizeof(int32_t) * ((size_t)p.n_train + 1));
     L.splits = take(sizeof(SplitTile) * pl.splits.size());

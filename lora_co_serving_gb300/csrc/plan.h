@@ -54,6 +54,9 @@ struct Plan {
     std::vector<int32_t> rowaux;     // 128 per tile: forward: xa_save element offset or -1; backward: -1
     std::vector<int32_t> atoms_a;    // per tile, per 8 LoRA columns: first A-pool row of that 8-row atom
     std::vector<int32_t> atoms_b;    // same for the B pool
+    std::vector<int32_t> boxes_a;    // per atom: atoms loaded by one TMA box starting at it (1, 2, 4 or 8: a run of
+    std::vector<int32_t> boxes_b;    //   consecutive pool rows inside one chunk and one 64-column block), 0 if an
+                                     //   earlier atom's box covers it
     std::vector<WorkItem> items[3];  // shrink items (1-CTA kernel), main pair items (2-CTA kernel), grad items
     std::vector<ShrinkUnit> units;   // shrink passes (each finalized by its last K-split)
     std::vector<GradGroup> groups;
@@ -84,7 +87,7 @@ struct Layout {
     size_t status = 0;
     size_t counters = 0, zero_end = 0;   // [status, zero_end) is zeroed at the start of every call
     size_t tiles = 0, chunks = 0, rowmap = 0, rowchunk = 0, rowaux = 0, groups = 0, tsegs = 0;
-    size_t atoms_a = 0, atoms_b = 0, units = 0, seg_flags = 0, splits = 0;
+    size_t atoms_a = 0, atoms_b = 0, boxes_a = 0, boxes_b = 0, units = 0, seg_flags = 0, splits = 0;
     size_t items[3] = {0, 0, 0}, cta_off[3] = {0, 0, 0}, cta_list[3] = {0, 0, 0};
     size_t plan_end = 0;
     size_t xg = 0, z = 0, xat = 0, dybt = 0, part = 0, part_main = 0;

@@ -633,18 +633,25 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
         }
         // LoRA k-blocks: this tile's Z block and, per 8-row atom of stacked adapter rows, two 64-column MN boxes;
         // only the atoms of the item's LoRA columns [ext_c0, ext_c1)
-        // (lane L < 16 loads half L & 1 of 8-row atom L >> 1; its pool row is read one block ahead)
+        // (lane L < 16 loads half L & 1 of the box that starts at 8-row atom L >> 1, if one does: a run of atoms with
+        // consecutive pool rows inside one chunk comes as one box of 16, 32 or 64 rows; the atom's pool row and box
+        // size are read one block ahead)
         const CUtensorMap* mp = fwd ? &P.tm_pb : &P.tm_pa;
+        const CUtensorMap* mph = fwd ? P.tm_pb_h : P.tm_pa_h;
         const int32_t* atoms = (fwd ? P.atoms_b : P.atoms_a) + td.atom0;
+        const int32_t* boxes = (fwd ? P.boxes_b : P.boxes_a) + td.atom0;
         const int n_atoms = td.ext_k / 8;
         const int e0 = w.ext_c0 / kBK;
-        auto atom_row = [&](int e) -> int32_t {
+        auto atom_at = [&](int e, int32_t* box) -> int32_t {
             const int i = e * 8 + (lane >> 1);
-            return (lane < 16 && i < n_atoms) ? atoms[i] : 0;
+            const bool in = lane < 16 && i < n_atoms;
+            *box = in ? boxes[i] : 0;
+            return in ? atoms[i] : 0;
         };
-        int32_t cur = (w.n_ext > 0) ? atom_row(e0) : 0;
+        int32_t cur_box = 0, nxt_box = 0;
+        int32_t cur = (w.n_ext > 0) ? atom_at(e0, &cur_box) : 0;
         for (int e = e0; e < e0 + w.n_ext; ++e) {
-            const int32_t nxt = (e + 1 < e0 + w.n_ext) ? atom_row(e + 1) : 0;
+            const int32_t nxt = (e + 1 < e0 + w.n_ext) ? atom_at(e + 1, &nxt_box) : 0;
             const int q0 = (max(w.ext_c0, e * kBK) - e * kBK) / 8;
             const int q1 = (min(w.ext_c1, e * kBK + kBK) - e * kBK) / 8;
             if (!acquire_stage2(ring, bar_full, bar_empty, kZBlockBytes + (q1 - q0) * 2048, leader, lane, abort_flag,
@@ -654,9 +661,13 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
             const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
             if (lane == 0) tma_load_2d_pair(sa, &P.tm_z, 0, (td.z_blk0 + e) * kTileM, full);
             const int q = lane >> 1, m = lane & 1;
-            if (lane < 16 && q >= q0 && q < q1) tma_load_2d_pair(sb + m * 8192 + q * 1024, mp, nb + 64 * m, cur, full);
+            if (lane < 16 && q >= q0 && q < q1 && cur_box > 0) {
+                const CUtensorMap* map = (cur_box == 1) ? mp : mph + (cur_box == 2 ? 0 : (cur_box == 4 ? 1 : 2));
+                tma_load_2d_pair(sb + m * 8192 + q * 1024, map, nb + 64 * m, cur, full);
+            }
             ring.next();
             cur = nxt;
+            cur_box = nxt_box;
         }
     }
 }

@@ -19,6 +19,8 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     CUtensorMap tm_w;      // Wt [N, K]: forward box {64, 128} (K-major B half); backward box {64, 64} (MN-major)
     CUtensorMap tm_pa;     // A pool viewed as [rows, K], box {64, 8}
     CUtensorMap tm_pb;     // B pool viewed as [rows, N], box {64, 8}
+    CUtensorMap tm_pa_h[3];  // A pool with boxes of 16, 32 and 64 rows (runs of 2, 4, 8 atoms)
+    CUtensorMap tm_pb_h[3];  // B pool, same
     CUtensorMap tm_xat;    // xA^T  [128, P], box {64, 8}
     CUtensorMap tm_dybt;   // dYB^T [128, P], box {64, 8}
     CUtensorMap tm_z;      // Z blocks as [blocks*128, 64] bf16 rows of 128 B, box {64, 128}, no swizzle (the blocks
@@ -38,6 +40,8 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     const int32_t* cta_list;
     const int32_t* atoms_a;  // per tile, per 8 LoRA columns: A-pool row of the atom
     const int32_t* atoms_b;  // same for the B pool
+    const int32_t* boxes_a;  // per atom: atoms in the TMA box that starts at it (0: covered by an earlier box)
+    const int32_t* boxes_b;
     float* part;             // shrink items: fp32 partial sums, [columns][128 rows]
     float* part_main;        // split main items: fp32 partial tiles, [slot][CTA][256 columns][128 rows]
     const int32_t* seg_flags;  // backward with a per-segment flag table: snapshot, nonzero = saved xA is used
