@@ -579,8 +579,12 @@ int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x
         return fail(LORA_ERR_CUDA, err);
     if (p.rows_a > 0 && !encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (p.rows_b > 0 && !encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    for (int h = 0; h < 3 && p.rows_b > 0; ++h)        // taller boxes for runs of consecutive atoms (main pass)
-        if (!encode_2d(&P.tm_pb_h[h], pool->B, N, p.rows_b, N, 64, 16u << h, &err)) return fail(LORA_ERR_CUDA, err);
+    for (int h = 0; h < 3; ++h) {      // taller boxes for runs of consecutive atoms (shrink: A rows; main: B rows)
+        if (p.rows_a > 0 && !encode_2d(&P.tm_pa_h[h], pool->A, K, p.rows_a, K, 64, 16u << h, &err))
+            return fail(LORA_ERR_CUDA, err);
+        if (p.rows_b > 0 && !encode_2d(&P.tm_pb_h[h], pool->B, N, p.rows_b, N, 64, 16u << h, &err))
+            return fail(LORA_ERR_CUDA, err);
+    }
     P.zin = ws + L.z;
     P.zout = ws + L.z;
     P.out = static_cast<__nv_bfloat16*>(y);
@@ -717,8 +721,10 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
     if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    for (int h = 0; h < 3; ++h)                         // taller boxes for runs of consecutive atoms (dX pass)
+    for (int h = 0; h < 3; ++h) {      // taller boxes for runs of consecutive atoms (shrinks and the dX pass)
         if (!encode_2d(&P.tm_pa_h[h], pool->A, K, p.rows_a, K, 64, 16u << h, &err)) return fail(LORA_ERR_CUDA, err);
+        if (!encode_2d(&P.tm_pb_h[h], pool->B, N, p.rows_b, N, 64, 16u << h, &err)) return fail(LORA_ERR_CUDA, err);
+    }
     const uint64_t trows = (uint64_t)p.S * LORA_MAX_RANK;
     if (!encode_2d(&P.tm_xat, ws + L.xat, Pcols, trows, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_dybt, ws + L.dybt, Pcols, trows, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);

@@ -201,13 +201,21 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
         const CUtensorMap* mp = use_b ? &P.tm_pb : &P.tm_pa;
         const int natoms = w.mma_n / 8;
         const int32_t my_row = (lane < natoms) ? (use_b ? P.atoms_b : P.atoms_a)[td.atom0 + w.n0 / 8 + lane] : 0;
+        // atom `lane` of the pass comes in a taller box when a run of atoms with consecutive pool rows starts at it
+        // and ends inside the pass; atoms that no such box covers come one by one
+        const int32_t my_box = (lane < natoms) ? (use_b ? P.boxes_b : P.boxes_a)[td.atom0 + w.n0 / 8 + lane] : 0;
+        const bool lead = my_box > 1 && lane + my_box <= natoms;
+        const uint32_t covered = __reduce_or_sync(0xffffffffu, lead ? (((1u << my_box) - 1u) << lane) : 0u);
+        const int n_mine = (lane >= natoms) ? 0 : (lead ? my_box : (((covered >> lane) & 1u) ? 0 : 1));
+        const CUtensorMap* my_map =
+            (n_mine <= 1) ? mp : (use_b ? P.tm_pb_h : P.tm_pa_h) + (n_mine == 2 ? 0 : (n_mine == 4 ? 1 : 2));
         for (int kb = w.kb0; kb < w.kb0 + w.nk; ++kb) {
             if (!acquire_stage(ring, bar_full, bar_empty, kABytes + natoms * 1024, lane, abort_flag, P.status))
                 return;
             const uint32_t full = bar_full + ring.stage * 8;
             const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
             if (lane == 0) tma_load_2d(sa, ma, kb * kBK, td.a_row0, full);
-            if (lane < natoms) tma_load_2d(sb + lane * 1024, mp, kb * kBK, my_row, full);
+            if (n_mine > 0) tma_load_2d(sb + lane * 1024, my_map, kb * kBK, my_row, full);
             ring.next();
         }
     }
