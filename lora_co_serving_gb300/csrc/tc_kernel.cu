@@ -23,6 +23,8 @@
 #include "common.h"
 #include "tc_kernel.h"
 
+#include <utility>
+
 namespace lora {
 
 namespace {
@@ -92,6 +94,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
 }
+
+// Programmatic dependent launch: the kernels of a call are launched so that each may start (its prologue: barrier
+// setup, TMEM allocation) while the previous one drains; this wait holds the CTA until every earlier kernel of the
+// stream has finished and its writes are visible, before anything it produced (or the caller's inputs) is read.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -480,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) lora_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dep_wait();
     const int i0 = P.cta_off[blockIdx.x], i1 = P.cta_off[blockIdx.x + 1];
 
     if (warp == 0) {
@@ -813,6 +821,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dep_wait();
     const int pair = blockIdx.x >> 1;
     const int i0 = P.cta_off[pair], i1 = P.cta_off[pair + 1];
 
@@ -841,6 +850,7 @@ __global__ void __launch_bounds__(256) main_reduce_kernel(const SplitTile* __res
                                                           const int32_t* __restrict__ rowmap,
                                                           const float* __restrict__ part, __nv_bfloat16* out,
                                                           int32_t out_ld, int32_t out_cols) {
+    grid_dep_wait();
     const int b = blockIdx.x;
     const SplitTile st = splits[b / 32];
     const int half = (b / 16) & 1, quarter = (b / 4) & 3, cgrp = b & 3;
@@ -894,6 +904,23 @@ cudaError_t selftest_timeout_launch(int32_t* status, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// cudaLaunchKernelEx with programmatic stream serialization (see grid_dep_wait)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream) {
     static int configured[64] = {0};
     int dev = 0;
@@ -904,15 +931,14 @@ cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    lora_main2_kernel<<<2 * pairs, kThreads, tc2_smem_bytes(), stream>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(lora_main2_kernel, dim3(2 * pairs), dim3(kThreads), tc2_smem_bytes(), stream, P);
 }
 
 cudaError_t main_reduce_launch(const SplitTile* splits, int32_t n_splits, const int32_t* rowmap, const float* part,
                                __nv_bfloat16* out, int32_t out_ld, int32_t out_cols, cudaStream_t stream) {
     if (n_splits <= 0) return cudaSuccess;
-    main_reduce_kernel<<<n_splits * 32, 256, 0, stream>>>(splits, rowmap, part, out, out_ld, out_cols);
-    return cudaGetLastError();
+    return launch_pdl(main_reduce_kernel, dim3(n_splits * 32), dim3(256), 0, stream, splits, rowmap, part, out, out_ld,
+                      out_cols);
 }
 
 cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream) {
@@ -925,8 +951,7 @@ cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    lora_tc_kernel<<<grid, kThreads, tc_smem_bytes(), stream>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(lora_tc_kernel, dim3(grid), dim3(kThreads), tc_smem_bytes(), stream, P);
 }
 
 }  // namespace lora
