@@ -101,3 +101,52 @@ def test_layer_chain_matches_oracle_and_is_workspace_independent():
     for n in ORDER:
         for a, b in zip(got[n], again[n]):
             assert torch.equal(a, b), n + ": shared-workspace chain differs from per-call workspaces"
+
+
+def test_layer_full_size_sampled():
+    """The benchmark's layer (Llama-3-8B shapes, 8192-token co-serving batch, 320 adapters), every projection
+    computed in full on the GPU and checked on sampled rows and columns: a sliced projection slice by slice through
+    the plain oracle (each slice is a plain LoRA layer on the shared input), its dX as the sum over slices."""
+    import gc
+    import torch
+    import lora_co_serving_gb300 as lm
+    from test_gpu_fullsize import sample_rows
+    L = workloads.llama_layer()
+    rng = np.random.default_rng(3)
+    for n in ORDER:
+        wl = L[n]
+        d = Dev(wl)
+        if wl.bounds is not None:
+            y = lm.sliced_forward(d.x, d.Wt, d.pool, wl.bounds, d.segs)
+            dX, dA, dB = lm.sliced_backward(d.x, d.Wt, d.pool, wl.bounds, d.segs, d.dY, recompute=True)
+        else:
+            y = lm.forward(d.x, d.Wt, d.pool, d.segs)
+            dX, dA, dB = lm.backward(d.x, d.Wt, d.pool, d.segs, d.dY, recompute=True)
+        torch.cuda.synchronize()
+        y, dX, dA, dB = to_np(y), to_np(dX), to_np(dA), to_np(dB)
+        del d
+        gc.collect()
+        torch.cuda.empty_cache()
+        rows = sample_rows(wl, cap=16)
+        trows = wl.train_rows()
+        pick = trows[np.unique(np.concatenate([[0, trows.shape[0] - 1], rng.integers(0, trows.shape[0], 6)]))]
+        a = int(wl.meta["train_adapter"])
+        r = int(wl.rank[a])
+        ca = np.unique(np.concatenate([[0, wl.K - 1], rng.integers(0, wl.K, 24)]))
+        parts = [workloads.slice_of(wl, i) for i in range(wl.n_slices)] if wl.bounds is not None else [wl]
+        bounds = wl.bounds if wl.bounds is not None else np.array([0, wl.N])
+        rX = 0.0
+        for i, sw in enumerate(parts):
+            c0, c1 = int(bounds[i]), int(bounds[i + 1])
+            compare(y[rows, c0:c1], oracle.forward_wl(sw, rows=rows), "%s slice %d: y (sampled rows)" % (n, i))
+            cb = np.unique(np.concatenate([[0, sw.N - 1], rng.integers(0, sw.N, 24)]))
+            sX, sA, sB = oracle.backward_wl(sw, dx_rows=pick, cols_b=cb, cols_a=ca)
+            rX = rX + sX
+            gB = dB.reshape(-1, wl.N)[int(wl.b_off[a]) // wl.N:int(wl.b_off[a]) // wl.N + r, c0:c1][:, cb]
+            eB = sB[sw.b_off[a]:sw.b_off[a] + r * sw.N].reshape(r, sw.N)[:, cb]
+            compare(gB, eB, "%s slice %d: dB (sampled columns)" % (n, i))
+            row0 = int(wl.a_off[a]) // wl.K + i * r
+            gA = dA.reshape(-1, wl.K)[row0:row0 + r][:, ca]
+            eA = sA[sw.a_off[a]:sw.a_off[a] + r * wl.K].reshape(r, wl.K)[:, ca]
+            compare(gA, eA, "%s slice %d: dA (sampled columns)" % (n, i))
+        compare(dX[pick], rX, "%s: dX (sampled rows, summed over slices)" % n)
