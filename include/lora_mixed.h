@@ -47,6 +47,10 @@
  *     after its previous copy has completed), so the host-side segment array
  *     may be reused as soon as the call returns.
  *   - Two calls that share a workspace must not overlap on the GPU.
+ *   - CUDA graphs: a call made while `stream` is being captured records the same work into the graph and
+ *     blocks on nothing; its plan is uploaded from a pinned host copy of its own that the library keeps for
+ *     the life of the process (one per captured call), so the graph may be replayed any number of times, at
+ *     any later point.  A replay reads the device buffers and the workspace that were captured.
  *   - Kernels never wait without a bound.  If one gives up, it records a
  *     nonzero code in the workspace's status word; lora_workspace_status()
  *     reads it.
@@ -161,7 +165,8 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
  * allocates nothing.  A batch whose scratch would exceed the array is rejected with LORA_ERR_LIMIT before
  * any launch.  All calls share the array: two calls that overlap on the GPU race and must be ordered by the
  * caller.  The first call on a device looks up the array's address for that device; make it before
- * capturing a stream into a graph.  Its status word is not reachable through lora_workspace_status. */
+ * capturing a stream into a graph; a call made during a capture keeps a pinned host copy of its plan, like
+ * every other entry point.  Its status word is not reachable through lora_workspace_status. */
 #define LORA_STATIC_WORKSPACE_BYTES (64u << 20)
 int lora_mixed_forward_static(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
                               const lora_pool_t* pool, const lora_segment_t* segs /* HOST */, int32_t n_segs,

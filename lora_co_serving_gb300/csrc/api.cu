@@ -116,8 +116,32 @@ StagingRing g_rings[64];
 // straight from the (pageable) host blob instead of through the pinned ring, which allocates on first use.
 thread_local bool g_direct_upload = false;
 
+// Plans uploaded by calls made while their stream is being captured into a CUDA graph: the graph's copy node
+// reads this host memory at every replay, so each such copy is kept for the life of the process.
+std::mutex g_captured_mu;
+std::vector<void*> g_captured;
+
 int stage_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
     if (bytes == 0) return LORA_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    CUDA_TRY(cudaStreamIsCapturing(stream, &cs));
+    if (cs == cudaStreamCaptureStatusActive) {
+        // no ring slot (a later call would overwrite it before a replay) and no wait: a pinned copy of its own,
+        // allocated with this thread's capture rules relaxed (an allocation is not stream work)
+        cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+        CUDA_TRY(cudaThreadExchangeStreamCaptureMode(&mode));
+        void* h = nullptr;
+        const cudaError_t e = cudaHostAlloc(&h, bytes, cudaHostAllocPortable);
+        cudaThreadExchangeStreamCaptureMode(&mode);
+        if (e != cudaSuccess) return fail(LORA_ERR_CUDA, std::string("cudaHostAlloc: ") + cudaGetErrorString(e));
+        std::memcpy(h, src, bytes);
+        {
+            std::lock_guard<std::mutex> lock(g_captured_mu);
+            g_captured.push_back(h);
+        }
+        CUDA_TRY(cudaMemcpyAsync(dst, h, bytes, cudaMemcpyHostToDevice, stream));
+        return LORA_OK;
+    }
     if (g_direct_upload) {
         CUDA_TRY(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, stream));
         return LORA_OK;
