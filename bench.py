@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--out", default=None, help="sweep: also write the fitted coefficients to this JSON file")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
                     help="override a workload parameter (e.g. N=4096) for profiling a reduced case")
     return ap.parse_args()
@@ -355,11 +356,14 @@ def run_ours(args):
     dB = torch.zeros(B.numel(), dtype=torch.float32, device="cuda") if wl.backward else None
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step_on(st):
         if wl.forward:
-            lm.forward(x, Wt, pool, segs, y=y, xa_save=xs, save_xa=save, workspace=ws, stream=stream)
+            lm.forward(x, Wt, pool, segs, y=y, xa_save=xs, save_xa=save, workspace=ws, stream=st)
         if wl.backward:
-            lm.backward(x, Wt, pool, segs, dY, dX=dX, dA=dA, dB=dB, workspace=ws, stream=stream)
+            lm.backward(x, Wt, pool, segs, dY, dX=dX, dA=dA, dB=dB, workspace=ws, stream=st)
+
+    def step():
+        step_on(stream)
 
     for _ in range(args.warmup):
         step()
@@ -398,6 +402,41 @@ def run_ours(args):
         dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
     ms_max = float(t_max.item())
     value = acc["tokens"] * world / (ms_max / 1e3)
+
+    # ---- the same step captured once into a CUDA graph and replayed (as a serving engine replays decode steps):
+    # the library's host work (validation, planning, launches) leaves the timed region
+    graph = None
+    if not args.no_graph:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            for _ in range(2):
+                step_on(gs)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=gs):
+            step_on(gs)
+        for _ in range(3):
+            cg.replay()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        n_g = max(3, args.steps)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(gs):
+            g0.record(gs)
+            for _ in range(n_g):
+                cg.replay()
+            g1.record(gs)
+        torch.cuda.synchronize()
+        gms = torch.tensor([g0.elapsed_time(g1) / n_g], device="cuda", dtype=torch.float64)
+        if dist:
+            dist.all_reduce(gms, op=dist.ReduceOp.MAX)
+        graph = {"value": acc["tokens"] * world / (float(gms.item()) / 1e3), "unit": UNIT,
+                 "ms_per_step": float(gms.item()), "steps": n_g,
+                 "note": "one step captured into a CUDA graph, replayed back to back (no host work per step)"}
+        del cg
+        lm.workspace_status(ws)
 
     # ---- the optimizer step that follows (AdamW on the fine-tuning adapters, fp32 masters + bf16 pool), timed
     # on its own: it is not part of the forward+backward step the metric is about
@@ -540,7 +579,7 @@ def run_ours(args):
                            "l2": "inputs larger than L2 (W alone %.0f MB); no flush" % (2 * K * N / 1e6),
                            "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
                 "roofline": roof, "step": step_stats, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
-                "adamw": adamw_stats,
+                "graph_replay": graph, "adamw": adamw_stats,
                 "gpu_launches": launches_per_step(wl, fwd_tiles) * args.steps}
         print(json.dumps(line), flush=True)
     if dist:
