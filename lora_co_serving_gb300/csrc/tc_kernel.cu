@@ -520,10 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1) lora_tc_kernel(const __grid_const
 #define LORA_MAIN_STAGES 7
 #endif
 // L2 eviction priority of the main pass's TMA loads of the row operand (x / dY) and of W:
-// 0 = normal, 1 = evict_first, 2 = evict_last.  Keeping the rows of the current band of tiles resident while W
-// streams through measured +21 % on an 8192 x 8192 x 28672 product; seven 32-KB stages another +12 %.
+// 0 = normal, 1 = evict_first, 2 = evict_last.  evict_last on the rows once measured +21 % on an
+// 8192 x 8192 x 28672 product, when each k-block still paid a call into the bounded wait; since that call is
+// gone the plain policy is ~1 % faster on the co-serving step and the backward (seven 32-KB stages: +12 %).
 #ifndef LORA_HINT_ROWS
-#define LORA_HINT_ROWS 2
+#define LORA_HINT_ROWS 0
 #endif
 #ifndef LORA_HINT_W
 #define LORA_HINT_W 0
