@@ -337,7 +337,10 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    lm.build()
+    if rank == 0:
+        lm.build()                   # one rank compiles (if anything is stale); the others wait, then load it
+    if dist:
+        dist.barrier()
 
     wl = make_workload(args.config, rank, args.set)
     acc = accounting(wl)
@@ -602,7 +605,10 @@ def run_layer(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    lm.build()
+    if rank == 0:
+        lm.build()                   # one rank compiles (if anything is stale); the others wait, then load it
+    if dist:
+        dist.barrier()
     L = make_layer(rank, args.set)
     T = L["qkv"].T
     acc = {n: accounting(L[n]) for n in LAYER_ORDER}
