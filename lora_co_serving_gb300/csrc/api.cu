@@ -201,6 +201,7 @@ void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&of
     put(b, at(L.boxes_b), pl.boxes_b);
     put(b, at(L.units), pl.units);
     put(b, at(L.splits), pl.splits);
+    put(b, at(L.bgmv), pl.bgmv);
     for (int k = 0; k < 3; ++k) {
         put(b, at(L.items[k]), pl.items[k]);
         put(b, at(L.cta_off[k]), off[k]);
@@ -624,6 +625,10 @@ int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x
     if (pl.n_gtiles > 0)
         CUDA_TRY(gather_rows(x, K, reinterpret_cast<const int32_t*>(ws + L.rowmap) + (size_t)pl.g_tile0 * kTileM,
                              ws + L.xg, pl.n_gtiles * kTileM, stream));
+    if (!pl.bgmv.empty())
+        CUDA_TRY(bgmv_shrink(ws + L.xg, K, pool->A, reinterpret_cast<const BgmvGroup*>(ws + L.bgmv),
+                             int32_t(pl.bgmv.size()), reinterpret_cast<const Chunk*>(ws + L.chunks),
+                             reinterpret_cast<const TileDesc*>(ws + L.tiles), p.S, ws + L.z, stream));
     CUDA_TRY(launch_group(0, &P, ws, L, grid, stream));
     CUDA_TRY(trace(0, 1, stream));
     CUDA_TRY(trace(1, 0, stream));

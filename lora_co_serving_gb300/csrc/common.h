@@ -93,7 +93,29 @@ struct SplitTile {
     int32_t n0;       // first output column
     int32_t part;     // first partial slot
     int32_t nsplit;
+    int32_t pad0, pad1, pad2, pad3;
 };
+
+// The shrink of the gathered decode rows on CUDA cores: each run of up to kBgmvRows consecutive gathered rows that
+// share a chunk is one group; a work unit is one group and 8 of its LoRA columns.  The unit reads its adapter's 8
+// rows of A once, sums x . A_j in fp32 over K in a fixed order (so a row's value depends on its own x and A rows
+// alone) and writes Z = bf16(s * xA) into the tile's Z image, where the main pass's K-extension reads it.  Sliced
+// forward layers: LoRA column j of the group (j < S * rank) is slice j / rank's column j % rank, in that slice's
+// Z region.
+struct BgmvGroup {
+    int32_t g_row0;   // first row in the gathered buffer
+    int32_t n_rows;   // rows of the run (at most kBgmvRows)
+    int32_t chunk;    // the rows' chunk (adapter, Z column, rank, scale, first A row)
+    int32_t j0;       // first LoRA column of this work unit (multiple of 8, below S * rank)
+    int32_t tile;     // tile of the rows
+    int32_t row0;     // row of g_row0 in the tile
+    int32_t pad0, pad1;
+};
+constexpr int kBgmvRows = 8;
+#ifndef LORA_BGMV_MAX_ROWS
+#define LORA_BGMV_MAX_ROWS 1024
+#endif
+constexpr int kBgmvMaxRows = LORA_BGMV_MAX_ROWS;   // gathered rows (whole tiles) up to which the CUDA-core shrink runs
 
 // One shrink pass of one tile.  Its K-splits write fp32 partial sums; the last split to finish (counted per row
 // quarter) sums them in split order and writes Z and the saved or transposed copies.

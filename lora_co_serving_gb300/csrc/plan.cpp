@@ -262,13 +262,17 @@ static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t
 // Few output tiles (less than ~1.5 waves of CTA pairs): the K loop of every output tile is split (see
 // kMainTargetItems).  The number of dense splits is the same for every tile of the call; forward LoRA splits are
 // cut at chunk boundaries and hold about as many k-blocks as a dense split.
+// Dense K-splits of every output tile of a launch with tiles_out output tiles and nk k-blocks (1: no split).
+static int32_t dense_splits(int64_t tiles_out, int32_t nk) {
+    if (tiles_out <= 0 || tiles_out >= kMainTargetItems) return 1;
+    return int32_t(std::max<int64_t>(1, std::min<int64_t>({cdiv(kMainTargetItems, tiles_out), nk / 4, 16})));
+}
+
 template <class TileOf>
 static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk, size_t n_pairs, TileOf tile_of) {
     const size_t band = kBandTiles / 2;
     const int64_t tiles_out = (int64_t)n_pairs * n_nt;
-    int32_t nsb_all = 1;
-    if (tiles_out > 0 && tiles_out < kMainTargetItems)
-        nsb_all = int32_t(std::max<int64_t>(1, std::min<int64_t>({cdiv(kMainTargetItems, tiles_out), nk / 4, 16})));
+    const int32_t nsb_all = dense_splits(tiles_out, nk);
     const int32_t nsb_fwd = nsb_all;
     const bool fwd = (kind == kMainFwd);
     const bool split_all = nsb_all > 1 || (fwd && tiles_out > 0 && tiles_out < kMainTargetItems);
@@ -330,7 +334,7 @@ static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk, siz
                     pl->items[1].push_back(w);
                 }
                 if (nsplit > 1) {
-                    pl->splits.push_back(SplitTile{tile, nt * kBN, slot0, nsplit});
+                    pl->splits.push_back(SplitTile{tile, nt * kBN, slot0, nsplit, 0, 0, 0, 0});
                     pl->main_slots += nsplit;
                 }
             }
@@ -405,16 +409,34 @@ void plan_forward(const Problem& p, Plan* out) {
     // items: shrink passes (per slice region), then main items banded for L2 reuse
     const int32_t nk = int32_t(cdiv(p.K, kBK));
     const size_t n_orig = pl.tiles.size();
+    // the shrink of the gathered decode rows runs on CUDA cores (BgmvGroup) when they are few: per group of rows
+    // sharing an adapter it reads the adapter's rows of A once, where a tensor-core pass runs over the whole tile
+    const bool bgmv = pl.n_gtiles > 0 && pl.n_gtiles * kTileM <= kBgmvMaxRows;
+    if (bgmv) {
+        const int32_t n_g = pl.n_gtiles * kTileM;
+        for (int32_t g = 0; g < n_g;) {
+            const int32_t idx = pl.g_tile0 * kTileM + g;
+            const int32_t c = pl.rowchunk[idx];
+            if (pl.rowmap[idx] < 0 || c < 0) { ++g; continue; }
+            int32_t n = 1;     // a run stays inside one tile
+            while (n < kBgmvRows && (g + n) % kTileM != 0 && pl.rowmap[idx + n] >= 0 && pl.rowchunk[idx + n] == c) ++n;
+            for (int32_t j0 = 0; j0 < p.S * pl.chunks[c].r; j0 += 8)
+                pl.bgmv.push_back(BgmvGroup{g, n, c, j0, pl.g_tile0 + g / kTileM, g % kTileM, 0, 0});
+            g += n;
+        }
+    }
     const int64_t nsplit = std::max<int64_t>(1, cdiv(nk, shrink_split_kb(p.T)));
     auto shrink_items = [&](int32_t width) {
         int64_t n = 0;
         for (size_t ti = 0; ti < n_orig; ++ti)
-            n += p.S * cdiv(std::max(0, pl.tiles[ti].sh_c1 - pl.tiles[ti].sh_c0), width);
+            if (!(bgmv && int32_t(ti) >= pl.g_tile0))
+                n += p.S * cdiv(std::max(0, pl.tiles[ti].sh_c1 - pl.tiles[ti].sh_c0), width);
         return n * nsplit;
     };
     int32_t width = kPassCols;
     while (width > 64 && shrink_items(width) < kShrinkTargetItems) width /= 2;
     for (size_t ti = 0; ti < n_orig; ++ti) {
+        if (bgmv && int32_t(ti) >= pl.g_tile0) continue;     // computed on CUDA cores
         const TileDesc& td = pl.tiles[ti];
         for (int32_t reg = 0; reg < p.S; ++reg) {
             const int32_t base = reg * td.zstride;
@@ -631,6 +653,7 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     L.units = take(sizeof(ShrinkUnit) * pl.units.size());
     L.seg_flags = take(sizeof(int32_t) * ((size_t)p.n_train + 1));
     L.splits = take(sizeof(SplitTile) * pl.splits.size());
+    L.bgmv = take(sizeof(BgmvGroup) * pl.bgmv.size());
     for (int k = 0; k < 3; ++k) {
         L.items[k] = take(sizeof(WorkItem) * pl.items[k].size());
         L.cta_off[k] = take(sizeof(int32_t) * (std::max<size_t>(kMaxCtas, pl.items[k].size()) + 1));

@@ -68,6 +68,7 @@ struct Plan {
     int64_t part_cols = 0;           // columns (of 128 fp32 each) of the shrink partial-sum buffer
     int64_t main_slots = 0;          // K-split partial slots of the main pass (each 2 CTAs x 128 x 256 fp32)
     std::vector<SplitTile> splits;   // split output tiles of the main pass (summed by the reduce launch)
+    std::vector<BgmvGroup> bgmv;     // CUDA-core shrink units of the gathered decode rows (few of them)
     int64_t T = 0;                   // tokens of the batch (sets the shrink split size)
 };
 
@@ -87,7 +88,7 @@ struct Layout {
     size_t status = 0;
     size_t counters = 0, zero_end = 0;   // [status, zero_end) is zeroed at the start of every call
     size_t tiles = 0, chunks = 0, rowmap = 0, rowchunk = 0, rowaux = 0, groups = 0, tsegs = 0;
-    size_t atoms_a = 0, atoms_b = 0, boxes_a = 0, boxes_b = 0, units = 0, seg_flags = 0, splits = 0;
+    size_t atoms_a = 0, atoms_b = 0, boxes_a = 0, boxes_b = 0, units = 0, seg_flags = 0, splits = 0, bgmv = 0;
     size_t items[3] = {0, 0, 0}, cta_off[3] = {0, 0, 0}, cta_list[3] = {0, 0, 0};
     size_t plan_end = 0;
     size_t xg = 0, z = 0, xat = 0, dybt = 0, part = 0, part_main = 0;

@@ -29,6 +29,87 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, int32_t k8, cons
     }
 }
 
+// The shrink of the gathered decode rows on CUDA cores (see BgmvGroup).  Block = one work unit: a run of up to 8
+// rows sharing a chunk, and 8 of its LoRA columns.  Thread i takes the 16-byte pieces i, i + 256, ... of K; per
+// piece it loads the unit's 8 rows of A and the run's rows of x and accumulates the 64 products in fp32.  A warp's
+// 64 partial sums are combined by a halving shuffle tree (lane l ends with sums 2l and 2l + 1; every sum is formed
+// by the same tree over the lanes), the 8 warps' in warp order through shared memory, so each result depends on
+// its own row of x and row of A alone.  Thread t < 64 writes Z = bf16(s * xA) of run row t / 8, column t % 8.
+__global__ void __launch_bounds__(256) bgmv_z_kernel(const uint4* __restrict__ xg, int32_t k8,
+                                                     const uint4* __restrict__ A, const BgmvGroup* __restrict__ groups,
+                                                     const Chunk* __restrict__ chunks,
+                                                     const TileDesc* __restrict__ tiles, int32_t S,
+                                                     uint8_t* __restrict__ zout) {
+    __shared__ float red[8][64];
+    const BgmvGroup u = groups[blockIdx.x];
+    const Chunk ch = chunks[u.chunk];
+    const int32_t r_all = S * ch.r;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    float acc[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int32_t v = threadIdx.x; v < k8; v += 256) {
+        uint4 a[8], x[kBgmvRows];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            a[j] = (u.j0 + j < r_all) ? A[(size_t)(ch.prow_a + u.j0 + j) * k8 + v] : zero;
+#pragma unroll
+        for (int i = 0; i < kBgmvRows; ++i) x[i] = (i < u.n_rows) ? xg[(size_t)(u.g_row0 + i) * k8 + v] : zero;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float af[8][2], xf[kBgmvRows][2];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&a[j])[h]);
+                af[j][0] = f.x;
+                af[j][1] = f.y;
+            }
+#pragma unroll
+            for (int i = 0; i < kBgmvRows; ++i) {
+                const float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&x[i])[h]);
+                xf[i][0] = f.x;
+                xf[i][1] = f.y;
+            }
+#pragma unroll
+            for (int i = 0; i < kBgmvRows; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    acc[i * 8 + j] = fmaf(xf[i][0], af[j][0], acc[i * 8 + j]);
+                    acc[i * 8 + j] = fmaf(xf[i][1], af[j][1], acc[i * 8 + j]);
+                }
+        }
+    }
+#pragma unroll
+    for (int st = 0; st < 5; ++st) {
+        const int off = 16 >> st, half = 32 >> st;
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < half; ++k) {
+            const float send = up ? acc[k] : acc[k + half];
+            const float keep = up ? acc[k + half] : acc[k];
+            acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    red[warp][2 * lane] = acc[0];
+    red[warp][2 * lane + 1] = acc[1];
+    __syncthreads();
+    const int t = threadIdx.x;
+    if (t >= 64) return;
+    float sum = red[0][t];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) sum += red[w][t];
+    const int i = t / 8, j = u.j0 + t % 8;
+    if (i >= u.n_rows || j >= r_all) return;
+    const TileDesc td = tiles[u.tile];
+    const int32_t reg = j / ch.r, jj = j - reg * ch.r;
+    const int32_t zc = reg * td.zstride + ch.zcol + jj;
+    const int row = u.row0 + i;
+    uint8_t* blk = zout + (size_t)(td.z_blk0 + zc / 64) * kZBlockBytes + row * 128;
+    const int chunk16 = ((zc % 64) / 8) ^ (row & 7);
+    *reinterpret_cast<__nv_bfloat16*>(blk + chunk16 * 16 + (zc % 8) * 2) = __float2bfloat16_rn(ch.scale * sum);
+}
+
 // xat[j, tpos0 + t] = xa_saved[xoff + t*r + j] for t < len, 0 for len <= t < roundup(len, 128); with a flag
 // table, only for the segments it marks as saved (the others are recomputed by the shrink)
 __global__ void xat_from_saved_kernel(const __nv_bfloat16* __restrict__ xa_saved, const TrainSeg* __restrict__ tsegs,
@@ -178,6 +259,14 @@ cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out
     if (n_rows <= 0) return cudaSuccess;
     gather_rows_kernel<<<n_rows < 65535 ? n_rows : 65535, 256, 0, s>>>(
         static_cast<const uint4*>(x), K / 8, rows, static_cast<uint4*>(out), n_rows);
+    return cudaGetLastError();
+}
+
+cudaError_t bgmv_shrink(const void* xg, int32_t K, const void* A, const BgmvGroup* groups, int32_t n_groups,
+                        const Chunk* chunks, const TileDesc* tiles, int32_t S, void* zout, cudaStream_t s) {
+    if (n_groups <= 0) return cudaSuccess;
+    bgmv_z_kernel<<<n_groups, 256, 0, s>>>(static_cast<const uint4*>(xg), K / 8, static_cast<const uint4*>(A), groups,
+                                           chunks, tiles, S, static_cast<uint8_t*>(zout));
     return cudaGetLastError();
 }
 
