@@ -95,17 +95,24 @@ def accounting(wl):
     return out
 
 
-def launches_per_step(wl, fwd_tiles=None):
-    """Kernel launches of one step.  fwd_tiles: tiles of the forward plan (from lora_plan_describe) when known; a
-    main pass with fewer output tiles than kMainTargetItems (114) is split and adds a reduce launch."""
+def launches_per_step(wl, fwd_info=None):
+    """Kernel launches of one step.  fwd_info: the forward tile plan (info rows of lora_plan_describe: gathered,
+    adapters, LoRA columns, x row).  Gathered decode tiles of up to 1024 rows are shrunk on CUDA cores (one launch)
+    and leave the tensor-core shrink; a main pass with fewer output tiles than kMainTargetItems (114) is split and
+    adds a reduce launch."""
     segs = wl.segs.tolist()
     n_nt = lambda cols: -(-cols // 256)
     n = 0
     if wl.forward:
-        n += 1 if any(ln < 16 and not tr and ln > 0 for _, ln, _, tr in segs) else 0    # row gather
-        n += 1 if any(a >= 0 for _, _, a, _ in segs) else 0                                # shrink pass
+        info = np.asarray(fwd_info) if fwd_info is not None else np.zeros((0, 4), np.int64)
+        n_g = int(info[:, 0].sum()) if len(info) else 0
+        bgmv = 0 < n_g * 128 <= 1024
+        n += 1 if n_g > 0 else 0                                                            # row gather
+        n += 1 if bgmv else 0                                                               # CUDA-core shrink
+        tc_shrink = [(g, ext) for g, _, ext, _ in info.tolist() if ext > 0 and not (g and bgmv)]
+        n += 1 if tc_shrink else 0                                                          # tensor-core shrink
         n += 1                                                                              # main pass
-        if fwd_tiles is not None and 0 < (fwd_tiles // 2) * n_nt(wl.N) < 114:
+        if 0 < (len(info) // 2) * n_nt(wl.N) < 114:
             n += 1                                                                          # split reduce
     if wl.backward and any(tr for *_, tr in segs):
         n += 3                                                                              # shrink, dX, dA/dB
@@ -350,7 +357,7 @@ def run_ours(args):
     segs = lm.segments(wl.segs)
     T, K, N = wl.T, wl.K, wl.N
     ws = torch.empty(lm.workspace_size(T, K, N, 0, pool, segs), dtype=torch.uint8, device="cuda")
-    fwd_tiles = lm.plan_describe(T, K, N, pool, segs)[0].shape[0] if wl.forward else None
+    fwd_info = lm.plan_describe(T, K, N, pool, segs)[1] if wl.forward else None
     y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
     save = wl.xa_mode == "save"
     xs = torch.empty(max(1, lm.xa_size(0, pool, segs) // 2), dtype=torch.bfloat16, device="cuda") if save else None
@@ -373,8 +380,20 @@ def run_ours(args):
     torch.cuda.synchronize()
     lm.workspace_status(ws)
 
+    # ---- L2: inputs that fit in L2 would stay resident from one step to the next, so then L2 is flushed (a write
+    # of twice its size) before every step, outside that step's own events
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or 129 * 2 ** 20)
+    in_bytes = sum(t.numel() * t.element_size() for t in (x, Wt, A, B, dY) if t is not None)
+    flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if in_bytes <= l2_bytes else None
+    l2_note = ("inputs (x, W, adapter pool, dY: %.0f MB) fit in L2 (%.0f MB): L2 flushed before every step by a "
+               "%.0f MB write outside the step's events" % (in_bytes / 1e6, l2_bytes / 1e6, 2 * l2_bytes / 1e6)
+               if flush_buf is not None else
+               "inputs larger than L2 (x, W, adapter pool, dY: %.0f MB; L2 %.0f MB); no flush"
+               % (in_bytes / 1e6, l2_bytes / 1e6))
+
     # ---- device-timed region: K steps, per-step trace events around each launch group
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    per = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for row in ev:          # torch creates the CUDA event on first record
         for e in row:
             e.record(stream)
@@ -387,8 +406,12 @@ def run_ours(args):
     wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
+        if flush_buf is not None:
+            flush_buf.fill_(i & 255)
+        per[i][0].record(stream)
         lm.set_trace_events(ev[i])
         step()
+        per[i][1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -397,7 +420,10 @@ def run_ours(args):
     if dist:
         dist.barrier()
     lm.workspace_status(ws)
-    ms = start.elapsed_time(stop) / args.steps
+    if flush_buf is not None:
+        ms = statistics.mean(per[i][0].elapsed_time(per[i][1]) for i in range(args.steps))
+    else:
+        ms = start.elapsed_time(stop) / args.steps
     group_ms = [statistics.mean(ev[i][2 * g].elapsed_time(ev[i][2 * g + 1]) for i in range(args.steps))
                 for g in range(4)]
     t_max = torch.tensor([ms], device="cuda", dtype=torch.float64)
@@ -426,13 +452,20 @@ def run_ours(args):
             dist.barrier()
         n_g = max(3, args.steps)
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gper = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_g)]
         with torch.cuda.stream(gs):
             g0.record(gs)
-            for _ in range(n_g):
+            for i in range(n_g):
+                if flush_buf is not None:
+                    flush_buf.fill_(i & 255)
+                gper[i][0].record(gs)
                 cg.replay()
+                gper[i][1].record(gs)
             g1.record(gs)
         torch.cuda.synchronize()
-        gms = torch.tensor([g0.elapsed_time(g1) / n_g], device="cuda", dtype=torch.float64)
+        g_ms = (statistics.mean(gper[i][0].elapsed_time(gper[i][1]) for i in range(n_g)) if flush_buf is not None
+                else g0.elapsed_time(g1) / n_g)
+        gms = torch.tensor([g_ms], device="cuda", dtype=torch.float64)
         if dist:
             dist.all_reduce(gms, op=dist.ReduceOp.MAX)
         graph = {"value": acc["tokens"] * world / (float(gms.item()) / 1e3), "unit": UNIT,
@@ -579,11 +612,11 @@ def run_ours(args):
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the pages' workloads)",
                 "config": {"workload": wl.name, "T": T, "K": K, "N": N, "adapters": wl.n_adapters,
                            "train_tokens": acc.get("train_tokens", 0), "xa": wl.xa_mode,
-                           "l2": "inputs larger than L2 (W alone %.0f MB); no flush" % (2 * K * N / 1e6),
+                           "l2": l2_note,
                            "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
                 "roofline": roof, "step": step_stats, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
                 "graph_replay": graph, "adamw": adamw_stats,
-                "gpu_launches": launches_per_step(wl, fwd_tiles) * args.steps}
+                "gpu_launches": launches_per_step(wl, fwd_info) * args.steps}
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
@@ -621,6 +654,7 @@ def run_layer(args):
         d["pool"] = lm.Pool(d["A"], d["B"], wl.a_off, wl.b_off, wl.rank, wl.scale)
         d["segs"] = lm.segments(wl.segs)
         d["sl"] = lm.Slices(wl.bounds) if wl.bounds is not None else None
+        d["info"] = lm.plan_describe(T, wl.K, wl.N, d["pool"], d["segs"])[1]      # the tile plan (slices alike)
         d["y"] = torch.empty((T, wl.N), dtype=torch.bfloat16, device="cuda")
         d["dX"] = torch.zeros((T, wl.K), dtype=torch.bfloat16, device="cuda")
         d["dA"] = torch.zeros(d["A"].numel(), dtype=torch.float32, device="cuda")
@@ -731,7 +765,7 @@ def run_layer(args):
                          "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms,
                          "algorithmic_flops": flops, "algorithmic_bytes": nbytes, "call_ms": per_call},
                 "cpu_baseline": cpu, "clocks": clocks, "e2e": None,
-                "gpu_launches": sum(launches_per_step(L[n]) for n in LAYER_ORDER) * args.steps}
+                "gpu_launches": sum(launches_per_step(L[n], dev[n]["info"]) for n in LAYER_ORDER) * args.steps}
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

@@ -26,9 +26,14 @@ def _built():
     lm.build()
 
 
-def mixed_small(seed=1005):
-    return workloads.config5(seed=seed, K=384, N=640, n_adapters=30, n_decode=200, prefill_tokens=600, len_lo=40,
+def mixed_small(seed=1005, N=640):
+    return workloads.config5(seed=seed, K=384, N=N, n_adapters=30, n_decode=200, prefill_tokens=600, len_lo=40,
                              len_hi=300, train_len=120)
+
+
+# N = 640: the forward main pass is split along K (few output tiles, chunk-aligned LoRA splits, a reduce launch);
+# N = 7680: unsplit (every output tile one item that writes y)
+WIDTHS = [640, 7680]
 
 
 def bits(t):
@@ -36,8 +41,9 @@ def bits(t):
     return t.detach().contiguous().view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).cpu().numpy()
 
 
-def test_zero_B_is_base_bitwise():
-    wl = mixed_small()
+@pytest.mark.parametrize("N", WIDTHS)
+def test_zero_B_is_base_bitwise(N):
+    wl = mixed_small(N=N)
     zero = [a for a in range(wl.n_adapters) if a % 3 == 0]
     for a in zero:
         wl.B[wl.b_off[a]:wl.b_off[a] + wl.rank[a] * wl.N] = 0.0
@@ -58,8 +64,9 @@ def test_zero_B_is_base_bitwise():
     assert np.all(to_np(dA) == 0.0)
 
 
-def test_segment_order_bitwise():
-    wl = mixed_small()
+@pytest.mark.parametrize("N", WIDTHS)
+def test_segment_order_bitwise(N):
+    wl = mixed_small(N=N)
     d = Dev(wl)
     y0 = bits(d.forward())
     g0 = [bits(t) for t in d.backward()]
@@ -72,9 +79,9 @@ def test_segment_order_bitwise():
         assert np.array_equal(a, b)
 
 
-def test_pool_order_bitwise():
-    import lora_co_serving_gb300 as lm
-    wl = mixed_small()
+@pytest.mark.parametrize("N", WIDTHS)
+def test_pool_order_bitwise(N):
+    wl = mixed_small(N=N)
     d = Dev(wl)
     y0 = bits(d.forward())
     dX0, dA0, dB0 = [bits(t) for t in d.backward()]
@@ -93,13 +100,13 @@ def test_pool_order_bitwise():
         assert np.array_equal(dB1[b_off[i]:b_off[i] + r * wl.N], dB0[wl.b_off[p]:wl.b_off[p] + r * wl.N])
 
 
-@pytest.mark.parametrize("which", ["decode", "cosrv"])
+@pytest.mark.parametrize("which", ["decode", "cosrv", "cosrv_wide"])
 def test_routing_integer_pattern_exact(which):
     if which == "decode":
         wl = workloads.config2(T=256, K=256, N=512, n_adapters=64)
     else:
-        wl = workloads.config5(K=256, N=512, n_adapters=64, n_decode=512, prefill_tokens=700, len_lo=20,
-                               len_hi=200, train_len=150)
+        wl = workloads.config5(K=256, N=512 if which == "cosrv" else 6144, n_adapters=64, n_decode=512,
+                               prefill_tokens=700, len_lo=20, len_hi=200, train_len=150)
     wl = P.routing_pattern(wl)
     y = to_np(Dev(wl).forward())
     assert np.array_equal(y, P.routing_expected(wl))

@@ -93,6 +93,26 @@ def test_bf16_decode_small():
     check_forward(wl)
 
 
+def unsplit_with_decode_pairs(wl):
+    """True when the forward main pass is not split along K (at least 114 output tiles) and has gathered decode
+    pairs: every output tile is then one item that runs all its LoRA K-steps and writes y directly (no reduce)."""
+    import lora_co_serving_gb300 as lm
+    d = Dev(wl)
+    _, info = lm.plan_describe(wl.T, wl.K, wl.N, d.pool, d.segs)
+    return (info.shape[0] // 2) * -(-wl.N // 256) >= 114 and int(info[:, 0].sum()) > 0
+
+
+@pytest.mark.parametrize("N", [8192, 7432])
+def test_bf16_decode_pairs_unsplit_wide(N):
+    # 32 or 30 (the last one 8 columns wide) output tiles per pair: the unsplit main pass of the large calls, with
+    # gathered decode pairs (many adapters per pair, ranks up to 128) and prefill windows, at an oracle-sized K
+    wl = workloads.config5(K=256, N=N, n_adapters=40, n_decode=300, prefill_tokens=500, len_lo=30, len_hi=250,
+                           train_len=100, ranks=(8, 16, 24, 64, 128))
+    assert unsplit_with_decode_pairs(wl)
+    d, _ = check_forward(wl)
+    check_backward(wl, d)
+
+
 def test_bf16_odd_ranks():
     segs = [(0, 40, 0, 0), (40, 1, 1, 0), (41, 1, 2, 0), (42, 86, 3, 0), (128, 3, 4, 0), (131, 61, 1, 0)]
     wl = workloads.custom(10, 192, 256, 256, segs, [1, 4, 13, 100, 127])
