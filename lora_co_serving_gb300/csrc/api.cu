@@ -83,6 +83,26 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
     return true;
 }
 
+// The main pass's output map: [rows, cols] bf16 rows ld elements apart, 32 x 32 boxes with 64-byte swizzle (the
+// epilogue's staging layout)
+bool encode_out(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld, std::string* err) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) { *err = "cuTensorMapEncodeTiled is not available from the driver"; return false; }
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, LORA_L2_PROMOTION,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ") for the [" + std::to_string(rows) +
+               ", " + std::to_string(cols) + "] output";
+        return false;
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------------------------------------ device info
 int sm_count() {
     static int cache[64] = {0};
@@ -615,6 +635,7 @@ int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x
     P.out = static_cast<__nv_bfloat16*>(y);
     P.out_ld = N;
     P.out_cols = N;
+    if (!encode_out(&P.tm_out, y, N, T, N, &err)) return fail(LORA_ERR_CUDA, err);
     P.xa_save = save ? static_cast<__nv_bfloat16*>(xa_save) : nullptr;
     P.K = K;
     P.N = N;
@@ -774,6 +795,7 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
     P.out = static_cast<__nv_bfloat16*>(dX);
     P.out_ld = K;
     P.out_cols = K;
+    if (dX != nullptr && !encode_out(&P.tm_out, dX, K, T, K, &err)) return fail(LORA_ERR_CUDA, err);
     P.xat = reinterpret_cast<__nv_bfloat16*>(ws + L.xat);
     P.dybt = reinterpret_cast<__nv_bfloat16*>(ws + L.dybt);
     P.t_ld = int32_t(Pcols);

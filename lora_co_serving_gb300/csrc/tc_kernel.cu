@@ -516,8 +516,14 @@ __global__ void __launch_bounds__(kThreads, 1) lora_tc_kernel(const __grid_const
 // Both CTAs' TMA loads complete on the leader's "full" barrier; the leader's commits arrive on both CTAs'
 // "empty" and "accumulator full" barriers; both CTAs' epilogue warps release the accumulator on the leader.
 // =============================================================================================================
+// Main-pass epilogue: a warp whose 32 rows are 32 consecutive output rows stages each 32-column chunk in shared
+// memory and writes it with one TMA store (other warps, e.g. those of gathered decode tiles, store row by row).
+// The staging buffers take the seventh pipeline stage's shared memory (6 and 7 stages measured alike).
+#ifndef LORA_TMA_STORE
+#define LORA_TMA_STORE 1
+#endif
 #ifndef LORA_MAIN_STAGES
-#define LORA_MAIN_STAGES 7
+#define LORA_MAIN_STAGES (LORA_TMA_STORE ? 6 : 7)
 #endif
 // L2 eviction priority of the main pass's TMA loads of the row operand (x / dY) and of W:
 // 0 = normal, 1 = evict_first, 2 = evict_last.  evict_last on the rows once measured +21 % on an
@@ -534,6 +540,8 @@ constexpr int kHalfN = kBN / 2;
 constexpr int kA2Bytes = kTileM * kBK * 2;        // 16 KB
 constexpr int kB2Bytes = kHalfN * kBK * 2;        // 16 KB
 constexpr int kStage2Bytes = kA2Bytes + kB2Bytes;
+constexpr int kOutChunkBytes = 32 * 32 * 2;       // 32 rows x 32 bf16 columns, 64-byte swizzled rows
+constexpr int kOutStageBytes = LORA_TMA_STORE ? 4 * 2 * kOutChunkBytes : 0;   // 4 epilogue warps, 2 buffers each
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -746,17 +754,38 @@ __device__ __forceinline__ void store_row_bf16(const KParams& P, int32_t t, int3
     }
 }
 
+// TMA store of one staged 32 x 32 chunk (shared -> global), as its own bulk group
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n\t"
+                 "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+// a warp's 32 rows x 32 columns into its staging buffer: lane = row, 64-byte rows, 16-byte granules swizzled the
+// way the tensor map's 64-byte swizzle reads them (granule g of row r at g ^ ((r >> 1) & 3))
+__device__ __forceinline__ void stage_row_bf16(uint32_t buf, int lane, const float (&v)[32]) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t a = buf + lane * 64 + ((g ^ ((lane >> 1) & 3)) * 16);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pack_bf16(v[8 * g + 0], v[8 * g + 1])),
+                     "r"(pack_bf16(v[8 * g + 2], v[8 * g + 3])), "r"(pack_bf16(v[8 * g + 4], v[8 * g + 5])),
+                     "r"(pack_bf16(v[8 * g + 6], v[8 * g + 7]))
+                     : "memory");
+    }
+}
+
 __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t tmem, uint32_t rank,
-                              int i0, int i1, volatile int* abort_flag) {
+                              int i0, int i1, volatile int* abort_flag, uint32_t stage_out) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t nstore = 0;      // TMA stores issued by this warp (their buffers alternate)
     for (int ii = i0; ii < i1; ++ii) {
         const WorkItem w = P.items[P.cta_list[ii]];
-        if (!wait_phase(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) return;
+        if (!wait_phase(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) break;
         tc_fence_after();
         const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);
         const int32_t t = P.rowmap[(w.tile + rank) * kTileM + row];
@@ -765,6 +794,8 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
         float* part = (w.nsplit > 1)
                           ? P.part_main + ((size_t)(w.part + w.split) * 2 + rank) * kMainPartialFloats + row
                           : nullptr;
+        const int32_t t0 = __shfl_sync(0xffffffffu, t, 0);
+        const bool bulk = LORA_TMA_STORE && part == nullptr && __all_sync(0xffffffffu, t >= 0 && t == t0 + lane);
         for (int c = 0; c < kBN; c += 32) {
             float v[32];
             ld32_cols(taddr + c, v);
@@ -773,6 +804,18 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
+            }
+            if (bulk) {
+                if (w.n0 + c >= P.out_cols) continue;          // past the last output column
+                const uint32_t buf = stage_out + (nstore & 1u) * kOutChunkBytes;
+                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");   // buf's last store
+                __syncwarp();
+                stage_row_bf16(buf, lane, v);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) tma_store_2d(&P.tm_out, buf, w.n0 + c, t0);
+                ++nstore;
+                continue;
             }
             if (t < 0) continue;
             if (part) {
@@ -785,13 +828,16 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
     }
+    // the staged chunks must be read, and written out, before the CTA exits
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lora_main2_kernel(const __grid_constant__ KParams P) {
     extern __shared__ uint8_t dsmem[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages2 * kStage2Bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages2 * kStage2Bytes + kOutStageBytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages2 + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + kStages2 * 8;
@@ -832,7 +878,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (rank == 0 && lane == 0)
             run_mma2(P, smem, bar_full, bar_empty, bar_tfull, bar_tempty, tmem, i0, i1, abort_flag);
     } else {
-        run_epilogue2(P, bar_tfull, bar_tempty, tmem, rank, i0, i1, abort_flag);
+        run_epilogue2(P, bar_tfull, bar_tempty, tmem, rank, i0, i1, abort_flag,
+                      smem_u32(smem + kStages2 * kStage2Bytes) + (uint32_t)((warp - 2) * 2 * kOutChunkBytes));
     }
     __syncwarp();
     tc_fence_before();
@@ -898,7 +945,7 @@ __global__ void selftest_timeout_kernel(int32_t* status) {
 }  // namespace
 
 size_t tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024 + 1024; }
-size_t tc2_smem_bytes() { return (size_t)kStages2 * kStage2Bytes + 1024 + 1024; }
+size_t tc2_smem_bytes() { return (size_t)kStages2 * kStage2Bytes + kOutStageBytes + 1024 + 1024; }
 
 cudaError_t selftest_timeout_launch(int32_t* status, cudaStream_t stream) {
     selftest_timeout_kernel<<<1, 32, 0, stream>>>(status);

@@ -23,6 +23,7 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     CUtensorMap tm_pb_h[3];  // B pool, same
     CUtensorMap tm_xat;    // xA^T  [128, P], box {64, 8}
     CUtensorMap tm_dybt;   // dYB^T [128, P], box {64, 8}
+    CUtensorMap tm_out;    // main-pass output (y or dX) [rows, out_cols], ld out_ld, box {32, 32}, 64B swizzle
     CUtensorMap tm_z;      // Z blocks as [blocks*128, 64] bf16 rows of 128 B, box {64, 128}, no swizzle (the blocks
                            // already hold the swizzled shared-memory image)
     CUtensorMap tm_seg_dy[kMaxTrainSegs];   // dY rows of fine-tuning segment q, [len, N], box {64, 64}
