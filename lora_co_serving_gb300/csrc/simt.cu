@@ -30,17 +30,21 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, int32_t k8, cons
 }
 
 // The shrink of the gathered decode rows on CUDA cores (see BgmvGroup).  Block = one work unit: a run of up to 8
-// rows sharing a chunk, and 8 of its LoRA columns.  Thread i takes the 16-byte pieces i, i + 256, ... of K; per
-// piece it loads the unit's 8 rows of A and the run's rows of x and accumulates the 64 products in fp32.  A warp's
-// 64 partial sums are combined by a halving shuffle tree (lane l ends with sums 2l and 2l + 1; every sum is formed
-// by the same tree over the lanes), the 8 warps' in warp order through shared memory, so each result depends on
-// its own row of x and row of A alone.  Thread t < 64 writes Z = bf16(s * xA) of run row t / 8, column t % 8.
-__global__ void __launch_bounds__(256) bgmv_z_kernel(const uint4* __restrict__ xg, int32_t k8,
+// rows sharing a chunk, and 8 of its LoRA columns.  Thread i of the block's kBgmvThreads takes the 16-byte pieces
+// i, i + kBgmvThreads, ... of K; per piece it loads the unit's 8 rows of A and the run's rows of x and accumulates
+// the 64 products in fp32.  A warp's 64 partial sums are combined by a halving shuffle tree (lane l ends with sums
+// 2l and 2l + 1; every sum is formed by the same tree over the lanes), the warps' in warp order through shared
+// memory, so each result depends on its own row of x and row of A alone.  Thread t < 64 writes Z = bf16(s * xA) of run row t / 8, column t % 8.
+#ifndef LORA_BGMV_THREADS
+#define LORA_BGMV_THREADS 128
+#endif
+constexpr int kBgmvThreads = LORA_BGMV_THREADS;   // 128: two blocks fit an SM's registers (one with 256)
+__global__ void __launch_bounds__(kBgmvThreads) bgmv_z_kernel(const uint4* __restrict__ xg, int32_t k8,
                                                      const uint4* __restrict__ A, const BgmvGroup* __restrict__ groups,
                                                      const Chunk* __restrict__ chunks,
                                                      const TileDesc* __restrict__ tiles, int32_t S,
                                                      uint8_t* __restrict__ zout) {
-    __shared__ float red[8][64];
+    __shared__ float red[kBgmvThreads / 32][64];
     const BgmvGroup u = groups[blockIdx.x];
     const Chunk ch = chunks[u.chunk];
     const int32_t r_all = S * ch.r;
@@ -49,7 +53,7 @@ __global__ void __launch_bounds__(256) bgmv_z_kernel(const uint4* __restrict__ x
 #pragma unroll
     for (int i = 0; i < 64; ++i) acc[i] = 0.f;
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int32_t v = threadIdx.x; v < k8; v += 256) {
+    for (int32_t v = threadIdx.x; v < k8; v += kBgmvThreads) {
         uint4 a[8], x[kBgmvRows];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -98,7 +102,7 @@ __global__ void __launch_bounds__(256) bgmv_z_kernel(const uint4* __restrict__ x
     if (t >= 64) return;
     float sum = red[0][t];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) sum += red[w][t];
+    for (int w = 1; w < kBgmvThreads / 32; ++w) sum += red[w][t];
     const int i = t / 8, j = u.j0 + t % 8;
     if (i >= u.n_rows || j >= r_all) return;
     const TileDesc td = tiles[u.tile];
@@ -265,7 +269,7 @@ cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out
 cudaError_t bgmv_shrink(const void* xg, int32_t K, const void* A, const BgmvGroup* groups, int32_t n_groups,
                         const Chunk* chunks, const TileDesc* tiles, int32_t S, void* zout, cudaStream_t s) {
     if (n_groups <= 0) return cudaSuccess;
-    bgmv_z_kernel<<<n_groups, 256, 0, s>>>(static_cast<const uint4*>(xg), K / 8, static_cast<const uint4*>(A), groups,
+    bgmv_z_kernel<<<n_groups, kBgmvThreads, 0, s>>>(static_cast<const uint4*>(xg), K / 8, static_cast<const uint4*>(A), groups,
                                            chunks, tiles, S, static_cast<uint8_t*>(zout));
     return cudaGetLastError();
 }
