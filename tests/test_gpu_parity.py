@@ -113,6 +113,29 @@ def test_bf16_decode_pairs_unsplit_wide(N):
     check_backward(wl, d)
 
 
+EDGE = {
+    # one decode token; the smallest K and N the layer accepts (multiples of 8)
+    "one_token": (1, 64, 64, [(0, 1, 0, 0)], [8]),
+    "one_token_k8_n8": (1, 8, 8, [(0, 1, 1, 0)], [4, 16]),
+    # a handful of tokens: decode, a 2-token prefill, a 1-token fine-tuning segment, a base-only token
+    "few_mixed": (5, 136, 72, [(0, 1, 0, 0), (1, 2, 1, 0), (3, 1, 2, 1), (4, 1, -1, 0)], [8, 32, 16]),
+    # one 129-token fine-tuning segment (a tile and one row), ranks at the ends of the range
+    "train_129_rank128": (129, 200, 264, [(0, 129, 1, 1)], [1, 128]),
+    # decode rows of 40 adapters of rank 1..128 around a 300-token prefill and a 20-token fine-tuning segment
+    "decode_mixed_ranks": (360, 256, 256, [(t, 1, t % 40, 0) for t in range(40)] + [(40, 300, 7, 0), (340, 20, 3, 1)],
+                           [1 + (a * 37) % 128 for a in range(40)]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EDGE))
+def test_bf16_edge_shapes(case):
+    T, K, N, segs, ranks = EDGE[case]
+    wl = workloads.custom(31, T, K, N, segs, ranks)
+    d, _ = check_forward(wl)
+    if any(s[3] for s in segs):
+        check_backward(wl, d)
+
+
 def test_bf16_odd_ranks():
     segs = [(0, 40, 0, 0), (40, 1, 1, 0), (41, 1, 2, 0), (42, 86, 3, 0), (128, 3, 4, 0), (131, 61, 1, 0)]
     wl = workloads.custom(10, 192, 256, 256, segs, [1, 4, 13, 100, 127])
