@@ -476,6 +476,42 @@ def run_ours(args):
         del cg
         lm.workspace_status(ws)
 
+    # ---- the backward with a per-segment flag table read on the device: every other fine-tuning segment (in
+    # increasing start order) takes the xA its forward saved, the rest recompute it (and a table marking all
+    # saved); timed on their own beside the all-recompute backward and the saved-xA backward without a table
+    flagged = None
+    n_train = sum(1 for _, ln, _, t in wl.segs.tolist() if t and ln > 0)
+    if wl.backward and n_train > 0 and lm.xa_size(0, pool, segs) > 0:
+        xs_f = torch.empty(lm.xa_size(0, pool, segs) // 2, dtype=torch.bfloat16, device="cuda")
+        lm.forward(x, Wt, pool, segs, y=y, xa_save=xs_f, save_xa=True, workspace=ws, stream=stream)
+        modes = {"recompute_all": None, "saved_no_table": None,
+                 "saved_half": torch.tensor([1 - (i % 2) for i in range(n_train)], dtype=torch.int32, device="cuda"),
+                 "saved_all": torch.ones(n_train, dtype=torch.int32, device="cuda")}
+
+        def bwd_mode(m):
+            if m == "recompute_all":
+                lm.backward(x, Wt, pool, segs, dY, dX=dX, dA=dA, dB=dB, recompute=True, workspace=ws, stream=stream)
+            elif m == "saved_no_table":
+                lm.backward(x, Wt, pool, segs, dY, xa_saved=xs_f, dX=dX, dA=dA, dB=dB, workspace=ws, stream=stream)
+            else:
+                lm.backward_flagged(x, Wt, pool, segs, dY, xs_f, modes[m], dX=dX, dA=dA, dB=dB, workspace=ws,
+                                    stream=stream)
+        n_f = max(3, min(args.steps, 50))
+        flagged = {"segments": n_train}
+        for m in modes:
+            for _ in range(3):
+                bwd_mode(m)
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            f0.record(stream)
+            for _ in range(n_f):
+                bwd_mode(m)
+            f1.record(stream)
+            torch.cuda.synchronize()
+            flagged[m + "_ms"] = f0.elapsed_time(f1) / n_f
+        lm.workspace_status(ws)
+        del xs_f
+
     # ---- the optimizer step that follows (AdamW on the fine-tuning adapters, fp32 masters + bf16 pool), timed
     # on its own: it is not part of the forward+backward step the metric is about
     adamw_stats = None
@@ -617,7 +653,7 @@ def run_ours(args):
                            "l2": l2_note,
                            "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
                 "roofline": roof, "step": step_stats, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
-                "graph_replay": graph, "adamw": adamw_stats,
+                "graph_replay": graph, "adamw": adamw_stats, "flagged_backward": flagged,
                 "gpu_launches": launches_per_step(wl, fwd_info) * args.steps}
         print(json.dumps(line), flush=True)
     if dist:

@@ -812,9 +812,12 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
         CUDA_TRY(cudaMemcpyAsync(ws + L.seg_flags, xa_valid, sizeof(int32_t) * p.n_train, cudaMemcpyDeviceToDevice,
                                  stream));
     CUDA_TRY(trace(2, 0, stream));
-    if (!recompute && dB)
+    if (!recompute && dB) {
+        int32_t max_r = 0;
+        for (const TrainSeg& s : pl.tsegs) max_r = std::max(max_r, s.r);
         CUDA_TRY(xat_from_saved(xa_saved, reinterpret_cast<const TrainSeg*>(ws + L.tsegs), int32_t(pl.tsegs.size()),
-                                max_len, ws + L.xat, int32_t(Pcols), P.seg_flags, stream));
+                                max_len, max_r, ws + L.xat, int32_t(Pcols), P.seg_flags, stream));
+    }
     CUDA_TRY(launch_group(0, &P, ws, L, grid, stream));
     CUDA_TRY(trace(2, 1, stream));
     CUDA_TRY(trace(3, 0, stream));

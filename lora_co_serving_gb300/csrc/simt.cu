@@ -115,19 +115,31 @@ __global__ void __launch_bounds__(kBgmvThreads) bgmv_z_kernel(const uint4* __res
 }
 
 // xat[j, tpos0 + t] = xa_saved[xoff + t*r + j] for t < len, 0 for len <= t < roundup(len, 128); with a flag
-// table, only for the segments it marks as saved (the others are recomputed by the shrink)
-__global__ void xat_from_saved_kernel(const __nv_bfloat16* __restrict__ xa_saved, const TrainSeg* __restrict__ tsegs,
-                                      int32_t n_tsegs, __nv_bfloat16* __restrict__ xat, int32_t P,
-                                      const int32_t* __restrict__ seg_flags) {
-    const TrainSeg s = tsegs[blockIdx.y];
+// table, only for the segments it marks as saved (the others are recomputed by the shrink).  A transpose in 32 x 32
+// tiles through shared memory: block (t tile, j tile, segment), reads along j and writes along t are coalesced.
+__global__ void __launch_bounds__(256) xat_from_saved_kernel(const __nv_bfloat16* __restrict__ xa_saved,
+                                                             const TrainSeg* __restrict__ tsegs, int32_t n_tsegs,
+                                                             __nv_bfloat16* __restrict__ xat, int32_t P,
+                                                             const int32_t* __restrict__ seg_flags) {
+    __shared__ __nv_bfloat16 tile[32][34];
+    const TrainSeg s = tsegs[blockIdx.z];
     if (seg_flags != nullptr && seg_flags[s.order] == 0) return;
     const int32_t span = (s.len + 127) / 128 * 128;
-    for (int32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < span; t += gridDim.x * blockDim.x) {
-        for (int32_t j = 0; j < s.r; ++j) {
-            __nv_bfloat16 v = __float2bfloat16_rn(0.f);
-            if (t < s.len) v = xa_saved[(size_t)s.xoff + (size_t)t * s.r + j];
-            xat[(size_t)j * P + s.tpos0 + t] = v;
-        }
+    const int32_t t0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+    if (t0 >= span || j0 >= s.r) return;
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int32_t t = t0 + ty + 8 * k, j = j0 + tx;
+        __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+        if (t < s.len && j < s.r) v = xa_saved[(size_t)s.xoff + (size_t)t * s.r + j];
+        tile[ty + 8 * k][tx] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int32_t j = j0 + ty + 8 * k, t = t0 + tx;
+        if (j < s.r && t < span) xat[(size_t)j * P + s.tpos0 + t] = tile[tx][ty + 8 * k];
     }
 }
 
@@ -274,11 +286,11 @@ cudaError_t bgmv_shrink(const void* xg, int32_t K, const void* A, const BgmvGrou
     return cudaGetLastError();
 }
 
-cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len, void* xat,
-                           int32_t P, const int32_t* seg_flags, cudaStream_t s) {
+cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len,
+                           int32_t max_r, void* xat, int32_t P, const int32_t* seg_flags, cudaStream_t s) {
     if (n_tsegs <= 0) return cudaSuccess;
-    dim3 grid((max_len + 127) / 128, n_tsegs);
-    xat_from_saved_kernel<<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(xa_saved), tsegs, n_tsegs,
+    dim3 grid((max_len + 127) / 128 * 4, (max_r + 31) / 32, n_tsegs);
+    xat_from_saved_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(xa_saved), tsegs, n_tsegs,
                                                static_cast<__nv_bfloat16*>(xat), P, seg_flags);
     return cudaGetLastError();
 }

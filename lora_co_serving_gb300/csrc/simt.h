@@ -59,8 +59,8 @@ cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out
 // their tiles (zout: the zeroed Z blocks).
 cudaError_t bgmv_shrink(const void* xg, int32_t K, const void* A, const BgmvGroup* groups, int32_t n_groups,
                         const Chunk* chunks, const TileDesc* tiles, int32_t S, void* zout, cudaStream_t s);
-cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len, void* xat,
-                           int32_t P, const int32_t* seg_flags, cudaStream_t s);
+cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len,
+                           int32_t max_r, void* xat, int32_t P, const int32_t* seg_flags, cudaStream_t s);
 cudaError_t f32_forward(const F32Args& a, cudaStream_t s);
 cudaError_t f32_backward(const F32Args& a, cudaStream_t s);
 
