@@ -83,6 +83,23 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
     return true;
 }
 
+// Wt [N, K] as a 3-D tensor [K/64][N][64] (K a multiple of 64): a {64, 64, 2} box holds rows [n, n + 64) of two
+// consecutive 64-column chunks, one 8 KB MN-major atom block after the other, as the backward's B operand wants
+#ifndef LORA_W3
+#define LORA_W3 1
+#endif
+bool encode_w3(CUtensorMap* m, const void* base, uint64_t K, uint64_t N) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || K % 64 != 0) return false;
+    cuuint64_t dims[3] = {64, N, K / 64};
+    cuuint64_t strides[2] = {K * 2, 128};
+    cuuint32_t box[3] = {64, 64, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, LORA_L2_PROMOTION,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The main pass's output map: [rows, cols] bf16 rows ld elements apart, 32 x 32 boxes with 64-byte swizzle (the
 // epilogue's staging layout)
 bool encode_out(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld, std::string* err) {
@@ -769,6 +786,7 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
     if (!encode_2d(&P.tm_x, x, K, T, K, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_dy, dY, N, T, N, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
+    P.w3 = (LORA_W3 && encode_w3(&P.tm_w3, Wt, K, N)) ? 1 : 0;      // else two 2-D boxes per stage
     if (!encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     if (!encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
     for (int h = 0; h < 3; ++h) {      // taller boxes for runs of consecutive atoms (shrinks and the dX pass)

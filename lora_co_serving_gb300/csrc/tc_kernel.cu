@@ -566,6 +566,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
         : "memory");
 }
+// 3-D tile load of the same kind (pair-leader barrier)
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                 int32_t c2, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
+        : "memory");
+}
 // Same, with an L2 cache-eviction policy (createpolicy) attached to the load
 __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
                                                       uint32_t bar_cluster, uint64_t policy) {
@@ -650,6 +659,8 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
             if (lane == 0) tma_load_hinted<LORA_HINT_ROWS>(sa, ma, kb * kBK, td.a_row0, full);
             if (fwd) {
                 if (lane == 1) tma_load_hinted<LORA_HINT_W>(sb, &P.tm_w, kb * kBK, nb, full);     // Wt rows, K-major
+            } else if (P.w3) {
+                if (lane == 1) tma_load_3d_pair(sb, &P.tm_w3, 0, kb * kBK, nb / 64, full);        // both MN atoms
             } else if (lane == 1 || lane == 2) {
                 const int m = lane - 1;
                 tma_load_hinted<LORA_HINT_W>(sb + m * 8192, &P.tm_w, nb + 64 * m, kb * kBK, full);  // Wt, MN-major

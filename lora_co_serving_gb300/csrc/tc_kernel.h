@@ -17,6 +17,8 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     CUtensorMap tm_xg;     // gathered rows buffer, [G*128, K], box {64, 128}
     CUtensorMap tm_dy;     // dY rows, [T, N], box {64, 128}
     CUtensorMap tm_w;      // Wt [N, K]: forward box {64, 128} (K-major B half); backward box {64, 64} (MN-major)
+    CUtensorMap tm_w3;     // backward, K a multiple of 64: Wt as [K/64][N][64] (64-column chunks outermost), box
+                           //   {64, 64, 2}: both 64-column MN atoms of a CTA's B half in one load
     CUtensorMap tm_pa;     // A pool viewed as [rows, K], box {64, 8}
     CUtensorMap tm_pb;     // B pool viewed as [rows, N], box {64, 8}
     CUtensorMap tm_pa_h[3];  // A pool with boxes of 16, 32 and 64 rows (runs of 2, 4, 8 atoms)
@@ -64,6 +66,7 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     int32_t t_ld;           // P
     int32_t K, N;
     int32_t accumulate;
+    int32_t w3;              // backward: tm_w3 is valid
 };
 
 size_t tc_smem_bytes();
