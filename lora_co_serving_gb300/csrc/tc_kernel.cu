@@ -32,6 +32,14 @@ namespace {
 constexpr int kABytes = kTileM * kBK * 2;            // 16 KB: 128 rows x 64 bf16
 constexpr int kBBytes = kBN * kBK * 2;               // 32 KB: 256 rows x 64 bf16
 constexpr int kStageBytes = kABytes + kBBytes;
+// grad items of at most 64 LoRA columns: two token blocks per stage, block s at s * kGradSubBytes (A: 16 KB, then
+// B: up to 8 KB)
+constexpr int kGradSubBytes = kABytes + 64 * kBK * 2;    // 24 KB
+static_assert(2 * kGradSubBytes <= kStageBytes, "two grad blocks must fit a stage");
+#ifndef LORA_GRAD_PACK
+#define LORA_GRAD_PACK 1
+#endif
+__device__ __forceinline__ int grad_blocks_per_stage(int mma_n) { return (LORA_GRAD_PACK && mma_n <= 64) ? 2 : 1; }
 constexpr int kThreads = 192;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;      // 1 s
 constexpr uint32_t kTmemCols = 512;                   // two 256-column fp32 accumulators
@@ -181,21 +189,31 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
         const WorkItem w = P.items[P.cta_list[ii]];
         if (skipped_item(P, w)) continue;
         if (w.kind == kGradDb || w.kind == kGradDa) {
-            // A: [128 of N or K] x 64 tokens, MN-major (two 64-wide boxes); B: r_pad rows of xA^T / dYB^T
+            // A: [128 of N or K] x 64 tokens, MN-major (two 64-wide boxes); B: r_pad rows of xA^T / dYB^T.  Items
+            // of at most 64 LoRA columns take two token blocks per stage (grad_sub layout), so that twice the bytes
+            // are in flight
             const GradGroup g = P.groups[w.tile];
             const CUtensorMap* mb = (w.kind == kGradDb) ? &P.tm_xat : &P.tm_dybt;
             const int natoms = w.mma_n / 8;
-            const uint32_t bytes = kABytes + natoms * 1024;
+            const int per = grad_blocks_per_stage(w.mma_n);
+            int gb = 0;           // token block index over the item's segments
             for (int q = 0; q < g.nseg; ++q) {
                 const TrainSeg s = P.tsegs[g.seg0 + q];
                 const CUtensorMap* ma = (w.kind == kGradDb) ? &P.tm_seg_dy[g.seg0 + q] : &P.tm_seg_x[g.seg0 + q];
-                for (int b = 0; b * kBK < s.len; ++b) {
-                    if (!acquire_stage(ring, bar_full, bar_empty, bytes, lane, abort_flag, P.status)) return;
+                for (int b = 0; b * kBK < s.len; ++b, ++gb) {
+                    const int sub = gb % per;
+                    if (sub == 0) {
+                        const int nsub = min(per, w.nk - gb);
+                        if (!acquire_stage(ring, bar_full, bar_empty, nsub * (kABytes + natoms * 1024), lane,
+                                           abort_flag, P.status))
+                            return;
+                    }
                     const uint32_t full = bar_full + ring.stage * 8;
-                    const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
+                    const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes) + sub * kGradSubBytes;
+                    const uint32_t sb = sa + kABytes;
                     if (lane < 2) tma_load_2d(sa + lane * 8192, ma, w.n0 + 64 * lane, b * kBK, full);
                     if (lane < natoms) tma_load_2d(sb + lane * 1024, mb, s.tpos0 + b * kBK, w.j0 + lane * 8, full);
-                    ring.next();
+                    if (sub == per - 1 || gb == w.nk - 1) ring.next();
                 }
             }
             continue;
@@ -241,17 +259,20 @@ __device__ void run_mma(const KParams& P, uint8_t* smem, uint32_t bar_full, uint
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)acc * kBN;
         uint32_t accumulate = 0;
-        // one k-block: wait for the stage, issue `steps` MMAs of K=16, release the stage
-        auto kblock = [&](int steps, uint32_t idesc, int a_mn, int b_mn) -> bool {
+        // one stage: wait for it, issue `steps` MMAs of K=16 for each of its `nsub` blocks (`stride` bytes apart),
+        // release it
+        auto kblock = [&](int nsub, uint32_t stride, int steps, uint32_t idesc, int a_mn, int b_mn) -> bool {
             const uint32_t full = bar_full + ring.stage * 8, empty = bar_empty + ring.stage * 8;
             if (!wait_phase(full, ring.phase, abort_flag, P.status)) return false;
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
-            for (int k = 0; k < steps; ++k) {
-                const uint64_t ad = a_mn ? smem_desc(sa + k * 2048, 8192, 1024) : smem_desc(sa + k * 32, 16, 1024);
-                const uint64_t bd = b_mn ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
-                mma_bf16(d, ad, bd, idesc, accumulate);
-                accumulate = 1;
+            for (int s = 0; s < nsub; ++s) {
+                const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes) + s * stride, sb = sa + kABytes;
+                for (int k = 0; k < steps; ++k) {
+                    const uint64_t ad = a_mn ? smem_desc(sa + k * 2048, 8192, 1024) : smem_desc(sa + k * 32, 16, 1024);
+                    const uint64_t bd = b_mn ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
+                    mma_bf16(d, ad, bd, idesc, accumulate);
+                    accumulate = 1;
+                }
             }
             mma_commit(empty);
             ring.next();
@@ -260,10 +281,11 @@ __device__ void run_mma(const KParams& P, uint8_t* smem, uint32_t bar_full, uint
         bool ok = true;
         if (w.kind == kGradDb || w.kind == kGradDa) {
             const uint32_t id = instr_desc(kTileM, w.mma_n, 1, 0);
-            for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id, 1, 0);
+            const int per = grad_blocks_per_stage(w.mma_n);
+            for (int kb = 0; kb < w.nk && ok; kb += per) ok = kblock(min(per, w.nk - kb), kGradSubBytes, 4, id, 1, 0);
         } else {
             const uint32_t id = instr_desc(kTileM, w.mma_n, 0, 0);
-            for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(4, id, 0, 0);
+            for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(1, 0, 4, id, 0, 0);
         }
         if (!ok) return;
         mma_commit(bar_tfull + acc * 8);
