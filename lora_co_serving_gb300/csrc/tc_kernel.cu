@@ -32,14 +32,20 @@ namespace {
 constexpr int kABytes = kTileM * kBK * 2;            // 16 KB: 128 rows x 64 bf16
 constexpr int kBBytes = kBN * kBK * 2;               // 32 KB: 256 rows x 64 bf16
 constexpr int kStageBytes = kABytes + kBBytes;
-// grad items of at most 64 LoRA columns: two token blocks per stage, block s at s * kGradSubBytes (A: 16 KB, then
-// B: up to 8 KB)
-constexpr int kGradSubBytes = kABytes + 64 * kBK * 2;    // 24 KB
-static_assert(2 * kGradSubBytes <= kStageBytes, "two grad blocks must fit a stage");
+// 1-CTA items of at most 64 LoRA columns (shrink passes, dA/dB): two k-blocks per stage, block s at s * kSubBytes
+// (A: 16 KB, then B: up to 8 KB), so that twice the bytes are in flight
+constexpr int kSubBytes = kABytes + 64 * kBK * 2;    // 24 KB
+static_assert(2 * kSubBytes <= kStageBytes, "two k-blocks must fit a stage");
 #ifndef LORA_GRAD_PACK
 #define LORA_GRAD_PACK 1
 #endif
+#ifndef LORA_SHRINK_PACK
+#define LORA_SHRINK_PACK 1
+#endif
 __device__ __forceinline__ int grad_blocks_per_stage(int mma_n) { return (LORA_GRAD_PACK && mma_n <= 64) ? 2 : 1; }
+__device__ __forceinline__ int shrink_blocks_per_stage(int mma_n) {
+    return (LORA_SHRINK_PACK && mma_n <= 64) ? 2 : 1;
+}
 constexpr int kThreads = 192;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;      // 1 s
 constexpr uint32_t kTmemCols = 512;                   // two 256-column fp32 accumulators
@@ -190,8 +196,7 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
         if (skipped_item(P, w)) continue;
         if (w.kind == kGradDb || w.kind == kGradDa) {
             // A: [128 of N or K] x 64 tokens, MN-major (two 64-wide boxes); B: r_pad rows of xA^T / dYB^T.  Items
-            // of at most 64 LoRA columns take two token blocks per stage (grad_sub layout), so that twice the bytes
-            // are in flight
+            // of at most 64 LoRA columns take two token blocks per stage
             const GradGroup g = P.groups[w.tile];
             const CUtensorMap* mb = (w.kind == kGradDb) ? &P.tm_xat : &P.tm_dybt;
             const int natoms = w.mma_n / 8;
@@ -209,7 +214,7 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
                             return;
                     }
                     const uint32_t full = bar_full + ring.stage * 8;
-                    const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes) + sub * kGradSubBytes;
+                    const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes) + sub * kSubBytes;
                     const uint32_t sb = sa + kABytes;
                     if (lane < 2) tma_load_2d(sa + lane * 8192, ma, w.n0 + 64 * lane, b * kBK, full);
                     if (lane < natoms) tma_load_2d(sb + lane * 1024, mb, s.tpos0 + b * kBK, w.j0 + lane * 8, full);
@@ -234,14 +239,18 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
         const int n_mine = (lane >= natoms) ? 0 : (lead ? my_box : (((covered >> lane) & 1u) ? 0 : 1));
         const CUtensorMap* my_map =
             (n_mine <= 1) ? mp : (use_b ? P.tm_pb_h : P.tm_pa_h) + (n_mine == 2 ? 0 : (n_mine == 4 ? 1 : 2));
-        for (int kb = w.kb0; kb < w.kb0 + w.nk; ++kb) {
-            if (!acquire_stage(ring, bar_full, bar_empty, kABytes + natoms * 1024, lane, abort_flag, P.status))
+        const int per = shrink_blocks_per_stage(w.mma_n);
+        for (int i = 0; i < w.nk; ++i) {
+            const int sub = i % per, kb = w.kb0 + i;
+            if (sub == 0 &&
+                !acquire_stage(ring, bar_full, bar_empty, min(per, w.nk - i) * (kABytes + natoms * 1024), lane,
+                               abort_flag, P.status))
                 return;
             const uint32_t full = bar_full + ring.stage * 8;
-            const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes), sb = sa + kABytes;
+            const uint32_t sa = smem_u32(smem + ring.stage * kStageBytes) + sub * kSubBytes, sb = sa + kABytes;
             if (lane == 0) tma_load_2d(sa, ma, kb * kBK, td.a_row0, full);
             if (n_mine > 0) tma_load_2d(sb + lane * 1024, my_map, kb * kBK, my_row, full);
-            ring.next();
+            if (sub == per - 1 || i == w.nk - 1) ring.next();
         }
     }
 }
@@ -282,10 +291,11 @@ __device__ void run_mma(const KParams& P, uint8_t* smem, uint32_t bar_full, uint
         if (w.kind == kGradDb || w.kind == kGradDa) {
             const uint32_t id = instr_desc(kTileM, w.mma_n, 1, 0);
             const int per = grad_blocks_per_stage(w.mma_n);
-            for (int kb = 0; kb < w.nk && ok; kb += per) ok = kblock(min(per, w.nk - kb), kGradSubBytes, 4, id, 1, 0);
+            for (int kb = 0; kb < w.nk && ok; kb += per) ok = kblock(min(per, w.nk - kb), kSubBytes, 4, id, 1, 0);
         } else {
             const uint32_t id = instr_desc(kTileM, w.mma_n, 0, 0);
-            for (int kb = 0; kb < w.nk && ok; ++kb) ok = kblock(1, 0, 4, id, 0, 0);
+            const int per = shrink_blocks_per_stage(w.mma_n);
+            for (int kb = 0; kb < w.nk && ok; kb += per) ok = kblock(min(per, w.nk - kb), kSubBytes, 4, id, 0, 0);
         }
         if (!ok) return;
         mma_commit(bar_tfull + acc * 8);
