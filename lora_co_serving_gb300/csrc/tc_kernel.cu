@@ -438,15 +438,20 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                     out.put16(c, v);
                 }
             } else {
-                // raw fp32 partial sums, column-major [mma_n][128]; the last split to arrive (per row quarter)
-                // sums all splits in split order and finalizes those 32 rows
-                float* dst = P.part + (size_t)w.part * kTileM + row;
+                // raw fp32 partial sums; the last split to arrive (per row quarter) sums all splits in split order
+                // and finalizes those 32 rows.  Layout: per 4 columns [C, C + 4) of the partial buffer, 128 rows
+                // of 4 floats (P.part + C * 128 + row * 4), so that a row's 4 columns are one 16-byte access and a
+                // warp's 32 rows one 512-byte run
+                float* dst = P.part + (size_t)w.part * kTileM + row * 4;
                 for (int c = 0; c < w.mma_n; c += 16) {
                     uint32_t a[16];
                     tmem_ld16(taddr + c, a);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[(size_t)(c + i) * kTileM] = __uint_as_float(a[i]);
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<float4*>(dst + (size_t)(c + 4 * q) * kTileM) =
+                            make_float4(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1]),
+                                        __uint_as_float(a[4 * q + 2]), __uint_as_float(a[4 * q + 3]));
                 }
                 tc_fence_before();
                 mbar_arrive(bar_tempty + acc * 8);       // the accumulator is free; the rest reads global memory
@@ -461,15 +466,34 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 if (last) {
                     __threadfence();
                     ShrinkRowOut out(P, u, row);
-                    const float* p0 = P.part + (size_t)u.part0 * kTileM + row;
+                    // the splits' 16-column groups are loaded four splits at a time (16 loads of 16 bytes in
+                    // flight per thread), then added in split order
+                    const float* p0 = P.part + (size_t)u.part0 * kTileM + row * 4;
                     for (int c = 0; c < w.mma_n; c += 16) {
                         float v[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[i] = 0.f;
-                        for (int sp = 0; sp < u.nsplit; ++sp) {
-                            const float* ps = p0 + ((size_t)sp * u.mma_n + c) * kTileM;
+                        for (int s0 = 0; s0 < u.nsplit; s0 += 4) {
+                            float4 a[4][4];
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] += __ldcg(ps + (size_t)i * kTileM);
+                            for (int sp = 0; sp < 4; ++sp)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    a[sp][q] = (s0 + sp < u.nsplit)
+                                                   ? __ldcg(reinterpret_cast<const float4*>(
+                                                         p0 + ((size_t)(s0 + sp) * u.mma_n + c + 4 * q) * kTileM))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int sp = 0; sp < 4; ++sp) {
+                                if (s0 + sp >= u.nsplit) break;
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    v[4 * q] += a[sp][q].x;
+                                    v[4 * q + 1] += a[sp][q].y;
+                                    v[4 * q + 2] += a[sp][q].z;
+                                    v[4 * q + 3] += a[sp][q].w;
+                                }
+                            }
                         }
                         out.put16(c, v);
                     }

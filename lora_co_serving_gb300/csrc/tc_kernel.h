@@ -45,7 +45,7 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     const int32_t* atoms_b;  // same for the B pool
     const int32_t* boxes_a;  // per atom: atoms in the TMA box that starts at it (0: covered by an earlier box)
     const int32_t* boxes_b;
-    float* part;             // shrink items: fp32 partial sums, [columns][128 rows]
+    float* part;             // shrink items: fp32 partial sums, per 4 columns [128 rows][4]
     float* part_main;        // split main items: fp32 partial tiles, [slot][CTA][256 columns][128 rows]
     const int32_t* seg_flags;  // backward with a per-segment flag table: snapshot, nonzero = saved xA is used
                                // (the segment's x A recompute items are skipped); null otherwise
