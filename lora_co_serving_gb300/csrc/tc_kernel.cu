@@ -856,10 +856,12 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
         tc_fence_after();
         const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);
         const int32_t t = P.rowmap[(w.tile + rank) * kTileM + row];
-        // K-split tiles: this split's fp32 partial goes to its slot, column-major [256][128] per CTA (coalesced
-        // across the warp's rows; rows without a token are skipped); the reduce launch sums the slots
+        // K-split tiles: this split's fp32 partial goes to its slot, per CTA in 16-byte groups of 4 columns
+        // ([64][128 rows][4]: a warp's rows write 512 contiguous bytes per group; rows without a token are
+        // skipped); the reduce launch sums the slots
         float* part = (w.nsplit > 1)
-                          ? P.part_main + ((size_t)(w.part + w.split) * 2 + rank) * kMainPartialFloats + row
+                          ? P.part_main + ((size_t)(w.part + w.split) * 2 + rank) * kMainPartialFloats +
+                                row * 4
                           : nullptr;
         const int32_t t0 = __shfl_sync(0xffffffffu, t, 0);
         const bool bulk = LORA_TMA_STORE && part == nullptr && __all_sync(0xffffffffu, t >= 0 && t == t0 + lane);
@@ -887,7 +889,9 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
             if (t < 0) continue;
             if (part) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) __stcg(part + (size_t)(c + i) * kTileM, v[i]);
+                for (int i = 0; i < 32; i += 4)
+                    __stcg(reinterpret_cast<float4*>(part + (size_t)(c + i) * kTileM),
+                           make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
             } else {
                 store_row_bf16(P, t, w.n0 + c, v);
             }
@@ -976,15 +980,23 @@ __global__ void __launch_bounds__(256) main_reduce_kernel(const SplitTile* __res
     const int32_t col = st.n0 + c0;
     if (t < 0 || col + 8 > out_cols) return;
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const float* p = part + ((size_t)st.part * 2 + half) * kMainPartialFloats + (size_t)c0 * kTileM + r;
-#pragma unroll 2
-    for (int sp = 0; sp < st.nsplit; ++sp) {
-        float a[8];
+    // a row's 8 columns are two 16-byte groups; four splits' groups are loaded before they are added in order
+    const float* p = part + ((size_t)st.part * 2 + half) * kMainPartialFloats + (size_t)c0 * kTileM + r * 4;
+    for (int s0 = 0; s0 < st.nsplit; s0 += 4) {
+        float4 a[4][2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = __ldcg(p + (size_t)i * kTileM);
+        for (int sp = 0; sp < 4; ++sp) {
+            const float* ps = p + (size_t)(s0 + sp) * 2 * kMainPartialFloats;
+            const bool in = s0 + sp < st.nsplit;
+            a[sp][0] = in ? __ldcg(reinterpret_cast<const float4*>(ps)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            a[sp][1] = in ? __ldcg(reinterpret_cast<const float4*>(ps + 4 * kTileM)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] += a[i];
-        p += (size_t)2 * kMainPartialFloats;
+        for (int sp = 0; sp < 4; ++sp) {
+            if (s0 + sp >= st.nsplit) break;
+            v[0] += a[sp][0].x; v[1] += a[sp][0].y; v[2] += a[sp][0].z; v[3] += a[sp][0].w;
+            v[4] += a[sp][1].x; v[5] += a[sp][1].y; v[6] += a[sp][1].z; v[7] += a[sp][1].w;
+        }
     }
     uint4 q;
     q.x = pack_bf16(v[0], v[1]);

@@ -46,7 +46,7 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     const int32_t* boxes_a;  // per atom: atoms in the TMA box that starts at it (0: covered by an earlier box)
     const int32_t* boxes_b;
     float* part;             // shrink items: fp32 partial sums, per 4 columns [128 rows][4]
-    float* part_main;        // split main items: fp32 partial tiles, [slot][CTA][256 columns][128 rows]
+    float* part_main;        // split main items: fp32 partial tiles, [slot][CTA][64 column groups][128 rows][4]
     const int32_t* seg_flags;  // backward with a per-segment flag table: snapshot, nonzero = saved xA is used
                                // (the segment's x A recompute items are skipped); null otherwise
     const ShrinkUnit* units; // shrink passes (splits of one pass share a unit)
