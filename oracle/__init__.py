@@ -36,7 +36,7 @@ def _lib():
         lib.oracle_forward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, I32, P, I32, P, I64, P, P]
         lib.oracle_forward.restype = ctypes.c_int
         lib.oracle_backward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, I32, P, I32, P, P, I64, P, P,
-                                        P, ctypes.c_int, P, I64, P, I64]
+                                        P, ctypes.c_int, P, I64, P, I64, P]
         lib.oracle_backward.restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -55,7 +55,7 @@ def load_library(path):
     lib.oracle_forward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, I32, P, I32, P, I64, P, P]
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_backward.argtypes = [I64, I64, I64, P, P, P, P, P, P, P, P, I32, P, I32, P, P, I64, P, P,
-                                    P, ctypes.c_int, P, I64, P, I64]
+                                    P, ctypes.c_int, P, I64, P, I64, P]
     lib.oracle_backward.restype = ctypes.c_int
     return lib
 
@@ -99,7 +99,7 @@ def forward(x, Wt, A, B, a_off, b_off, rank, scale, segs, rows=None, want_u=Fals
 
 
 def backward(x, Wt, A, B, a_off, b_off, rank, scale, segs, dY, dx_rows=None, want_dx=True, want_grads=True,
-             accumulate=False, dA_init=None, dB_init=None, cols_b=None, cols_a=None, lib=None):
+             accumulate=False, dA_init=None, dB_init=None, cols_b=None, cols_a=None, u_saved=None, lib=None):
     """(dX, dA, dB) in float64.
 
     dX holds the rows listed in ``dx_rows`` (default: every training token in
@@ -107,6 +107,10 @@ def backward(x, Wt, A, B, a_off, b_off, rank, scale, segs, dY, dx_rows=None, wan
     training segments keep ``dA_init``/``dB_init`` (zeros by default).
     ``cols_b`` / ``cols_a`` restrict dB to the listed columns n and dA to the
     listed columns k (other entries keep their initial values).
+    ``u_saved``: captured shrink activations xA in the saved-activation layout
+    (per training segment in increasing start order, a [len, r_a] block); dB
+    then uses them instead of recomputing xA (DeltaServe section 3.2,
+    "Backward subprocess"; MOLT section 4.3).  None = recompute.
     """
     g = _Args(x, Wt, A, B, a_off, b_off, rank, scale, segs)
     dYa = _f32(dY)
@@ -122,6 +126,12 @@ def backward(x, Wt, A, B, a_off, b_off, rank, scale, segs, dY, dx_rows=None, wan
         dX = np.zeros((n, g.K), dtype=np.float64)
     else:
         dX = None
+    us = None if u_saved is None else np.ascontiguousarray(u_saved, dtype=np.float64).reshape(-1)
+    if us is not None:
+        tr = g.segs[(g.segs[:, 3] != 0) & (g.segs[:, 1] > 0)]
+        need = int(sum(int(ln) * int(g.rank[a]) for _, ln, a, _ in tr.tolist()))
+        if us.shape[0] < need:
+            raise ValueError("u_saved holds %d values, the training segments need %d" % (us.shape[0], need))
     dA = dB = None
     if want_grads:
         dA = np.zeros(g.A.shape[0], np.float64) if dA_init is None else np.array(dA_init, np.float64).reshape(-1)
@@ -131,7 +141,7 @@ def backward(x, Wt, A, B, a_off, b_off, rank, scale, segs, dY, dx_rows=None, wan
                                          g.segs.shape[0], _ptr(dYa), _ptr(rows_a),
                                          0 if rows_a is None else rows_a.shape[0], _ptr(dX), _ptr(dA), _ptr(dB),
                                          1 if accumulate else 0, _ptr(cb), 0 if cb is None else cb.shape[0],
-                                         _ptr(ca), 0 if ca is None else ca.shape[0])
+                                         _ptr(ca), 0 if ca is None else ca.shape[0], _ptr(us))
     if rc != 0:
         raise ValueError("oracle_backward: malformed segment table")
     return dX, dA, dB
@@ -144,7 +154,17 @@ def forward_wl(wl, rows=None, want_u=False, lib=None):
 
 
 def backward_wl(wl, dx_rows=None, want_dx=True, want_grads=True, accumulate=False, dA_init=None, dB_init=None,
-                cols_b=None, cols_a=None, lib=None):
+                cols_b=None, cols_a=None, u_saved=None, lib=None):
     return backward(wl.x, wl.Wt, wl.A, wl.B, wl.a_off, wl.b_off, wl.rank, wl.scale, wl.segs, wl.dY,
                     dx_rows=dx_rows, want_dx=want_dx, want_grads=want_grads, accumulate=accumulate,
-                    dA_init=dA_init, dB_init=dB_init, cols_b=cols_b, cols_a=cols_a, lib=lib)
+                    dA_init=dA_init, dB_init=dB_init, cols_b=cols_b, cols_a=cols_a, u_saved=u_saved, lib=lib)
+
+
+def saved_u(wl, u):
+    """The saved-activation layout (per training segment in increasing start order, a [len, r_a] block, flat) of
+    per-row shrink values ``u`` [T, >= r] (e.g. forward(..., want_u=True)'s second result)."""
+    out = []
+    for st, ln, a, tr in sorted(np.asarray(wl.segs).tolist()):
+        if tr and ln > 0:
+            out.append(np.asarray(u, np.float64)[st:st + ln, :int(wl.rank[a])].reshape(-1))
+    return np.concatenate(out) if out else np.zeros(0, np.float64)

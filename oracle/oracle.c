@@ -144,6 +144,16 @@ static int32_t train_segments_sorted(const int32_t* segs, int32_t n_segs, int32_
  *   cols_b / cols_a (optional): compute only the listed columns n of dB_a
  *         (entries dB_a[j, n], all j) and columns k of dA_a; the other
  *         entries keep their initial values.  NULL = every column.
+ *   u_saved (optional): the shrink activations u = xA captured by a forward
+ *         pass, used for dB in place of recomputing them -- DeltaServe
+ *         section 3.2 ("Backward subprocess": the LoRA gradients come from
+ *         the activations captured during the mixed forward; only what was
+ *         not captured is recomputed) and MOLT section 4.3 (flexible
+ *         activation checkpointing: a saved activation is read back, an
+ *         unsaved one recomputed).  Layout: for every training segment in
+ *         increasing start order, a [len, r_a] row-major block (row p =
+ *         token start + p).  Only dB reads u; v = dY B^T, dX and dA do not
+ *         depend on it.  NULL = recompute u from x and A.
  * Returns 0, or -1 on a malformed table (a training segment on id -1 or out
  * of range, or a dX row that is not a training token).
  */
@@ -152,7 +162,7 @@ int oracle_backward(int64_t T, int64_t K, int64_t N, const float* x, const float
                     const double* scale, int32_t n_adapters, const int32_t* segs, int32_t n_segs,
                     const float* dY, const int64_t* dx_rows, int64_t n_dx_rows, double* dX, double* dA,
                     double* dB, int accumulate, const int64_t* cols_b, int64_t n_cols_b, const int64_t* cols_a,
-                    int64_t n_cols_a) {
+                    int64_t n_cols_a, const double* u_saved) {
     int32_t* tsegs = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_segs > 0 ? n_segs : 1));
     int32_t n_train = train_segments_sorted(segs, n_segs, tsegs);
     for (int32_t q = 0; q < n_train; ++q) {
@@ -209,18 +219,27 @@ int oracle_backward(int64_t T, int64_t K, int64_t N, const float* x, const float
         double* vv = (double*)calloc((size_t)(n_all > 0 ? n_all : 1) * ORACLE_MAX_RANK, sizeof(double));
         int64_t* tok = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_all > 0 ? n_all : 1));
         int32_t* tad = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_all > 0 ? n_all : 1));
-        int64_t p = 0;
-        for (int32_t q = 0; q < n_train; ++q)
+        int64_t* uoff = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_all > 0 ? n_all : 1));
+        int64_t p = 0, blk = 0;
+        for (int32_t q = 0; q < n_train; ++q) {
+            int32_t r_q = rank[SEG_ADAPTER(segs, tsegs[q])];
             for (int32_t i = 0; i < SEG_LEN(segs, tsegs[q]); ++i) {
                 tok[p] = SEG_START(segs, tsegs[q]) + i;
                 tad[p] = SEG_ADAPTER(segs, tsegs[q]);
+                uoff[p] = blk + (int64_t)i * r_q;      /* row i of segment q's block of u_saved */
                 ++p;
             }
+            blk += (int64_t)SEG_LEN(segs, tsegs[q]) * r_q;
+        }
 #pragma omp parallel for schedule(dynamic, 4)
         for (int64_t i = 0; i < n_all; ++i) {
             int32_t a = tad[i];
             int32_t r = rank[a];
-            shrink_row(K, x + tok[i] * K, A + a_off[a], r, uu + i * ORACLE_MAX_RANK);
+            if (u_saved) {
+                for (int32_t j = 0; j < r; ++j) uu[i * ORACLE_MAX_RANK + j] = u_saved[uoff[i] + j];
+            } else {
+                shrink_row(K, x + tok[i] * K, A + a_off[a], r, uu + i * ORACLE_MAX_RANK);
+            }
             const float* dyrow = dY + tok[i] * N;
             const float* Ba = B + b_off[a];
             for (int32_t j = 0; j < r; ++j) {
@@ -264,7 +283,7 @@ int oracle_backward(int64_t T, int64_t K, int64_t N, const float* x, const float
                 }
             }
         }
-        free(uu); free(vv); free(tok); free(tad);
+        free(uu); free(vv); free(tok); free(tad); free(uoff);
     }
     free(tsegs);
     return 0;

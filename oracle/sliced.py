@@ -74,8 +74,24 @@ def forward(x, Wt, A, B, a_off, b_off, rank, scale, segs, bounds, want_u=False, 
     return (y, u) if want_u else y
 
 
-def backward(x, Wt, A, B, a_off, b_off, rank, scale, segs, bounds, dY, lib=None):
-    """(dX over the training rows in increasing start order, dA pool-shaped like A, dB pool-shaped like B)."""
+def _slice_saved(u_saved, segs, rank, S, i):
+    """Slice i's captured xA in the plain saved-activation layout ([len, r_a] per training segment, increasing
+    start) out of the sliced layout ([len, S r_a] per segment, slice i in columns [i r_a, (i+1) r_a))."""
+    u = np.asarray(u_saved, np.float64).reshape(-1)
+    out, off = [], 0
+    for st, ln, a, tr in sorted(np.asarray(segs).reshape(-1, 4).tolist()):
+        if tr and ln > 0:
+            r = int(rank[a])
+            blk = u[off:off + ln * S * r].reshape(ln, S * r)
+            out.append(blk[:, i * r:(i + 1) * r].reshape(-1))
+            off += ln * S * r
+    return np.concatenate(out) if out else np.zeros(0, np.float64)
+
+
+def backward(x, Wt, A, B, a_off, b_off, rank, scale, segs, bounds, dY, u_saved=None, lib=None):
+    """(dX over the training rows in increasing start order, dA pool-shaped like A, dB pool-shaped like B).
+    ``u_saved``: captured xA in the sliced saved-activation layout (each slice's dB then uses its columns of it,
+    DeltaServe section 3.2, "Backward subprocess"); None = recompute."""
     x = np.asarray(x, np.float32)
     Wt = np.asarray(Wt, np.float32)
     dY = np.asarray(dY, np.float32)
@@ -88,7 +104,9 @@ def backward(x, Wt, A, B, a_off, b_off, rank, scale, segs, bounds, dY, lib=None)
     for i in range(S):
         c0, c1 = int(bounds[i]), int(bounds[i + 1])
         Ai, Bi, ao, bo = _slice_pool(A, B, a_off, b_off, rank, K, N, bounds, i)
-        dXi, dAi, dBi = _backward(x, Wt[c0:c1], Ai, Bi, ao, bo, rank, scale, segs, dY[:, c0:c1], lib=lib)
+        ui = None if u_saved is None else _slice_saved(u_saved, segs, rank, S, i)
+        dXi, dAi, dBi = _backward(x, Wt[c0:c1], Ai, Bi, ao, bo, rank, scale, segs, dY[:, c0:c1], u_saved=ui,
+                                  lib=lib)
         dX = dXi if dX is None else dX + dXi
         for a in range(len(rank)):
             r = int(rank[a])
@@ -104,6 +122,6 @@ def forward_wl(wl, want_u=False, lib=None):
                    want_u=want_u, lib=lib)
 
 
-def backward_wl(wl, lib=None):
+def backward_wl(wl, u_saved=None, lib=None):
     return backward(wl.x, wl.Wt, wl.A, wl.B, wl.a_off, wl.b_off, wl.rank, wl.scale, wl.segs, wl.bounds, wl.dY,
-                    lib=lib)
+                    u_saved=u_saved, lib=lib)

@@ -286,6 +286,58 @@ def pin_sampled_columns(lib=None):
     assert np.array_equal(sX, dX[pick]), "row-sampled dX"
 
 
+def _saved_case():
+    """Three fine-tuning segments on two adapters of different ranks, given out of start order, plus inference
+    segments: the saved-activation layout then has blocks of different widths at nonzero offsets."""
+    segs = [(30, 7, 1, 1), (0, 9, 0, 1), (9, 5, -1, 0), (14, 6, 2, 0), (20, 10, 0, 1)]
+    return workloads.custom(4242, 37, 12, 10, segs, [3, 5, 2], scale=[2.0, 0.5, 1.0], dtype="f32")
+
+
+def pin_saved_u_exact(lib=None):
+    """Captured xA equal to what the backward would recompute: every gradient bit for bit the recompute's."""
+    wl = _saved_case()
+    _, u = oracle.forward_wl(wl, want_u=True, lib=lib)
+    us = oracle.saved_u(wl, u)
+    g0 = oracle.backward_wl(wl, lib=lib)
+    g1 = oracle.backward_wl(wl, u_saved=us, lib=lib)
+    for a, b, n in zip(g0, g1, ("dX", "dA", "dB")):
+        assert np.array_equal(a, b), "saved exact u changed " + n
+
+
+def pin_saved_u_onehot(lib=None):
+    """Captured xA that is zero except u[t, j] = 1 (t the p-th row of the q-th fine-tuning segment in start order):
+    dB_a = s_a e_j dY[t] exactly (a the segment's adapter), every other dB entry 0; dA and dX do not read u."""
+    wl = _saved_case()
+    g0 = oracle.backward_wl(wl, lib=lib)
+    train = sorted(q for q in wl.segs.tolist() if q[3])
+    n_u = sum(ln * int(wl.rank[a]) for _, ln, a, _ in train)
+    off = 0
+    picks = []
+    for st, ln, a, _ in train:
+        r = int(wl.rank[a])
+        picks += [(off + p * r + j, st + p, a, j) for p, j in ((0, 0), (ln - 1, r - 1), (ln // 2, r // 2))]
+        off += ln * r
+    for idx, t, a, j in picks:
+        us = np.zeros(n_u, np.float64)
+        us[idx] = 1.0
+        dX, dA, dB = oracle.backward_wl(wl, u_saved=us, lib=lib)
+        assert np.array_equal(dX, g0[0]) and np.array_equal(dA, g0[1]), "dX / dA read the saved u"
+        exp = np.zeros_like(dB)
+        b0 = int(wl.b_off[a]) + j * wl.N
+        exp[b0:b0 + wl.N] = float(wl.scale[a]) * wl.dY[t].astype(np.float64)
+        assert np.array_equal(dB, exp), ("one-hot saved u", idx, t, a, j)
+
+
+def pin_saved_u_double(lib=None):
+    """Doubling the captured xA doubles dB exactly (dB is linear in u; scaling by 2 is exact)."""
+    wl = _saved_case()
+    us = np.random.default_rng(17).standard_normal(
+        sum(ln * int(wl.rank[a]) for _, ln, a, tr in wl.segs.tolist() if tr))
+    _, _, dB1 = oracle.backward_wl(wl, u_saved=us, lib=lib)
+    _, _, dB2 = oracle.backward_wl(wl, u_saved=2.0 * us, lib=lib)
+    assert np.array_equal(dB2, 2.0 * dB1), "dB not linear in the saved u"
+
+
 def _tiny_sliced(seed):
     """A tiny fp32 sliced projection: 2-3 slices of random widths, 1-3 adapters of rank 1-3."""
     rng = np.random.default_rng(seed)
@@ -420,7 +472,44 @@ def pin_sliced_one_slice(lib=None):
         assert np.array_equal(u, v), "one-slice backward"
 
 
+def sliced_saved_u(wl, u):
+    """The sliced saved-activation layout (per training segment in increasing start order, a [len, S r_a] block,
+    slice i in columns [i r_a, (i+1) r_a)) of sliced.forward(..., want_u=True)'s per-row values (slice i's xA in
+    columns [128 i, 128 i + r_a))."""
+    out = []
+    for st, ln, a, tr in sorted(wl.segs.tolist()):
+        if tr and ln > 0:
+            r = int(wl.rank[a])
+            out.append(np.concatenate([u[st:st + ln, 128 * i:128 * i + r] for i in range(wl.n_slices)], axis=1)
+                       .reshape(-1))
+    return np.concatenate(out)
+
+
+def pin_sliced_saved_u(lib=None, seeds=range(3)):
+    """Sliced layer: captured xA equal to the recompute gives the recompute's gradients bit for bit, and a one-hot
+    captured xA in slice i reaches only slice i's columns of dB (= s e_j dY[t] there)."""
+    for sd in seeds:
+        wl = _tiny_sliced(sd + 300)
+        _, u = sliced.forward_wl(wl, want_u=True, lib=lib)
+        us = sliced_saved_u(wl, u)
+        g0 = sliced.backward_wl(wl, lib=lib)
+        g1 = sliced.backward_wl(wl, u_saved=us, lib=lib)
+        for a, b in zip(g0, g1):
+            assert np.array_equal(a, b), ("sliced saved exact u", sd)
+        st, ln, a, _ = sorted(q for q in wl.segs.tolist() if q[3])[0]
+        r = int(wl.rank[a])
+        for i in range(wl.n_slices):
+            oh = np.zeros_like(us)
+            p, j = ln - 1, r - 1
+            oh[p * wl.n_slices * r + i * r + j] = 1.0
+            _, _, dB = sliced.backward_wl(wl, u_saved=oh, lib=lib)
+            exp = np.zeros(wl.B.shape[0], np.float64).reshape(-1, wl.N)
+            c0, c1 = int(wl.bounds[i]), int(wl.bounds[i + 1])
+            exp[int(wl.b_off[a]) // wl.N + j, c0:c1] = float(wl.scale[a]) * wl.dY[st + p, c0:c1]
+            assert np.array_equal(dB, exp.reshape(-1)), ("sliced one-hot saved u", sd, i)
+
+
 ALL_PINS = [pin_brute_forward, pin_brute_backward, pin_merged_weight_config1, pin_zero_B, pin_finite_differences,
             pin_segment_order, pin_pool_order, pin_routing, pin_trainable_count, pin_accumulate,
             pin_sampled_columns, pin_sliced_block_diagonal, pin_sliced_merged_weight, pin_sliced_finite_differences,
-            pin_sliced_one_slice]
+            pin_sliced_one_slice, pin_saved_u_exact, pin_saved_u_onehot, pin_saved_u_double, pin_sliced_saved_u]

@@ -29,6 +29,8 @@ MUTANTS = [
      "dAa[(int64_t)j * K + k] = acc;"),
     ("wrong_B_row", "lora += ut[j] * (double)Ba[(int64_t)j * N + n];",
      "lora += ut[j] * (double)Ba[(int64_t)(r - 1 - j) * N + n];"),
+    ("saved_u_ignored", "            if (u_saved) {", "            if (0) {"),
+    ("saved_u_segment_offset_dropped", "uoff[p] = blk + (int64_t)i * r_q;", "uoff[p] = (int64_t)i * r_q;"),
 ]
 
 
@@ -61,8 +63,11 @@ SLICED_MUTANTS = [
     ("dx_last_slice_only", "dX = dXi if dX is None else dX + dXi", "dX = dXi"),
     ("dA_into_slice_zero", "dA[base + i * r * K:base + (i + 1) * r * K] = dAi[ao[a]:ao[a] + r * K]",
      "dA[base:base + r * K] += dAi[ao[a]:ao[a] + r * K]"),
+    ("saved_u_slice_zero_columns", "out.append(blk[:, i * r:(i + 1) * r].reshape(-1))",
+     "out.append(blk[:, 0:r].reshape(-1))"),
 ]
-SLICED_PINS = [P.pin_sliced_block_diagonal, P.pin_sliced_merged_weight, P.pin_sliced_finite_differences]
+SLICED_PINS = [P.pin_sliced_block_diagonal, P.pin_sliced_merged_weight, P.pin_sliced_finite_differences,
+               P.pin_sliced_saved_u]
 
 
 @pytest.mark.parametrize("name,orig,bad", SLICED_MUTANTS, ids=[m[0] for m in SLICED_MUTANTS])
