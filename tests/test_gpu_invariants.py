@@ -4,6 +4,7 @@
   - the order of the segment table does not change a single bit of y, dX, dA, dB;
   - permuting the adapter pool (ids remapped) does not change a bit of y or dX, and permutes dA/dB blocks;
   - an integer routing pattern (W = 0, A = e_0, integer B, s = 1) reproduces the adapter of every token exactly;
+  - all of the above also on the full co-serving segment table (2048 decode rows: the tensor-core gathered shrink);
   - repeated calls are bitwise identical (no atomics in any reduction);
   - a single base-only segment matches torch.matmul as a second witness.
 """
@@ -31,9 +32,23 @@ def mixed_small(seed=1005, N=640):
                              len_hi=300, train_len=120)
 
 
+def cosrv_full_table(N):
+    """The full co-serving segment table (2048 Zipf(1.1) decode tokens over 320 adapters of ranks 8..128, 4096
+    prefill tokens, 2 x 1024 fine-tuning tokens) at a reduced layer width: its 2048 gathered decode rows exceed the
+    CUDA-core decode-shrink limit (1024 rows), so they take the tensor-core shrink of gathered tiles."""
+    return workloads.config5(K=256, N=N)
+
+
 # N = 640: the forward main pass is split along K (few output tiles, chunk-aligned LoRA splits, a reduce launch);
-# N = 7680: unsplit (every output tile one item that writes y)
-WIDTHS = [640, 7680]
+# N = 7680: unsplit (every output tile one item that writes y).  "full_*": the full co-serving table, split (512)
+# and unsplit (1024) main pass.
+WIDTHS = [640, 7680, "full_512", "full_1024"]
+
+
+def table(N):
+    if isinstance(N, str):
+        return cosrv_full_table(int(N.split("_")[1]))
+    return mixed_small(N=N)
 
 
 def bits(t):
@@ -43,7 +58,7 @@ def bits(t):
 
 @pytest.mark.parametrize("N", WIDTHS)
 def test_zero_B_is_base_bitwise(N):
-    wl = mixed_small(N=N)
+    wl = table(N)
     zero = [a for a in range(wl.n_adapters) if a % 3 == 0]
     for a in zero:
         wl.B[wl.b_off[a]:wl.b_off[a] + wl.rank[a] * wl.N] = 0.0
@@ -66,7 +81,7 @@ def test_zero_B_is_base_bitwise(N):
 
 @pytest.mark.parametrize("N", WIDTHS)
 def test_segment_order_bitwise(N):
-    wl = mixed_small(N=N)
+    wl = table(N)
     d = Dev(wl)
     y0 = bits(d.forward())
     g0 = [bits(t) for t in d.backward()]
@@ -81,7 +96,7 @@ def test_segment_order_bitwise(N):
 
 @pytest.mark.parametrize("N", WIDTHS)
 def test_pool_order_bitwise(N):
-    wl = mixed_small(N=N)
+    wl = table(N)
     d = Dev(wl)
     y0 = bits(d.forward())
     dX0, dA0, dB0 = [bits(t) for t in d.backward()]
@@ -100,16 +115,38 @@ def test_pool_order_bitwise(N):
         assert np.array_equal(dB1[b_off[i]:b_off[i] + r * wl.N], dB0[wl.b_off[p]:wl.b_off[p] + r * wl.N])
 
 
-@pytest.mark.parametrize("which", ["decode", "cosrv", "cosrv_wide"])
+@pytest.mark.parametrize("which", ["decode", "cosrv", "cosrv_wide", "cosrv_full_512", "cosrv_full_1024"])
 def test_routing_integer_pattern_exact(which):
     if which == "decode":
         wl = workloads.config2(T=256, K=256, N=512, n_adapters=64)
+    elif which.startswith("cosrv_full"):
+        wl = cosrv_full_table(int(which.split("_")[-1]))
     else:
         wl = workloads.config5(K=256, N=512 if which == "cosrv" else 6144, n_adapters=64, n_decode=512,
                                prefill_tokens=700, len_lo=20, len_hi=200, train_len=150)
     wl = P.routing_pattern(wl)
     y = to_np(Dev(wl).forward())
     assert np.array_equal(y, P.routing_expected(wl))
+
+
+@pytest.mark.parametrize("N", [512, 1024])
+def test_full_table_matches_oracle(N):
+    """Every row and every fine-tuning gradient of the full co-serving table against the oracle (the tensor-core
+    shrink of the 2048 gathered decode rows included), at a reduced layer width."""
+    import torch
+    import oracle
+    from gpu_util import train_blocks
+    wl = cosrv_full_table(N)
+    d = Dev(wl)
+    y = d.forward()
+    dX, dA, dB = d.backward()
+    torch.cuda.synchronize()
+    compare(to_np(y), oracle.forward_wl(wl), "y")
+    rX, rA, rB = oracle.backward_wl(wl)
+    ia, ib = train_blocks(wl)
+    compare(to_np(dX)[wl.train_rows()], rX, "dX")
+    compare(to_np(dA)[ia], rA[ia], "dA")
+    compare(to_np(dB)[ib], rB[ib], "dB")
 
 
 def test_repeatable_bitwise():
