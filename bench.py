@@ -46,6 +46,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' summaries (20 timed steps each) in the headline line")
+    ap.add_argument("--selftest-ranks", action="store_true",
+                    help="start the ranks as --gpus asks and only check that they meet (gloo, no GPU)")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
                     help="override a workload parameter (e.g. N=4096) for profiling a reduced case")
     return ap.parse_args()
@@ -86,6 +90,9 @@ def accounting(wl):
         lora = sum(2 * ln * r_of(a) * (2 * S * K + 2 * N) for _, ln, a in tr)
         recompute = sum(2 * ln * S * K * r_of(a) for _, ln, a in tr) if wl.xa_mode != "save" else 0
         out["bwd_flops"] = 2 * Tt * K * N + lora + recompute
+        # the backward main pass: dX (dense + its LoRA K-steps) and dA, dB (the backward shrink dY B^T and the x A
+        # recompute run before it)
+        out["bwd_main_flops"] = 2 * Tt * K * N + sum(2 * ln * r_of(a) * (2 * S * K + N) for _, ln, a in tr)
         tads = sorted(set(a for _, _, a in tr))
         out["bwd_bytes"] = 2 * (Tt * N + K * N + 2 * Tt * K) + sum(6 * r_of(a) * (S * K + N) for a in tads)
         out["train_tokens"] = Tt
@@ -121,6 +128,46 @@ def launches_per_step(wl, fwd_info=None):
         if (tiles < 114 and nk // 4 >= 2) or (tiles >= 114 and 0 < tiles % 76 <= 38 and nk // 4 >= 2):
             n += 1                                                                          # split reduce
     return n
+
+
+L2_NOMINAL = 129 * 2 ** 20          # GB300 L2 size used for the flush decision (both arms decide alike)
+
+
+def input_bytes(wl):
+    """Bytes of the step's inputs (x, W, adapter pool, dY) in the layer's element type."""
+    es = 2 if wl.dtype == "bf16" else 4
+    return es * sum(int(a.size) for a in (wl.x, wl.Wt, wl.A, wl.B, wl.dY) if a is not None)
+
+
+def needs_flush(in_bytes):
+    """Inputs not well above the L2 size would largely stay resident from one step to the next: flush unless they
+    exceed twice the L2 size."""
+    return in_bytes <= 2 * L2_NOMINAL
+
+
+def l2_note(in_bytes):
+    if needs_flush(in_bytes):
+        return ("inputs (x, W, adapter pool, dY: %.0f MB) within twice the L2 size: L2 flushed before every step "
+                "by a write of twice its size, outside the step's events" % (in_bytes / 1e6))
+    return "inputs larger than twice the L2 size (x, W, adapter pool, dY: %.0f MB); no flush" % (in_bytes / 1e6)
+
+
+def config_dict(wl, acc, world):
+    """The `config` object of a line (identical in both arms for one workload)."""
+    return {"workload": wl.name, "T": wl.T, "K": wl.K, "N": wl.N, "adapters": wl.n_adapters,
+            "train_tokens": acc.get("train_tokens", 0), "xa": wl.xa_mode, "l2": l2_note(input_bytes(wl)),
+            "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world}
+
+
+def layer_config_dict(L, acc, world):
+    q = L["qkv"]
+    return {"workload": layer_name(L), "T": q.T, "hidden": q.K, "kv": (q.N - q.K) // 2,
+            "intermediate": L["down"].K, "adapters": q.n_adapters,
+            "train_tokens": acc["qkv"].get("train_tokens", 0), "xa": "recompute",
+            "projections": "q|k|v (3 slices), o, gate|up (2 slices), down",
+            "l2": "inputs larger than L2 (weights %.0f MB); no flush"
+                  % (sum(2 * L[n].K * L[n].N for n in LAYER_ORDER) / 1e6),
+            "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world}
 
 
 def peaks():
@@ -201,11 +248,22 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------------------------- CPU oracle sample
+def oracle_threads():
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def sample_size():
+    """The oracle sample of one step, the same in the reference arm and the cpu_baseline leg: at least one forward
+    row per host thread (so that every thread has work), 16 dX rows, 32 + 32 gradient columns."""
+    return {"fwd_rows": max(32, oracle_threads()), "dx_rows": 16, "cols": 32}
+
+
 def oracle_sample(wl, fwd_rows=32, dx_rows=16, cols=32, seed=0):
     """Time the float64 oracle on a bounded, stratified sample of one step and extrapolate to the full step.
 
-    Returns (seconds per full step, description, threads)."""
+    Returns (seconds per full step, description, threads, seconds the sample took)."""
     import oracle
+    t_start = time.perf_counter()
     rng = np.random.default_rng(seed)
     T, K, N = wl.T, wl.K, wl.N
     t_total = 0.0
@@ -249,8 +307,8 @@ def oracle_sample(wl, fwd_rows=32, dx_rows=16, cols=32, seed=0):
         t_total += t1 + per_col * (N + K)
         desc.append("%d dX rows x %d/%d; dA/dB: shrink of all fine-tuning rows + %d+%d gradient columns "
                     "extrapolated to %d+%d" % (dx_rows, trows.shape[0], dx_rows, cols, cols, K, N))
-    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return t_total, "; ".join(desc) + "; linear extrapolation to one full step", threads
+    return (t_total, "; ".join(desc) + "; linear extrapolation to one full step", oracle_threads(),
+            time.perf_counter() - t_start)
 
 
 LAYER_ORDER = ["qkv", "o", "gate_up", "down"]
@@ -267,15 +325,16 @@ def make_layer(rank=0, overrides=()):
 def layer_oracle_sample(L, seed=0, fwd_rows=8, dx_rows=4, cols=8):
     """The oracle on a bounded sample of one layer step: every projection, a sliced one slice by slice (each slice
     is a plain LoRA layer on the shared input)."""
-    t = 0.0
+    t = spent = 0.0
     desc = threads = None
     for n in LAYER_ORDER:
         wl = L[n]
         parts = [workloads.slice_of(wl, i) for i in range(wl.n_slices)] if wl.bounds is not None else [wl]
         for part in parts:
-            dt, desc, threads = oracle_sample(part, fwd_rows=fwd_rows, dx_rows=dx_rows, cols=cols, seed=seed)
+            dt, desc, threads, sp = oracle_sample(part, fwd_rows=fwd_rows, dx_rows=dx_rows, cols=cols, seed=seed)
             t += dt
-    return t, "per projection (a sliced one per slice): " + desc, threads
+            spent += sp
+    return t, "per projection (a sliced one per slice): " + desc, threads, spent
 
 
 def layer_name(L):
@@ -283,46 +342,48 @@ def layer_name(L):
     return "llama3_8b_layer_h%d_kv%d_i%d_T%d_P%d" % (q.K, (q.N - q.K) // 2, L["down"].K, q.T, q.n_adapters)
 
 
+def reference_line(args, tokens, config, steps_fn):
+    """The reference arm's line.  Each step is one bounded oracle sample (sample_size()) of the workload: its
+    wall time is ms_per_step; value is the workload's tokens over the sample's linear extrapolation to a whole
+    step, the same figure the GPU arm's cpu_baseline leg reports."""
+    full, spent = [], []
+    desc = threads = None
+    for i in range(args.warmup + args.steps):
+        t, desc, threads, sp = steps_fn(i)
+        if i >= args.warmup:
+            full.append(t)
+            spent.append(sp)
+    t = statistics.mean(full) if full else float("nan")
+    v = tokens / t
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(spent) * 1e3 if spent else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config,
+            "step": "one bounded oracle sample of the workload per step (ms_per_step is its measured wall time); "
+                    "value extrapolates the sample linearly to whole steps (%.1f s per step)" % t,
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    if "WORLD_SIZE" in os.environ:
+        # rank 0 alone does the work; the launcher's one-thread-per-rank default would idle the other host cores
+        # (the oracle's OpenMP runtime reads this when the oracle library is first loaded, below)
+        os.environ["OMP_NUM_THREADS"] = str(os.cpu_count() or 1)
+    sz = sample_size()
     if args.workload == "layer":
         L = make_layer(0, args.set)
-        tokens = L["qkv"].T
-        times = []
-        desc = threads = None
-        for i in range(args.warmup + args.steps):
-            t, desc, threads = layer_oracle_sample(L, seed=i)
-            if i >= args.warmup:
-                times.append(t)
-        t = statistics.mean(times) if times else float("nan")
-        v = tokens / t
-        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": layer_name(L), "T": tokens},
-                "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
-                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return 0
-    wl = make_workload(args.config, 0, args.set)
-    acc = accounting(wl)
-    times = []
-    desc = threads = None
-    for i in range(args.warmup + args.steps):
-        # each step a smaller sample so that the whole run stays within minutes
-        t, desc, threads = oracle_sample(wl, fwd_rows=8, dx_rows=4, cols=8, seed=i)
-        if i >= args.warmup:
-            times.append(t)
-    t = statistics.mean(times) if times else float("nan")
-    v = acc["tokens"] / t
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "T": wl.T, "K": wl.K, "N": wl.N},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
-            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        acc = {n: accounting(L[n]) for n in LAYER_ORDER}
+        line = reference_line(args, L["qkv"].T, layer_config_dict(L, acc, args.gpus),
+                              lambda i: layer_oracle_sample(L, seed=i, fwd_rows=16, dx_rows=8, cols=16))
+    else:
+        wl = make_workload(args.config, 0, args.set)
+        acc = accounting(wl)
+        line = reference_line(args, acc["tokens"], config_dict(wl, acc, args.gpus),
+                              lambda i: oracle_sample(wl, seed=i, **sz))
     print(json.dumps(line), flush=True)
     return 0
 
@@ -332,7 +393,8 @@ def to_dev(a, torch):
     return torch.from_numpy(workloads.bf16_bits(a).view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def run_ours(args):
+def init_ranks():
+    """(rank, world, local rank, torch.distributed or None); rank 0 builds the library, the others wait for it."""
     import torch
     import lora_co_serving_gb300 as lm
 
@@ -348,8 +410,64 @@ def run_ours(args):
         lm.build()                   # one rank compiles (if anything is stale); the others wait, then load it
     if dist:
         dist.barrier()
+    return rank, world, local, dist
 
-    wl = make_workload(args.config, rank, args.set)
+
+def kernel_roofline(kernel, flops, nbytes, ms, pk, traffic=None):
+    """Roofline of one launch group: bound by whichever of its FLOPs at the bf16 peak and its bytes at the HBM peak
+    takes longer.  The launches run for milliseconds at most inside a short timed region, so the peak is the burst
+    figure (frac_of_sustained: against the seconds-long figure, for reference)."""
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    if t_tc >= t_hbm:
+        achieved = flops / (ms / 1e3) / 1e12
+        return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                "peak_source": pk["source"] + " (burst bf16)",
+                "frac_of_sustained": achieved / pk["bf16_tflops_sustained"], "ms_per_launch": ms,
+                "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes}
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"] + " (HBM copy)",
+            "ms_per_launch": ms, "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes}
+
+
+def step_roofline(flops, nbytes, ms, pk):
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_roof = max(t_tc, t_hbm)
+    return {"tflops": flops / (ms / 1e3) / 1e12, "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
+            "bound": "tensor" if t_tc >= t_hbm else "hbm", "roofline_ms": t_roof * 1e3,
+            "roofline_frac": t_roof * 1e3 / ms, "peak_source": pk["source"] + " (burst bf16, HBM copy)",
+            "roofline_frac_of_sustained": max(flops / (pk["bf16_tflops_sustained"] * 1e12), t_hbm) * 1e3 / ms,
+            "algorithmic_flops": flops, "algorithmic_bytes": nbytes}
+
+
+def compact(line):
+    """The per-workload summary carried in the headline line's `configs` object."""
+    if line is None:
+        return None
+    out = {"workload": line["config"]["workload"], "ms_per_step": line["ms_per_step"], "tokens_per_s": line["value"],
+           "steps": line["steps"], "warmup": line["warmup"], "l2": line["config"]["l2"],
+           "dominant": {k: line["roofline"][k] for k in ("kernel", "bound", "achieved", "unit", "frac")},
+           "step_roofline_frac": line["step"]["roofline_frac"], "step_bound": line["step"]["bound"],
+           "tflops": line["step"]["tflops"], "hbm_gbs": line["step"]["hbm_gbs"],
+           "hbm_frac": line["step"]["hbm_gbs"] / peaks()["hbm_gbs"], "clocks": line["clocks"],
+           "gpu_launches": line["gpu_launches"]}
+    if line.get("graph_replay"):
+        out["graph_replay_ms_per_step"] = line["graph_replay"]["ms_per_step"]
+    return out
+
+
+def measure(args, cfg, rank, world, dist, steps, warmup, extras=True):
+    """Time `steps` steps of workload `cfg` after `warmup` steps; returns rank 0's line (None elsewhere).  extras:
+    also the flagged backward, AdamW, end-to-end and oracle legs (the headline); otherwise the step, its launch
+    groups and its graph replay only."""
+    import torch
+    import lora_co_serving_gb300 as lm
+
+    local = torch.cuda.current_device()
+    wl = make_workload(cfg, rank, args.set if cfg == args.config else ())
     acc = accounting(wl)
     x, Wt, A, B = to_dev(wl.x, torch), to_dev(wl.Wt, torch), to_dev(wl.A, torch), to_dev(wl.B, torch)
     dY = to_dev(wl.dY, torch) if wl.dY is not None else None
@@ -375,27 +493,19 @@ def run_ours(args):
     def step():
         step_on(stream)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     lm.workspace_status(ws)
 
-    # ---- L2: inputs that are not well above the L2 size would largely stay resident from one step to the next, so
-    # unless they exceed twice the L2 size, L2 is flushed (a write of twice its size) before every step, outside
-    # that step's own events
-    l2_bytes = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or 129 * 2 ** 20)
-    in_bytes = sum(t.numel() * t.element_size() for t in (x, Wt, A, B, dY) if t is not None)
-    flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if in_bytes <= 2 * l2_bytes else None
-    l2_note = ("inputs (x, W, adapter pool, dY: %.0f MB) within twice the L2 size (%.0f MB): L2 flushed before "
-               "every step by a %.0f MB write outside the step's events"
-               % (in_bytes / 1e6, l2_bytes / 1e6, 2 * l2_bytes / 1e6)
-               if flush_buf is not None else
-               "inputs larger than twice the L2 size (x, W, adapter pool, dY: %.0f MB; L2 %.0f MB); no flush"
-               % (in_bytes / 1e6, l2_bytes / 1e6))
+    # ---- L2: unless the inputs exceed twice the L2 size, L2 is flushed (a write of twice its size) before every
+    # step, outside that step's own events
+    l2_bytes = max(L2_NOMINAL, int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or 0))
+    flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if needs_flush(input_bytes(wl)) else None
 
     # ---- device-timed region: K steps, per-step trace events around each launch group
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
-    per = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(steps)]
+    per = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     for row in ev:          # torch creates the CUDA event on first record
         for e in row:
             e.record(stream)
@@ -407,7 +517,7 @@ def run_ours(args):
     sampler.start()
     wall0 = time.time()
     start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         if flush_buf is not None:
             flush_buf.fill_(i & 255)
         per[i][0].record(stream)
@@ -423,10 +533,10 @@ def run_ours(args):
         dist.barrier()
     lm.workspace_status(ws)
     if flush_buf is not None:
-        ms = statistics.mean(per[i][0].elapsed_time(per[i][1]) for i in range(args.steps))
+        ms = statistics.mean(per[i][0].elapsed_time(per[i][1]) for i in range(steps))
     else:
-        ms = start.elapsed_time(stop) / args.steps
-    group_ms = [statistics.mean(ev[i][2 * g].elapsed_time(ev[i][2 * g + 1]) for i in range(args.steps))
+        ms = start.elapsed_time(stop) / steps
+    group_ms = [statistics.mean(ev[i][2 * g].elapsed_time(ev[i][2 * g + 1]) for i in range(steps))
                 for g in range(4)]
     t_max = torch.tensor([ms], device="cuda", dtype=torch.float64)
     if dist:
@@ -452,7 +562,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        n_g = max(3, args.steps)
+        n_g = max(3, steps)
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         gper = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_g)]
         with torch.cuda.stream(gs):
@@ -481,7 +591,7 @@ def run_ours(args):
     # saved); timed on their own beside the all-recompute backward and the saved-xA backward without a table
     flagged = None
     n_train = sum(1 for _, ln, _, t in wl.segs.tolist() if t and ln > 0)
-    if wl.backward and n_train > 0 and lm.xa_size(0, pool, segs) > 0:
+    if extras and wl.backward and n_train > 0 and lm.xa_size(0, pool, segs) > 0:
         xs_f = torch.empty(lm.xa_size(0, pool, segs) // 2, dtype=torch.bfloat16, device="cuda")
         lm.forward(x, Wt, pool, segs, y=y, xa_save=xs_f, save_xa=True, workspace=ws, stream=stream)
         modes = {"recompute_all": None, "saved_no_table": None,
@@ -496,7 +606,7 @@ def run_ours(args):
             else:
                 lm.backward_flagged(x, Wt, pool, segs, dY, xs_f, modes[m], dX=dX, dA=dA, dB=dB, workspace=ws,
                                     stream=stream)
-        n_f = max(3, min(args.steps, 50))
+        n_f = max(3, min(steps, 50))
         flagged = {"segments": n_train}
         for m in modes:
             for _ in range(3):
@@ -515,7 +625,7 @@ def run_ours(args):
     # ---- the optimizer step that follows (AdamW on the fine-tuning adapters, fp32 masters + bf16 pool), timed
     # on its own: it is not part of the forward+backward step the metric is about
     adamw_stats = None
-    if wl.backward:
+    if extras and wl.backward:
         tads_u = sorted(set(int(a) for _, _, a, t in wl.segs.tolist() if t))
         masterA, masterB = A.float(), B.float()
         mA, vA = torch.zeros_like(masterA), torch.zeros_like(masterA)
@@ -523,7 +633,7 @@ def run_ours(args):
         for i in range(3):
             lm.adamw_step(pool, K, N, dA, dB, mA, vA, mB, vB, tads_u, step=1 + i, A_master=masterA, B_master=masterB,
                           stream=stream)
-        n_ad = max(3, min(args.steps, 50))
+        n_ad = max(3, min(steps, 50))
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         a0.record(stream)
@@ -543,7 +653,7 @@ def run_ours(args):
     # memory.  Two device buffer sets let the inputs of step i+1 and the results of step i-1 move on two copy
     # streams (the copy engines) while step i computes, as a serving loop would run it.
     e2e = None
-    if not args.no_e2e:
+    if extras and not args.no_e2e:
         x_h = torch.empty_like(x, device="cpu").pin_memory()
         x_h.copy_(x)
         trows = wl.train_rows() if wl.backward else np.zeros(0, np.int64)
@@ -595,7 +705,7 @@ def run_ours(args):
                     dB_h[bo:bo + r * N].copy_(d["dB"][bo:bo + r * N], non_blocking=True)
             ev["out"][b].record(s_out)
 
-        n_e2e = max(4, min(args.steps, 30))
+        n_e2e = max(4, min(steps, 30))
         for i in range(2):
             e2e_step(i)
         torch.cuda.synchronize()
@@ -615,46 +725,54 @@ def run_ours(args):
                "overlap": "inputs of step i+1 and results of step i-1 on copy streams during step i"}
         del sets
 
-    # ---- roofline of the dominant launch (the forward main pass) and of the whole step
+    # ---- roofline of the dominant launch (the forward main pass; the backward main pass without a forward) and of
+    # the whole step
     pk = peaks()
     line = None
     if rank == 0:
         if wl.forward:
-            main_ms = group_ms[1]
-            achieved = acc["fwd_main_flops"] / (main_ms / 1e3) / 1e12
-            tr = profiled_traffic(args.config)
-            roof = {"kernel": "lora_main2_kernel (forward main pass: x W + fused LoRA expand, CTA pairs)", "bound": "tensor",
-                    "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                    "frac": achieved / pk["bf16_tflops_sustained"], "traffic": tr,
-                    "peak_source": pk["source"] + " (sustained bf16)", "ms_per_launch": main_ms,
-                    "algorithmic_flops_per_launch": acc["fwd_main_flops"]}
+            roof = kernel_roofline("lora_main2_kernel (forward main pass: x W + fused LoRA expand, CTA pairs)",
+                                   acc["fwd_main_flops"], acc["fwd_main_bytes"], group_ms[1], pk,
+                                   profiled_traffic(cfg))
         else:
-            main_ms = group_ms[3]
-            achieved = acc["bwd_flops"] / (main_ms / 1e3) / 1e12
-            roof = {"kernel": "lora_main2_kernel (backward dX pass) + lora_tc_kernel (dA, dB)", "bound": "tensor", "achieved": achieved,
-                    "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                    "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
-                    "peak_source": pk["source"] + " (sustained bf16)", "ms_per_launch": main_ms}
-        t_roof = max(acc["flops"] / (pk["bf16_tflops_sustained"] * 1e12), acc["bytes"] / (pk["hbm_gbs"] * 1e9))
-        step_stats = {"tflops": acc["flops"] / (ms / 1e3) / 1e12, "hbm_gbs": acc["bytes"] / (ms / 1e3) / 1e9,
-                      "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms,
-                      "algorithmic_flops": acc["flops"], "algorithmic_bytes": acc["bytes"],
-                      "group_ms": {"fwd_shrink": group_ms[0], "fwd_main": group_ms[1], "bwd_shrink": group_ms[2],
-                                   "bwd_main": group_ms[3]}}
+            roof = kernel_roofline("lora_main2_kernel (backward dX pass) + lora_tc_kernel (dA, dB)",
+                                   acc["bwd_main_flops"], acc["bwd_bytes"], group_ms[3], pk)
+        step_stats = step_roofline(acc["flops"], acc["bytes"], ms, pk)
+        step_stats["group_ms"] = {"fwd_shrink": group_ms[0], "fwd_main": group_ms[1], "bwd_shrink": group_ms[2],
+                                  "bwd_main": group_ms[3]}
         cpu = None
-        if not args.no_cpu_baseline and world == 1:
-            t_cpu, desc, threads = oracle_sample(wl)
+        if extras and not args.no_cpu_baseline and world == 1:
+            t_cpu, desc, threads, _ = oracle_sample(wl, **sample_size())
             cpu = {"value": acc["tokens"] / t_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+                "warmup": warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the pages' workloads)",
-                "config": {"workload": wl.name, "T": T, "K": K, "N": N, "adapters": wl.n_adapters,
-                           "train_tokens": acc.get("train_tokens", 0), "xa": wl.xa_mode,
-                           "l2": l2_note,
-                           "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
+                "config": config_dict(wl, acc, world),
                 "roofline": roof, "step": step_stats, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
                 "graph_replay": graph, "adamw": adamw_stats, "flagged_backward": flagged,
-                "gpu_launches": launches_per_step(wl, fwd_info) * args.steps}
+                "gpu_launches": launches_per_step(wl, fwd_info) * steps}
+    if dist:
+        dist.barrier()
+    return line
+
+
+def run_ours(args):
+    rank, world, local, dist = init_ranks()
+    if args.workload == "layer":
+        line = measure_layer(args, rank, world, dist, args.steps, args.warmup, extras=True)
+    else:
+        line = measure(args, args.config, rank, world, dist, args.steps, args.warmup, extras=True)
+    # the other workloads at one GPU, 20 timed steps each, so that their numbers are measured in the same run
+    if world == 1 and not args.no_configs and not args.set:
+        configs = {}
+        for cfg in (2, 3, 4, 5):
+            if args.workload == "config" and cfg == args.config:
+                continue
+            configs["config%d" % cfg] = compact(measure(args, cfg, 0, 1, None, 20, 5, extras=False))
+        if args.workload != "layer":
+            configs["layer"] = compact(measure_layer(args, 0, 1, None, 20, 5, extras=False))
+        line["configs"] = configs
+    if line is not None:
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
@@ -662,25 +780,14 @@ def run_ours(args):
     return 0
 
 
-def run_layer(args):
+def measure_layer(args, rank, world, dist, steps, warmup, extras=True):
     """One decoder layer's LoRA projections per step: forward q|k|v -> o -> gate|up -> down over every token, then
-    the LoRA backward of the fine-tuning tokens in reverse order, all on one stream with one shared workspace."""
+    the LoRA backward of the fine-tuning tokens in reverse order, all on one stream with one shared workspace.
+    Returns rank 0's line (None elsewhere); extras: also the oracle leg."""
     import torch
     import lora_co_serving_gb300 as lm
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    if rank == 0:
-        lm.build()                   # one rank compiles (if anything is stale); the others wait, then load it
-    if dist:
-        dist.barrier()
-    L = make_layer(rank, args.set)
+    L = make_layer(rank, args.set if args.workload == "layer" else ())
     T = L["qkv"].T
     acc = {n: accounting(L[n]) for n in LAYER_ORDER}
     dev = {}
@@ -730,15 +837,15 @@ def run_layer(args):
         if evs is not None:
             evs[len(calls)].record(stream)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     lm.workspace_status(ws)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(steps)]
     for row in evs:
         for e in row:
             e.record(stream)
-    tev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    tev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(steps)]
     for row in tev:
         for e in row:
             e.record(stream)
@@ -748,7 +855,7 @@ def run_layer(args):
     torch.cuda.synchronize()
     sampler.start()
     wall0 = time.time()
-    for i in range(args.steps):
+    for i in range(steps):
         # trace the launch groups of the gate|up forward (the layer's largest launch)
         for j, (kind, n) in enumerate(calls):
             evs[i][j].record(stream)
@@ -762,53 +869,38 @@ def run_layer(args):
     wall1 = time.time()
     clocks = sampler.stop(wall0, wall1)
     lm.workspace_status(ws)
-    ms_steps = [evs[i][0].elapsed_time(evs[i][len(calls)]) for i in range(args.steps)]
+    ms_steps = [evs[i][0].elapsed_time(evs[i][len(calls)]) for i in range(steps)]
     ms = statistics.mean(ms_steps)
-    per_call = {"%s_%s" % c: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+    per_call = {"%s_%s" % c: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
                 for j, c in enumerate(calls)}
-    gu_main_ms = statistics.mean(tev[i][2].elapsed_time(tev[i][3]) for i in range(args.steps))
+    gu_main_ms = statistics.mean(tev[i][2].elapsed_time(tev[i][3]) for i in range(steps))
     t_max = torch.tensor([ms], device="cuda", dtype=torch.float64)
     if dist:
         dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
     ms_max = float(t_max.item())
     value = T * world / (ms_max / 1e3)
     pk = peaks()
+    line = None
     if rank == 0:
         flops = sum(a["flops"] for a in acc.values())
         nbytes = sum(a["bytes"] for a in acc.values())
-        t_roof = max(flops / (pk["bf16_tflops_sustained"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
-        achieved = acc["gate_up"]["fwd_main_flops"] / (gu_main_ms / 1e3) / 1e12
-        roof = {"kernel": "lora_main2_kernel (gate|up forward main pass: x W + fused LoRA expand, 2 slices)",
-                "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
-                "peak_source": pk["source"] + " (sustained bf16)", "ms_per_launch": gu_main_ms,
-                "algorithmic_flops_per_launch": acc["gate_up"]["fwd_main_flops"]}
+        roof = kernel_roofline("lora_main2_kernel (gate|up forward main pass: x W + fused LoRA expand, 2 slices)",
+                               acc["gate_up"]["fwd_main_flops"], acc["gate_up"]["fwd_main_bytes"], gu_main_ms, pk)
+        step_stats = step_roofline(flops, nbytes, ms, pk)
+        step_stats["call_ms"] = per_call
         cpu = None
-        if not args.no_cpu_baseline and world == 1:
-            t_cpu, desc, threads = layer_oracle_sample(L, fwd_rows=16, dx_rows=8, cols=16)
+        if extras and not args.no_cpu_baseline and world == 1:
+            t_cpu, desc, threads, _ = layer_oracle_sample(L, fwd_rows=16, dx_rows=8, cols=16)
             cpu = {"value": T / t_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
-        q = L["qkv"]
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+                "warmup": warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the pages' workloads)",
-                "config": {"workload": layer_name(L), "T": T, "hidden": q.K, "kv": (q.N - q.K) // 2,
-                           "intermediate": L["down"].K, "adapters": q.n_adapters,
-                           "train_tokens": acc["qkv"].get("train_tokens", 0), "xa": "recompute",
-                           "projections": "q|k|v (3 slices), o, gate|up (2 slices), down",
-                           "l2": "inputs larger than L2 (weights %.0f MB); no flush"
-                                 % (sum(2 * L[n].K * L[n].N for n in LAYER_ORDER) / 1e6),
-                           "parallelism": "replicas" if world == 1 else "dp%d (independent batches)" % world},
-                "roofline": roof,
-                "step": {"tflops": flops / (ms / 1e3) / 1e12, "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
-                         "roofline_ms": t_roof * 1e3, "roofline_frac": t_roof * 1e3 / ms,
-                         "algorithmic_flops": flops, "algorithmic_bytes": nbytes, "call_ms": per_call},
+                "config": layer_config_dict(L, acc, world), "roofline": roof, "step": step_stats,
                 "cpu_baseline": cpu, "clocks": clocks, "e2e": None,
-                "gpu_launches": sum(launches_per_step(L[n], dev[n]["info"]) for n in LAYER_ORDER) * args.steps}
-        print(json.dumps(line), flush=True)
+                "gpu_launches": sum(launches_per_step(L[n], dev[n]["info"]) for n in LAYER_ORDER) * steps}
     if dist:
         dist.barrier()
-        dist.destroy_process_group()
-    return 0
+    return line
 
 
 def sweep_tables(L, seed=77):
@@ -956,12 +1048,43 @@ def run_sweep(args):
     return 0
 
 
+def spawn_ranks(n):
+    """Run this command again as n ranks of one node (torch.distributed.run, rendezvous on 127.0.0.1), one per GPU;
+    returns the launcher's exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n), "--master-addr",
+           "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def selftest_ranks(args):
+    """Each rank joins a gloo group and contributes its rank; rank 0 prints what met."""
+    import torch
+    import torch.distributed as dist
+    dist.init_process_group("gloo")
+    t = torch.tensor([float(dist.get_rank())])
+    dist.all_reduce(t)
+    if dist.get_rank() == 0:
+        print(json.dumps({"ranks": dist.get_world_size(), "rank_sum": float(t.item()), "gpus": args.gpus}), flush=True)
+    dist.barrier()
+    dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: the command starts its own ranks when no launcher did
+        return spawn_ranks(args.gpus)
+    if "WORLD_SIZE" in os.environ and int(os.environ["WORLD_SIZE"]) != args.gpus:
+        raise SystemExit("--gpus %d but %s ranks were launched" % (args.gpus, os.environ["WORLD_SIZE"]))
+    if args.selftest_ranks:
+        return selftest_ranks(args)
     if args.impl == "reference":
         return run_reference(args)
-    if args.workload == "layer":
-        return run_layer(args)
     if args.workload == "sweep":
         return run_sweep(args)
     return run_ours(args)
