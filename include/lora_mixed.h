@@ -162,15 +162,21 @@ int lora_mixed_backward(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const 
  * deployment concern of this library, not part of the method).  Same arguments and results as
  * lora_mixed_forward, but its scratch lives in a fixed library-owned device array of
  * LORA_STATIC_WORKSPACE_BYTES, held by every GPU that loads the library until the process exits; the call
- * allocates nothing.  A batch whose scratch would exceed the array is rejected with LORA_ERR_LIMIT before
- * any launch.  All calls share the array: two calls that overlap on the GPU race and must be ordered by the
- * caller.  The first call on a device looks up the array's address for that device; make it before
- * capturing a stream into a graph; a call made during a capture keeps a pinned host copy of its plan, like
- * every other entry point.  Its status word is not reachable through lora_workspace_status. */
+ * allocates nothing.  A batch whose forward scratch (the workspace lora_mixed_forward would need for it)
+ * exceeds the array is rejected with LORA_ERR_LIMIT before any launch.  All calls share the array: two calls
+ * that overlap on the GPU race and must be ordered by the caller.  Every call that is not being captured into
+ * a CUDA graph looks up the array's address on the current device; a call made during a capture reuses the
+ * address found last on that device, so make one call on the device before capturing (a captured call keeps
+ * a pinned host copy of its plan, like every other entry point). */
 #define LORA_STATIC_WORKSPACE_BYTES (64u << 20)
 int lora_mixed_forward_static(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
                               const lora_pool_t* pool, const lora_segment_t* segs /* HOST */, int32_t n_segs,
                               void* y, void* xa_save, uint32_t flags, void* stream);
+
+/* lora_workspace_status for the library-owned array of lora_mixed_forward_static on the current device: waits for
+ * `stream`, then returns LORA_OK or LORA_ERR_TIMEOUT if a kernel of the last static call gave up a bounded wait
+ * (that call's outputs are then incomplete).  Blocking.  No counterpart on the pages. */
+int lora_static_status(void* stream);
 
 /* AdamW hyperparameters for lora_adamw_step (DeltaServe section 4.1 trains with lr 1e-3, weight decay
  * 0.01; betas and eps are the usual 0.9, 0.999, 1e-8).  step is the 1-based update count. */

@@ -41,7 +41,8 @@ EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_m
             "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events", "lora_mixed_forward_static",
             "lora_selftest_wait_timeout", "lora_adamw_step", "lora_mixed_backward_flagged",
             "lora_sliced_workspace_size", "lora_sliced_xa_size", "lora_sliced_forward", "lora_sliced_backward",
-            "lora_latency_terms", "lora_latency_features", "lora_latency_fit", "lora_latency_predict"]
+            "lora_latency_terms", "lora_latency_features", "lora_latency_fit", "lora_latency_predict",
+            "lora_static_status"]
 
 
 class LoraError(RuntimeError):
@@ -106,6 +107,8 @@ def library(path=None):
     lib.lora_set_trace_events.restype = ctypes.c_int
     lib.lora_mixed_forward_static.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, I32, P, P, ctypes.c_uint32, P]
     lib.lora_mixed_forward_static.restype = ctypes.c_int
+    lib.lora_static_status.argtypes = [P]
+    lib.lora_static_status.restype = ctypes.c_int
     lib.lora_selftest_wait_timeout.argtypes = [P, SZ, P]
     lib.lora_selftest_wait_timeout.restype = ctypes.c_int
     lib.lora_adamw_step.argtypes = [ctypes.c_int, P, I32, I32, P, P, P, P, P, P, P, P, P, P, P, I32, P, P]
@@ -268,6 +271,11 @@ def forward_static(x, Wt, pool, segs, y=None, xa_save=None, save_xa=False, strea
     _check(library().lora_mixed_forward_static(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), _ptr(s), s.shape[0],
                                                _ptr(y), _ptr(xa_save), flags, _stream_ptr(stream)))
     return (y, xa_save) if save_xa else y
+
+
+def static_status(stream=None):
+    """Raise LoraError if a kernel of the last lora_mixed_forward_static call on this device gave up a wait."""
+    _check(library().lora_static_status(_stream_ptr(stream)))
 
 
 def backward(x, Wt, pool, segs, dY, xa_saved=None, dX=None, dA=None, dB=None, want_dx=True, want_grads=True,

@@ -455,6 +455,24 @@ void assign_for(Prepared* e, int sms) {
 }  // namespace
 
 namespace lora {
+int forward_scratch_bytes(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool,
+                          const lora_segment_t* segs, int32_t n_segs, size_t* out) {
+    if (dt == LORA_BF16) {
+        Prepared* pr = nullptr;
+        const int rc = prepare(0, T, K, N, pool, nullptr, segs, n_segs, 0, &pr);
+        if (rc != LORA_OK) return rc;
+        *out = pr->L.total;
+        return LORA_OK;
+    }
+    Problem p;
+    std::string err;
+    const int rc = validate(T, K, N, dt, pool, segs, n_segs, &p, &err);
+    if (rc != LORA_OK) return fail(rc, err);
+    Plan empty;
+    *out = layout_of(p, empty, false).total;
+    return LORA_OK;
+}
+
 // Scoped switch to direct (non-staged) plan uploads for the calling thread; see g_direct_upload.
 DirectUpload::DirectUpload() : prev_(g_direct_upload) { g_direct_upload = true; }
 DirectUpload::~DirectUpload() { g_direct_upload = prev_; }

@@ -109,6 +109,11 @@ class DirectUpload {
 };
 void set_last_error(const char* msg);
 
+// Bytes of workspace lora_mixed_forward needs for this call (its forward layout alone; the bf16 plan comes from the
+// per-thread plan cache that the forward itself uses).  Returns LORA_OK or a validation error (message set).
+int forward_scratch_bytes(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool,
+                          const lora_segment_t* segs, int32_t n_segs, size_t* out);
+
 // The float32 path keeps per-token adapter ids and an xA scratch of [T, 128] floats.
 size_t simt_scratch_bytes(const Problem& p);
 

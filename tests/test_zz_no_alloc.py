@@ -3,9 +3,11 @@
 Serving engines that own every byte of the GPU through their own memory pool (or code that runs while the
 allocator must not be touched) cannot hand the layer a freshly allocated workspace.  This entry point keeps
 the forward pass's scratch in a fixed device array owned by the library.  These tests call it through the
-C ABI and check it against the regular entry point (which uses a caller workspace) on two different batches
-in a row, so the second call starts from whatever the first one left in the shared array; and check that a
-batch too large for the array is refused before anything runs.
+C ABI and check it against the regular entry point (which uses a caller workspace) and against the float64
+oracle on two different batches in a row, so the second call starts from whatever the first one left in the
+shared array; check that the second call leaves the device's free memory unchanged (it allocates nothing) and
+that its status word reads clean; and check that a batch too large for the array is refused before anything
+runs.
 
 This file is collected last on purpose.
 """
@@ -15,6 +17,7 @@ import numpy as np
 import pytest
 
 import lora_co_serving_gb300 as lm
+import oracle
 import workloads
 from gpu_util import Dev, compare, to_np
 
@@ -47,10 +50,17 @@ def test_static_scratch_forward_matches_workspace_forward_twice(lib):
         d = Dev(wl)
         ref = d.forward()                                  # regular entry point, caller workspace
         y = torch.full_like(ref, float("nan"))
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         rc = _static(lib, d, y, stream)
         assert rc == 0, lib.lora_last_error().decode()
         torch.cuda.synchronize()
-        compare(to_np(y), to_np(ref), "static-scratch forward, call %d" % (i + 1))
+        if i > 0:
+            # the first call on a device may load the library's array; later calls allocate nothing
+            assert torch.cuda.mem_get_info()[0] == free0, "the static-scratch forward changed free device memory"
+        assert lib.lora_static_status(stream) == 0, lib.lora_last_error().decode()
+        compare(to_np(y), to_np(ref), "static-scratch forward vs workspace forward, call %d" % (i + 1))
+        compare(to_np(y), oracle.forward_wl(wl), "static-scratch forward vs oracle, call %d" % (i + 1))
 
 
 def test_static_scratch_rejects_oversized_batch(lib):
