@@ -104,8 +104,8 @@ def accounting(wl):
 
 def launches_per_step(wl, fwd_info=None):
     """Kernel launches of one step.  fwd_info: the forward tile plan (info rows of lora_plan_describe: gathered,
-    adapters, LoRA columns, x row).  Gathered decode tiles of up to 1024 rows are shrunk on CUDA cores (one launch)
-    and leave the tensor-core shrink; a main pass with fewer output tiles than kMainTargetItems (114) is split and
+    adapters, LoRA columns, x row).  Gathered decode tiles of up to 1024 rows are shrunk on CUDA cores (one launch,
+    which also gathers the rows) and leave the tensor-core shrink; a main pass with fewer output tiles than kMainTargetItems (114) is split and
     adds a reduce launch."""
     segs = wl.segs.tolist()
     n_nt = lambda cols: -(-cols // 256)
@@ -114,8 +114,7 @@ def launches_per_step(wl, fwd_info=None):
         info = np.asarray(fwd_info) if fwd_info is not None else np.zeros((0, 4), np.int64)
         n_g = int(info[:, 0].sum()) if len(info) else 0
         bgmv = 0 < n_g * 128 <= 1024
-        n += 1 if n_g > 0 else 0                                                            # row gather
-        n += 1 if bgmv else 0                                                               # CUDA-core shrink
+        n += 1 if bgmv else (1 if n_g > 0 else 0)            # CUDA-core shrink (gathers the rows) or row gather
         tc_shrink = [(g, ext) for g, _, ext, _ in info.tolist() if ext > 0 and not (g and bgmv)]
         n += 1 if tc_shrink else 0                                                          # tensor-core shrink
         n += 1                                                                              # main pass

@@ -360,7 +360,7 @@ cudaError_t launch_reduce(const Plan& pl, const KParams& P, uint8_t* ws, const L
     if (pl.splits.empty()) return cudaSuccess;
     return main_reduce_launch(reinterpret_cast<const SplitTile*>(ws + L.splits), int32_t(pl.splits.size()),
                               reinterpret_cast<const int32_t*>(ws + L.rowmap), reinterpret_cast<const float*>(ws + L.part_main),
-                              P.out, P.out_ld, P.out_cols, stream);
+                              P.out, P.out_ld, P.out_cols, P, stream);
 }
 
 
@@ -555,6 +555,20 @@ int lora_workspace_status(const void* workspace, void* stream) {
     return LORA_OK;
 }
 
+int lora_plan_check(int32_t T, int32_t K, int32_t N, const lora_pool_t* pool, const lora_slices_t* slices,
+                    const lora_segment_t* segs, int32_t n_segs, int32_t backward) {
+    Problem p;
+    std::string err;
+    int rc = validate(T, K, N, LORA_BF16, pool, segs, n_segs, &p, &err, slices);
+    if (rc != LORA_OK) return fail(rc, err);
+    Plan pl;
+    if (backward) plan_backward(p, true, true, true, true, &pl);
+    else plan_forward(p, &pl);
+    rc = check_plan(p, pl, backward != 0, &err);
+    if (rc != LORA_OK) return fail(rc, err);
+    return LORA_OK;
+}
+
 int lora_plan_describe(int32_t T, int32_t K, int32_t N, const lora_pool_t* pool, const lora_segment_t* segs,
                        int32_t n_segs, int32_t* n_tiles_out, int32_t* rows_out, int32_t* info_out, int32_t cap) {
     Problem p;
@@ -674,17 +688,27 @@ int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x
     P.xa_save = save ? static_cast<__nv_bfloat16*>(xa_save) : nullptr;
     P.K = K;
     P.N = N;
+    SimtDebug dbg{};
+    if (flags & LORA_DEBUG_CHECKS) {
+        rc = check_plan(p, pl, false, &err);
+        if (rc != LORA_OK) return fail(rc, err);
+        P.debug = 1;
+        P.db = DebugBounds{T, pl.z_blocks, save ? p.xa_elems : 0, 0, pl.part_cols * kTileM, pl.main_slots, 0, 0, T,
+                           (int64_t)pl.n_gtiles * kTileM};
+    }
+    dbg = SimtDebug{P.debug, reinterpret_cast<int32_t*>(ws + L.status), T, (int64_t)pl.n_gtiles * kTileM, pl.z_blocks,
+                    P.db.xa_elems, 0};
 
     rc = begin_call(L, pl, workspace, blob.size(), blob.data(), stream);
     if (rc) return rc;
     CUDA_TRY(trace(0, 0, stream));
-    if (pl.n_gtiles > 0)
-        CUDA_TRY(gather_rows(x, K, reinterpret_cast<const int32_t*>(ws + L.rowmap) + (size_t)pl.g_tile0 * kTileM,
-                             ws + L.xg, pl.n_gtiles * kTileM, stream));
-    if (!pl.bgmv.empty())
-        CUDA_TRY(bgmv_shrink(ws + L.xg, K, pool->A, reinterpret_cast<const BgmvGroup*>(ws + L.bgmv),
+    const int32_t* grows = reinterpret_cast<const int32_t*>(ws + L.rowmap) + (size_t)pl.g_tile0 * kTileM;
+    if (!pl.bgmv.empty())       // the CUDA-core decode shrink, which also fills the gathered buffer
+        CUDA_TRY(bgmv_shrink(x, grows, ws + L.xg, K, pool->A, reinterpret_cast<const BgmvGroup*>(ws + L.bgmv),
                              int32_t(pl.bgmv.size()), reinterpret_cast<const Chunk*>(ws + L.chunks),
-                             reinterpret_cast<const TileDesc*>(ws + L.tiles), p.S, ws + L.z, stream));
+                             reinterpret_cast<const TileDesc*>(ws + L.tiles), p.S, ws + L.z, dbg, stream));
+    else if (pl.n_gtiles > 0)
+        CUDA_TRY(gather_rows(x, K, grows, ws + L.xg, pl.n_gtiles * kTileM, dbg, stream));
     CUDA_TRY(launch_group(0, &P, ws, L, grid, stream));
     CUDA_TRY(trace(0, 1, stream));
     CUDA_TRY(trace(1, 0, stream));
@@ -841,6 +865,15 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
     P.N = N;
     P.accumulate = acc ? 1 : 0;
     P.seg_flags = per_segment ? reinterpret_cast<const int32_t*>(ws + L.seg_flags) : nullptr;
+    if (flags & LORA_DEBUG_CHECKS) {
+        rc = check_plan(p, pl, true, &err);
+        if (rc != LORA_OK) return fail(rc, err);
+        P.debug = 1;
+        P.db = DebugBounds{T, pl.z_blocks, recompute ? 0 : p.xa_elems, (int64_t)p.S * LORA_MAX_RANK * pl.tcols,
+                           pl.part_cols * kTileM, pl.main_slots, p.rows_a * K, p.rows_b * N, T, 0};
+    }
+    const SimtDebug dbg{P.debug, reinterpret_cast<int32_t*>(ws + L.status), T, 0, pl.z_blocks, P.db.xa_elems,
+                        P.db.t_elems};
 
     rc = begin_call(L, pl, workspace, blob.size(), blob.data(), stream);
     if (rc) return rc;
@@ -852,7 +885,7 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
         int32_t max_r = 0;
         for (const TrainSeg& s : pl.tsegs) max_r = std::max(max_r, s.r);
         CUDA_TRY(xat_from_saved(xa_saved, reinterpret_cast<const TrainSeg*>(ws + L.tsegs), int32_t(pl.tsegs.size()),
-                                max_len, max_r, ws + L.xat, int32_t(Pcols), P.seg_flags, stream));
+                                max_len, max_r, ws + L.xat, int32_t(Pcols), P.seg_flags, dbg, stream));
     }
     CUDA_TRY(launch_group(0, &P, ws, L, grid, stream));
     CUDA_TRY(trace(2, 1, stream));

@@ -97,21 +97,26 @@ struct SplitTile {
 };
 
 // The shrink of the gathered decode rows on CUDA cores: each run of up to kBgmvRows consecutive gathered rows that
-// share a chunk is one group; a work unit is one group and 8 of its LoRA columns.  The unit reads its adapter's 8
-// rows of A once, sums x . A_j in fp32 over K in a fixed order (so a row's value depends on its own x and A rows
-// alone) and writes Z = bf16(s * xA) into the tile's Z image, where the main pass's K-extension reads it.  Sliced
-// forward layers: LoRA column j of the group (j < S * rank) is slice j / rank's column j % rank, in that slice's
-// Z region.
+// share a chunk is one group; a work unit is one group and 8 of its LoRA columns.  The unit reads the rows from x
+// and its adapter's 8 rows of A once, sums x . A_j in fp32 over K in a fixed order (so a row's value depends on its
+// own x and A rows alone) and writes Z = bf16(s * xA) into the tile's Z image, where the main pass's K-extension
+// reads it.  The unit of LoRA columns 0..7 also writes the run's rows into the gathered buffer (the main pass's row
+// operand), so no separate gather launch runs; gathered rows without an adapter (and the empty rows that pad the
+// last tile) form copy-only units (chunk -1).  Sliced forward layers: LoRA column j of the group (j < S * rank) is
+// slice j / rank's column j % rank, in that slice's Z region.
 struct BgmvGroup {
     int32_t g_row0;   // first row in the gathered buffer
     int32_t n_rows;   // rows of the run (at most kBgmvRows)
-    int32_t chunk;    // the rows' chunk (adapter, Z column, rank, scale, first A row)
+    int32_t chunk;    // the rows' chunk (adapter, Z column, rank, scale, first A row); -1: copy the rows only
     int32_t j0;       // first LoRA column of this work unit (multiple of 8, below S * rank)
     int32_t tile;     // tile of the rows
     int32_t row0;     // row of g_row0 in the tile
     int32_t pad0, pad1;
 };
-constexpr int kBgmvRows = 8;
+#ifndef LORA_BGMV_ROWS
+#define LORA_BGMV_ROWS 4
+#endif
+constexpr int kBgmvRows = LORA_BGMV_ROWS;   // rows per CUDA-core shrink unit (4 or 8)
 #ifndef LORA_BGMV_MAX_ROWS
 #define LORA_BGMV_MAX_ROWS 1024
 #endif
@@ -151,6 +156,20 @@ constexpr int kMainTargetItems = LORA_MAIN_TARGET_ITEMS;
 // CTA pairs the planner sizes waves for (76 on a 152-SM GB300; plans stay valid on any device).
 constexpr int kPairsPlanned = 76;
 constexpr int kMainPartialFloats = kBN * kTileM;   // one CTA's fp32 partial of a 128 x 256 output tile
+
+// Extents of the buffers a launch writes, against which the kernels check every store index they derive from the
+// plan when a call sets LORA_DEBUG_CHECKS (a failing check skips the store and records LORA_ERR_BOUNDS).
+struct DebugBounds {
+    int64_t out_rows;       // rows of y (forward) or dX (backward)
+    int64_t z_blocks;       // Z blocks of the workspace
+    int64_t xa_elems;       // elements of the saved-activation buffer
+    int64_t t_elems;        // elements of each transposed buffer (xA^T, dYB^T)
+    int64_t part_floats;    // floats of the shrink partials
+    int64_t main_slots;     // split partial slots of the main pass
+    int64_t grad_a, grad_b; // elements of dA and dB (the pools' extents)
+    int64_t x_rows;         // rows of x
+    int64_t g_rows;         // rows of the gathered buffer
+};
 
 struct GradGroup {    // one fine-tuning adapter of a backward call
     int32_t adapter;

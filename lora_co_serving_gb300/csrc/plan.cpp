@@ -416,12 +416,16 @@ void plan_forward(const Problem& p, Plan* out) {
         const int32_t n_g = pl.n_gtiles * kTileM;
         for (int32_t g = 0; g < n_g;) {
             const int32_t idx = pl.g_tile0 * kTileM + g;
-            const int32_t c = pl.rowchunk[idx];
-            if (pl.rowmap[idx] < 0 || c < 0) { ++g; continue; }
-            int32_t n = 1;     // a run stays inside one tile
-            while (n < kBgmvRows && (g + n) % kTileM != 0 && pl.rowmap[idx + n] >= 0 && pl.rowchunk[idx + n] == c) ++n;
-            for (int32_t j0 = 0; j0 < p.S * pl.chunks[c].r; j0 += 8)
-                pl.bgmv.push_back(BgmvGroup{g, n, c, j0, pl.g_tile0 + g / kTileM, g % kTileM, 0, 0});
+            const int32_t c = pl.rowmap[idx] < 0 ? -1 : pl.rowchunk[idx];
+            int32_t n = 1;     // a run stays inside one tile; rows without an adapter (or token) form copy-only runs
+            auto chunk_at = [&](int32_t i) { return pl.rowmap[i] < 0 ? -1 : pl.rowchunk[i]; };
+            while (n < kBgmvRows && (g + n) % kTileM != 0 && chunk_at(idx + n) == c) ++n;
+            if (c < 0) {
+                pl.bgmv.push_back(BgmvGroup{g, n, -1, 0, pl.g_tile0 + g / kTileM, g % kTileM, 0, 0});
+            } else {
+                for (int32_t j0 = 0; j0 < p.S * pl.chunks[c].r; j0 += 8)
+                    pl.bgmv.push_back(BgmvGroup{g, n, c, j0, pl.g_tile0 + g / kTileM, g % kTileM, 0, 0});
+            }
             g += n;
         }
     }
@@ -571,6 +575,145 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
                     pl.items[2].push_back(w);
                 }
     }
+}
+
+int check_plan(const Problem& p, const Plan& pl, bool backward, std::string* err) {
+    const int64_t nt = int64_t(pl.tiles.size());
+    const int64_t n_chunks = int64_t(pl.chunks.size());
+    const int64_t n_atoms = int64_t(pl.atoms_a.size());
+    const int64_t g_rows = int64_t(pl.n_gtiles) * kTileM;
+    const int64_t out_cols = backward ? p.K : p.N;
+    const int64_t kb_main = cdiv(backward ? p.N : p.K, kBK);
+    auto bad = [&](const std::string& what) {
+        *err = "plan check: " + what;
+        return LORA_ERR_BOUNDS;
+    };
+    if (int64_t(pl.rowmap.size()) != nt * kTileM || int64_t(pl.rowchunk.size()) != nt * kTileM ||
+        int64_t(pl.rowaux.size()) != nt * kTileM || pl.atoms_b.size() != pl.atoms_a.size() ||
+        pl.boxes_a.size() != pl.atoms_a.size() || pl.boxes_b.size() != pl.atoms_a.size())
+        return bad("per-row or per-atom tables of the wrong length");
+    // LoRA columns of a tile's Z (all slice regions of a forward sliced tile)
+    auto z_cols = [&](const TileDesc& td) -> int64_t {
+        return (!backward && p.S > 1) ? int64_t(p.S) * td.zstride : td.ext_k;
+    };
+    for (int64_t i = 0; i < nt; ++i) {
+        const TileDesc& td = pl.tiles[i];
+        const std::string at = "tile " + std::to_string(i) + ": ";
+        // a window's second tile may start past the last row (its rows then read as zero)
+        if (td.a_src == 0 ? (td.a_row0 < 0 || td.a_row0 >= p.T + kTileM) : (td.a_row0 < 0 || td.a_row0 + kTileM > g_rows))
+            return bad(at + "row window outside its source");
+        if (td.chunk0 < 0 || td.nchunk < 0 || td.chunk0 + td.nchunk > n_chunks) return bad(at + "chunk range");
+        if (td.ext_k < 0 || td.ext_k % 16 != 0) return bad(at + "LoRA columns not a multiple of 16");
+        if (td.atom0 < 0 || td.atom0 + cdiv(z_cols(td), 8) > n_atoms) return bad(at + "atom range");
+        if (td.z_blk0 < 0 || td.z_blk0 + cdiv(td.ext_k, kBK) > pl.z_blocks) return bad(at + "Z blocks");
+        if (td.sh_c0 < 0 || td.sh_c0 > td.sh_c1 || td.sh_c1 > td.ext_k) return bad(at + "shrink columns");
+        if (backward && (td.tpos0 < 0 || td.tpos0 + kTileM > pl.tcols || td.seg < 0 ||
+                         td.seg >= int32_t(pl.tsegs.size())))
+            return bad(at + "transposed-buffer columns or segment");
+        for (int r = 0; r < kTileM; ++r) {
+            const int64_t k = i * kTileM + r;
+            const int32_t t = pl.rowmap[k], c = pl.rowchunk[k], aux = pl.rowaux[k];
+            if (t < -1 || t >= p.T) return bad(at + "row " + std::to_string(r) + " maps outside [0, T)");
+            if (c != -1 && (c < td.chunk0 || c >= td.chunk0 + td.nchunk)) return bad(at + "row chunk outside the tile");
+            if (aux != -1) {
+                if (c < 0) return bad(at + "saved-activation offset on a row without an adapter");
+                if (aux < 0 || aux + int64_t(p.S) * pl.chunks[c].r > p.xa_elems) return bad(at + "saved-activation offset");
+            }
+        }
+    }
+    // an atom is loaded as an 8-row TMA box (or the first of a taller box's runs of consecutive atoms); a rank that
+    // is not a multiple of 8 rounds the last atom up, and rows past the pool's end read as zero, so what must hold
+    // is that every atom starts inside the pool and a box's atoms follow one another
+    for (int64_t i = 0; i < n_atoms; ++i) {
+        const int32_t ra = pl.atoms_a[i], rb = pl.atoms_b[i];
+        if (ra < 0 || ra >= p.rows_a || rb < 0 || rb >= p.rows_b)
+            return bad("atom " + std::to_string(i) + ": starts outside the pool");
+        for (int pass = 0; pass < 2; ++pass) {
+            const std::vector<int32_t>& rows = pass ? pl.atoms_b : pl.atoms_a;
+            const int32_t box = (pass ? pl.boxes_b : pl.boxes_a)[i];
+            if (box < 0 || box > 8 || i + box > n_atoms) return bad("atom " + std::to_string(i) + ": box size");
+            for (int32_t k = 1; k < box; ++k)
+                if (rows[i + k] != rows[i] + 8 * k) return bad("atom " + std::to_string(i) + ": box of unrelated rows");
+        }
+    }
+    for (int64_t c = 0; c < n_chunks; ++c) {
+        const Chunk& ch = pl.chunks[c];
+        if (ch.adapter < 0 || ch.adapter >= p.n_adapters || ch.r != p.rank[ch.adapter] || ch.zcol % 16 != 0 ||
+            ch.prow_a < 0 || ch.prow_a + int64_t(p.S) * ch.r > p.rows_a || ch.prow_b < 0 || ch.prow_b + ch.r > p.rows_b)
+            return bad("chunk " + std::to_string(c));
+    }
+    for (size_t u = 0; u < pl.units.size(); ++u) {
+        const ShrinkUnit& su = pl.units[u];
+        if (su.tile < 0 || su.tile >= nt || su.nsplit < 1 || su.part0 < 0 ||
+            su.part0 + int64_t(su.nsplit) * su.mma_n > pl.part_cols)
+            return bad("shrink unit " + std::to_string(u));
+    }
+    for (int k = 0; k < 3; ++k) {
+        for (size_t j = 0; j < pl.items[k].size(); ++j) {
+            const WorkItem& w = pl.items[k][j];
+            const std::string at = "item " + std::to_string(k) + "." + std::to_string(j) + ": ";
+            if (w.mma_n < 16 || w.mma_n > kPassCols || w.mma_n % 16 != 0) return bad(at + "MMA N");
+            if (w.kind == kMainFwd || w.kind == kMainDx) {
+                if (w.tile < 0 || w.tile + 1 >= nt) return bad(at + "tile pair");
+                if (w.n0 < 0 || w.n0 >= out_cols) return bad(at + "output columns");
+                if (w.kb0 < 0 || w.nk < 0 || w.kb0 + w.nk > kb_main) return bad(at + "k-blocks");
+                const int32_t ek = pl.tiles[w.tile].ext_k;
+                if (w.ext_c0 < 0 || w.ext_c0 > w.ext_c1 || w.ext_c1 > ek) return bad(at + "LoRA columns");
+                if (w.ext_c0 / kBK + w.n_ext > cdiv(ek, kBK)) return bad(at + "LoRA k-blocks");
+                if (w.nsplit > 1 && (w.part < 0 || w.part + w.split >= pl.main_slots)) return bad(at + "split slot");
+            } else if (w.kind == kGradDb || w.kind == kGradDa) {
+                if (w.tile < 0 || w.tile >= int32_t(pl.groups.size())) return bad(at + "gradient group");
+                const GradGroup& g = pl.groups[w.tile];
+                if (w.n0 < 0 || w.n0 >= (w.kind == kGradDb ? p.N : p.K)) return bad(at + "gradient rows");
+                if (w.j0 < 0 || w.j0 + w.mma_n > int64_t(p.S) * LORA_MAX_RANK) return bad(at + "transposed rows");
+                if (w.kind == kGradDa && w.j0 >= int64_t(g.nslice) * g.r) return bad(at + "down-factor rows");
+            } else {
+                if (w.tile < 0 || w.tile >= nt) return bad(at + "tile");
+                if (w.n_ext < 0 || w.n_ext >= int32_t(pl.units.size()) || pl.units[w.n_ext].tile != w.tile)
+                    return bad(at + "shrink unit");
+                const TileDesc& td = pl.tiles[w.tile];
+                const int64_t kb_all = cdiv(w.kind == kShrinkDyb ? p.N : p.K, kBK);
+                if (w.kb0 < 0 || w.nk < 1 || w.kb0 + w.nk > kb_all) return bad(at + "k-blocks");
+                if (w.n0 < 0 || w.n0 + w.mma_n > cdiv(z_cols(td), 16) * 16 || td.atom0 + (w.n0 + w.mma_n) / 8 > n_atoms)
+                    return bad(at + "LoRA columns");
+                if (w.part < 0 || w.part + w.mma_n > pl.part_cols) return bad(at + "partial columns");
+                if (w.kind != kShrinkXa && td.z_blk0 + cdiv(w.n0 + w.mma_n, kBK) > pl.z_blocks) return bad(at + "Z blocks");
+            }
+        }
+    }
+    for (size_t i = 0; i < pl.splits.size(); ++i) {
+        const SplitTile& st = pl.splits[i];
+        if (st.tile < 0 || st.tile + 1 >= nt || st.n0 < 0 || st.n0 >= out_cols || st.part < 0 ||
+            st.part + st.nsplit > pl.main_slots)
+            return bad("split tile " + std::to_string(i));
+    }
+    for (size_t i = 0; i < pl.bgmv.size(); ++i) {
+        const BgmvGroup& g = pl.bgmv[i];
+        const std::string at = "decode-shrink unit " + std::to_string(i) + ": ";
+        if (g.g_row0 < 0 || g.n_rows < 1 || g.n_rows > kBgmvRows || g.g_row0 + g.n_rows > g_rows) return bad(at + "rows");
+        if (g.tile < pl.g_tile0 || g.tile >= nt || g.row0 < 0 || g.row0 + g.n_rows > kTileM) return bad(at + "tile rows");
+        if (g.chunk >= 0) {
+            if (g.chunk >= n_chunks) return bad(at + "chunk");
+            const Chunk& ch = pl.chunks[g.chunk];
+            if (g.j0 < 0 || g.j0 >= int64_t(p.S) * ch.r) return bad(at + "LoRA columns");
+            const TileDesc& td = pl.tiles[g.tile];
+            const int64_t last = int64_t(p.S - 1) * td.zstride + ch.zcol + ch.r;   // one past the last Z column
+            if (last > cdiv(z_cols(td), kBK) * kBK) return bad(at + "Z columns");
+        }
+    }
+    for (size_t q = 0; q < pl.tsegs.size(); ++q) {
+        const TrainSeg& s = pl.tsegs[q];
+        if (s.start < 0 || s.start + s.len > p.T || s.tpos0 < 0 || s.tpos0 + cdiv(s.len, 2 * kTileM) * 2 * kTileM > pl.tcols ||
+            s.xoff < 0 || s.xoff + int64_t(s.len) * s.r > p.xa_elems || s.group < 0 || s.group >= int32_t(pl.groups.size()))
+            return bad("fine-tuning segment " + std::to_string(q));
+    }
+    for (size_t g = 0; g < pl.groups.size(); ++g) {
+        const GradGroup& gg = pl.groups[g];
+        if (gg.seg0 < 0 || gg.seg0 + gg.nseg > int32_t(pl.tsegs.size()) || gg.prow_a < 0 ||
+            gg.prow_a + int64_t(gg.nslice) * gg.r > p.rows_a || gg.prow_b < 0 || gg.prow_b + gg.r > p.rows_b)
+            return bad("gradient group " + std::to_string(g));
+    }
+    return LORA_OK;
 }
 
 static int64_t item_cost(const WorkItem& w) {

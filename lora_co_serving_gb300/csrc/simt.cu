@@ -14,10 +14,18 @@ namespace lora {
 
 namespace {
 
+// LORA_DEBUG_CHECKS: idx inside [0, extent), else LORA_ERR_BOUNDS is recorded and the caller skips the access
+__device__ __forceinline__ bool dbg_ok(const SimtDebug& d, int64_t idx, int64_t extent) {
+    if (!d.on || (idx >= 0 && idx < extent)) return true;
+    atomicCAS(d.status, 0, LORA_ERR_BOUNDS);
+    return false;
+}
+
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, int32_t k8, const int32_t* __restrict__ rows,
-                                   uint4* __restrict__ out, int32_t n_rows) {
+                                   uint4* __restrict__ out, int32_t n_rows, const SimtDebug dbg) {
     for (int32_t i = blockIdx.x; i < n_rows; i += gridDim.x) {
         const int32_t t = rows[i];
+        if (t >= 0 && !dbg_ok(dbg, t, dbg.x_rows)) continue;
         uint4* dst = out + (size_t)i * k8;
         if (t >= 0) {
             const uint4* src = x + (size_t)t * k8;
@@ -29,37 +37,65 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, int32_t k8, cons
     }
 }
 
-// The shrink of the gathered decode rows on CUDA cores (see BgmvGroup).  Block = one work unit: a run of up to 8
-// rows sharing a chunk, and 8 of its LoRA columns.  Thread i of the block's kBgmvThreads takes the 16-byte pieces
-// i, i + kBgmvThreads, ... of K; per piece it loads the unit's 8 rows of A and the run's rows of x and accumulates
-// the 64 products in fp32.  A warp's 64 partial sums are combined by a halving shuffle tree (lane l ends with sums
-// 2l and 2l + 1; every sum is formed by the same tree over the lanes), the warps' in warp order through shared
-// memory, so each result depends on its own row of x and row of A alone.  Thread t < 64 writes Z = bf16(s * xA) of run row t / 8, column t % 8.
+// The shrink of the gathered decode rows on CUDA cores (see BgmvGroup).  Block = one work unit: a run of up to
+// kBgmvRows rows sharing a chunk, and 8 of its LoRA columns.  Thread i of the block's kBgmvThreads takes the 16-byte
+// pieces i, i + kBgmvThreads, ... of K; per piece it loads the unit's 8 rows of A and the run's rows of x and
+// accumulates the kBgmvRows x 8 products in fp32.  A warp's partial sums are combined by a halving shuffle tree
+// (every sum is formed by the same tree over the lanes), the warps' in warp order through shared memory, so each
+// result depends on its own row of x and row of A alone.  Thread t < kBgmvRows * 8 writes Z = bf16(s * xA) of run
+// row t / 8, column t % 8.
 #ifndef LORA_BGMV_THREADS
 #define LORA_BGMV_THREADS 128
 #endif
-constexpr int kBgmvThreads = LORA_BGMV_THREADS;   // 128: two blocks fit an SM's registers (one with 256)
-__global__ void __launch_bounds__(kBgmvThreads) bgmv_z_kernel(const uint4* __restrict__ xg, int32_t k8,
+constexpr int kBgmvThreads = LORA_BGMV_THREADS;   // 128 threads and 4 rows per unit measured fastest (decode batches of
+                                                  // 256 and 1024 tokens: 16 and 24 us against 18 and 26 with 8 rows)
+__global__ void __launch_bounds__(kBgmvThreads) bgmv_z_kernel(const uint4* __restrict__ xsrc, int32_t k8,
+                                                     const int32_t* __restrict__ grows, uint4* __restrict__ xg,
                                                      const uint4* __restrict__ A, const BgmvGroup* __restrict__ groups,
                                                      const Chunk* __restrict__ chunks,
                                                      const TileDesc* __restrict__ tiles, int32_t S,
-                                                     uint8_t* __restrict__ zout) {
-    __shared__ float red[kBgmvThreads / 32][64];
+                                                     uint8_t* __restrict__ zout, const SimtDebug dbg) {
+    constexpr int kSums = kBgmvRows * 8;      // the unit's row x column sums
+    static_assert(kSums == 32 || kSums == 64, "4 or 8 rows per unit");
+    __shared__ float red[kBgmvThreads / 32][kSums];
     const BgmvGroup u = groups[blockIdx.x];
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    if (dbg.on) {      // the run's gathered rows and their token rows must lie in their buffers
+        bool ok = dbg_ok(dbg, (int64_t)u.g_row0 + u.n_rows - 1, dbg.g_rows);
+        for (int i = 0; ok && i < u.n_rows; ++i) ok = dbg_ok(dbg, max(grows[u.g_row0 + i], 0), dbg.x_rows);
+        if (!ok) return;
+    }
+    if (u.chunk < 0) {
+        // copy-only unit: rows of base-only decode tokens (and zeros for the empty rows of the last tile)
+        for (int i = 0; i < u.n_rows; ++i) {
+            const int32_t t = grows[u.g_row0 + i];
+            uint4* dst = xg + (size_t)(u.g_row0 + i) * k8;
+            for (int32_t v = threadIdx.x; v < k8; v += kBgmvThreads) dst[v] = (t >= 0) ? xsrc[(size_t)t * k8 + v] : zero;
+        }
+        return;
+    }
     const Chunk ch = chunks[u.chunk];
     const int32_t r_all = S * ch.r;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    float acc[64];
+    const bool copy = (u.j0 == 0);      // this unit also writes the run's rows into the gathered buffer
+    const uint4* xr[kBgmvRows];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < kBgmvRows; ++i) xr[i] = xsrc + (size_t)(i < u.n_rows ? grows[u.g_row0 + i] : 0) * k8;
+    float acc[kSums];
+#pragma unroll
+    for (int i = 0; i < kSums; ++i) acc[i] = 0.f;
     for (int32_t v = threadIdx.x; v < k8; v += kBgmvThreads) {
         uint4 a[8], x[kBgmvRows];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             a[j] = (u.j0 + j < r_all) ? A[(size_t)(ch.prow_a + u.j0 + j) * k8 + v] : zero;
 #pragma unroll
-        for (int i = 0; i < kBgmvRows; ++i) x[i] = (i < u.n_rows) ? xg[(size_t)(u.g_row0 + i) * k8 + v] : zero;
+        for (int i = 0; i < kBgmvRows; ++i) x[i] = (i < u.n_rows) ? xr[i][v] : zero;
+        if (copy) {
+#pragma unroll
+            for (int i = 0; i < kBgmvRows; ++i)
+                if (i < u.n_rows) xg[(size_t)(u.g_row0 + i) * k8 + v] = x[i];
+        }
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             float af[8][2], xf[kBgmvRows][2];
@@ -84,9 +120,11 @@ __global__ void __launch_bounds__(kBgmvThreads) bgmv_z_kernel(const uint4* __res
                 }
         }
     }
+    // halving tree: at each stage a lane keeps one half of its sums and adds its partner's copy of that half;
+    // afterwards lane l holds sums [l * kSums / 32, (l + 1) * kSums / 32)
 #pragma unroll
     for (int st = 0; st < 5; ++st) {
-        const int off = 16 >> st, half = 32 >> st;
+        const int off = 16 >> st, half = (kSums / 2) >> st;
         const bool up = (lane & off) != 0;
 #pragma unroll
         for (int k = 0; k < half; ++k) {
@@ -95,11 +133,11 @@ __global__ void __launch_bounds__(kBgmvThreads) bgmv_z_kernel(const uint4* __res
             acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
-    red[warp][2 * lane] = acc[0];
-    red[warp][2 * lane + 1] = acc[1];
+#pragma unroll
+    for (int k = 0; k < kSums / 32; ++k) red[warp][lane * (kSums / 32) + k] = acc[k];
     __syncthreads();
     const int t = threadIdx.x;
-    if (t >= 64) return;
+    if (t >= kSums) return;
     float sum = red[0][t];
 #pragma unroll
     for (int w = 1; w < kBgmvThreads / 32; ++w) sum += red[w][t];
@@ -109,6 +147,7 @@ __global__ void __launch_bounds__(kBgmvThreads) bgmv_z_kernel(const uint4* __res
     const int32_t reg = j / ch.r, jj = j - reg * ch.r;
     const int32_t zc = reg * td.zstride + ch.zcol + jj;
     const int row = u.row0 + i;
+    if (!dbg_ok(dbg, td.z_blk0 + zc / 64, dbg.z_blocks)) return;
     uint8_t* blk = zout + (size_t)(td.z_blk0 + zc / 64) * kZBlockBytes + row * 128;
     const int chunk16 = ((zc % 64) / 8) ^ (row & 7);
     *reinterpret_cast<__nv_bfloat16*>(blk + chunk16 * 16 + (zc % 8) * 2) = __float2bfloat16_rn(ch.scale * sum);
@@ -120,7 +159,8 @@ __global__ void __launch_bounds__(kBgmvThreads) bgmv_z_kernel(const uint4* __res
 __global__ void __launch_bounds__(256) xat_from_saved_kernel(const __nv_bfloat16* __restrict__ xa_saved,
                                                              const TrainSeg* __restrict__ tsegs, int32_t n_tsegs,
                                                              __nv_bfloat16* __restrict__ xat, int32_t P,
-                                                             const int32_t* __restrict__ seg_flags) {
+                                                             const int32_t* __restrict__ seg_flags,
+                                                             const SimtDebug dbg) {
     __shared__ __nv_bfloat16 tile[32][34];
     const TrainSeg s = tsegs[blockIdx.z];
     if (seg_flags != nullptr && seg_flags[s.order] == 0) return;
@@ -132,14 +172,16 @@ __global__ void __launch_bounds__(256) xat_from_saved_kernel(const __nv_bfloat16
     for (int k = 0; k < 4; ++k) {
         const int32_t t = t0 + ty + 8 * k, j = j0 + tx;
         __nv_bfloat16 v = __float2bfloat16_rn(0.f);
-        if (t < s.len && j < s.r) v = xa_saved[(size_t)s.xoff + (size_t)t * s.r + j];
+        if (t < s.len && j < s.r && dbg_ok(dbg, (int64_t)s.xoff + (int64_t)t * s.r + j, dbg.xa_elems))
+            v = xa_saved[(size_t)s.xoff + (size_t)t * s.r + j];
         tile[ty + 8 * k][tx] = v;
     }
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int32_t j = j0 + ty + 8 * k, t = t0 + tx;
-        if (j < s.r && t < span) xat[(size_t)j * P + s.tpos0 + t] = tile[tx][ty + 8 * k];
+        if (j < s.r && t < span && dbg_ok(dbg, (int64_t)j * P + s.tpos0 + t, dbg.t_elems))
+            xat[(size_t)j * P + s.tpos0 + t] = tile[tx][ty + 8 * k];
     }
 }
 
@@ -271,27 +313,31 @@ inline int grid_for(int64_t n) {
 
 }  // namespace
 
-cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out, int32_t n_rows, cudaStream_t s) {
+cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out, int32_t n_rows, const SimtDebug& dbg,
+                        cudaStream_t s) {
     if (n_rows <= 0) return cudaSuccess;
     gather_rows_kernel<<<n_rows < 65535 ? n_rows : 65535, 256, 0, s>>>(
-        static_cast<const uint4*>(x), K / 8, rows, static_cast<uint4*>(out), n_rows);
+        static_cast<const uint4*>(x), K / 8, rows, static_cast<uint4*>(out), n_rows, dbg);
     return cudaGetLastError();
 }
 
-cudaError_t bgmv_shrink(const void* xg, int32_t K, const void* A, const BgmvGroup* groups, int32_t n_groups,
-                        const Chunk* chunks, const TileDesc* tiles, int32_t S, void* zout, cudaStream_t s) {
+cudaError_t bgmv_shrink(const void* x, const int32_t* grows, void* xg, int32_t K, const void* A,
+                        const BgmvGroup* groups, int32_t n_groups, const Chunk* chunks, const TileDesc* tiles, int32_t S,
+                        void* zout, const SimtDebug& dbg, cudaStream_t s) {
     if (n_groups <= 0) return cudaSuccess;
-    bgmv_z_kernel<<<n_groups, kBgmvThreads, 0, s>>>(static_cast<const uint4*>(xg), K / 8, static_cast<const uint4*>(A), groups,
-                                           chunks, tiles, S, static_cast<uint8_t*>(zout));
+    bgmv_z_kernel<<<n_groups, kBgmvThreads, 0, s>>>(static_cast<const uint4*>(x), K / 8, grows, static_cast<uint4*>(xg),
+                                                    static_cast<const uint4*>(A), groups, chunks, tiles, S,
+                                                    static_cast<uint8_t*>(zout), dbg);
     return cudaGetLastError();
 }
 
 cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len,
-                           int32_t max_r, void* xat, int32_t P, const int32_t* seg_flags, cudaStream_t s) {
+                           int32_t max_r, void* xat, int32_t P, const int32_t* seg_flags, const SimtDebug& dbg,
+                           cudaStream_t s) {
     if (n_tsegs <= 0) return cudaSuccess;
     dim3 grid((max_len + 127) / 128 * 4, (max_r + 31) / 32, n_tsegs);
     xat_from_saved_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(xa_saved), tsegs, n_tsegs,
-                                               static_cast<__nv_bfloat16*>(xat), P, seg_flags);
+                                               static_cast<__nv_bfloat16*>(xat), P, seg_flags, dbg);
     return cudaGetLastError();
 }
 

@@ -54,13 +54,25 @@ struct F32Args {
     const int64_t* group_b_off;
 };
 
-cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out, int32_t n_rows, cudaStream_t s);
+// LORA_DEBUG_CHECKS for the CUDA-core kernels: when `on`, store (and row) indices are checked against these extents;
+// a failing check skips the access and records LORA_ERR_BOUNDS in *status.
+struct SimtDebug {
+    int32_t on;
+    int32_t* status;
+    int64_t x_rows, g_rows, z_blocks, xa_elems, t_elems;
+};
+
+cudaError_t gather_rows(const void* x, int32_t K, const int32_t* rows, void* out, int32_t n_rows, const SimtDebug& dbg,
+                        cudaStream_t s);
 // Z = bf16(s x A) of the gathered rows listed in `groups` (device arrays; S slices), written into the Z images of
-// their tiles (zout: the zeroed Z blocks).
-cudaError_t bgmv_shrink(const void* xg, int32_t K, const void* A, const BgmvGroup* groups, int32_t n_groups,
-                        const Chunk* chunks, const TileDesc* tiles, int32_t S, void* zout, cudaStream_t s);
+// their tiles (zout: the zeroed Z blocks); also fills the gathered buffer xg from x (grows: token row of every
+// gathered row, -1 for none).
+cudaError_t bgmv_shrink(const void* x, const int32_t* grows, void* xg, int32_t K, const void* A,
+                        const BgmvGroup* groups, int32_t n_groups, const Chunk* chunks, const TileDesc* tiles, int32_t S,
+                        void* zout, const SimtDebug& dbg, cudaStream_t s);
 cudaError_t xat_from_saved(const void* xa_saved, const TrainSeg* tsegs, int32_t n_tsegs, int32_t max_len,
-                           int32_t max_r, void* xat, int32_t P, const int32_t* seg_flags, cudaStream_t s);
+                           int32_t max_r, void* xat, int32_t P, const int32_t* seg_flags, const SimtDebug& dbg,
+                           cudaStream_t s);
 cudaError_t f32_forward(const F32Args& a, cudaStream_t s);
 cudaError_t f32_backward(const F32Args& a, cudaStream_t s);
 
