@@ -96,7 +96,11 @@ enum {
     LORA_SAVE_XA = 1,          /* forward: write x A_a of fine-tuning rows to xa_save */
     LORA_RECOMPUTE_XA = 2,     /* backward: recompute x A_a even if xa_saved is given */
     LORA_ACCUMULATE_GRAD = 4,  /* backward: add into dA/dB instead of overwriting */
-    LORA_DEBUG_CHECKS = 8      /* reserved: extra host-side checks */
+    LORA_DEBUG_CHECKS = 8      /* bf16 calls: before any launch the host checks every index of the call's plan
+                                  against the buffer it addresses (LORA_ERR_BOUNDS on a violation, nothing
+                                  launched), and every kernel checks each store index it derives from the plan;
+                                  a failing store is skipped and LORA_ERR_BOUNDS recorded in the status word
+                                  (lora_workspace_status).  Slower; a stand-in for a memory checker. */
 };
 
 /* return codes */
@@ -112,7 +116,9 @@ enum {
     LORA_ERR_CUDA = -8,         /* a CUDA runtime call failed (message in lora_last_error) */
     LORA_ERR_RANK = -9,         /* rank outside [1, 128] */
     LORA_ERR_LIMIT = -10,       /* beyond a documented size limit (see below) */
-    LORA_ERR_TIMEOUT = -11      /* reported by lora_workspace_status: a kernel gave up waiting */
+    LORA_ERR_TIMEOUT = -11,     /* reported by lora_workspace_status: a kernel gave up waiting */
+    LORA_ERR_BOUNDS = -12       /* LORA_DEBUG_CHECKS: a plan index outside its buffer (host check, or a kernel
+                                   skipped a store and recorded it in the status word) */
 };
 
 /* Limits: T, K, N < 2^31; sum over segments of len*r fits in int32;
@@ -289,6 +295,12 @@ int lora_set_trace_events(void* const* events);
  * lora_workspace_status() then reports LORA_ERR_TIMEOUT and the CUDA context stays usable.  Needs the first
  * 256 bytes of a 256-byte aligned workspace. */
 int lora_selftest_wait_timeout(void* workspace, size_t ws_bytes, void* stream);
+
+/* Diagnostic (no counterpart on the pages): plans a bf16 forward (backward = 0) or backward (backward != 0, every
+ * output requested, x A recomputed) for this table and runs the host check of LORA_DEBUG_CHECKS on it: LORA_OK, a
+ * validation error, or LORA_ERR_BOUNDS (lora_last_error names the index).  Host only; slices may be NULL. */
+int lora_plan_check(int32_t T, int32_t K, int32_t N, const lora_pool_t* pool, const lora_slices_t* slices,
+                    const lora_segment_t* segs /* HOST */, int32_t n_segs, int32_t backward);
 
 /* Diagnostic: the forward tile plan of a segment table, for host-side tests.
  *   n_tiles_out: number of 128-row tiles.

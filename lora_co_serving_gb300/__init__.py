@@ -25,24 +25,27 @@ from . import _build
 
 __all__ = ["Pool", "forward", "backward", "sliced_forward", "sliced_backward", "sliced_workspace_size",
            "sliced_xa_size", "workspace_size", "xa_size", "workspace_status", "plan_describe",
-           "LoraError", "LibraryNotBuilt", "library", "build", "SAVE_XA", "RECOMPUTE_XA", "ACCUMULATE_GRAD"]
+           "LoraError", "LibraryNotBuilt", "library", "build", "SAVE_XA", "RECOMPUTE_XA", "ACCUMULATE_GRAD",
+           "DEBUG_CHECKS", "plan_check", "static_status"]
 
 SAVE_XA = 1
 RECOMPUTE_XA = 2
 ACCUMULATE_GRAD = 4
+DEBUG_CHECKS = 8
 BF16 = 0
 F32 = 1
 
 ERRORS = {0: "LORA_OK", -1: "LORA_ERR_INVALID_ARG", -2: "LORA_ERR_SEGMENTS", -3: "LORA_ERR_ADAPTER",
           -4: "LORA_ERR_TRAIN_BASE", -5: "LORA_ERR_ALIGNMENT", -6: "LORA_ERR_WORKSPACE", -7: "LORA_ERR_DTYPE",
-          -8: "LORA_ERR_CUDA", -9: "LORA_ERR_RANK", -10: "LORA_ERR_LIMIT", -11: "LORA_ERR_TIMEOUT"}
+          -8: "LORA_ERR_CUDA", -9: "LORA_ERR_RANK", -10: "LORA_ERR_LIMIT", -11: "LORA_ERR_TIMEOUT",
+          -12: "LORA_ERR_BOUNDS"}
 
 EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_mixed_backward", "lora_last_error",
             "lora_workspace_status", "lora_plan_describe", "lora_set_trace_events", "lora_mixed_forward_static",
             "lora_selftest_wait_timeout", "lora_adamw_step", "lora_mixed_backward_flagged",
             "lora_sliced_workspace_size", "lora_sliced_xa_size", "lora_sliced_forward", "lora_sliced_backward",
             "lora_latency_terms", "lora_latency_features", "lora_latency_fit", "lora_latency_predict",
-            "lora_static_status"]
+            "lora_static_status", "lora_plan_check"]
 
 
 class LoraError(RuntimeError):
@@ -107,6 +110,8 @@ def library(path=None):
     lib.lora_set_trace_events.restype = ctypes.c_int
     lib.lora_mixed_forward_static.argtypes = [I32, I32, I32, ctypes.c_int, P, P, P, P, I32, P, P, ctypes.c_uint32, P]
     lib.lora_mixed_forward_static.restype = ctypes.c_int
+    lib.lora_plan_check.argtypes = [I32, I32, I32, P, P, P, I32, I32]
+    lib.lora_plan_check.restype = ctypes.c_int
     lib.lora_static_status.argtypes = [P]
     lib.lora_static_status.restype = ctypes.c_int
     lib.lora_selftest_wait_timeout.argtypes = [P, SZ, P]
@@ -235,8 +240,13 @@ def _workspace(T, K, N, code, pool, s, workspace, device):
     return workspace
 
 
-def forward(x, Wt, pool, segs, y=None, xa_save=None, save_xa=False, workspace=None, stream=None):
-    """y [T, N] = x W + per-segment LoRA; returns y, or (y, xa_save) when save_xa is set."""
+def forward(x, Wt, pool, segs, y=None, xa_save=None, save_xa=False, workspace=None, stream=None, debug=False,
+            check_status=False):
+    """y [T, N] = x W + per-segment LoRA; returns y, or (y, xa_save) when save_xa is set.
+
+    debug: LORA_DEBUG_CHECKS (host plan check, in-kernel bounds checks on every store).  check_status: wait for the
+    call and raise LoraError if a kernel reported a problem in the workspace status word (a bounded wait that gave
+    up, or a debug bounds check)."""
     import torch
     T, K = x.shape
     N = Wt.shape[0]
@@ -248,9 +258,11 @@ def forward(x, Wt, pool, segs, y=None, xa_save=None, save_xa=False, workspace=No
         n = xa_size(code, pool, s) // x.element_size()
         xa_save = torch.empty(max(n, 1), dtype=x.dtype, device=x.device)
     ws = _workspace(T, K, N, code, pool, s, workspace, x.device)
-    flags = SAVE_XA if save_xa else 0
+    flags = (SAVE_XA if save_xa else 0) | (DEBUG_CHECKS if debug else 0)
     _check(library().lora_mixed_forward(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), _ptr(s), s.shape[0], _ptr(y),
                                         _ptr(xa_save), flags, _ptr(ws), ws.numel(), _stream_ptr(stream)))
+    if check_status:
+        workspace_status(ws, stream)
     return (y, xa_save) if save_xa else y
 
 
@@ -279,8 +291,9 @@ def static_status(stream=None):
 
 
 def backward(x, Wt, pool, segs, dY, xa_saved=None, dX=None, dA=None, dB=None, want_dx=True, want_grads=True,
-             recompute=False, accumulate=False, workspace=None, stream=None):
-    """LoRA backward of the fine-tuning segments; returns (dX, dA, dB) (dA/dB float32, pool-shaped)."""
+             recompute=False, accumulate=False, workspace=None, stream=None, debug=False, check_status=False):
+    """LoRA backward of the fine-tuning segments; returns (dX, dA, dB) (dA/dB float32, pool-shaped).
+    debug / check_status: as in forward()."""
     import torch
     T, K = x.shape
     N = Wt.shape[0]
@@ -293,11 +306,13 @@ def backward(x, Wt, pool, segs, dY, xa_saved=None, dX=None, dA=None, dB=None, wa
     if want_grads and dB is None:
         dB = torch.zeros(pool.B.numel(), dtype=torch.float32, device=x.device)
     ws = _workspace(T, K, N, code, pool, s, workspace, x.device)
-    flags = (RECOMPUTE_XA if recompute else 0) | (ACCUMULATE_GRAD if accumulate else 0)
+    flags = (RECOMPUTE_XA if recompute else 0) | (ACCUMULATE_GRAD if accumulate else 0) | (DEBUG_CHECKS if debug else 0)
     _check(library().lora_mixed_backward(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), _ptr(s), s.shape[0],
                                          _ptr(dY), _ptr(xa_saved), _ptr(dX) if want_dx else None,
                                          _ptr(dA) if want_grads else None, _ptr(dB) if want_grads else None, flags,
                                          _ptr(ws), ws.numel(), _stream_ptr(stream)))
+    if check_status:
+        workspace_status(ws, stream)
     return dX, dA, dB
 
 
@@ -337,6 +352,14 @@ def set_trace_events(events):
     assert len(events) == 8
     arr = (ctypes.c_void_p * 8)(*[e.cuda_event for e in events])
     _check(library().lora_set_trace_events(ctypes.cast(arr, ctypes.c_void_p)))
+
+
+def plan_check(T, K, N, pool, segs, backward=False, bounds=None):
+    """Host check of the bf16 plan of this table (LORA_DEBUG_CHECKS' host half); raises LoraError on a violation."""
+    s = segments(segs)
+    sl = None if bounds is None else _slices(bounds)
+    _check(library().lora_plan_check(T, K, N, pool.cptr(), None if sl is None else sl.cptr(), _ptr(s), s.shape[0],
+                                     1 if backward else 0))
 
 
 def plan_describe(T, K, N, pool, segs, cap=None):

@@ -78,6 +78,12 @@ void plan_forward(const Problem& p, Plan* out);
 void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out,
                    bool per_segment = false);
 
+// Host cross-check of a plan (LORA_DEBUG_CHECKS, lora_plan_check): every index the kernels derive from it -- rows
+// of x and of the gathered buffer, pool rows of the adapter-row atoms and their boxes, Z blocks and columns, saved
+// and transposed activation offsets, shrink and split partial slots, output columns, gradient rows -- lies inside
+// the buffer it addresses.  Returns LORA_OK, or LORA_ERR_BOUNDS with the first violation in *err.
+int check_plan(const Problem& p, const Plan& pl, bool backward, std::string* err);
+
 // Greedy list scheduling of the items (in order) onto G persistent CTAs by estimated cost.
 // off has G+1 entries; list holds item indices grouped by CTA, each CTA's in increasing order.
 void assign_items(const std::vector<WorkItem>& items, const Plan& plan, int G, std::vector<int32_t>* off,

@@ -93,6 +93,14 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, vola
         }
     }
 }
+// LORA_DEBUG_CHECKS: a store index derived from the plan is checked against its buffer's extent; a failing check
+// records LORA_ERR_BOUNDS in the status word and the caller skips the store.
+__device__ __forceinline__ bool dbg_ok(int32_t debug, int32_t* status, int64_t idx, int64_t extent) {
+    if (!debug || (idx >= 0 && idx < extent)) return true;
+    atomicCAS(status, 0, LORA_ERR_BOUNDS);
+    return false;
+}
+
 // The first test of the phase is inlined, so a wait that is already satisfied costs no call (a call would also
 // make every load still in flight complete first).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
@@ -356,7 +364,7 @@ struct ShrinkRowOut {
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = (live && d0 >= 0 && j0 + i < zr) ? acc[i] : 0.f;
-        if (u.kind != kShrinkXa) {
+        if (u.kind != kShrinkXa && dbg_ok(P.debug, P.status, td.z_blk0 + (u.n0 + c) / kBK, P.db.z_blocks)) {
             const int zc = u.n0 + c;
             uint8_t* blk = P.zout + (size_t)(td.z_blk0 + zc / kBK) * kZBlockBytes + row * 128;
 #pragma unroll
@@ -371,12 +379,13 @@ struct ShrinkRowOut {
             }
         }
         if (d0 < 0) return;
-        if (save_off >= 0) {
+        if (save_off >= 0 && dbg_ok(P.debug, P.status, (int64_t)save_off + p0 + min(16, zr - j0) - 1, P.db.xa_elems)) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 if (j0 + i < zr) P.xa_save[save_off + p0 + i] = __float2bfloat16_rn(v[i]);
         }
-        if (tdst) {
+        if (tdst && dbg_ok(P.debug, P.status,
+                           (int64_t)(p0 + min(16, zr - j0) - 1) * P.t_ld + td.tpos0 + row, P.db.t_elems)) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 if (j0 + i < zr) tdst[(size_t)(p0 + i) * P.t_ld + td.tpos0 + row] = __float2bfloat16_rn(v[i]);
@@ -411,7 +420,8 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 uint32_t a[16];
                 tmem_ld16(taddr + c, a);
                 tmem_ld_wait();
-                if (m < ld) {
+                const int64_t last = ((int64_t)(is_b ? g.prow_b : g.prow_a) + jbase + min(c + 16, jend - jbase) - 1) * ld + m;
+                if (m < ld && dbg_ok(P.debug, P.status, last, is_b ? P.db.grad_b : P.db.grad_a)) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int j = c + i;
@@ -443,7 +453,9 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 // of 4 floats (P.part + C * 128 + row * 4), so that a row's 4 columns are one 16-byte access and a
                 // warp's 32 rows one 512-byte run
                 float* dst = P.part + (size_t)w.part * kTileM + row * 4;
-                for (int c = 0; c < w.mma_n; c += 16) {
+                const bool part_ok = dbg_ok(P.debug, P.status, ((int64_t)u.part0 + (int64_t)u.nsplit * u.mma_n) * kTileM - 1,
+                                            P.db.part_floats);
+                for (int c = 0; c < w.mma_n && part_ok; c += 16) {
                     uint32_t a[16];
                     tmem_ld16(taddr + c, a);
                     tmem_ld_wait();
@@ -463,7 +475,7 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 int32_t* cnt = P.counters + w.n_ext * 4 + quarter;
                 if (lane == 0) last = (atomicAdd(cnt, 1) == u.nsplit - 1) ? 1 : 0;
                 last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
+                if (last && part_ok) {
                     __threadfence();
                     ShrinkRowOut out(P, u, row);
                     // the splits' 16-column groups are loaded four splits at a time (16 loads of 16 bytes in
@@ -864,7 +876,14 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
                                 row * 4
                           : nullptr;
         const int32_t t0 = __shfl_sync(0xffffffffu, t, 0);
-        const bool bulk = LORA_TMA_STORE && part == nullptr && __all_sync(0xffffffffu, t >= 0 && t == t0 + lane);
+        bool bulk = LORA_TMA_STORE && part == nullptr && __all_sync(0xffffffffu, t >= 0 && t == t0 + lane);
+        if (P.debug) {
+            // the split slot, the row of this lane and the bulk store's 32 rows must lie in their buffers
+            if (part && !dbg_ok(1, P.status, (int64_t)w.part + w.split, P.db.main_slots)) part = nullptr;
+            if (bulk && !dbg_ok(1, P.status, (int64_t)t0 + 31, P.db.out_rows)) bulk = false;
+        }
+        const bool row_ok = t >= 0 && dbg_ok(P.debug, P.status, t, P.db.out_rows);
+        const bool skip_split = (w.nsplit > 1 && part == nullptr);
         for (int c = 0; c < kBN; c += 32) {
             float v[32];
             ld32_cols(taddr + c, v);
@@ -886,7 +905,7 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
                 ++nstore;
                 continue;
             }
-            if (t < 0) continue;
+            if (!row_ok || skip_split) continue;
             if (part) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 4)
@@ -968,7 +987,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) main_reduce_kernel(const SplitTile* __restrict__ splits,
                                                           const int32_t* __restrict__ rowmap,
                                                           const float* __restrict__ part, __nv_bfloat16* out,
-                                                          int32_t out_ld, int32_t out_cols) {
+                                                          int32_t out_ld, int32_t out_cols, int32_t debug,
+                                                          int32_t* status, int64_t out_rows, int64_t main_slots) {
     grid_dep_wait();
     const int b = blockIdx.x;
     const SplitTile st = splits[b / 32];
@@ -979,6 +999,8 @@ __global__ void __launch_bounds__(256) main_reduce_kernel(const SplitTile* __res
     const int32_t t = rowmap[(st.tile + half) * kTileM + r];
     const int32_t col = st.n0 + c0;
     if (t < 0 || col + 8 > out_cols) return;
+    if (!dbg_ok(debug, status, t, out_rows) || !dbg_ok(debug, status, (int64_t)st.part + st.nsplit - 1, main_slots))
+        return;
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     // a row's 8 columns are two 16-byte groups; four splits' groups are loaded before they are added in order
     const float* p = part + ((size_t)st.part * 2 + half) * kMainPartialFloats + (size_t)c0 * kTileM + r * 4;
@@ -1062,10 +1084,11 @@ cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream) {
 }
 
 cudaError_t main_reduce_launch(const SplitTile* splits, int32_t n_splits, const int32_t* rowmap, const float* part,
-                               __nv_bfloat16* out, int32_t out_ld, int32_t out_cols, cudaStream_t stream) {
+                               __nv_bfloat16* out, int32_t out_ld, int32_t out_cols, const KParams& P,
+                               cudaStream_t stream) {
     if (n_splits <= 0) return cudaSuccess;
     return launch_pdl(main_reduce_kernel, dim3(n_splits * 32), dim3(256), 0, stream, splits, rowmap, part, out, out_ld,
-                      out_cols);
+                      out_cols, P.debug, P.status, P.db.out_rows, P.db.main_slots);
 }
 
 cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream) {

@@ -67,6 +67,8 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     int32_t K, N;
     int32_t accumulate;
     int32_t w3;              // backward: tm_w3 is valid
+    int32_t debug;           // LORA_DEBUG_CHECKS: check every store index against `db` (see common.h)
+    DebugBounds db;
 };
 
 size_t tc_smem_bytes();
@@ -74,7 +76,8 @@ cudaError_t tc_launch(const KParams& P, int grid, cudaStream_t stream);      // 
 size_t tc2_smem_bytes();
 // Sums the partials of the split output tiles (device array of n_splits records) and writes their output rows.
 cudaError_t main_reduce_launch(const SplitTile* splits, int32_t n_splits, const int32_t* rowmap, const float* part,
-                               __nv_bfloat16* out, int32_t out_ld, int32_t out_cols, cudaStream_t stream);
+                               __nv_bfloat16* out, int32_t out_ld, int32_t out_cols, const KParams& P,
+                               cudaStream_t stream);
 cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream);    // main items, clusters of 2 CTAs
 cudaError_t selftest_timeout_launch(int32_t* status, cudaStream_t stream);
 

@@ -1,0 +1,131 @@
+"""The host half of LORA_DEBUG_CHECKS (CPU only).
+
+lora_plan_check plans a table and checks every index the kernels derive from the plan against the buffer it
+addresses.  These tests run it on the workloads' full-size tables and on many seeded random tables (decode,
+prefill and fine-tuning segments, ranks 1..128, ragged K and N, sliced layers), forward and backward; and they
+plant a mistake in a copy of the planner, built on its own with the host compiler, and check that the checker
+reports it.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import lora_co_serving_gb300 as lm
+import workloads
+
+CSRC = os.path.join(os.path.dirname(lm.__file__), "csrc")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(lm.__file__)), "include")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lm.build()
+    lm.library()
+
+
+def _pool(wl):
+    return lm.Pool(None, None, wl.a_off, wl.b_off, wl.rank, wl.scale)
+
+
+def _check(wl, bounds=None):
+    for bwd in (False, True):
+        lm.plan_check(wl.T, wl.K, wl.N, _pool(wl), wl.segs, backward=bwd, bounds=bounds)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_full_size_tables(cfg):
+    kw = {"K": 512, "N": 1024} if cfg in (3, 4, 5) else {}
+    _check(workloads.config(cfg, **kw))
+
+
+def _random_table(rng):
+    n_ad = int(rng.integers(1, 40))
+    rank = [int(rng.integers(1, 129)) for _ in range(n_ad)]
+    segs, t, n_train = [], 0, 0
+    for _ in range(int(rng.integers(1, 60))):
+        kind = rng.integers(0, 3)
+        if kind == 0:
+            ln, tr = 1, 0
+        elif kind == 1:
+            ln, tr = int(rng.integers(2, 700)), 0
+        else:
+            ln, tr = int(rng.integers(1, 600)), 1
+        if tr and n_train >= 40:
+            tr = 0
+        a = int(rng.integers(0 if tr else -1, n_ad))
+        segs.append((t, ln, a, tr))
+        n_train += tr
+        t += ln
+    order = rng.permutation(len(segs))
+    return [segs[i] for i in order], t, rank
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_tables(seed):
+    rng = np.random.default_rng(seed)
+    segs, T, rank = _random_table(rng)
+    K = int(rng.choice([8, 64, 136, 520, 1024]))
+    N = int(rng.choice([8, 72, 256, 776, 2048]))
+    _check(workloads.custom(seed, T, K, N, segs, rank, want_dy=False))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_sliced_tables(seed):
+    rng = np.random.default_rng(100 + seed)
+    segs, T, rank = _random_table(rng)
+    S = int(rng.integers(2, 5))
+    widths = [256 * int(rng.integers(1, 4)) for _ in range(S - 1)] + [int(rng.choice([8, 136, 256]))]
+    bounds = np.concatenate([[0], np.cumsum(widths)]).astype(np.int32)
+    wl = workloads.sliced(seed, T, int(rng.choice([64, 520])), bounds, segs, rank, want_dy=False)
+    _check(wl, bounds=bounds)
+
+
+# A driver for a planner built on its own with g++: validate, plan, check (the same calls lora_plan_check makes).
+DRIVER = r'''
+#include <string>
+#include "plan.h"
+namespace lora { void set_last_error(const char*) {} }
+extern "C" int check_table(int T, int K, int N, const lora_pool_t* pool, const lora_segment_t* segs, int n,
+                           int backward) {
+    lora::Problem p;
+    std::string err;
+    int rc = lora::validate(T, K, N, LORA_BF16, pool, segs, n, &p, &err);
+    if (rc) return rc;
+    lora::Plan pl;
+    if (backward) lora::plan_backward(p, true, true, true, true, &pl);
+    else lora::plan_forward(p, &pl);
+    return lora::check_plan(p, pl, backward != 0, &err);
+}
+'''
+
+# (name, original text in plan.cpp, planted mistake)
+PLANTED = [
+    ("atom_row_past_block", "pl->atoms_a.push_back(ch.prow_a + sl * ch.r + std::min(o, last));",
+     "pl->atoms_a.push_back(ch.prow_a + sl * ch.r + o + 8);"),
+    ("split_slot_reused", "pl->main_slots += nsplit;", "pl->main_slots += nsplit - 1;"),
+]
+
+
+@pytest.mark.parametrize("name,orig,bad", PLANTED, ids=[p[0] for p in PLANTED])
+def test_planted_planner_mistake_is_reported(tmp_path, name, orig, bad):
+    src = open(os.path.join(CSRC, "plan.cpp")).read()
+    assert src.count(orig) == 1, "anchor not unique: " + orig
+    (tmp_path / "plan.cpp").write_text(src.replace(orig, bad))
+    (tmp_path / "driver.cpp").write_text(DRIVER)
+    so = str(tmp_path / "libplan.so")
+    cxx = os.environ.get("CXX", "g++")
+    res = subprocess.run([cxx, "-O1", "-std=c++17", "-shared", "-fPIC", "-I", CSRC, "-I", INCLUDE,
+                          str(tmp_path / "plan.cpp"), str(tmp_path / "driver.cpp"), "-o", so],
+                         capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    lib = ctypes.CDLL(so)
+    lib.check_table.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+    # decode rows (atoms of several adapters) and a small split main pass
+    wl = workloads.config2(T=256, K=256, N=512, n_adapters=20)
+    pool = _pool(wl)
+    segs = lm.segments(wl.segs)
+    rc = lib.check_table(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0], 0)
+    assert rc == -12, "planted mistake %s not reported (rc %d)" % (name, rc)
