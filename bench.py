@@ -246,6 +246,74 @@ class ClockSampler:
                 "power_w_max": max([float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()] or [0])}
 
 
+class NvmlSampler:
+    """Clock, power and clock-event samples every ~2 ms from the driver's NVML library (read-only queries), so that
+    a timed region of tens of milliseconds still gets tens of samples; falls back to nvidia-smi when NVML is
+    unavailable."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.samples = []
+        self.fallback = None
+        self.thread = None
+        self.stop_flag = False
+        try:
+            import ctypes
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(self.h)) != 0:
+                raise OSError("no NVML handle")
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))        # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+            self.reasons_fn = None
+            for name in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
+                try:
+                    self.reasons_fn = getattr(self.nv, name)
+                    break
+                except AttributeError:
+                    pass
+        except (OSError, AttributeError):
+            self.nv = None
+            self.fallback = ClockSampler(gpu_index)
+
+    def _poll(self):
+        import ctypes
+        mhz, reasons, mw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        while not self.stop_flag:
+            t = time.time()
+            ok = self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0
+            if self.reasons_fn is not None:
+                self.reasons_fn(self.h, ctypes.byref(reasons))
+            self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw))
+            if ok:
+                self.samples.append((t, float(mhz.value), int(reasons.value), mw.value / 1e3))
+            time.sleep(0.002)
+
+    def start(self):
+        if self.fallback is not None:
+            return self.fallback.start()
+        import threading
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+        time.sleep(0.01)
+
+    def stop(self, t0=None, t1=None):
+        if self.fallback is not None:
+            return self.fallback.stop(t0, t1)
+        self.stop_flag = True
+        self.thread.join()
+        rows = [r for r in self.samples if t0 is None or t0 <= r[0] <= t1]
+        reasons = sorted(set(name for r in rows for bit, name in self.REASONS.items() if r[2] & bit))
+        return {"sm_mhz": statistics.median(r[1] for r in rows) if rows else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(rows), "source": "NVML, every ~2 ms",
+                "power_w_max": max((r[3] for r in rows), default=0.0)}
+
+
 # ----------------------------------------------------------------------------------------------- CPU oracle sample
 def oracle_threads():
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
@@ -509,7 +577,7 @@ def measure(args, cfg, rank, world, dist, steps, warmup, extras=True):
         for e in row:
             e.record(stream)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(torch.cuda.current_device())
+    sampler = NvmlSampler(torch.cuda.current_device())
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -848,7 +916,7 @@ def measure_layer(args, rank, world, dist, steps, warmup, extras=True):
     for row in tev:
         for e in row:
             e.record(stream)
-    sampler = ClockSampler(torch.cuda.current_device())
+    sampler = NvmlSampler(torch.cuda.current_device())
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -1005,7 +1073,7 @@ def run_sweep(args):
             ts.append(e0.elapsed_time(e1))
         return statistics.median(ts)
 
-    sampler = ClockSampler(torch.cuda.current_device())
+    sampler = NvmlSampler(torch.cuda.current_device())
     sampler.start()
     wall0 = time.time()
     res = {}

@@ -79,12 +79,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `ns` nanoseconds while the phase is incomplete (it
+// resumes as soon as the phase completes): for waits that are usually long, so that the waiting warp does not take
+// issue slots from the warps it shares a scheduler with
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting (this wait timed out, or
-// another role's did).
-__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
+// another role's did).  suspend_ns > 0: hinted try_wait (see mbar_try_wait_hint).
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
+                                             uint32_t suspend_ns = 0) {
     const uint64_t t0 = global_timer();
     for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (suspend_ns ? mbar_try_wait_hint(bar, parity, suspend_ns) : mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if ((spin & 31u) == 0 && global_timer() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -106,6 +122,13 @@ __device__ __forceinline__ bool dbg_ok(int32_t debug, int32_t* status, int64_t i
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
     if (mbar_try_wait(bar, parity)) return true;
     return wait_phase_slow(bar, parity, abort_flag, status);
+}
+// The epilogue's wait for a finished accumulator (one per item: usually long)
+constexpr uint32_t kLongWaitNs = 20000;
+__device__ __forceinline__ bool wait_phase_long(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                int32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_phase_slow(bar, parity, abort_flag, status, kLongWaitNs);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
@@ -403,7 +426,7 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
     for (int ii = i0; ii < i1; ++ii) {
         const WorkItem w = P.items[P.cta_list[ii]];
         if (skipped_item(P, w)) continue;
-        if (!wait_phase(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) return;
+        if (!wait_phase_long(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) return;
         tc_fence_after();
         const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);
         if (w.kind == kGradDb || w.kind == kGradDa) {
@@ -694,6 +717,11 @@ struct Ring2 {
     __device__ __forceinline__ void next() {
         if (++stage == kStages2) { stage = 0; phase ^= 1u; }
     }
+    __device__ __forceinline__ void advance(int n) {     // n x next()
+        const int s = stage + n;
+        phase ^= (uint32_t)((s / kStages2) & 1);
+        stage = s % kStages2;
+    }
 };
 
 // Lane 0 waits for this CTA's ring slot; the leader also arms its "full" barrier with the bytes of both CTAs.
@@ -720,21 +748,31 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
         const bool fwd = (w.kind == kMainFwd);
         const CUtensorMap* ma = fwd ? (td.a_src ? &P.tm_xg : &P.tm_x) : &P.tm_dy;
         const int32_t nb = w.n0 + kHalfN * (int32_t)rank;     // first B column of this CTA's half
-        for (int kb = w.kb0; kb < w.kb0 + w.nk; ++kb) {
-            if (!acquire_stage2(ring, bar_full, bar_empty, kStage2Bytes, leader, lane, abort_flag, P.status)) return;
-            const uint32_t full = full_leader + ring.stage * 8;
-            const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
-            if (lane == 0) tma_load_hinted<LORA_HINT_ROWS>(sa, ma, kb * kBK, td.a_row0, full);
-            if (fwd) {
-                if (lane == 1) tma_load_hinted<LORA_HINT_W>(sb, &P.tm_w, kb * kBK, nb, full);     // Wt rows, K-major
-            } else if (P.w3) {
-                if (lane == 1) tma_load_3d_pair(sb, &P.tm_w3, 0, kb * kBK, nb / 64, full);        // both MN atoms
-            } else if (lane == 1 || lane == 2) {
-                const int m = lane - 1;
-                tma_load_hinted<LORA_HINT_W>(sb + m * 8192, &P.tm_w, nb + 64 * m, kb * kBK, full);  // Wt, MN-major
+        // dense k-blocks: lane 0 alone waits for each free stage, arms the barrier and issues the stage's loads
+        // (a freed stage is refilled with no warp-wide exchange on the way: the refill latency is what bounds the
+        // pass); the other lanes only keep the ring position
+        int ok = 1;
+        if (lane == 0) {
+            for (int kb = w.kb0; kb < w.kb0 + w.nk; ++kb) {
+                if (!wait_phase(bar_empty + ring.stage * 8, ring.phase ^ 1u, abort_flag, P.status)) { ok = 0; break; }
+                if (leader) mbar_expect_tx(bar_full + ring.stage * 8, 2 * kStage2Bytes);
+                const uint32_t full = full_leader + ring.stage * 8;
+                const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
+                tma_load_hinted<LORA_HINT_ROWS>(sa, ma, kb * kBK, td.a_row0, full);
+                if (fwd) {
+                    tma_load_hinted<LORA_HINT_W>(sb, &P.tm_w, kb * kBK, nb, full);                // Wt rows, K-major
+                } else if (P.w3) {
+                    tma_load_3d_pair(sb, &P.tm_w3, 0, kb * kBK, nb / 64, full);                   // both MN atoms
+                } else {
+                    tma_load_hinted<LORA_HINT_W>(sb, &P.tm_w, nb, kb * kBK, full);                // Wt, MN-major
+                    tma_load_hinted<LORA_HINT_W>(sb + 8192, &P.tm_w, nb + 64, kb * kBK, full);
+                }
+                ring.next();
             }
-            ring.next();
+        } else {
+            ring.advance(w.nk);
         }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
         // LoRA k-blocks: this tile's Z block and, per 8-row atom of stacked adapter rows, two 64-column MN boxes;
         // only the atoms of the item's LoRA columns [ext_c0, ext_c1)
         // (lane L < 16 loads half L & 1 of the box that starts at 8-row atom L >> 1, if one does: a run of atoms with
@@ -864,7 +902,7 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
     uint32_t nstore = 0;      // TMA stores issued by this warp (their buffers alternate)
     for (int ii = i0; ii < i1; ++ii) {
         const WorkItem w = P.items[P.cta_list[ii]];
-        if (!wait_phase(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) break;
+        if (!wait_phase_long(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) break;
         tc_fence_after();
         const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);
         const int32_t t = P.rowmap[(w.tile + rank) * kTileM + row];
