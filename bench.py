@@ -998,7 +998,8 @@ def sweep_tables(L, seed=77):
             left -= ln
         return np.asarray(segs, np.int32), t
 
-    decode = [table(b, 0, 0) for b in (16, 32, 64, 128, 256, 512, 768, 1024, 1536, 2048)]
+    decode = [table(b, 0, 0) for b in (1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 80, 96, 128, 160, 192, 256, 320, 384,
+                                       448, 512, 640, 768, 896, 1024, 1152, 1280, 1408, 1536, 1792, 2048)]
     mixed = []
     for b_d in (0, 256, 1024, 2048):
         for t_in in (0, 1024, 2048, 4096):
@@ -1039,7 +1040,7 @@ def run_sweep(args):
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def step(segs, T):
+    def step(segs, T, stream=stream):
         train = bool((segs[:, 3] != 0).any())
         for n in LAYER_ORDER:
             d = dev[n]
@@ -1059,19 +1060,42 @@ def run_sweep(args):
 
     reps = max(3, min(args.steps, 10))
 
+    gs = torch.cuda.Stream()
+
     def time_point(segs, T):
+        """Median device time of the step replayed from a CUDA graph (as an engine replays its steps: no host work
+        in the timed region), and the median of the same step launched eagerly."""
         for _ in range(max(3, args.warmup)):
             step(segs, T)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ts = []
+        eager = []
         for _ in range(reps):
             torch.cuda.synchronize()
             e0.record(stream)
             step(segs, T)
             e1.record(stream)
             torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+            eager.append(e0.elapsed_time(e1))
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            step(segs, T, gs)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            step(segs, T, gs)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        with torch.cuda.stream(gs):
+            for _ in range(reps):
+                e0.record(gs)
+                g.replay()
+                e1.record(gs)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+        del g
+        return statistics.median(ts), statistics.median(eager)
 
     sampler = NvmlSampler(torch.cuda.current_device())
     sampler.start()
@@ -1079,7 +1103,9 @@ def run_sweep(args):
     res = {}
     for name, pts, model in (("decode", decode, lm.EQ_II), ("mixed", mixed, lm.EQ_I)):
         F = np.array([lm.latency_features(model, segs) for segs, _ in pts])
-        t = np.array([time_point(segs, T) for segs, T in pts])
+        both = [time_point(segs, T) for segs, T in pts]
+        t = np.array([b[0] for b in both])
+        t_eager = np.array([b[1] for b in both])
         coef = lm.latency_fit(model, F, t)
         pred = F @ coef
         rel = np.abs(pred - t) / t
@@ -1096,12 +1122,15 @@ def run_sweep(args):
                      "coefficients_ms": dict(zip(names, coef.tolist())), "r2": r2,
                      "median_rel_err": float(np.median(rel)), "max_rel_err": float(rel.max()),
                      "cv_median_rel_err": float(np.median(cv)), "cv_max_rel_err": float(cv.max()),
-                     "samples": [{"features": f.tolist(), "ms": float(x)} for f, x in zip(F, t)]}
+                     "samples": [{"features": f.tolist(), "ms": float(x), "eager_ms": float(xe)}
+                                 for f, x, xe in zip(F, t, t_eager)]}
     wall1 = time.time()
     clocks = sampler.stop(wall0, wall1)
     line = {"metric": "step-latency model fit (DeltaServe Eq. I / II) over the layer step", "unit": "ms",
             "n_gpus": 1, "data": "synthetic (seeded; shapes of the pages' workloads)",
             "config": {"workload": layer_name(L) + "_sweep", "reps_per_point": reps,
+                       "timing": "each point's step replayed from a CUDA graph (device time, no host work); the "
+                                 "eager median is kept per sample as eager_ms",
                        "step": "forward of q|k|v, o, gate|up, down over every token + LoRA backward of the "
                                "fine-tuning tokens (xA recomputed)",
                        "features": "Eq. I {sum (n_i+B_d)^2, T_in+B_d, T_ft, K=0, 1}; Eq. II {B_d, K=0, 1}"},

@@ -157,7 +157,7 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
     // pool row of every 8-column atom; the padding of a chunk to 16 repeats its last atom, so every loaded row
     // stays inside the adapter's own block (sliced: the slice's own rows or the next slice's)
     const int32_t atom0 = int32_t(pl->atoms_a.size());
-    std::vector<uint8_t> brk;        // per atom: starts a chunk's (or a slice's, or a region padding's) columns
+    std::vector<uint8_t> brk;        // per atom: starts a region padding's columns (no box runs into padding)
     const int32_t n_reg = (S > 1 && !side_by_side) ? S : 1;
     const int32_t W = (n_reg > 1) ? int32_t(cdiv(zcol, kBK) * kBK) : zcol;
     for (int32_t reg = 0; reg < n_reg; ++reg) {
@@ -170,7 +170,7 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
                 for (int32_t o = 0; o < pad16(ch.r); o += 8) {
                     pl->atoms_a.push_back(ch.prow_a + sl * ch.r + std::min(o, last));
                     pl->atoms_b.push_back(ch.prow_b + std::min(o, last));
-                    brk.push_back(o == 0 ? 1 : 0);
+                    brk.push_back(0);
                 }
             }
         }
@@ -180,8 +180,10 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
             brk.push_back(1);
         }
     }
-    // TMA boxes: runs of atoms whose pool rows follow one another, cut at chunk starts and at 64-column blocks
-    // (relative to the tile's first LoRA column), split greedily into 8-, 4-, 2- and 1-atom boxes
+    // TMA boxes: runs of atoms whose pool rows follow one another (across chunks too: adapters that are neighbours
+    // in the pool, in the chunks' id order), cut at 64-column blocks (relative to the tile's first LoRA column) and
+    // at region padding, split greedily into 8-, 4-, 2- and 1-atom boxes.  A loader takes a box whole only when it
+    // lies inside the columns it loads, so boxes may straddle the LoRA splits of an item.
     auto boxes_of = [&](const std::vector<int32_t>& rows, std::vector<int32_t>* out) {
         const size_t n = brk.size();
         for (size_t i = 0; i < n;) {
@@ -288,12 +290,23 @@ static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk, siz
             if (nsb_tail > 1) tail_from = tiles_out - rem;
         }
     }
-    int64_t o = 0;                   // output tiles emitted so far
-    std::vector<int32_t> cuts;       // LoRA split bounds (Z columns) of the current pair
+    // the order of the output tiles (pair q, column tile nt): bands of kBandTiles tile rows sweeping every column
+    // tile before the next band (column bands, alternating sweep directions and bands of 8 or 32 tile rows measured
+    // alike)
+    std::vector<std::pair<size_t, int32_t>> order;
+    order.reserve(n_pairs * (size_t)n_nt);
     for (size_t b0 = 0; b0 < n_pairs; b0 += band) {
         const size_t b1 = std::min(n_pairs, b0 + band);
         for (int32_t nt = 0; nt < n_nt; ++nt)
-            for (size_t q = b0; q < b1; ++q, ++o) {
+            for (size_t q = b0; q < b1; ++q) order.push_back({q, nt});
+    }
+    int64_t o = 0;                   // output tiles emitted so far
+    std::vector<int32_t> cuts;       // LoRA split bounds (Z columns) of the current pair
+    for (const auto& qn : order) {
+        {
+            const size_t q = qn.first;
+            const int32_t nt = qn.second;
+            {
                 const int32_t tile = tile_of(q, nt);
                 const TileDesc& td = pl->tiles[tile];
                 const bool split = split_all || o >= tail_from;
@@ -337,7 +350,9 @@ static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk, siz
                     pl->splits.push_back(SplitTile{tile, nt * kBN, slot0, nsplit, 0, 0, 0, 0});
                     pl->main_slots += nsplit;
                 }
+                ++o;
             }
+        }
     }
 }
 

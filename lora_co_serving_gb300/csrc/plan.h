@@ -20,6 +20,7 @@ constexpr int kShortSegment = 16;
 #endif
 constexpr int kBandTiles = LORA_BAND_TILES;
 
+
 struct Problem {
     int32_t T = 0, K = 0, N = 0;
     lora_dtype_t dt = LORA_BF16;

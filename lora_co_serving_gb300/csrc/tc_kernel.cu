@@ -748,6 +748,20 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
         const bool fwd = (w.kind == kMainFwd);
         const CUtensorMap* ma = fwd ? (td.a_src ? &P.tm_xg : &P.tm_x) : &P.tm_dy;
         const int32_t nb = w.n0 + kHalfN * (int32_t)rank;     // first B column of this CTA's half
+        // LoRA k-blocks' stacked adapter rows: per 8-row atom its pool row and the size of the TMA box that starts
+        // there (lane L < 16: atom L >> 1 of block e, half L & 1)
+        const CUtensorMap* mp = fwd ? &P.tm_pb : &P.tm_pa;
+        const CUtensorMap* mph = fwd ? P.tm_pb_h : P.tm_pa_h;
+        const int32_t* atoms = (fwd ? P.atoms_b : P.atoms_a) + td.atom0;
+        const int32_t* boxes = (fwd ? P.boxes_b : P.boxes_a) + td.atom0;
+        const int n_atoms = td.ext_k / 8;
+        const int e0 = w.ext_c0 / kBK;
+        auto atom_at = [&](int e, int32_t* box) -> int32_t {
+            const int i = e * 8 + (lane >> 1);
+            const bool in = lane < 16 && i < n_atoms;
+            *box = in ? boxes[i] : 0;
+            return in ? atoms[i] : 0;
+        };
         // dense k-blocks: lane 0 alone waits for each free stage, arms the barrier and issues the stage's loads
         // (a freed stage is refilled with no warp-wide exchange on the way: the refill latency is what bounds the
         // pass); the other lanes only keep the ring position
@@ -778,18 +792,6 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
         // (lane L < 16 loads half L & 1 of the box that starts at 8-row atom L >> 1, if one does: a run of atoms with
         // consecutive pool rows inside one chunk comes as one box of 16, 32 or 64 rows; the atom's pool row and box
         // size are read one block ahead)
-        const CUtensorMap* mp = fwd ? &P.tm_pb : &P.tm_pa;
-        const CUtensorMap* mph = fwd ? P.tm_pb_h : P.tm_pa_h;
-        const int32_t* atoms = (fwd ? P.atoms_b : P.atoms_a) + td.atom0;
-        const int32_t* boxes = (fwd ? P.boxes_b : P.boxes_a) + td.atom0;
-        const int n_atoms = td.ext_k / 8;
-        const int e0 = w.ext_c0 / kBK;
-        auto atom_at = [&](int e, int32_t* box) -> int32_t {
-            const int i = e * 8 + (lane >> 1);
-            const bool in = lane < 16 && i < n_atoms;
-            *box = in ? boxes[i] : 0;
-            return in ? atoms[i] : 0;
-        };
         int32_t cur_box = 0, nxt_box = 0;
         int32_t cur = (w.n_ext > 0) ? atom_at(e0, &cur_box) : 0;
         for (int e = e0; e < e0 + w.n_ext; ++e) {
@@ -802,9 +804,16 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
             const uint32_t full = full_leader + ring.stage * 8;
             const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
             if (lane == 0) tma_load_2d_pair(sa, &P.tm_z, 0, (td.z_blk0 + e) * kTileM, full);
+            // a box that starts and ends inside the item's atoms [q0, q1) is loaded whole; every other atom of the
+            // range comes on its own (a run of consecutive pool rows may straddle the item's first or last atom)
             const int q = lane >> 1, m = lane & 1;
-            if (lane < 16 && q >= q0 && q < q1 && cur_box > 0) {
-                const CUtensorMap* map = (cur_box == 1) ? mp : mph + (cur_box == 2 ? 0 : (cur_box == 4 ? 1 : 2));
+            const bool in = lane < 16 && q >= q0 && q < q1;
+            const int box = in ? cur_box : 0;
+            const bool lead = box > 1 && q + box <= q1;
+            const uint32_t covered = __reduce_or_sync(0xffffffffu, (lead && m == 0) ? (((1u << box) - 1u) << q) : 0u);
+            const int n_load = !in ? 0 : (lead ? box : (((covered >> q) & 1u) ? 0 : 1));
+            if (n_load > 0) {
+                const CUtensorMap* map = (n_load == 1) ? mp : mph + (n_load == 2 ? 0 : (n_load == 4 ? 1 : 2));
                 tma_load_2d_pair(sb + m * 8192 + q * 1024, map, nb + 64 * m, cur, full);
             }
             ring.next();
