@@ -38,10 +38,12 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=5, choices=[2, 3, 4, 5])
-    ap.add_argument("--workload", choices=["config", "layer", "sweep"], default="config",
+    ap.add_argument("--workload", choices=["config", "layer", "sweep", "gemm"], default="config",
                     help="layer: the LoRA projections of one Llama-3-8B decoder layer (q|k|v, o, gate|up, down) "
                          "on a co-serving batch, chained on one stream; sweep: that layer step over a grid of batch "
-                         "compositions, with the step-latency model (Eq. I / II) fitted to the timings")
+                         "compositions, with the step-latency model (Eq. I / II) fitted to the timings; gemm: the "
+                         "main pass alone (one base-only segment) beside cuBLAS (torch.matmul) on the shape "
+                         "--set M=.. --set K=.. --set N=.. (default 4096 x 4096 x 4864)")
     ap.add_argument("--out", default=None, help="sweep: also write the fitted coefficients to this JSON file")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -105,7 +107,7 @@ def accounting(wl):
 def launches_per_step(wl, fwd_info=None):
     """Kernel launches of one step.  fwd_info: the forward tile plan (info rows of lora_plan_describe: gathered,
     adapters, LoRA columns, x row).  Gathered decode tiles of up to 1024 rows are shrunk on CUDA cores (one launch,
-    which also gathers the rows) and leave the tensor-core shrink; a main pass with fewer output tiles than kMainTargetItems (114) is split and
+    which also gathers the rows) and leave the tensor-core shrink; a main pass with fewer output tiles than kMainTargetItems (96) is split and
     adds a reduce launch."""
     segs = wl.segs.tolist()
     n_nt = lambda cols: -(-cols // 256)
@@ -118,13 +120,13 @@ def launches_per_step(wl, fwd_info=None):
         tc_shrink = [(g, ext) for g, _, ext, _ in info.tolist() if ext > 0 and not (g and bgmv)]
         n += 1 if tc_shrink else 0                                                          # tensor-core shrink
         n += 1                                                                              # main pass
-        if 0 < (len(info) // 2) * n_nt(wl.N) < 114:
+        if 0 < (len(info) // 2) * n_nt(wl.N) < 96:
             n += 1                                                                          # split reduce
     if wl.backward and any(tr for *_, tr in segs):
         n += 3                                                                              # shrink, dX, dA/dB
         pairs = sum(-(-ln // 256) for _, ln, _, tr in segs if tr and ln > 0)
         tiles, nk = pairs * n_nt(wl.K), -(-wl.N // 64)
-        if (tiles < 114 and nk // 4 >= 2) or (tiles >= 114 and 0 < tiles % 76 <= 38 and nk // 4 >= 2):
+        if (tiles < 96 and nk // 4 >= 2) or (tiles >= 96 and 0 < tiles % 76 <= 38 and nk // 4 >= 2):
             n += 1                                                                          # split reduce
     return n
 
@@ -1144,6 +1146,67 @@ def run_sweep(args):
     return 0
 
 
+def run_gemm(args):
+    """Calibration: the layer's main pass on a base-only batch (x W alone, no adapters) and cuBLAS's GEMM for the
+    same product, each captured into a CUDA graph and replayed (median of `--steps` replays after `--warmup`); L2 is
+    flushed before every replay when the operands fit in twice its size."""
+    import torch
+    import lora_co_serving_gb300 as lm
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    lm.build()
+    kw = {"M": 4096, "K": 4096, "N": 4864, "flush": 1}
+    for item in args.set:
+        k, v = item.split("=", 1)
+        kw[k] = int(v)
+    M, K, N = kw["M"], kw["K"], kw["N"]
+    g = torch.Generator(device="cuda").manual_seed(1007)
+    x = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    Wt = (torch.randn(N, K, device="cuda", generator=g) / K ** 0.5).to(torch.bfloat16)
+    y = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    A = torch.zeros(16 * K, device="cuda", dtype=torch.bfloat16)
+    B = torch.zeros(16 * N, device="cuda", dtype=torch.bfloat16)
+    pool = lm.Pool(A, B, [0], [0], [16], [2.0])
+    segs = lm.segments([(0, M, -1, 0)])
+    ws = torch.empty(lm.workspace_size(M, K, N, 0, pool, segs), dtype=torch.uint8, device="cuda")
+    # --set flush=0 keeps operands that fit in L2 resident between replays (the kernel's own rate, no DRAM)
+    flush = torch.empty(2 * L2_NOMINAL, dtype=torch.uint8, device="cuda") \
+        if kw.get("flush", 1) and 2 * (M + N) * K <= 2 * L2_NOMINAL else None
+
+    def timed(fn):
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            for _ in range(max(3, args.warmup)):
+                fn(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            fn(s)
+        ts = []
+        for i in range(max(3, args.warmup) + args.steps):
+            if flush is not None:
+                flush.fill_(i & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= max(3, args.warmup):
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    t_ours = timed(lambda s: lm.forward(x, Wt, pool, segs, y=y, workspace=ws, stream=s))
+    t_ref = timed(lambda s: torch.matmul(x, Wt.t(), out=y))
+    f = 2.0 * M * N * K
+    pk = peaks()
+    print(json.dumps({"metric": "base-only main pass vs cuBLAS", "unit": "TFLOP/s", "M": M, "K": K, "N": N,
+                      "ours_ms": t_ours, "cublas_ms": t_ref, "ours_tflops": f / t_ours / 1e9,
+                      "cublas_tflops": f / t_ref / 1e9, "ratio": t_ref / t_ours,
+                      "ours_frac_of_burst": f / t_ours / 1e9 / pk["bf16_tflops"],
+                      "l2": "flushed before every replay" if flush is not None else "no flush",
+                      "steps": args.steps, "warmup": args.warmup}), flush=True)
+    return 0
+
+
 def spawn_ranks(n):
     """Run this command again as n ranks of one node (torch.distributed.run, rendezvous on 127.0.0.1), one per GPU;
     returns the launcher's exit code."""
@@ -1183,6 +1246,8 @@ def main():
         return run_reference(args)
     if args.workload == "sweep":
         return run_sweep(args)
+    if args.workload == "gemm":
+        return run_gemm(args)
     return run_ours(args)
 
 

@@ -143,14 +143,15 @@ inline int shrink_split_kb(int64_t T) { return T <= 1024 ? 8 : (T <= 4096 ? 16 :
 // over more SMs and shrink each unit's partial sums.  A column's sum does not depend on the pass width.
 constexpr int kShrinkTargetItems = 148;
 
-// Main pass K-splits: when a launch has fewer output tiles than ~1.5 waves of CTA pairs, each tile's K loop is
-// split, the splits write fp32 partials, and a reduce launch sums them in split order.  Forward tiles keep their
+// Main pass K-splits: when a launch has fewer output tiles than ~1.25 waves of CTA pairs, each tile's K loop is
+// split, the splits write fp32 partials, and a reduce launch sums them in split order (96 measured best against 38,
+// 57, 76, 114, 152 and 228 on decode batches of 64-1024 tokens: 256 tokens 59 -> 54 us replayed from a graph).  Forward tiles keep their
 // LoRA K-steps out of the dense splits and cut them only at chunk boundaries, so every row's own adapter columns
 // sit in one split: a row's sum is (dense splits, in K order) + (its LoRA term) + exact zeros, whatever the other
 // rows of its tile, and stays independent of the segment and pool order.  Backward tiles hold one adapter; their
 // LoRA K-steps go with the last dense split.
 #ifndef LORA_MAIN_TARGET_ITEMS
-#define LORA_MAIN_TARGET_ITEMS 114
+#define LORA_MAIN_TARGET_ITEMS 96
 #endif
 constexpr int kMainTargetItems = LORA_MAIN_TARGET_ITEMS;
 // CTA pairs the planner sizes waves for (76 on a 152-SM GB300; plans stay valid on any device).
