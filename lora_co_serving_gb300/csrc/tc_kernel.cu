@@ -626,6 +626,11 @@ __global__ void __launch_bounds__(kThreads, 1) lora_tc_kernel(const __grid_const
 #ifndef LORA_HINT_W
 #define LORA_HINT_W 0
 #endif
+// How many LoRA k-blocks ahead the pair kernel's producer reads the adapter-row table.
+#ifndef LORA_ATOM_AHEAD
+#define LORA_ATOM_AHEAD 4
+#endif
+constexpr int kAtomAhead = LORA_ATOM_AHEAD;
 constexpr int kStages2 = LORA_MAIN_STAGES;
 constexpr int kHalfN = kBN / 2;
 constexpr int kA2Bytes = kTileM * kBK * 2;        // 16 KB
@@ -762,6 +767,15 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
             *box = in ? boxes[i] : 0;
             return in ? atoms[i] : 0;
         };
+        // the LoRA k-blocks' atom rows and box sizes are read kAtomAhead blocks ahead of their use (a read of the
+        // table is an L2 round trip, longer than a k-block's MMAs); the first blocks' are read before the dense
+        // k-blocks, while lanes 1..31 have nothing else to do
+        int32_t pre_row[kAtomAhead], pre_box[kAtomAhead];
+#pragma unroll
+        for (int j = 0; j < kAtomAhead; ++j) {
+            pre_box[j] = 0;
+            pre_row[j] = (j < w.n_ext) ? atom_at(e0 + j, &pre_box[j]) : 0;
+        }
         // dense k-blocks: lane 0 alone waits for each free stage, arms the barrier and issues the stage's loads
         // (a freed stage is refilled with no warp-wide exchange on the way: the refill latency is what bounds the
         // pass); the other lanes only keep the ring position
@@ -790,17 +804,13 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
         // LoRA k-blocks: this tile's Z block and, per 8-row atom of stacked adapter rows, two 64-column MN boxes;
         // only the atoms of the item's LoRA columns [ext_c0, ext_c1)
         // (lane L < 16 loads half L & 1 of the box that starts at 8-row atom L >> 1, if one does: a run of atoms with
-        // consecutive pool rows inside one chunk comes as one box of 16, 32 or 64 rows; the atom's pool row and box
-        // size are read one block ahead)
-        int32_t cur_box = 0, nxt_box = 0;
-        int32_t cur = (w.n_ext > 0) ? atom_at(e0, &cur_box) : 0;
-        for (int e = e0; e < e0 + w.n_ext; ++e) {
-            const int32_t nxt = (e + 1 < e0 + w.n_ext) ? atom_at(e + 1, &nxt_box) : 0;
+        // consecutive pool rows inside one chunk comes as one box of 16, 32 or 64 rows)
+        auto lora_block = [&](int e, int32_t row, int32_t row_box) -> bool {
             const int q0 = (max(w.ext_c0, e * kBK) - e * kBK) / 8;
             const int q1 = (min(w.ext_c1, e * kBK + kBK) - e * kBK) / 8;
             if (!acquire_stage2(ring, bar_full, bar_empty, kZBlockBytes + (q1 - q0) * 2048, leader, lane, abort_flag,
                                 P.status))
-                return;
+                return false;
             const uint32_t full = full_leader + ring.stage * 8;
             const uint32_t sa = smem_u32(smem + ring.stage * kStage2Bytes), sb = sa + kA2Bytes;
             if (lane == 0) tma_load_2d_pair(sa, &P.tm_z, 0, (td.z_blk0 + e) * kTileM, full);
@@ -808,17 +818,27 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
             // range comes on its own (a run of consecutive pool rows may straddle the item's first or last atom)
             const int q = lane >> 1, m = lane & 1;
             const bool in = lane < 16 && q >= q0 && q < q1;
-            const int box = in ? cur_box : 0;
+            const int box = in ? row_box : 0;
             const bool lead = box > 1 && q + box <= q1;
             const uint32_t covered = __reduce_or_sync(0xffffffffu, (lead && m == 0) ? (((1u << box) - 1u) << q) : 0u);
             const int n_load = !in ? 0 : (lead ? box : (((covered >> q) & 1u) ? 0 : 1));
             if (n_load > 0) {
                 const CUtensorMap* map = (n_load == 1) ? mp : mph + (n_load == 2 ? 0 : (n_load == 4 ? 1 : 2));
-                tma_load_2d_pair(sb + m * 8192 + q * 1024, map, nb + 64 * m, cur, full);
+                tma_load_2d_pair(sb + m * 8192 + q * 1024, map, nb + 64 * m, row, full);
             }
             ring.next();
-            cur = nxt;
-            cur_box = nxt_box;
+            return true;
+        };
+        const int e_end = e0 + w.n_ext;
+        for (int eb = e0; eb < e_end; eb += kAtomAhead) {
+#pragma unroll
+            for (int j = 0; j < kAtomAhead; ++j) {
+                const int e = eb + j;
+                if (e >= e_end) break;
+                const int32_t row = pre_row[j], row_box = pre_box[j];
+                if (e + kAtomAhead < e_end) pre_row[j] = atom_at(e + kAtomAhead, &pre_box[j]);
+                if (!lora_block(e, row, row_box)) return;
+            }
         }
     }
 }
