@@ -72,14 +72,14 @@ struct WorkItem {
     int32_t kind;
     int32_t tile;     // tile index; for grad items: grad-group index
     int32_t n0;       // main: first output column; shrink: first LoRA column of the pass; grad: first row m0
-    int32_t nk;       // main/shrink: k-blocks of the dense loop; grad: total token blocks
+    int32_t nk;       // main/shrink: k-blocks of the dense loop; grad: token blocks of this item (or split)
     int32_t mma_n;    // N of the MMA
-    int32_t n_ext;    // main: LoRA k-blocks of this item (Z blocks it touches); shrink: its shrink-unit index
-    int32_t kb0;      // shrink and split main items: first k-block of this split of the reduction
-    int32_t part;     // shrink: column offset of this split's fp32 partial [mma_n, 128] in the partial buffer;
-                      // main: first partial slot of the output tile (split s writes slot part + s)
-    int32_t nsplit;   // main: number of K-splits of the output tile (1 = no split)
-    int32_t split;    // main: index of this split
+    int32_t n_ext;    // main: LoRA k-blocks of this item (Z blocks it touches); shrink and split grad: its unit index
+    int32_t kb0;      // shrink, split main and grad items: first k-block (token block) of this split
+    int32_t part;     // shrink and split grad: column offset of this split's fp32 partial [mma_n, 128] in the
+                      // partial buffer; main: first partial slot of the output tile (split s writes slot part + s)
+    int32_t nsplit;   // main and grad: number of splits of the reduction (0 or 1 = no split)
+    int32_t split;    // main and grad: index of this split
     int32_t ext_c0;   // main: LoRA columns [ext_c0, ext_c1) of the tile's Z that this item multiplies (16-aligned)
     int32_t ext_c1;
     int32_t j0;       // grad: first row of the transposed xA / dYB buffer this item reads (the slice's rows)
@@ -122,10 +122,12 @@ constexpr int kBgmvRows = LORA_BGMV_ROWS;   // rows per CUDA-core shrink unit (4
 #endif
 constexpr int kBgmvMaxRows = LORA_BGMV_MAX_ROWS;   // gathered rows (whole tiles) up to which the CUDA-core shrink runs
 
-// One shrink pass of one tile.  Its K-splits write fp32 partial sums; the last split to finish (counted per row
-// quarter) sums them in split order and writes Z and the saved or transposed copies.
+// One shrink pass of one tile, or one gradient item whose token range is split.  Its splits write fp32 partial
+// sums; the last split to finish (counted per row quarter) sums them in split order and writes Z and the saved or
+// transposed copies (a gradient item: its rows of dA or dB).
 struct ShrinkUnit {
-    int32_t kind;     // kShrinkFwd, kShrinkDyb or kShrinkXa
+    int32_t kind;     // kShrinkFwd, kShrinkDyb or kShrinkXa; kGradDb or kGradDa for a split gradient item
+                      // (then tile is its gradient group and n0 its first row)
     int32_t tile;
     int32_t n0;       // first LoRA column of the pass
     int32_t mma_n;

@@ -482,6 +482,49 @@ void plan_forward(const Problem& p, Plan* out) {
     });
 }
 
+// Gradient items: when they fill less of the last wave of CTAs than a split of their token ranges would, every
+// item is split the same number of ways (at most 8, at least 8 token blocks a split) so that the waves fill; the
+// splits' fp32 partials are summed in split order by the last split to finish.  The number of ways depends on the
+// number of items and their shortest token range alone, so it does not change with the segment or pool order.
+static void split_grad_items(Plan* pl) {
+    std::vector<WorkItem>& items = pl->items[2];
+    if (items.empty()) return;
+    const int64_t G = 2 * kPairsPlanned;              // CTAs of the gradient launch
+    const int64_t n = int64_t(items.size());
+    int32_t min_nk = items[0].nk;
+    for (const WorkItem& w : items) min_nk = std::min(min_nk, w.nk);
+    int32_t ways = 1;
+    double best = double(cdiv(n, G));                 // waves of whole items
+    for (int32_t s = 2; s <= 8 && min_nk / s >= 8; ++s) {
+        const double waves = double(cdiv(n * s, G)) / s;
+        if (waves < 0.8 * best) {
+            best = waves;
+            ways = s;
+        }
+    }
+    if (ways == 1) return;
+    std::vector<WorkItem> out;
+    out.reserve(items.size() * ways);
+    for (const WorkItem& w : items) {
+        ShrinkUnit u{};
+        u.kind = w.kind; u.tile = w.tile; u.n0 = w.n0; u.mma_n = w.mma_n; u.nsplit = ways;
+        u.part0 = int32_t(pl->part_cols);
+        for (int32_t sp = 0; sp < ways; ++sp) {
+            WorkItem v = w;
+            v.kb0 = int32_t((int64_t)sp * w.nk / ways);
+            v.nk = int32_t((int64_t)(sp + 1) * w.nk / ways) - v.kb0;
+            v.nsplit = ways;
+            v.split = sp;
+            v.part = u.part0 + sp * w.mma_n;
+            v.n_ext = int32_t(pl->units.size());     // split items carry their unit index here
+            out.push_back(v);
+        }
+        pl->part_cols += (int64_t)ways * w.mma_n;
+        pl->units.push_back(u);
+    }
+    items.swap(out);
+}
+
 void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, bool recompute, Plan* out,
                    bool per_segment) {
     Plan& pl = *out;
@@ -590,6 +633,7 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
                     pl.items[2].push_back(w);
                 }
     }
+    split_grad_items(&pl);
 }
 
 int check_plan(const Problem& p, const Plan& pl, bool backward, std::string* err) {
@@ -659,7 +703,9 @@ int check_plan(const Problem& p, const Plan& pl, bool backward, std::string* err
     }
     for (size_t u = 0; u < pl.units.size(); ++u) {
         const ShrinkUnit& su = pl.units[u];
-        if (su.tile < 0 || su.tile >= nt || su.nsplit < 1 || su.part0 < 0 ||
+        const bool grad = su.kind == kGradDb || su.kind == kGradDa;
+        const int64_t n_tiles = grad ? int64_t(pl.groups.size()) : nt;    // a gradient unit's tile is its group
+        if (su.tile < 0 || su.tile >= n_tiles || su.nsplit < 1 || su.part0 < 0 ||
             su.part0 + int64_t(su.nsplit) * su.mma_n > pl.part_cols)
             return bad("shrink unit " + std::to_string(u));
     }
@@ -682,6 +728,20 @@ int check_plan(const Problem& p, const Plan& pl, bool backward, std::string* err
                 if (w.n0 < 0 || w.n0 >= (w.kind == kGradDb ? p.N : p.K)) return bad(at + "gradient rows");
                 if (w.j0 < 0 || w.j0 + w.mma_n > int64_t(p.S) * LORA_MAX_RANK) return bad(at + "transposed rows");
                 if (w.kind == kGradDa && w.j0 >= int64_t(g.nslice) * g.r) return bad(at + "down-factor rows");
+                if (g.seg0 < 0 || g.nseg < 1 || g.seg0 + g.nseg > int32_t(pl.tsegs.size()))
+                    return bad(at + "gradient group segments");
+                int64_t blocks = 0;                  // token blocks of the group's segments
+                for (int32_t q = 0; q < g.nseg; ++q) blocks += cdiv(pl.tsegs[g.seg0 + q].len, kBK);
+                if (w.kb0 < 0 || w.nk < 1 || w.kb0 + w.nk > blocks) return bad(at + "token blocks");
+                if (w.nsplit > 1) {
+                    if (w.n_ext < 0 || w.n_ext >= int32_t(pl.units.size()) || pl.units[w.n_ext].kind != w.kind ||
+                        pl.units[w.n_ext].tile != w.tile || pl.units[w.n_ext].nsplit != w.nsplit ||
+                        w.split < 0 || w.split >= w.nsplit)
+                        return bad(at + "split unit");
+                    const ShrinkUnit& su = pl.units[w.n_ext];
+                    if (su.mma_n != w.mma_n || w.part != su.part0 + w.split * w.mma_n)
+                        return bad(at + "partial columns");
+                }
             } else {
                 if (w.tile < 0 || w.tile >= nt) return bad(at + "tile");
                 if (w.n_ext < 0 || w.n_ext >= int32_t(pl.units.size()) || pl.units[w.n_ext].tile != w.tile)

@@ -232,14 +232,23 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
             const CUtensorMap* mb = (w.kind == kGradDb) ? &P.tm_xat : &P.tm_dybt;
             const int natoms = w.mma_n / 8;
             const int per = grad_blocks_per_stage(w.mma_n);
+            // token blocks [kb0, kb0 + nk) of the group's segments taken one after another (a split of the
+            // reduction covers part of them)
+            const int kb_end = w.kb0 + w.nk;
             int gb = 0;           // token block index over the item's segments
-            for (int q = 0; q < g.nseg; ++q) {
+            for (int q = 0; q < g.nseg && gb < kb_end; ++q) {
                 const TrainSeg s = P.tsegs[g.seg0 + q];
+                const int nb = (s.len + kBK - 1) / kBK;
+                if (gb + nb <= w.kb0) {
+                    gb += nb;
+                    continue;
+                }
                 const CUtensorMap* ma = (w.kind == kGradDb) ? &P.tm_seg_dy[g.seg0 + q] : &P.tm_seg_x[g.seg0 + q];
-                for (int b = 0; b * kBK < s.len; ++b, ++gb) {
-                    const int sub = gb % per;
+                for (int b = max(0, w.kb0 - gb); b < nb && gb + b < kb_end; ++b) {
+                    const int i = gb + b - w.kb0;          // index of the block within the split
+                    const int sub = i % per;
                     if (sub == 0) {
-                        const int nsub = min(per, w.nk - gb);
+                        const int nsub = min(per, w.nk - i);
                         if (!acquire_stage(ring, bar_full, bar_empty, nsub * (kABytes + natoms * 1024), lane,
                                            abort_flag, P.status))
                             return;
@@ -249,8 +258,9 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
                     const uint32_t sb = sa + kABytes;
                     if (lane < 2) tma_load_2d(sa + lane * 8192, ma, w.n0 + 64 * lane, b * kBK, full);
                     if (lane < natoms) tma_load_2d(sb + lane * 1024, mb, s.tpos0 + b * kBK, w.j0 + lane * 8, full);
-                    if (sub == per - 1 || gb == w.nk - 1) ring.next();
+                    if (sub == per - 1 || i == w.nk - 1) ring.next();
                 }
+                gb += nb;
             }
             continue;
         }
@@ -416,6 +426,52 @@ struct ShrinkRowOut {
     }
 };
 
+// Columns [c, c + 16) of one row of a split reduction: the sum, in split order, of the unit's fp32 partials
+// (p0: the row's first 4-column group of split 0; split s sits u.mma_n columns further per split).  The splits'
+// 16-column groups are loaded four splits at a time (16 loads of 16 bytes in flight per thread), then added.
+__device__ __forceinline__ void sum_split_partials(const float* p0, const ShrinkUnit& u, int c, float (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    for (int s0 = 0; s0 < u.nsplit; s0 += 4) {
+        float4 a[4][4];
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                a[sp][q] = (s0 + sp < u.nsplit)
+                               ? __ldcg(reinterpret_cast<const float4*>(p0 + ((size_t)(s0 + sp) * u.mma_n + c + 4 * q) *
+                                                                                  kTileM))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp) {
+            if (s0 + sp >= u.nsplit) break;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                v[4 * q] += a[sp][q].x;
+                v[4 * q + 1] += a[sp][q].y;
+                v[4 * q + 2] += a[sp][q].z;
+                v[4 * q + 3] += a[sp][q].w;
+            }
+        }
+    }
+}
+
+// Writes one split's raw fp32 accumulator columns [0, mma_n) of this thread's row to its slot of the partial buffer
+// (per 4 columns [C, C + 4): 128 rows of 4 floats at part + C * 128 + row * 4, so that a row's 4 columns are one
+// 16-byte store and a warp's 32 rows one 512-byte run).
+__device__ __forceinline__ void store_split_partial(float* dst, uint32_t taddr, int mma_n) {
+    for (int c = 0; c < mma_n; c += 16) {
+        uint32_t a[16];
+        tmem_ld16(taddr + c, a);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(dst + (size_t)(c + 4 * q) * kTileM) =
+                make_float4(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1]), __uint_as_float(a[4 * q + 2]),
+                            __uint_as_float(a[4 * q + 3]));
+    }
+}
+
 __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_tempty, uint32_t tmem, int i0, int i1,
                              volatile int* abort_flag) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -439,10 +495,8 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
             const int32_t jbase = is_b ? 0 : w.j0;
             const int32_t jend = is_b ? g.r : g.r * g.nslice;
             float* base = (is_b ? P.dB + (size_t)g.prow_b * P.N : P.dA + (size_t)g.prow_a * P.K) + (size_t)jbase * ld;
-            for (int c = 0; c < w.mma_n; c += 16) {
-                uint32_t a[16];
-                tmem_ld16(taddr + c, a);
-                tmem_ld_wait();
+            // accumulator columns [c, c + 16) of this thread's row, scaled, into (or onto) the gradient
+            auto put16 = [&](int c, const float (&v)[16]) {
                 const int64_t last = ((int64_t)(is_b ? g.prow_b : g.prow_a) + jbase + min(c + 16, jend - jbase) - 1) * ld + m;
                 if (m < ld && dbg_ok(P.debug, P.status, last, is_b ? P.db.grad_b : P.db.grad_a)) {
 #pragma unroll
@@ -450,11 +504,52 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                         const int j = c + i;
                         if (jbase + j < jend) {
                             float* p = base + (size_t)j * ld + m;
-                            const float val = g.scale * __uint_as_float(a[i]);
+                            const float val = g.scale * v[i];
                             *p = P.accumulate ? (*p + val) : val;
                         }
                     }
                 }
+            };
+            if (w.nsplit <= 1) {
+                for (int c = 0; c < w.mma_n; c += 16) {
+                    uint32_t a[16];
+                    tmem_ld16(taddr + c, a);
+                    tmem_ld_wait();
+                    float v[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(a[i]);
+                    put16(c, v);
+                }
+            } else {
+                // a split of the token range (the item's n_ext field holds its unit): raw fp32 partial sums; the
+                // last split to arrive (per row quarter) sums all splits in split order and writes those 32 rows
+                const ShrinkUnit u = P.units[w.n_ext];
+                float* dst = P.part + (size_t)w.part * kTileM + row * 4;
+                const bool part_ok = dbg_ok(P.debug, P.status, ((int64_t)u.part0 + (int64_t)u.nsplit * u.mma_n) * kTileM - 1,
+                                            P.db.part_floats);
+                if (part_ok) store_split_partial(dst, taddr, w.mma_n);
+                tc_fence_before();
+                mbar_arrive(bar_tempty + acc * 8);       // the accumulator is free; the rest reads global memory
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                int32_t* cnt = P.counters + w.n_ext * 4 + quarter;
+                if (lane == 0) last = (atomicAdd(cnt, 1) == u.nsplit - 1) ? 1 : 0;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last && part_ok) {
+                    __threadfence();
+                    const float* p0 = P.part + (size_t)u.part0 * kTileM + row * 4;
+                    for (int c = 0; c < w.mma_n; c += 16) {
+                        float v[16];
+                        sum_split_partials(p0, u, c, v);
+                        put16(c, v);
+                    }
+                    __syncwarp();
+                    if (lane == 0) *cnt = 0;              // ready for the next call on this workspace
+                }
+                continue;
             }
         } else {
             // shrink split (the item's n_ext field holds its shrink-unit index)
@@ -472,22 +567,11 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 }
             } else {
                 // raw fp32 partial sums; the last split to arrive (per row quarter) sums all splits in split order
-                // and finalizes those 32 rows.  Layout: per 4 columns [C, C + 4) of the partial buffer, 128 rows
-                // of 4 floats (P.part + C * 128 + row * 4), so that a row's 4 columns are one 16-byte access and a
-                // warp's 32 rows one 512-byte run
+                // and finalizes those 32 rows
                 float* dst = P.part + (size_t)w.part * kTileM + row * 4;
                 const bool part_ok = dbg_ok(P.debug, P.status, ((int64_t)u.part0 + (int64_t)u.nsplit * u.mma_n) * kTileM - 1,
                                             P.db.part_floats);
-                for (int c = 0; c < w.mma_n && part_ok; c += 16) {
-                    uint32_t a[16];
-                    tmem_ld16(taddr + c, a);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<float4*>(dst + (size_t)(c + 4 * q) * kTileM) =
-                            make_float4(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1]),
-                                        __uint_as_float(a[4 * q + 2]), __uint_as_float(a[4 * q + 3]));
-                }
+                if (part_ok) store_split_partial(dst, taddr, w.mma_n);
                 tc_fence_before();
                 mbar_arrive(bar_tempty + acc * 8);       // the accumulator is free; the rest reads global memory
                 acc ^= 1;
@@ -501,35 +585,10 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 if (last && part_ok) {
                     __threadfence();
                     ShrinkRowOut out(P, u, row);
-                    // the splits' 16-column groups are loaded four splits at a time (16 loads of 16 bytes in
-                    // flight per thread), then added in split order
                     const float* p0 = P.part + (size_t)u.part0 * kTileM + row * 4;
                     for (int c = 0; c < w.mma_n; c += 16) {
                         float v[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = 0.f;
-                        for (int s0 = 0; s0 < u.nsplit; s0 += 4) {
-                            float4 a[4][4];
-#pragma unroll
-                            for (int sp = 0; sp < 4; ++sp)
-#pragma unroll
-                                for (int q = 0; q < 4; ++q)
-                                    a[sp][q] = (s0 + sp < u.nsplit)
-                                                   ? __ldcg(reinterpret_cast<const float4*>(
-                                                         p0 + ((size_t)(s0 + sp) * u.mma_n + c + 4 * q) * kTileM))
-                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                            for (int sp = 0; sp < 4; ++sp) {
-                                if (s0 + sp >= u.nsplit) break;
-#pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    v[4 * q] += a[sp][q].x;
-                                    v[4 * q + 1] += a[sp][q].y;
-                                    v[4 * q + 2] += a[sp][q].z;
-                                    v[4 * q + 3] += a[sp][q].w;
-                                }
-                            }
-                        }
+                        sum_split_partials(p0, u, c, v);
                         out.put16(c, v);
                     }
                     __syncwarp();
