@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import Dev, compare, to_np, train_blocks
+from gpu_util import Dev, compare, grad_split_table, to_np, train_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -175,6 +175,26 @@ def test_bf16_backward_accumulate():
     ia, ib = train_blocks(wl)
     compare(to_np(aA)[ia], to_np(dA0)[ia] + to_np(dA)[ia], "dA accumulate", max_err=1e-5, fro_err=1e-6)
     compare(to_np(aB)[ib], to_np(dB0)[ib] + to_np(dB)[ib], "dB accumulate", max_err=1e-5, fro_err=1e-6)
+
+
+def test_bf16_split_gradients():
+    """Gradient items split three ways along the tokens (the table's planning is pinned on the CPU), with splits
+    that cross segment boundaries: dX, dA, dB against the oracle, then accumulated onto random gradients."""
+    import torch
+    wl = grad_split_table()
+    d = Dev(wl)
+    check_backward(wl, d)
+    _, dA, dB = d.backward()
+    dA0 = torch.randn_like(dA)
+    dB0 = torch.randn_like(dB)
+    _, aA, aB = d.backward(dA=dA0.clone(), dB=dB0.clone(), accumulate=True)
+    torch.cuda.synchronize()
+    ia, ib = train_blocks(wl)
+    compare(to_np(aA)[ia], to_np(dA0)[ia] + to_np(dA)[ia], "dA accumulate", max_err=1e-5, fro_err=1e-6)
+    compare(to_np(aB)[ib], to_np(dB0)[ib] + to_np(dB)[ib], "dB accumulate", max_err=1e-5, fro_err=1e-6)
+    mA = np.ones(dA.numel(), bool)
+    mA[ia] = False
+    assert np.array_equal(to_np(aA)[mA], to_np(dA0)[mA])
 
 
 def test_bf16_backward_small_batch_split_k():

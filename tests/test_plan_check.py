@@ -15,6 +15,7 @@ import pytest
 
 import lora_co_serving_gb300 as lm
 import workloads
+from gpu_util import grad_split_table
 
 CSRC = os.path.join(os.path.dirname(lm.__file__), "csrc")
 INCLUDE = os.path.join(os.path.dirname(os.path.dirname(lm.__file__)), "include")
@@ -99,21 +100,19 @@ extern "C" int check_table(int T, int K, int N, const lora_pool_t* pool, const l
     else lora::plan_forward(p, &pl);
     return lora::check_plan(p, pl, backward != 0, &err);
 }
+// number of items of the backward's gradient launch (-1: the table does not validate)
+extern "C" int grad_items(int T, int K, int N, const lora_pool_t* pool, const lora_segment_t* segs, int n) {
+    lora::Problem p;
+    std::string err;
+    if (lora::validate(T, K, N, LORA_BF16, pool, segs, n, &p, &err)) return -1;
+    lora::Plan pl;
+    lora::plan_backward(p, true, true, true, true, &pl);
+    return int(pl.items[2].size());
+}
 '''
 
-# (name, original text in plan.cpp, planted mistake)
-PLANTED = [
-    ("atom_row_past_block", "pl->atoms_a.push_back(ch.prow_a + sl * ch.r + std::min(o, last));",
-     "pl->atoms_a.push_back(ch.prow_a + sl * ch.r + o + 8);"),
-    ("split_slot_reused", "pl->main_slots += nsplit;", "pl->main_slots += nsplit - 1;"),
-]
-
-
-@pytest.mark.parametrize("name,orig,bad", PLANTED, ids=[p[0] for p in PLANTED])
-def test_planted_planner_mistake_is_reported(tmp_path, name, orig, bad):
-    src = open(os.path.join(CSRC, "plan.cpp")).read()
-    assert src.count(orig) == 1, "anchor not unique: " + orig
-    (tmp_path / "plan.cpp").write_text(src.replace(orig, bad))
+def _build_driver(tmp_path, src):
+    (tmp_path / "plan.cpp").write_text(src)
     (tmp_path / "driver.cpp").write_text(DRIVER)
     so = str(tmp_path / "libplan.so")
     cxx = os.environ.get("CXX", "g++")
@@ -123,9 +122,42 @@ def test_planted_planner_mistake_is_reported(tmp_path, name, orig, bad):
     assert res.returncode == 0, res.stderr
     lib = ctypes.CDLL(so)
     lib.check_table.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
-    # decode rows (atoms of several adapters) and a small split main pass
-    wl = workloads.config2(T=256, K=256, N=512, n_adapters=20)
+    lib.grad_items.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    return lib
+
+
+def _decode_table():
+    """Decode rows (atoms of several adapters) and a small split main pass."""
+    return workloads.config2(T=256, K=256, N=512, n_adapters=20)
+
+
+# (name, original text in plan.cpp, planted mistake, table, backward)
+PLANTED = [
+    ("atom_row_past_block", "pl->atoms_a.push_back(ch.prow_a + sl * ch.r + std::min(o, last));",
+     "pl->atoms_a.push_back(ch.prow_a + sl * ch.r + o + 8);", _decode_table, 0),
+    ("split_slot_reused", "pl->main_slots += nsplit;", "pl->main_slots += nsplit - 1;", _decode_table, 0),
+    ("grad_split_partial_overlap", "v.part = u.part0 + sp * w.mma_n;", "v.part = u.part0;", grad_split_table, 1),
+]
+
+
+@pytest.mark.parametrize("name,orig,bad,table,backward", PLANTED, ids=[p[0] for p in PLANTED])
+def test_planted_planner_mistake_is_reported(tmp_path, name, orig, bad, table, backward):
+    src = open(os.path.join(CSRC, "plan.cpp")).read()
+    assert src.count(orig) == 1, "anchor not unique: " + orig
+    lib = _build_driver(tmp_path, src.replace(orig, bad))
+    wl = table()
     pool = _pool(wl)
     segs = lm.segments(wl.segs)
-    rc = lib.check_table(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0], 0)
+    rc = lib.check_table(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0], backward)
     assert rc == -12, "planted mistake %s not reported (rc %d)" % (name, rc)
+
+
+def test_gradient_items_split_three_ways(tmp_path):
+    """The table of the GPU test of split gradients does split: 12 gradient items, each into 3 token ranges (the
+    shortest group has 25 token blocks; 4 ways would leave splits under 8 blocks)."""
+    lib = _build_driver(tmp_path, open(os.path.join(CSRC, "plan.cpp")).read())
+    wl = grad_split_table()
+    pool = _pool(wl)
+    segs = lm.segments(wl.segs)
+    assert lib.grad_items(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0]) == 36
+    assert lib.check_table(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0], 1) == 0
