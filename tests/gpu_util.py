@@ -65,16 +65,23 @@ def train_blocks(wl):
     return ia, ib
 
 
-def grad_split_table(seed=4242, K=320, N=384):
+SPLIT_BOUNDS = [0, 256, 512, 640]      # the sliced variant: three slices (256, 256, 128 columns)
+
+
+def grad_split_table(seed=4242, K=320, N=384, sliced=False):
     """A backward whose gradient items are few enough for the planner to split their token ranges three ways:
     adapter 0 (rank 24) fine-tunes on three segments of 700, 333 and 1100 tokens (35 token blocks, so that splits
     cross segment boundaries), adapter 1 (rank 40) on one of 1600 tokens (25 blocks); decode, prefill and
     base-only rows of other adapters sit between them.  12 gradient items (dB: 3 column tiles, dA: 3 row tiles per
-    adapter) -> 36 split items."""
+    adapter) -> 36 split items.  sliced: the same table on a sliced layer of K = 256 and the three slices of
+    SPLIT_BOUNDS (dB: 5 column tiles over the slices, dA: 2 row tiles per adapter) -> 42 split items."""
     spans = [(700, 0, 1), (5, 2, 0), (333, 0, 1), (90, 3, 0), (1, 4, 0), (1600, 1, 1), (40, -1, 0), (1100, 0, 1),
              (1, 5, 0)]
     segs, t = [], 0
     for ln, a, tr in spans:
         segs.append((t, ln, a, tr))
         t += ln
-    return workloads.custom(seed, t, K, N, segs, [24, 40, 8, 16, 64, 128])
+    rank = [24, 40, 8, 16, 64, 128]
+    if sliced:
+        return workloads.sliced(seed, t, 256, np.asarray(SPLIT_BOUNDS, np.int32), segs, rank)
+    return workloads.custom(seed, t, K, N, segs, rank)

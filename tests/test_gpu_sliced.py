@@ -155,3 +155,11 @@ def test_sliced_gate_up_and_wide_ranks(bounds, r):
     d, y, xs = check_forward(wl)
     check_backward(wl, d)
     check_backward(wl, d, xs)
+
+
+def test_sliced_split_gradients():
+    """Gradient items of a three-slice layer split three ways along the tokens (pinned on the host), splits
+    crossing segment boundaries: dX, dA (every slice's down factor), dB against the sliced oracle."""
+    from gpu_util import grad_split_table
+    wl = grad_split_table(sliced=True)
+    check_backward(wl, Dev(wl))

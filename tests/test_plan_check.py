@@ -100,11 +100,12 @@ extern "C" int check_table(int T, int K, int N, const lora_pool_t* pool, const l
     else lora::plan_forward(p, &pl);
     return lora::check_plan(p, pl, backward != 0, &err);
 }
-// number of items of the backward's gradient launch (-1: the table does not validate)
-extern "C" int grad_items(int T, int K, int N, const lora_pool_t* pool, const lora_segment_t* segs, int n) {
+// number of items of the backward's gradient launch (-1: the table does not validate); slices may be NULL
+extern "C" int grad_items(int T, int K, int N, const lora_pool_t* pool, const lora_slices_t* slices,
+                          const lora_segment_t* segs, int n) {
     lora::Problem p;
     std::string err;
-    if (lora::validate(T, K, N, LORA_BF16, pool, segs, n, &p, &err)) return -1;
+    if (lora::validate(T, K, N, LORA_BF16, pool, segs, n, &p, &err, slices)) return -1;
     lora::Plan pl;
     lora::plan_backward(p, true, true, true, true, &pl);
     return int(pl.items[2].size());
@@ -122,7 +123,7 @@ def _build_driver(tmp_path, src):
     assert res.returncode == 0, res.stderr
     lib = ctypes.CDLL(so)
     lib.check_table.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
-    lib.grad_items.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.grad_items.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3 + [ctypes.c_int]
     return lib
 
 
@@ -152,12 +153,18 @@ def test_planted_planner_mistake_is_reported(tmp_path, name, orig, bad, table, b
     assert rc == -12, "planted mistake %s not reported (rc %d)" % (name, rc)
 
 
-def test_gradient_items_split_three_ways(tmp_path):
-    """The table of the GPU test of split gradients does split: 12 gradient items, each into 3 token ranges (the
-    shortest group has 25 token blocks; 4 ways would leave splits under 8 blocks)."""
+@pytest.mark.parametrize("sliced", [False, True], ids=["plain", "sliced"])
+def test_gradient_items_split_three_ways(tmp_path, sliced):
+    """The tables of the GPU tests of split gradients do split: 12 gradient items (14 on the sliced layer), each
+    into 3 token ranges (the shortest group has 25 token blocks; 4 ways would leave splits under 8 blocks)."""
     lib = _build_driver(tmp_path, open(os.path.join(CSRC, "plan.cpp")).read())
-    wl = grad_split_table()
+    wl = grad_split_table(sliced=sliced)
     pool = _pool(wl)
     segs = lm.segments(wl.segs)
-    assert lib.grad_items(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0]) == 36
-    assert lib.check_table(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0], 1) == 0
+    sl = lm.Slices(wl.bounds) if sliced else None
+    n = lib.grad_items(wl.T, wl.K, wl.N, pool.cptr(), sl.cptr() if sl else None, segs.ctypes.data, segs.shape[0])
+    assert n == (42 if sliced else 36)
+    if not sliced:
+        assert lib.check_table(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0], 1) == 0
+    else:
+        lm.plan_check(wl.T, wl.K, wl.N, pool, wl.segs, backward=True, bounds=wl.bounds)
