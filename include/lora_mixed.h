@@ -289,9 +289,18 @@ int lora_workspace_status(const void* workspace, void* stream);
  * A call that has no work in group i still records both of its events. */
 int lora_set_trace_events(void* const* events);
 
+/* Setup of the failure path (no counterpart on the pages): the limit, in nanoseconds, of every bounded wait in
+ * the library's kernels on the current device (default 1 s; accepted 1 ms to 60 s).  A kernel whose wait runs
+ * out records LORA_ERR_TIMEOUT in its workspace status word and returns (lora_workspace_status reports it); on a
+ * GPU shared by time slicing or preemption, where a healthy call can be held off the GPU for longer than that,
+ * raise it.  A synchronous copy to the device: call it before the calls it should govern, not while they run or
+ * while a stream is being captured.  Returns LORA_OK, LORA_ERR_INVALID_ARG (out of range; nothing changes) or
+ * LORA_ERR_CUDA. */
+int lora_set_wait_limit(uint64_t ns);
+
 /* Diagnostic of the failure path (no counterpart on the pages): launches one thread that waits, with the
  * same bounded wait as every kernel of the library, on a barrier that nothing ever completes.  After the
- * wait's limit (about one second) it records LORA_ERR_TIMEOUT in the workspace status word and returns, so
+ * wait's limit (about one second unless lora_set_wait_limit changed it) it records LORA_ERR_TIMEOUT in the workspace status word and returns, so
  * lora_workspace_status() then reports LORA_ERR_TIMEOUT and the CUDA context stays usable.  Needs the first
  * 256 bytes of a 256-byte aligned workspace. */
 int lora_selftest_wait_timeout(void* workspace, size_t ws_bytes, void* stream);

@@ -26,7 +26,7 @@ from . import _build
 __all__ = ["Pool", "forward", "backward", "sliced_forward", "sliced_backward", "sliced_workspace_size",
            "sliced_xa_size", "workspace_size", "xa_size", "workspace_status", "plan_describe",
            "LoraError", "LibraryNotBuilt", "library", "build", "SAVE_XA", "RECOMPUTE_XA", "ACCUMULATE_GRAD",
-           "DEBUG_CHECKS", "plan_check", "static_status"]
+           "DEBUG_CHECKS", "plan_check", "static_status", "set_wait_limit"]
 
 SAVE_XA = 1
 RECOMPUTE_XA = 2
@@ -45,7 +45,7 @@ EXPORTED = ["lora_workspace_size", "lora_xa_size", "lora_mixed_forward", "lora_m
             "lora_selftest_wait_timeout", "lora_adamw_step", "lora_mixed_backward_flagged",
             "lora_sliced_workspace_size", "lora_sliced_xa_size", "lora_sliced_forward", "lora_sliced_backward",
             "lora_latency_terms", "lora_latency_features", "lora_latency_fit", "lora_latency_predict",
-            "lora_static_status", "lora_plan_check"]
+            "lora_static_status", "lora_plan_check", "lora_set_wait_limit"]
 
 
 class LoraError(RuntimeError):
@@ -114,6 +114,8 @@ def library(path=None):
     lib.lora_plan_check.restype = ctypes.c_int
     lib.lora_static_status.argtypes = [P]
     lib.lora_static_status.restype = ctypes.c_int
+    lib.lora_set_wait_limit.argtypes = [ctypes.c_uint64]
+    lib.lora_set_wait_limit.restype = ctypes.c_int
     lib.lora_selftest_wait_timeout.argtypes = [P, SZ, P]
     lib.lora_selftest_wait_timeout.restype = ctypes.c_int
     lib.lora_adamw_step.argtypes = [ctypes.c_int, P, I32, I32, P, P, P, P, P, P, P, P, P, P, P, I32, P, P]
@@ -283,6 +285,11 @@ def forward_static(x, Wt, pool, segs, y=None, xa_save=None, save_xa=False, strea
     _check(library().lora_mixed_forward_static(T, K, N, code, _ptr(x), _ptr(Wt), pool.cptr(), _ptr(s), s.shape[0],
                                                _ptr(y), _ptr(xa_save), flags, _stream_ptr(stream)))
     return (y, xa_save) if save_xa else y
+
+
+def set_wait_limit(seconds):
+    """Limit of every bounded wait in the library's kernels on the current device (1 ms to 60 s; default 1 s)."""
+    _check(library().lora_set_wait_limit(int(round(seconds * 1e9))))
 
 
 def static_status(stream=None):

@@ -546,6 +546,13 @@ int lora_selftest_wait_timeout(void* workspace, size_t ws_bytes, void* stream_) 
     return LORA_OK;
 }
 
+int lora_set_wait_limit(uint64_t ns) {
+    if (ns < 1000000ull || ns > 60000000000ull)
+        return fail(LORA_ERR_INVALID_ARG, "the wait limit must lie between 1 ms and 60 s");
+    CUDA_TRY(set_wait_limit_ns(ns));
+    return LORA_OK;
+}
+
 int lora_workspace_status(const void* workspace, void* stream) {
     if (!workspace) return fail(LORA_ERR_WORKSPACE, "workspace is NULL");
     CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));

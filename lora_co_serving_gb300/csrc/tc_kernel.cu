@@ -47,7 +47,8 @@ __device__ __forceinline__ int shrink_blocks_per_stage(int mma_n) {
     return (LORA_SHRINK_PACK && mma_n <= 64) ? 2 : 1;
 }
 constexpr int kThreads = 192;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;      // 1 s
+// Limit of every bounded wait (ns) on this device: 1 s unless lora_set_wait_limit changed it
+__device__ uint64_t g_wait_limit_ns = 1000000000ull;
 constexpr uint32_t kTmemCols = 512;                   // two 256-column fp32 accumulators
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -99,10 +100,11 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
                                              uint32_t suspend_ns = 0) {
     const uint64_t t0 = global_timer();
+    const uint64_t limit = g_wait_limit_ns;
     for (uint32_t spin = 1;; ++spin) {
         if (suspend_ns ? mbar_try_wait_hint(bar, parity, suspend_ns) : mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if ((spin & 31u) == 0 && global_timer() - t0 > kWaitLimitNs) {
+        if ((spin & 31u) == 0 && global_timer() - t0 > limit) {
             *abort_flag = 1;
             atomicCAS(status, 0, LORA_ERR_TIMEOUT);
             return false;
@@ -1173,6 +1175,8 @@ __global__ void selftest_timeout_kernel(int32_t* status) {
 
 size_t tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024 + 1024; }
 size_t tc2_smem_bytes() { return (size_t)kStages2 * kStage2Bytes + kOutStageBytes + 1024 + 1024; }
+
+cudaError_t set_wait_limit_ns(uint64_t ns) { return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns)); }
 
 cudaError_t selftest_timeout_launch(int32_t* status, cudaStream_t stream) {
     selftest_timeout_kernel<<<1, 32, 0, stream>>>(status);

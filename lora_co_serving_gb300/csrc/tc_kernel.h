@@ -80,5 +80,7 @@ cudaError_t main_reduce_launch(const SplitTile* splits, int32_t n_splits, const 
                                cudaStream_t stream);
 cudaError_t tc2_launch(const KParams& P, int pairs, cudaStream_t stream);    // main items, clusters of 2 CTAs
 cudaError_t selftest_timeout_launch(int32_t* status, cudaStream_t stream);
+// The limit of every bounded wait of the library's kernels on the current device (synchronous copy).
+cudaError_t set_wait_limit_ns(uint64_t ns);
 
 }  // namespace lora

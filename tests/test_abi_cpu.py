@@ -205,3 +205,10 @@ def test_sliced_sizes(lib):
     sl1 = lm.Slices([0, 1024])
     one = lib.lora_sliced_workspace_size(36, K, N, 0, pool.cptr(), sl1.cptr(), segs.ctypes.data, 3)
     assert one == lib.lora_workspace_size(36, K, N, 0, pool.cptr(), segs.ctypes.data, 3)
+
+
+def test_wait_limit_range(lib):
+    """lora_set_wait_limit refuses limits outside 1 ms .. 60 s on the host, before any CUDA call."""
+    for ns in (0, 999_999, 60_000_000_001, 2**63):
+        assert lib.lora_set_wait_limit(ns) == -1, ns
+        assert "between 1 ms and 60 s" in lib.lora_last_error().decode()

@@ -4,6 +4,8 @@ Every wait in the library's kernels is bounded.  The self-test kernel waits on a
 completes; the wait must give up (about one second), record LORA_ERR_TIMEOUT in the workspace status word that
 the host reads back, and leave the CUDA context usable for the next call.
 """
+import time
+
 import numpy as np
 import pytest
 
@@ -12,6 +14,30 @@ import workloads
 from gpu_util import Dev, compare, to_np
 
 pytestmark = pytest.mark.gpu
+
+
+def test_wait_limit_is_settable():
+    """With the limit lowered to 50 ms the never-completed wait gives up in well under the default second; the
+    default is restored afterwards."""
+    import torch
+    import lora_co_serving_gb300 as lm
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lm.build()
+    lib = lm.library()
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    try:
+        lm.set_wait_limit(0.05)
+        t0 = time.perf_counter()
+        assert lib.lora_selftest_wait_timeout(ws.data_ptr(), ws.numel(), stream) == 0
+        rc = lib.lora_workspace_status(ws.data_ptr(), stream)
+        spent = time.perf_counter() - t0
+    finally:
+        lm.set_wait_limit(1.0)
+    assert rc == -11, rc                                   # LORA_ERR_TIMEOUT
+    assert 0.04 < spent < 0.5, spent
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
