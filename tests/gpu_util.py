@@ -74,7 +74,9 @@ def grad_split_table(seed=4242, K=320, N=384, sliced=False):
     cross segment boundaries), adapter 1 (rank 40) on one of 1600 tokens (25 blocks); decode, prefill and
     base-only rows of other adapters sit between them.  12 gradient items (dB: 3 column tiles, dA: 3 row tiles per
     adapter) -> 36 split items.  sliced: the same table on a sliced layer of K = 256 and the three slices of
-    SPLIT_BOUNDS (dB: 5 column tiles over the slices, dA: 2 row tiles per adapter) -> 42 split items."""
+    SPLIT_BOUNDS, adapter 0 of rank 128 so that its three stacked down factors (384 rank rows) span two dA items
+    per row tile (dB: 5 column tiles over the slices; dA: 2 row tiles x 2 rank ranges for adapter 0, x 1 for
+    adapter 1) -> 16 items, 48 split items."""
     spans = [(700, 0, 1), (5, 2, 0), (333, 0, 1), (90, 3, 0), (1, 4, 0), (1600, 1, 1), (40, -1, 0), (1100, 0, 1),
              (1, 5, 0)]
     segs, t = [], 0
@@ -83,5 +85,6 @@ def grad_split_table(seed=4242, K=320, N=384, sliced=False):
         t += ln
     rank = [24, 40, 8, 16, 64, 128]
     if sliced:
+        rank[0] = 128
         return workloads.sliced(seed, t, 256, np.asarray(SPLIT_BOUNDS, np.int32), segs, rank)
     return workloads.custom(seed, t, K, N, segs, rank)

@@ -159,7 +159,8 @@ def test_sliced_gate_up_and_wide_ranks(bounds, r):
 
 def test_sliced_split_gradients():
     """Gradient items of a three-slice layer split three ways along the tokens (pinned on the host), splits
-    crossing segment boundaries: dX, dA (every slice's down factor), dB against the sliced oracle."""
+    crossing segment boundaries, one adapter's 384 stacked rank rows over two dA items: dX, dA (every slice's
+    down factor), dB against the sliced oracle."""
     from gpu_util import grad_split_table
     wl = grad_split_table(sliced=True)
     check_backward(wl, Dev(wl))

@@ -155,7 +155,7 @@ def test_planted_planner_mistake_is_reported(tmp_path, name, orig, bad, table, b
 
 @pytest.mark.parametrize("sliced", [False, True], ids=["plain", "sliced"])
 def test_gradient_items_split_three_ways(tmp_path, sliced):
-    """The tables of the GPU tests of split gradients do split: 12 gradient items (14 on the sliced layer), each
+    """The tables of the GPU tests of split gradients do split: 12 gradient items (16 on the sliced layer), each
     into 3 token ranges (the shortest group has 25 token blocks; 4 ways would leave splits under 8 blocks)."""
     lib = _build_driver(tmp_path, open(os.path.join(CSRC, "plan.cpp")).read())
     wl = grad_split_table(sliced=sliced)
@@ -163,7 +163,7 @@ def test_gradient_items_split_three_ways(tmp_path, sliced):
     segs = lm.segments(wl.segs)
     sl = lm.Slices(wl.bounds) if sliced else None
     n = lib.grad_items(wl.T, wl.K, wl.N, pool.cptr(), sl.cptr() if sl else None, segs.ctypes.data, segs.shape[0])
-    assert n == (42 if sliced else 36)
+    assert n == (48 if sliced else 36)
     if not sliced:
         assert lib.check_table(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0], 1) == 0
     else:
