@@ -383,7 +383,23 @@ struct Prepared {
     std::vector<int32_t> off[3], lst[3];
     int grid[3] = {0, 0, 0};
     std::vector<uint8_t> blob;
+    // The launch parameters (tensor maps and pointers) of the last call made with this plan, and the pointers and
+    // flags they were built from: a call that repeats them copies the parameters instead of encoding every tensor
+    // map again (a dozen or more driver calls per call).
+    std::unique_ptr<KParams> params;
+    std::vector<uintptr_t> params_key;
 };
+
+// The cached launch parameters of `pr` when they were built from `key`, else null (the caller builds them and
+// keeps them with keep_params).
+const KParams* cached_params(const Prepared* pr, const std::vector<uintptr_t>& key) {
+    return (pr->params && pr->params_key == key) ? pr->params.get() : nullptr;
+}
+void keep_params(Prepared* pr, const KParams& P, std::vector<uintptr_t>&& key) {
+    if (!pr->params) pr->params.reset(new KParams);
+    *pr->params = P;
+    pr->params_key = std::move(key);
+}
 constexpr size_t kPlanCacheEntries = 8;
 thread_local std::list<std::unique_ptr<Prepared>> g_plans;
 
@@ -603,6 +619,47 @@ int lora_plan_describe(int32_t T, int32_t K, int32_t N, const lora_pool_t* pool,
 
 namespace {
 
+// The forward's launch parameters: tensor maps of x, the gathered rows, W, Z, the pools and y, and the pointers the
+// kernels use.  LORA_OK, LORA_ERR_CUDA (a tensor map the driver refused) or a LORA_DEBUG_CHECKS plan error.
+int forward_params(int32_t T, int32_t K, int32_t N, const void* x, const void* Wt, const lora_pool_t* pool,
+                   const Problem& p, const Plan& pl, const Layout& L, uint8_t* ws, void* y, bool save, void* xa_save,
+                   uint32_t flags, KParams* out, std::string* err) {
+    KParams& P = *out;
+    std::memset(&P, 0, sizeof(P));
+    if (!encode_2d(&P.tm_x, x, K, T, K, 64, 128, err)) return LORA_ERR_CUDA;
+    if (pl.n_gtiles > 0 && !encode_2d(&P.tm_xg, ws + L.xg, K, (uint64_t)pl.n_gtiles * kTileM, K, 64, 128, err))
+        return LORA_ERR_CUDA;
+    if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 128, err)) return LORA_ERR_CUDA;
+    if (pl.z_blocks > 0 &&
+        !encode_2d(&P.tm_z, ws + L.z, 64, (uint64_t)pl.z_blocks * kTileM, 64, 64, 128, err, false))
+        return LORA_ERR_CUDA;
+    if (p.rows_a > 0 && !encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, err)) return LORA_ERR_CUDA;
+    if (p.rows_b > 0 && !encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, err)) return LORA_ERR_CUDA;
+    for (int h = 0; h < 3; ++h) {      // taller boxes for runs of consecutive atoms (shrink: A rows; main: B rows)
+        if (p.rows_a > 0 && !encode_2d(&P.tm_pa_h[h], pool->A, K, p.rows_a, K, 64, 16u << h, err))
+            return LORA_ERR_CUDA;
+        if (p.rows_b > 0 && !encode_2d(&P.tm_pb_h[h], pool->B, N, p.rows_b, N, 64, 16u << h, err))
+            return LORA_ERR_CUDA;
+    }
+    P.zin = ws + L.z;
+    P.zout = ws + L.z;
+    P.out = static_cast<__nv_bfloat16*>(y);
+    P.out_ld = N;
+    P.out_cols = N;
+    if (!encode_out(&P.tm_out, y, N, T, N, err)) return LORA_ERR_CUDA;
+    P.xa_save = save ? static_cast<__nv_bfloat16*>(xa_save) : nullptr;
+    P.K = K;
+    P.N = N;
+    if (flags & LORA_DEBUG_CHECKS) {
+        const int rc = check_plan(p, pl, false, err);
+        if (rc != LORA_OK) return rc;
+        P.debug = 1;
+        P.db = DebugBounds{T, pl.z_blocks, save ? p.xa_elems : 0, 0, pl.part_cols * kTileM, pl.main_slots, 0, 0, T,
+                           (int64_t)pl.n_gtiles * kTileM};
+    }
+    return LORA_OK;
+}
+
 // The forward of lora_mixed_forward and lora_sliced_forward (slices: NULL = one slice).
 int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x, const void* Wt,
                  const lora_pool_t* pool, const lora_slices_t* slices, const lora_segment_t* segs, int32_t n_segs,
@@ -670,41 +727,17 @@ int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     KParams P;
-    std::memset(&P, 0, sizeof(P));
-    if (!encode_2d(&P.tm_x, x, K, T, K, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
-    if (pl.n_gtiles > 0 && !encode_2d(&P.tm_xg, ws + L.xg, K, (uint64_t)pl.n_gtiles * kTileM, K, 64, 128, &err))
-        return fail(LORA_ERR_CUDA, err);
-    if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
-    if (pl.z_blocks > 0 &&
-        !encode_2d(&P.tm_z, ws + L.z, 64, (uint64_t)pl.z_blocks * kTileM, 64, 64, 128, &err, false))
-        return fail(LORA_ERR_CUDA, err);
-    if (p.rows_a > 0 && !encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    if (p.rows_b > 0 && !encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    for (int h = 0; h < 3; ++h) {      // taller boxes for runs of consecutive atoms (shrink: A rows; main: B rows)
-        if (p.rows_a > 0 && !encode_2d(&P.tm_pa_h[h], pool->A, K, p.rows_a, K, 64, 16u << h, &err))
-            return fail(LORA_ERR_CUDA, err);
-        if (p.rows_b > 0 && !encode_2d(&P.tm_pb_h[h], pool->B, N, p.rows_b, N, 64, 16u << h, &err))
-            return fail(LORA_ERR_CUDA, err);
-    }
-    P.zin = ws + L.z;
-    P.zout = ws + L.z;
-    P.out = static_cast<__nv_bfloat16*>(y);
-    P.out_ld = N;
-    P.out_cols = N;
-    if (!encode_out(&P.tm_out, y, N, T, N, &err)) return fail(LORA_ERR_CUDA, err);
-    P.xa_save = save ? static_cast<__nv_bfloat16*>(xa_save) : nullptr;
-    P.K = K;
-    P.N = N;
-    SimtDebug dbg{};
-    if (flags & LORA_DEBUG_CHECKS) {
-        rc = check_plan(p, pl, false, &err);
+    std::vector<uintptr_t> key = {uintptr_t(x), uintptr_t(Wt), uintptr_t(pool->A), uintptr_t(pool->B),
+                                  uintptr_t(workspace), uintptr_t(y), uintptr_t(save ? xa_save : nullptr), flags};
+    if (const KParams* c = cached_params(pr, key)) {
+        P = *c;
+    } else {
+        rc = forward_params(T, K, N, x, Wt, pool, p, pl, L, ws, y, save, xa_save, flags, &P, &err);
         if (rc != LORA_OK) return fail(rc, err);
-        P.debug = 1;
-        P.db = DebugBounds{T, pl.z_blocks, save ? p.xa_elems : 0, 0, pl.part_cols * kTileM, pl.main_slots, 0, 0, T,
-                           (int64_t)pl.n_gtiles * kTileM};
+        keep_params(pr, P, std::move(key));
     }
-    dbg = SimtDebug{P.debug, reinterpret_cast<int32_t*>(ws + L.status), T, (int64_t)pl.n_gtiles * kTileM, pl.z_blocks,
-                    P.db.xa_elems, 0};
+    const SimtDebug dbg{P.debug, reinterpret_cast<int32_t*>(ws + L.status), T, (int64_t)pl.n_gtiles * kTileM,
+                        pl.z_blocks, P.db.xa_elems, 0};
 
     rc = begin_call(L, pl, workspace, blob.size(), blob.data(), stream);
     if (rc) return rc;
@@ -722,6 +755,64 @@ int forward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* x
     CUDA_TRY(launch_group(1, &P, ws, L, grid, stream));
     CUDA_TRY(launch_reduce(pl, P, ws, L, stream));
     CUDA_TRY(trace(1, 1, stream));
+    return LORA_OK;
+}
+
+// The backward's launch parameters: tensor maps of x, dY, W, the pools, the transposed xA / dYB buffers, Z, every
+// fine-tuning segment's rows of x and dY and dX, and the pointers the kernels use.  LORA_OK, LORA_ERR_CUDA (a tensor
+// map the driver refused) or a LORA_DEBUG_CHECKS plan error.
+int backward_params(int32_t T, int32_t K, int32_t N, const void* x, const void* Wt, const lora_pool_t* pool,
+                    const void* dY, void* dX, float* dA, float* dB, bool acc, bool recompute, bool per_segment,
+                    const Problem& p, const Plan& pl, const Layout& L, uint8_t* ws, uint32_t flags, KParams* out,
+                    std::string* err) {
+    KParams& P = *out;
+    std::memset(&P, 0, sizeof(P));
+    const uint64_t Pcols = (uint64_t)pl.tcols;
+    if (!encode_2d(&P.tm_x, x, K, T, K, 64, 128, err)) return LORA_ERR_CUDA;
+    if (!encode_2d(&P.tm_dy, dY, N, T, N, 64, 128, err)) return LORA_ERR_CUDA;
+    if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 64, err)) return LORA_ERR_CUDA;
+    P.w3 = (LORA_W3 && encode_w3(&P.tm_w3, Wt, K, N)) ? 1 : 0;      // else two 2-D boxes per stage
+    if (!encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, err)) return LORA_ERR_CUDA;
+    if (!encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, err)) return LORA_ERR_CUDA;
+    for (int h = 0; h < 3; ++h) {      // taller boxes for runs of consecutive atoms (shrinks and the dX pass)
+        if (!encode_2d(&P.tm_pa_h[h], pool->A, K, p.rows_a, K, 64, 16u << h, err)) return LORA_ERR_CUDA;
+        if (!encode_2d(&P.tm_pb_h[h], pool->B, N, p.rows_b, N, 64, 16u << h, err)) return LORA_ERR_CUDA;
+    }
+    const uint64_t trows = (uint64_t)p.S * LORA_MAX_RANK;
+    if (!encode_2d(&P.tm_xat, ws + L.xat, Pcols, trows, Pcols, 64, 8, err)) return LORA_ERR_CUDA;
+    if (!encode_2d(&P.tm_dybt, ws + L.dybt, Pcols, trows, Pcols, 64, 8, err)) return LORA_ERR_CUDA;
+    if (pl.z_blocks > 0 &&
+        !encode_2d(&P.tm_z, ws + L.z, 64, (uint64_t)pl.z_blocks * kTileM, 64, 64, 128, err, false))
+        return LORA_ERR_CUDA;
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    const __nv_bfloat16* db = static_cast<const __nv_bfloat16*>(dY);
+    for (size_t q = 0; q < pl.tsegs.size(); ++q) {
+        const TrainSeg& s = pl.tsegs[q];
+        if (!encode_2d(&P.tm_seg_dy[q], db + (size_t)s.start * N, N, s.len, N, 64, 64, err)) return LORA_ERR_CUDA;
+        if (!encode_2d(&P.tm_seg_x[q], xb + (size_t)s.start * K, K, s.len, K, 64, 64, err)) return LORA_ERR_CUDA;
+    }
+    P.zin = ws + L.z;
+    P.zout = ws + L.z;
+    P.out = static_cast<__nv_bfloat16*>(dX);
+    P.out_ld = K;
+    P.out_cols = K;
+    if (dX != nullptr && !encode_out(&P.tm_out, dX, K, T, K, err)) return LORA_ERR_CUDA;
+    P.xat = reinterpret_cast<__nv_bfloat16*>(ws + L.xat);
+    P.dybt = reinterpret_cast<__nv_bfloat16*>(ws + L.dybt);
+    P.t_ld = int32_t(Pcols);
+    P.dA = dA;
+    P.dB = dB;
+    P.K = K;
+    P.N = N;
+    P.accumulate = acc ? 1 : 0;
+    P.seg_flags = per_segment ? reinterpret_cast<const int32_t*>(ws + L.seg_flags) : nullptr;
+    if (flags & LORA_DEBUG_CHECKS) {
+        const int rc = check_plan(p, pl, true, err);
+        if (rc != LORA_OK) return rc;
+        P.debug = 1;
+        P.db = DebugBounds{T, pl.z_blocks, recompute ? 0 : p.xa_elems, (int64_t)p.S * LORA_MAX_RANK * pl.tcols,
+                           pl.part_cols * kTileM, pl.main_slots, p.rows_a * K, p.rows_b * N, T, 0};
+    }
     return LORA_OK;
 }
 
@@ -829,55 +920,21 @@ int backward_impl(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const void* 
     const std::vector<uint8_t>& blob = pr->blob;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    KParams P;
-    std::memset(&P, 0, sizeof(P));
     const uint64_t Pcols = (uint64_t)pl.tcols;
-    if (!encode_2d(&P.tm_x, x, K, T, K, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
-    if (!encode_2d(&P.tm_dy, dY, N, T, N, 64, 128, &err)) return fail(LORA_ERR_CUDA, err);
-    if (!encode_2d(&P.tm_w, Wt, K, N, K, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
-    P.w3 = (LORA_W3 && encode_w3(&P.tm_w3, Wt, K, N)) ? 1 : 0;      // else two 2-D boxes per stage
-    if (!encode_2d(&P.tm_pa, pool->A, K, p.rows_a, K, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    if (!encode_2d(&P.tm_pb, pool->B, N, p.rows_b, N, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    for (int h = 0; h < 3; ++h) {      // taller boxes for runs of consecutive atoms (shrinks and the dX pass)
-        if (!encode_2d(&P.tm_pa_h[h], pool->A, K, p.rows_a, K, 64, 16u << h, &err)) return fail(LORA_ERR_CUDA, err);
-        if (!encode_2d(&P.tm_pb_h[h], pool->B, N, p.rows_b, N, 64, 16u << h, &err)) return fail(LORA_ERR_CUDA, err);
-    }
-    const uint64_t trows = (uint64_t)p.S * LORA_MAX_RANK;
-    if (!encode_2d(&P.tm_xat, ws + L.xat, Pcols, trows, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    if (!encode_2d(&P.tm_dybt, ws + L.dybt, Pcols, trows, Pcols, 64, 8, &err)) return fail(LORA_ERR_CUDA, err);
-    if (pl.z_blocks > 0 &&
-        !encode_2d(&P.tm_z, ws + L.z, 64, (uint64_t)pl.z_blocks * kTileM, 64, 64, 128, &err, false))
-        return fail(LORA_ERR_CUDA, err);
-    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    const __nv_bfloat16* db = static_cast<const __nv_bfloat16*>(dY);
     int32_t max_len = 0;
-    for (size_t q = 0; q < pl.tsegs.size(); ++q) {
-        const TrainSeg& s = pl.tsegs[q];
-        max_len = std::max(max_len, s.len);
-        if (!encode_2d(&P.tm_seg_dy[q], db + (size_t)s.start * N, N, s.len, N, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
-        if (!encode_2d(&P.tm_seg_x[q], xb + (size_t)s.start * K, K, s.len, K, 64, 64, &err)) return fail(LORA_ERR_CUDA, err);
-    }
-    P.zin = ws + L.z;
-    P.zout = ws + L.z;
-    P.out = static_cast<__nv_bfloat16*>(dX);
-    P.out_ld = K;
-    P.out_cols = K;
-    if (dX != nullptr && !encode_out(&P.tm_out, dX, K, T, K, &err)) return fail(LORA_ERR_CUDA, err);
-    P.xat = reinterpret_cast<__nv_bfloat16*>(ws + L.xat);
-    P.dybt = reinterpret_cast<__nv_bfloat16*>(ws + L.dybt);
-    P.t_ld = int32_t(Pcols);
-    P.dA = dA;
-    P.dB = dB;
-    P.K = K;
-    P.N = N;
-    P.accumulate = acc ? 1 : 0;
-    P.seg_flags = per_segment ? reinterpret_cast<const int32_t*>(ws + L.seg_flags) : nullptr;
-    if (flags & LORA_DEBUG_CHECKS) {
-        rc = check_plan(p, pl, true, &err);
+    for (const TrainSeg& s : pl.tsegs) max_len = std::max(max_len, s.len);
+    KParams P;
+    std::vector<uintptr_t> key = {uintptr_t(x),  uintptr_t(Wt), uintptr_t(pool->A),  uintptr_t(pool->B),
+                                  uintptr_t(dY), uintptr_t(dX), uintptr_t(dA),       uintptr_t(dB),
+                                  uintptr_t(workspace), flags, uintptr_t(acc), uintptr_t(recompute),
+                                  uintptr_t(per_segment)};
+    if (const KParams* c = cached_params(pr, key)) {
+        P = *c;
+    } else {
+        rc = backward_params(T, K, N, x, Wt, pool, dY, dX, dA, dB, acc, recompute, per_segment, p, pl, L, ws, flags,
+                             &P, &err);
         if (rc != LORA_OK) return fail(rc, err);
-        P.debug = 1;
-        P.db = DebugBounds{T, pl.z_blocks, recompute ? 0 : p.xa_elems, (int64_t)p.S * LORA_MAX_RANK * pl.tcols,
-                           pl.part_cols * kTileM, pl.main_slots, p.rows_a * K, p.rows_b * N, T, 0};
+        keep_params(pr, P, std::move(key));
     }
     const SimtDebug dbg{P.debug, reinterpret_cast<int32_t*>(ws + L.status), T, 0, pl.z_blocks, P.db.xa_elems,
                         P.db.t_elems};
