@@ -42,6 +42,10 @@ static_assert(2 * kSubBytes <= kStageBytes, "two k-blocks must fit a stage");
 #ifndef LORA_SHRINK_PACK
 #define LORA_SHRINK_PACK 1
 #endif
+// 16-column groups a split finalize loads per round (1 or 2)
+#ifndef LORA_FINALIZE_GROUPS
+#define LORA_FINALIZE_GROUPS 2
+#endif
 __device__ __forceinline__ int grad_blocks_per_stage(int mma_n) { return (LORA_GRAD_PACK && mma_n <= 64) ? 2 : 1; }
 __device__ __forceinline__ int shrink_blocks_per_stage(int mma_n) {
     return (LORA_SHRINK_PACK && mma_n <= 64) ? 2 : 1;
@@ -428,18 +432,20 @@ struct ShrinkRowOut {
     }
 };
 
-// Columns [c, c + 16) of one row of a split reduction: the sum, in split order, of the unit's fp32 partials
-// (p0: the row's first 4-column group of split 0; split s sits u.mma_n columns further per split).  The splits'
-// 16-column groups are loaded four splits at a time (16 loads of 16 bytes in flight per thread), then added.
-__device__ __forceinline__ void sum_split_partials(const float* p0, const ShrinkUnit& u, int c, float (&v)[16]) {
+// Columns [c, c + 16 G) of one row of a split reduction: the sum, in split order, of the unit's fp32 partials
+// (p0: the row's first 4-column group of split 0; split s sits u.mma_n columns further per split).  Four splits'
+// G 16-column groups are loaded (16 G loads of 16 bytes in flight per thread: the finalize is bound by L2 latency)
+// before they are added.
+template <int G>
+__device__ __forceinline__ void sum_split_partials(const float* p0, const ShrinkUnit& u, int c, float (&v)[16 * G]) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    for (int i = 0; i < 16 * G; ++i) v[i] = 0.f;
     for (int s0 = 0; s0 < u.nsplit; s0 += 4) {
-        float4 a[4][4];
+        float4 a[4][4 * G];
 #pragma unroll
         for (int sp = 0; sp < 4; ++sp)
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 4 * G; ++q)
                 a[sp][q] = (s0 + sp < u.nsplit)
                                ? __ldcg(reinterpret_cast<const float4*>(p0 + ((size_t)(s0 + sp) * u.mma_n + c + 4 * q) *
                                                                                   kTileM))
@@ -448,13 +454,31 @@ __device__ __forceinline__ void sum_split_partials(const float* p0, const Shrink
         for (int sp = 0; sp < 4; ++sp) {
             if (s0 + sp >= u.nsplit) break;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 4 * G; ++q) {
                 v[4 * q] += a[sp][q].x;
                 v[4 * q + 1] += a[sp][q].y;
                 v[4 * q + 2] += a[sp][q].z;
                 v[4 * q + 3] += a[sp][q].w;
             }
         }
+    }
+}
+
+// The finalize of a split unit's row: the split sums of columns [0, mma_n), handed to put(c, v) 16 columns at a time
+// (two 16-column groups per round of loads where there are two)
+template <class Put>
+__device__ __forceinline__ void finalize_row(const float* p0, const ShrinkUnit& u, int mma_n, Put&& put) {
+    int c = 0;
+    for (; LORA_FINALIZE_GROUPS > 1 && c + 32 <= mma_n; c += 32) {
+        float v[32];
+        sum_split_partials<2>(p0, u, c, v);
+        put(c, *reinterpret_cast<const float(*)[16]>(&v[0]));
+        put(c + 16, *reinterpret_cast<const float(*)[16]>(&v[16]));
+    }
+    for (; c < mma_n; c += 16) {
+        float v[16];
+        sum_split_partials<1>(p0, u, c, v);
+        put(c, v);
     }
 }
 
@@ -543,11 +567,7 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                 if (last && part_ok) {
                     __threadfence();
                     const float* p0 = P.part + (size_t)u.part0 * kTileM + row * 4;
-                    for (int c = 0; c < w.mma_n; c += 16) {
-                        float v[16];
-                        sum_split_partials(p0, u, c, v);
-                        put16(c, v);
-                    }
+                    finalize_row(p0, u, w.mma_n, put16);
                     __syncwarp();
                     if (lane == 0) *cnt = 0;              // ready for the next call on this workspace
                 }
@@ -588,11 +608,7 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
                     __threadfence();
                     ShrinkRowOut out(P, u, row);
                     const float* p0 = P.part + (size_t)u.part0 * kTileM + row * 4;
-                    for (int c = 0; c < w.mma_n; c += 16) {
-                        float v[16];
-                        sum_split_partials(p0, u, c, v);
-                        out.put16(c, v);
-                    }
+                    finalize_row(p0, u, w.mma_n, [&](int c, const float (&v)[16]) { out.put16(c, v); });
                     __syncwarp();
                     if (lane == 0) *cnt = 0;              // ready for the next call on this workspace
                 }
