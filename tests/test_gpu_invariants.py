@@ -190,3 +190,31 @@ def test_empty_batch_is_a_no_op():
     dX, dA, dB = d.backward()
     torch.cuda.synchronize()
     assert np.all(to_np(dA) == 0)
+
+
+def test_launch_parameters_follow_each_call():
+    """Launch parameters kept from a call are reused only when a call repeats its pointers: alternating outputs and
+    inputs on one workspace and plan give each call its own result, and a call with the same pointers sees new
+    contents.  Scaling x by a power of two scales y exactly (every rounding step scales with it)."""
+    import torch
+    import lora_co_serving_gb300 as lm
+    wl = mixed_small(seed=91)
+    d = Dev(wl)
+    ws = torch.empty(lm.workspace_size(wl.T, wl.K, wl.N, 0, d.pool, wl.segs), dtype=torch.uint8, device="cuda")
+    yA = torch.empty((wl.T, wl.N), dtype=torch.bfloat16, device="cuda")
+    yB = torch.empty_like(yA)
+    x2 = d.x * 0.5
+    lm.forward(d.x, d.Wt, d.pool, wl.segs, y=yA, workspace=ws)
+    ref = yA.clone()
+    lm.forward(x2, d.Wt, d.pool, wl.segs, y=yB, workspace=ws)
+    assert torch.equal(yB, ref * 0.5)
+    lm.forward(d.x, d.Wt, d.pool, wl.segs, y=yA, workspace=ws)
+    assert torch.equal(yA, ref)
+    d.x.mul_(2.0)                                # same pointers, new contents
+    lm.forward(d.x, d.Wt, d.pool, wl.segs, y=yA, workspace=ws)
+    assert torch.equal(yA, ref * 2.0)
+    # the backward likewise: dX and dA scale with dY, dB with x
+    gA = [t.clone() for t in lm.backward(d.x, d.Wt, d.pool, wl.segs, d.dY, workspace=ws)]
+    gB = lm.backward(d.x, d.Wt, d.pool, wl.segs, d.dY * 0.25, workspace=ws)
+    for a, b in zip(gA, gB):
+        assert torch.equal(b, a * 0.25)
