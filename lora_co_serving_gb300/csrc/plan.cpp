@@ -2,6 +2,8 @@
 #include "plan.h"
 
 #include <algorithm>
+#include <cstdint>
+#include <functional>
 #include <cstring>
 #include <iterator>
 #include <utility>
@@ -11,6 +13,7 @@ namespace lora {
 static inline int32_t pad16(int32_t r) { return (r + 15) & ~15; }
 static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+static int64_t item_cost(const WorkItem& w);
 
 int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t* pool, const lora_segment_t* segs,
              int32_t n_segs, Problem* out, std::string* err, const lora_slices_t* slices) {
@@ -237,9 +240,10 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
 
 // Shrink items of one pass, split along the reduction at boundaries that depend on the k-block count alone.
 // kb_first: first k-block of the reduction (a slice's output columns, for the backward shrink over N).
+// nsplit: the number of splits (0: as many as the default split length for the call's token count gives).
 static void add_shrink(Plan* pl, int32_t kind, int32_t tile, int32_t n0, int32_t mma_n, int32_t nk,
-                       int32_t kb_first = 0) {
-    const int32_t nsplit = std::max<int32_t>(1, int32_t(cdiv(nk, shrink_split_kb(pl->T))));
+                       int32_t kb_first = 0, int32_t nsplit = 0) {
+    if (nsplit <= 0) nsplit = std::max<int32_t>(1, int32_t(cdiv(nk, shrink_split_kb(pl->T))));
     ShrinkUnit u{};
     u.kind = kind; u.tile = tile; u.n0 = n0; u.mma_n = mma_n; u.nsplit = nsplit;
     u.part0 = int32_t(pl->part_cols);
@@ -589,25 +593,83 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
     }
     const bool need_dyb = want_dx || want_da;
     const bool need_xa = want_db && (recompute || per_segment);
+    // The backward shrink passes in launch order: per tile its dY B^T passes (one per slice), then its x A passes.
+    struct Pass {
+        int32_t kind, tile, n0, mma_n, nk, kb_first;
+    };
+    std::vector<Pass> passes;
     for (size_t ti = 0; ti < pl.tiles.size(); ++ti) {
         const TileDesc& td = pl.tiles[ti];
         if (td.sh_c1 <= td.sh_c0) continue;      // the empty second tile of a short segment's pair
         if (need_dyb) {
             if (p.S == 1) {
-                add_shrink(&pl, kShrinkDyb, int32_t(ti), td.sh_c0, td.sh_c1 - td.sh_c0, int32_t(cdiv(p.N, kBK)));
+                passes.push_back({kShrinkDyb, int32_t(ti), td.sh_c0, td.sh_c1 - td.sh_c0, int32_t(cdiv(p.N, kBK)), 0});
             } else {
                 // slice i: dY's slice-i columns against the up factor's slice-i columns, into LoRA columns
                 // [i rp, (i+1) rp)
                 for (int32_t i = 0; i < p.S; ++i) {
                     const int32_t kb_a = p.bounds[i] / kBK, kb_b = int32_t(cdiv(p.bounds[i + 1], kBK));
-                    add_shrink(&pl, kShrinkDyb, int32_t(ti), i * td.zstride, td.zstride, kb_b - kb_a, kb_a);
+                    passes.push_back({kShrinkDyb, int32_t(ti), i * td.zstride, td.zstride, kb_b - kb_a, kb_a});
                 }
             }
         }
         if (need_xa)
             for (int32_t c0 = td.sh_c0; c0 < td.sh_c1; c0 += kPassCols)
-                add_shrink(&pl, kShrinkXa, int32_t(ti), c0, std::min(kPassCols, td.sh_c1 - c0), int32_t(cdiv(p.K, kBK)));
+                passes.push_back({kShrinkXa, int32_t(ti), c0, std::min(kPassCols, td.sh_c1 - c0),
+                                  int32_t(cdiv(p.K, kBK)), 0});
     }
+    // The x A passes keep the forward's splits, so that a recomputed xA equals the saved one bit for bit.  The
+    // dY B^T passes of an unsliced layer (all of one length) take the split count, from half to twice the
+    // default, whose greedy list schedule of the whole launch on 2 x kPairsPlanned CTAs ends first by the items'
+    // estimated costs, the default on a tie (waves of equal items can leave a nearly empty last wave: 320 items
+    // of 16 k-blocks on 152 CTAs end after 48 k-blocks, 288 with the dY B^T passes in 20-k-block pieces after
+    // 40).  It depends on the passes' shapes alone, not on the segment or pool order.
+    const int32_t kb_default = shrink_split_kb(p.T);
+    const int64_t G = 2 * kPairsPlanned;
+    auto default_splits = [&](int32_t nk) { return std::max<int32_t>(1, int32_t(cdiv(nk, kb_default))); };
+    auto n_items = [&](int32_t dyb_splits) {
+        int64_t n = 0;
+        for (const Pass& ps : passes) n += (ps.kind == kShrinkDyb) ? dyb_splits : default_splits(ps.nk);
+        return n;
+    };
+    // the end of the greedy schedule, or `bound` as soon as a CTA's load reaches it
+    std::vector<int64_t> load(G);
+    auto schedule_end = [&](int32_t dyb_splits, int64_t bound) {
+        std::fill(load.begin(), load.end(), 0);     // a min-heap of CTA loads
+        for (const Pass& ps : passes) {
+            const int32_t ns = (ps.kind == kShrinkDyb) ? dyb_splits : default_splits(ps.nk);
+            for (int32_t sp = 0; sp < ns; ++sp) {
+                WorkItem w{};
+                w.kind = ps.kind; w.mma_n = ps.mma_n;
+                w.nk = int32_t((int64_t)(sp + 1) * ps.nk / ns - (int64_t)sp * ps.nk / ns);
+                std::pop_heap(load.begin(), load.end(), std::greater<int64_t>());
+                load.back() += item_cost(w);
+                if (load.back() >= bound) return bound;
+                std::push_heap(load.begin(), load.end(), std::greater<int64_t>());
+            }
+        }
+        return *std::max_element(load.begin(), load.end());
+    };
+    int32_t dyb_splits = 0;                  // 0: the default
+    if (need_dyb && p.S == 1 && !passes.empty()) {
+        const int32_t nk = int32_t(cdiv(p.N, kBK)), s0 = default_splits(nk);
+        // searched only when the default's last wave is less than half full, among the two counts whose last
+        // waves are fullest (the fewer items first on a tie)
+        auto fill = [&](int32_t ns) { const int64_t r = n_items(ns) % G; return r == 0 ? G : r; };
+        if (2 * fill(s0) < G) {
+            std::vector<std::pair<int64_t, int32_t>> cand;     // (-fill, count)
+            for (int32_t ns = std::max(1, s0 / 2); ns <= std::min(2 * s0, std::max(1, nk / 4)); ++ns)
+                if (ns != s0) cand.push_back({-fill(ns), ns});
+            std::sort(cand.begin(), cand.end());
+            int64_t best = schedule_end(s0, INT64_MAX);
+            for (size_t i = 0; i < cand.size() && i < 2; ++i) {
+                const int64_t e = schedule_end(cand[i].second, best);
+                if (e < best) { best = e; dyb_splits = cand[i].second; }
+            }
+        }
+    }
+    for (const Pass& ps : passes)
+        add_shrink(&pl, ps.kind, ps.tile, ps.n0, ps.mma_n, ps.nk, ps.kb_first, ps.kind == kShrinkDyb ? dyb_splits : 0);
     if (want_dx)
         add_main_items(&pl, kMainDx, int32_t(cdiv(p.K, kBN)), int32_t(cdiv(p.N, kBK)), pl.tiles.size() / 2,
                        [](size_t q, int32_t) { return int32_t(2 * q); });

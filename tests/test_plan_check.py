@@ -110,6 +110,18 @@ extern "C" int grad_items(int T, int K, int N, const lora_pool_t* pool, const lo
     lora::plan_backward(p, true, true, true, true, &pl);
     return int(pl.items[2].size());
 }
+// backward shrink items: out[0] of the dY B^T passes, out[1] of the x A recompute (-1: the table does not validate)
+extern "C" int bwd_shrink_items(int T, int K, int N, const lora_pool_t* pool, const lora_segment_t* segs, int n,
+                                int* out) {
+    lora::Problem p;
+    std::string err;
+    if (lora::validate(T, K, N, LORA_BF16, pool, segs, n, &p, &err)) return -1;
+    lora::Plan pl;
+    lora::plan_backward(p, true, true, true, true, &pl);
+    out[0] = out[1] = 0;
+    for (const lora::WorkItem& w : pl.items[0]) out[w.kind == lora::kShrinkDyb ? 0 : 1]++;
+    return 0;
+}
 '''
 
 def _build_driver(tmp_path, src):
@@ -124,6 +136,7 @@ def _build_driver(tmp_path, src):
     lib = ctypes.CDLL(so)
     lib.check_table.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
     lib.grad_items.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3 + [ctypes.c_int]
+    lib.bwd_shrink_items.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_void_p]
     return lib
 
 
@@ -168,3 +181,35 @@ def test_gradient_items_split_three_ways(tmp_path, sliced):
         assert lib.check_table(wl.T, wl.K, wl.N, pool.cptr(), segs.ctypes.data, segs.shape[0], 1) == 0
     else:
         lm.plan_check(wl.T, wl.K, wl.N, pool, wl.segs, backward=True, bounds=wl.bounds)
+
+
+def _table_pool(K, N, rank):
+    rank = np.asarray(rank, np.int32)
+    a_off, b_off = workloads._pool_offsets(rank, K, N)
+    return lm.Pool(None, None, a_off, b_off, rank, np.full(rank.shape, 2.0, np.float32))
+
+
+@pytest.mark.parametrize("case", ["ftbwd_5120", "ftbwd_5120_reordered", "cosrv_8192x28672"])
+def test_backward_shrink_split_fills_waves(tmp_path, case):
+    """The dY B^T passes of the backward shrink take the split count whose schedule ends first: on the 5120^2
+    fine-tuning batch (32 tiles, 80 k-blocks a pass) 4 pieces of 20 k-blocks instead of 5 of 16 (288 items on 152
+    CTAs: two waves, against 320, whose third wave holds 16 items), the same whatever the segment order; the x A
+    recompute keeps the forward's 5 splits.  On the co-serving batch's fine-tuning rows (16 tiles, 448 k-blocks
+    a pass) the default 14 splits already fill two waves and stay."""
+    lib = _build_driver(tmp_path, open(os.path.join(CSRC, "plan.cpp")).read())
+    if case.startswith("ftbwd"):
+        K = N = 5120
+        segs = [(i * 1024, 1024, 0, 1) for i in range(4)]
+        if case.endswith("reordered"):
+            segs = segs[::-1]
+        T, rank, want = 4096, [16], (32 * 4, 32 * 5)
+    else:
+        K, N = 8192, 28672
+        segs = [(t, 1, t % 7, 0) for t in range(2048)] + [(2048, 4096, 3, 0), (6144, 1024, 5, 1), (7168, 1024, 5, 1)]
+        T, rank, want = 8192, [8, 16, 32, 64, 128, 64, 16], (16 * 14, 16 * 4)
+    pool = _table_pool(K, N, rank)
+    s = lm.segments(np.asarray(segs, np.int32))
+    out = (ctypes.c_int * 2)()
+    assert lib.bwd_shrink_items(T, K, N, pool.cptr(), s.ctypes.data, s.shape[0], out) == 0
+    assert (out[0], out[1]) == want
+    assert lib.check_table(T, K, N, pool.cptr(), s.ctypes.data, s.shape[0], 1) == 0
