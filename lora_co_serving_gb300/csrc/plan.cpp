@@ -619,11 +619,12 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
                                   int32_t(cdiv(p.K, kBK)), 0});
     }
     // The x A passes keep the forward's splits, so that a recomputed xA equals the saved one bit for bit.  The
-    // dY B^T passes of an unsliced layer (all of one length) take the split count, from half to twice the
-    // default, whose greedy list schedule of the whole launch on 2 x kPairsPlanned CTAs ends first by the items'
-    // estimated costs, the default on a tie (waves of equal items can leave a nearly empty last wave: 320 items
-    // of 16 k-blocks on 152 CTAs end after 48 k-blocks, 288 with the dY B^T passes in 20-k-block pieces after
-    // 40).  It depends on the passes' shapes alone, not on the segment or pool order.
+    // dY B^T passes of an unsliced layer (all of one length) may take another split count, from half to twice
+    // the default, when the default's items fill at least one wave of 2 x kPairsPlanned CTAs and leave the last
+    // one less than half full (320 items of 16 k-blocks on 152 CTAs end after 48 k-blocks; 288, with the dY B^T
+    // passes in 20-k-block pieces, after 40): the count whose greedy list schedule of the whole launch by the
+    // items' estimated costs ends first, if it ends before the default's.  It depends on the passes' shapes
+    // alone, not on the segment or pool order.
     const int32_t kb_default = shrink_split_kb(p.T);
     const int64_t G = 2 * kPairsPlanned;
     auto default_splits = [&](int32_t nk) { return std::max<int32_t>(1, int32_t(cdiv(nk, kb_default))); };
@@ -653,10 +654,10 @@ void plan_backward(const Problem& p, bool want_dx, bool want_da, bool want_db, b
     int32_t dyb_splits = 0;                  // 0: the default
     if (need_dyb && p.S == 1 && !passes.empty()) {
         const int32_t nk = int32_t(cdiv(p.N, kBK)), s0 = default_splits(nk);
-        // searched only when the default's last wave is less than half full, among the two counts whose last
-        // waves are fullest (the fewer items first on a tie)
+        // searched only when the default fills a wave and leaves the last one less than half full, among the
+        // two counts whose last waves are fullest (the fewer items first on a tie)
         auto fill = [&](int32_t ns) { const int64_t r = n_items(ns) % G; return r == 0 ? G : r; };
-        if (2 * fill(s0) < G) {
+        if (n_items(s0) >= G && 2 * fill(s0) < G) {
             std::vector<std::pair<int64_t, int32_t>> cand;     // (-fill, count)
             for (int32_t ns = std::max(1, s0 / 2); ns <= std::min(2 * s0, std::max(1, nk / 4)); ++ns)
                 if (ns != s0) cand.push_back({-fill(ns), ns});

@@ -88,3 +88,8 @@ def grad_split_table(seed=4242, K=320, N=384, sliced=False):
         rank[0] = 128
         return workloads.sliced(seed, t, 256, np.asarray(SPLIT_BOUNDS, np.int32), segs, rank)
     return workloads.custom(seed, t, K, N, segs, rank)
+
+
+# A fine-tuning table whose backward dY B^T shrink passes are cut into 8 pieces instead of the default 4: 32 tiles
+# of 64 k-blocks (N = 4096), whose 160 default items would leave a last wave of 8 on 152 CTAs.
+RESPLIT_SMALL = dict(T=4096, K=256, N=4096, segs=[(i * 512, 512, i % 2, 1) for i in range(8)], rank=[16, 40])

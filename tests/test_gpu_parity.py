@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import Dev, compare, grad_split_table, to_np, train_blocks
+from gpu_util import RESPLIT_SMALL, Dev, compare, grad_split_table, to_np, train_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -195,6 +195,25 @@ def test_bf16_split_gradients():
     mA = np.ones(dA.numel(), bool)
     mA[ia] = False
     assert np.array_equal(to_np(aA)[mA], to_np(dA0)[mA])
+
+
+def test_bf16_backward_shrink_resplit():
+    """A fine-tuning batch whose dY B^T shrink passes the planner cuts into 8 pieces instead of the default 4 (32
+    tiles of 64 k-blocks: the default's 160 items leave a last wave of 8 on 152 CTAs; the count is pinned on the
+    CPU): dX on sampled rows, dA and dB whole, against the oracle."""
+    c = RESPLIT_SMALL
+    wl = workloads.custom(77, c["T"], c["K"], c["N"], c["segs"], c["rank"])
+    d = Dev(wl)
+    dX, dA, dB = d.backward()
+    import torch
+    torch.cuda.synchronize()
+    rows = wl.train_rows()[np.random.default_rng(5).choice(wl.T, 96, replace=False)]
+    rows = np.unique(np.concatenate([rows, [0, wl.T - 1]]))
+    rX, rA, rB = oracle.backward_wl(wl, dx_rows=rows)
+    compare(to_np(dX)[rows], rX, "dX (sampled rows)")
+    ia, ib = train_blocks(wl)
+    compare(to_np(dA)[ia], rA[ia], "dA")
+    compare(to_np(dB)[ib], rB[ib], "dB")
 
 
 def test_bf16_backward_small_batch_split_k():

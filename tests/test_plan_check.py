@@ -15,7 +15,7 @@ import pytest
 
 import lora_co_serving_gb300 as lm
 import workloads
-from gpu_util import grad_split_table
+from gpu_util import RESPLIT_SMALL, grad_split_table
 
 CSRC = os.path.join(os.path.dirname(lm.__file__), "csrc")
 INCLUDE = os.path.join(os.path.dirname(os.path.dirname(lm.__file__)), "include")
@@ -189,13 +189,14 @@ def _table_pool(K, N, rank):
     return lm.Pool(None, None, a_off, b_off, rank, np.full(rank.shape, 2.0, np.float32))
 
 
-@pytest.mark.parametrize("case", ["ftbwd_5120", "ftbwd_5120_reordered", "cosrv_8192x28672"])
+@pytest.mark.parametrize("case", ["ftbwd_5120", "ftbwd_5120_reordered", "cosrv_8192x28672", "small_4096x256x4096"])
 def test_backward_shrink_split_fills_waves(tmp_path, case):
     """The dY B^T passes of the backward shrink take the split count whose schedule ends first: on the 5120^2
     fine-tuning batch (32 tiles, 80 k-blocks a pass) 4 pieces of 20 k-blocks instead of 5 of 16 (288 items on 152
     CTAs: two waves, against 320, whose third wave holds 16 items), the same whatever the segment order; the x A
     recompute keeps the forward's 5 splits.  On the co-serving batch's fine-tuning rows (16 tiles, 448 k-blocks
-    a pass) the default 14 splits already fill two waves and stay."""
+    a pass) the default 14 splits already fill two waves and stay.  The small table of the GPU test of this split
+    (32 tiles, 64 k-blocks a pass: 160 items at the default leave 8 in a last wave) takes 8 pieces instead of 4."""
     lib = _build_driver(tmp_path, open(os.path.join(CSRC, "plan.cpp")).read())
     if case.startswith("ftbwd"):
         K = N = 5120
@@ -203,6 +204,9 @@ def test_backward_shrink_split_fills_waves(tmp_path, case):
         if case.endswith("reordered"):
             segs = segs[::-1]
         T, rank, want = 4096, [16], (32 * 4, 32 * 5)
+    elif case.startswith("small"):
+        T, K, N, segs, rank = (RESPLIT_SMALL[k] for k in ("T", "K", "N", "segs", "rank"))
+        want = (32 * 8, 32)
     else:
         K, N = 8192, 28672
         segs = [(t, 1, t % 7, 0) for t in range(2048)] + [(2048, 4096, 3, 0), (6144, 1024, 5, 1), (7168, 1024, 5, 1)]
