@@ -219,7 +219,8 @@ void put(std::vector<uint8_t>& blob, size_t off, const std::vector<T>& v) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Write the plan (tiles ... per-CTA lists) into a host blob laid out exactly like the workspace prefix.
+// Write the plan (tiles ... per-CTA item ranges) into a host blob laid out exactly like the workspace prefix.  Each
+// launch's items go in the order of its CTA lists, so that CTA c runs items [off[c], off[c + 1]) in place.
 void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&off)[3],
                 const std::vector<int32_t> (&lst)[3], std::vector<uint8_t>* blob) {
     blob->assign(L.plan_end - L.tiles, 0);
@@ -240,9 +241,10 @@ void build_blob(const Plan& pl, const Layout& L, const std::vector<int32_t> (&of
     put(b, at(L.splits), pl.splits);
     put(b, at(L.bgmv), pl.bgmv);
     for (int k = 0; k < 3; ++k) {
-        put(b, at(L.items[k]), pl.items[k]);
+        std::vector<WorkItem> ordered(lst[k].size());
+        for (size_t j = 0; j < ordered.size(); ++j) ordered[j] = pl.items[k][lst[k][j]];
+        put(b, at(L.items[k]), ordered);
         put(b, at(L.cta_off[k]), off[k]);
-        put(b, at(L.cta_list[k]), lst[k]);
     }
 }
 
@@ -256,7 +258,6 @@ void fill_plan_pointers(KParams* P, uint8_t* ws, const Layout& L, int launch) {
     P->tsegs = reinterpret_cast<const TrainSeg*>(ws + L.tsegs);
     P->items = reinterpret_cast<const WorkItem*>(ws + L.items[launch]);
     P->cta_off = reinterpret_cast<const int32_t*>(ws + L.cta_off[launch]);
-    P->cta_list = reinterpret_cast<const int32_t*>(ws + L.cta_list[launch]);
     P->atoms_a = reinterpret_cast<const int32_t*>(ws + L.atoms_a);
     P->atoms_b = reinterpret_cast<const int32_t*>(ws + L.atoms_b);
     P->boxes_a = reinterpret_cast<const int32_t*>(ws + L.boxes_a);

@@ -938,7 +938,6 @@ Layout layout_of(const Problem& p, const Plan& pl, bool backward) {
     for (int k = 0; k < 3; ++k) {
         L.items[k] = take(sizeof(WorkItem) * pl.items[k].size());
         L.cta_off[k] = take(sizeof(int32_t) * (std::max<size_t>(kMaxCtas, pl.items[k].size()) + 1));
-        L.cta_list[k] = take(sizeof(int32_t) * pl.items[k].size());
     }
     L.plan_end = at;
     if (p.dt == LORA_BF16) {

@@ -96,7 +96,7 @@ struct Layout {
     size_t counters = 0, zero_end = 0;   // [status, zero_end) is zeroed at the start of every call
     size_t tiles = 0, chunks = 0, rowmap = 0, rowchunk = 0, rowaux = 0, groups = 0, tsegs = 0;
     size_t atoms_a = 0, atoms_b = 0, boxes_a = 0, boxes_b = 0, units = 0, seg_flags = 0, splits = 0, bgmv = 0;
-    size_t items[3] = {0, 0, 0}, cta_off[3] = {0, 0, 0}, cta_list[3] = {0, 0, 0};
+    size_t items[3] = {0, 0, 0}, cta_off[3] = {0, 0, 0};
     size_t plan_end = 0;
     size_t xg = 0, z = 0, xat = 0, dybt = 0, part = 0, part_main = 0;
     size_t simt = 0;                 // float32 path scratch

@@ -229,7 +229,7 @@ __device__ void run_producer(const KParams& P, uint8_t* smem, uint32_t bar_full,
     const int lane = threadIdx.x & 31;
     Ring ring;
     for (int ii = i0; ii < i1; ++ii) {
-        const WorkItem w = P.items[P.cta_list[ii]];
+        const WorkItem w = P.items[ii];
         if (skipped_item(P, w)) continue;
         if (w.kind == kGradDb || w.kind == kGradDa) {
             // A: [128 of N or K] x 64 tokens, MN-major (two 64-wide boxes); B: r_pad rows of xA^T / dYB^T.  Items
@@ -309,7 +309,7 @@ __device__ void run_mma(const KParams& P, uint8_t* smem, uint32_t bar_full, uint
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int ii = i0; ii < i1; ++ii) {
-        const WorkItem w = P.items[P.cta_list[ii]];
+        const WorkItem w = P.items[ii];
         if (skipped_item(P, w)) continue;
         if (!wait_phase(bar_tempty + acc * 8, acc_phase ^ 1u, abort_flag, P.status)) return;
         tc_fence_after();
@@ -506,7 +506,7 @@ __device__ void run_epilogue(const KParams& P, uint32_t bar_tfull, uint32_t bar_
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int ii = i0; ii < i1; ++ii) {
-        const WorkItem w = P.items[P.cta_list[ii]];
+        const WorkItem w = P.items[ii];
         if (skipped_item(P, w)) continue;
         if (!wait_phase_long(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) return;
         tc_fence_after();
@@ -825,7 +825,7 @@ __device__ void run_producer2(const KParams& P, uint8_t* smem, uint32_t bar_full
     const uint32_t full_leader = mapa_shared(bar_full, 0);
     Ring2 ring;
     for (int ii = i0; ii < i1; ++ii) {
-        const WorkItem w = P.items[P.cta_list[ii]];
+        const WorkItem w = P.items[ii];
         const TileDesc td = P.tiles[w.tile + rank];
         const bool fwd = (w.kind == kMainFwd);
         const CUtensorMap* ma = fwd ? (td.a_src ? &P.tm_xg : &P.tm_x) : &P.tm_dy;
@@ -926,7 +926,7 @@ __device__ void run_mma2(const KParams& P, uint8_t* smem, uint32_t bar_full, uin
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int ii = i0; ii < i1; ++ii) {
-        const WorkItem w = P.items[P.cta_list[ii]];
+        const WorkItem w = P.items[ii];
         if (!wait_phase(bar_tempty + acc * 8, acc_phase ^ 1u, abort_flag, P.status)) return;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)acc * kBN;
@@ -1007,7 +1007,7 @@ __device__ void run_epilogue2(const KParams& P, uint32_t bar_tfull, uint32_t bar
     uint32_t acc_phase = 0;
     uint32_t nstore = 0;      // TMA stores issued by this warp (their buffers alternate)
     for (int ii = i0; ii < i1; ++ii) {
-        const WorkItem w = P.items[P.cta_list[ii]];
+        const WorkItem w = P.items[ii];
         if (!wait_phase_long(bar_tfull + acc * 8, acc_phase, abort_flag, P.status)) break;
         tc_fence_after();
         const uint32_t taddr = tmem + (uint32_t)acc * kBN + ((uint32_t)(quarter * 32) << 16);

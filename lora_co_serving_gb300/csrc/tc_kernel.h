@@ -38,9 +38,8 @@ struct KParams {   // CUtensorMap members keep the 64-byte alignment the TMA uni
     const int32_t* rowaux;
     const GradGroup* groups;
     const TrainSeg* tsegs;
-    const WorkItem* items;
+    const WorkItem* items;   // in CTA order: CTA (pair, in the main pass) c runs items [cta_off[c], cta_off[c + 1])
     const int32_t* cta_off;
-    const int32_t* cta_list;
     const int32_t* atoms_a;  // per tile, per 8 LoRA columns: A-pool row of the atom
     const int32_t* atoms_b;  // same for the B pool
     const int32_t* boxes_a;  // per atom: atoms in the TMA box that starts at it (0: covered by an earlier box)
