@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import RESPLIT_SMALL, Dev, compare, grad_split_table, to_np, train_blocks
+from gpu_util import RESPLIT_SMALL, Dev, compare, grad_split_table, random_table, to_np, train_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -254,38 +254,6 @@ def test_max_fine_tuning_segments():
     _, xs = d.forward(save_xa=True)
     check_backward(wl, d, xa_saved=xs, recompute=False)
     check_backward(wl, d)
-
-
-def random_table(seed):
-    """A seeded random call: K and N up to 520 (multiples of 8 for bf16, any size for f32), 1..20 adapters of
-    ranks 1..128 (a few absent from the table), decode tokens, prefill segments of 2..300 tokens, fine-tuning
-    segments of 1..260 tokens (at most 12), some base-only tokens, the table listed in shuffled order."""
-    rng = np.random.default_rng(9000 + seed)
-    dtype = "f32" if seed % 4 == 3 else "bf16"
-    if dtype == "bf16":
-        K, N = 8 * int(rng.integers(1, 66)), 8 * int(rng.integers(1, 66))
-    else:
-        K, N = int(rng.integers(1, 300)), int(rng.integers(1, 300))
-    n_ad = int(rng.integers(1, 21))
-    rank = [int(rng.integers(1, 129)) for _ in range(n_ad)]
-    segs, t, n_train = [], 0, 0
-    for _ in range(int(rng.integers(1, 40))):
-        kind = int(rng.integers(0, 4))
-        if kind == 0:                                 # decode tokens (some base-only)
-            for _ in range(int(rng.integers(1, 30))):
-                segs.append((t, 1, int(rng.integers(-1, n_ad)), 0))
-                t += 1
-        elif kind == 1:
-            ln = int(rng.integers(2, 301))
-            segs.append((t, ln, int(rng.integers(-1, n_ad)), 0))
-            t += ln
-        elif n_train < 12:
-            ln = int(rng.integers(1, 261))
-            segs.append((t, ln, int(rng.integers(0, n_ad)), 1))
-            t += ln
-            n_train += 1
-    order = rng.permutation(len(segs))
-    return workloads.custom(5000 + seed, t, K, N, [segs[i] for i in order], rank, dtype=dtype), n_train
 
 
 @pytest.mark.parametrize("seed", range(16))

@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import MAX_ERR, Dev, compare, to_dev, to_np, train_blocks
+from gpu_util import MAX_ERR, Dev, compare, random_table, to_dev, to_np, train_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -146,3 +146,36 @@ def test_sliced_backward_reads_saved_xa():
     compare(to_np(dB)[ib], sB[ib], "sliced dB from the captured xA")
     compare(to_np(dA)[ia], rA[ia], "sliced dA")
     compare(to_np(dX)[wl.train_rows()], rX, "sliced dX")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 3, 4, 7, 11])
+def test_flag_table_random_tables(seed):
+    """The flag table on seeded random calls (ragged shapes, bf16 and f32, up to 12 fine-tuning segments on ranks
+    1..128): a random subset of segments flagged saved, given a substituted captured xA; the others recompute and
+    their captured blocks hold NaN.  dB against the oracle on the same mix of captured and exact activations."""
+    import torch
+    import lora_co_serving_gb300 as lm
+    wl, n_train = random_table(seed)
+    assert n_train > 0
+    d = Dev(wl)
+    blocks = _blocks(wl)
+    n = blocks[-1][1]
+    sub = _substitute(wl, n, 60 + seed)
+    _, u = oracle.forward_wl(wl, want_u=True)
+    exact = oracle.saved_u(wl, u)
+    rX, rA, _ = oracle.backward_wl(wl)
+    ia, ib = train_blocks(wl)
+    pattern = [int(v) for v in np.random.default_rng(900 + seed).integers(0, 2, len(blocks))]
+    ours = np.full(n, np.nan, np.float32)
+    ref_u = exact.copy()
+    for (lo, hi), f in zip(blocks, pattern):
+        if f:
+            ours[lo:hi] = sub[lo:hi]
+            ref_u[lo:hi] = sub[lo:hi]
+    _, _, sB = oracle.backward_wl(wl, want_dx=False, u_saved=ref_u)
+    flags = torch.tensor(pattern, dtype=torch.int32, device="cuda")
+    dX, dA, dB = lm.backward_flagged(d.x, d.Wt, d.pool, wl.segs, d.dY, to_dev(ours, wl.dtype), flags)
+    torch.cuda.synchronize()
+    compare(to_np(dB)[ib], sB[ib], "dB %s" % pattern)
+    compare(to_np(dA)[ia], rA[ia], "dA %s" % pattern)
+    compare(to_np(dX)[wl.train_rows()], rX, "dX %s" % pattern)

@@ -164,3 +164,43 @@ def test_sliced_split_gradients():
     from gpu_util import grad_split_table
     wl = grad_split_table(sliced=True)
     check_backward(wl, Dev(wl))
+
+
+def random_sliced(seed):
+    """A seeded random call on a sliced layer: 2..4 slices (all but the last a multiple of 256 wide, the last any
+    multiple of 8), K up to 520, 1..12 adapters of ranks 1..128, decode, prefill, fine-tuning and base-only segments
+    listed in shuffled order."""
+    rng = np.random.default_rng(7100 + seed)
+    S = int(rng.integers(2, 5))
+    widths = [256 * int(rng.integers(1, 3)) for _ in range(S - 1)] + [8 * int(rng.integers(1, 33))]
+    bounds = np.concatenate([[0], np.cumsum(widths)]).astype(np.int32)
+    K = 8 * int(rng.integers(1, 66))
+    n_ad = int(rng.integers(1, 13))
+    rank = [int(rng.integers(1, 129)) for _ in range(n_ad)]
+    segs, t, n_train = [], 0, 0
+    for _ in range(int(rng.integers(1, 25))):
+        kind = int(rng.integers(0, 4))
+        if kind == 0:
+            for _ in range(int(rng.integers(1, 20))):
+                segs.append((t, 1, int(rng.integers(-1, n_ad)), 0))
+                t += 1
+        elif kind == 1:
+            ln = int(rng.integers(2, 260))
+            segs.append((t, ln, int(rng.integers(-1, n_ad)), 0))
+            t += ln
+        elif n_train < 8:
+            ln = int(rng.integers(1, 200))
+            segs.append((t, ln, int(rng.integers(0, n_ad)), 1))
+            t += ln
+            n_train += 1
+    order = rng.permutation(len(segs))
+    return workloads.sliced(7300 + seed, t, K, bounds, [segs[i] for i in order], rank), n_train
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_sliced_random_tables(seed):
+    wl, n_train = random_sliced(seed)
+    d, y, xs = check_forward(wl)
+    if n_train:
+        check_backward(wl, d)          # recompute xA
+        check_backward(wl, d, xs)      # from the saved xA
