@@ -120,10 +120,13 @@ int validate(int32_t T, int32_t K, int32_t N, lora_dtype_t dt, const lora_pool_t
 //   sliced, backward:    one adapter; its slices side by side, slice i at [i rp, i rp + r), rp = roundup(r, 16)
 static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int32_t* row_ad, const int32_t* row_aux,
                      TileDesc t0, TileDesc t1, bool backward) {
+    // rows come in runs of one adapter (consecutive tokens of a segment, or gathered rows sorted by adapter): an id
+    // is collected once per run, then sorted and made unique
     std::vector<int32_t> A, B;
     for (int i = 0; i < kTileM; ++i) {
-        if (row_ad[i] >= 0) A.push_back(row_ad[i]);
-        if (row_ad[kTileM + i] >= 0) B.push_back(row_ad[kTileM + i]);
+        if (row_ad[i] >= 0 && (A.empty() || A.back() != row_ad[i])) A.push_back(row_ad[i]);
+        const int32_t b = row_ad[kTileM + i];
+        if (b >= 0 && (B.empty() || B.back() != b)) B.push_back(b);
     }
     std::sort(A.begin(), A.end());
     A.erase(std::unique(A.begin(), A.end()), A.end());
@@ -226,10 +229,16 @@ static void add_pair(const Problem& p, Plan* pl, const int32_t* rows, const int3
     t0.sh_c1 = A.empty() ? 0 : end_a;
     t1.sh_c0 = B.empty() ? zcol : start_b;
     t1.sh_c1 = zcol;
+    int32_t run_ad = -1, run_rc = -1;     // the chunk of the current run's adapter
     for (int i = 0; i < 2 * kTileM; ++i) {
         int32_t rc = -1;
-        if (row_ad[i] >= 0)
-            rc = chunk0 + int32_t(std::find(order.begin(), order.end(), row_ad[i]) - order.begin());
+        if (row_ad[i] >= 0) {
+            if (row_ad[i] != run_ad) {
+                run_ad = row_ad[i];
+                run_rc = chunk0 + int32_t(std::find(order.begin(), order.end(), run_ad) - order.begin());
+            }
+            rc = run_rc;
+        }
         pl->rowmap.push_back(rows[i]);
         pl->rowchunk.push_back(rc);
         pl->rowaux.push_back(row_aux ? row_aux[i] : -1);
@@ -297,20 +306,13 @@ static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk, siz
     // the order of the output tiles (pair q, column tile nt): bands of kBandTiles tile rows sweeping every column
     // tile before the next band (column bands, alternating sweep directions and bands of 8 or 32 tile rows measured
     // alike)
-    std::vector<std::pair<size_t, int32_t>> order;
-    order.reserve(n_pairs * (size_t)n_nt);
+    pl->items[1].reserve(pl->items[1].size() + (size_t)tiles_out * (split_all ? nsb_all + 2 : 1));
+    int64_t o = 0;                   // output tiles emitted so far
+    std::vector<int32_t> cuts;       // LoRA split bounds (Z columns) of the current pair
     for (size_t b0 = 0; b0 < n_pairs; b0 += band) {
         const size_t b1 = std::min(n_pairs, b0 + band);
         for (int32_t nt = 0; nt < n_nt; ++nt)
-            for (size_t q = b0; q < b1; ++q) order.push_back({q, nt});
-    }
-    int64_t o = 0;                   // output tiles emitted so far
-    std::vector<int32_t> cuts;       // LoRA split bounds (Z columns) of the current pair
-    for (const auto& qn : order) {
-        {
-            const size_t q = qn.first;
-            const int32_t nt = qn.second;
-            {
+            for (size_t q = b0; q < b1; ++q) {
                 const int32_t tile = tile_of(q, nt);
                 const TileDesc& td = pl->tiles[tile];
                 const bool split = split_all || o >= tail_from;
@@ -356,7 +358,6 @@ static void add_main_items(Plan* pl, int32_t kind, int32_t n_nt, int32_t nk, siz
                 }
                 ++o;
             }
-        }
     }
 }
 
