@@ -374,14 +374,12 @@ void plan_forward(const Problem& p, Plan* out) {
     // classify rows: long (windowed) or short (gathered)
     std::vector<int32_t> row_seg(p.T);
     std::vector<uint8_t> is_long(p.T, 0);
-    std::vector<std::pair<int64_t, int32_t>> gathered;   // (sort key, row)
     for (size_t i = 0; i < p.segs.size(); ++i) {
         const auto& s = p.segs[i];
         bool shortseg = s.len < kShortSegment && !s.is_train;
         for (int32_t t = s.start; t < s.start + s.len; ++t) {
             row_seg[t] = int32_t(i);
-            if (shortseg) gathered.push_back({((int64_t)(s.adapter_id + 1) << 32) | (uint32_t)t, t});
-            else is_long[t] = 1;
+            if (!shortseg) is_long[t] = 1;
         }
     }
     // per pair: token rows, their adapters and saved-activation offsets
@@ -412,11 +410,21 @@ void plan_forward(const Problem& p, Plan* out) {
         add_pair(p, &pl, rows, row_ad, row_aux, t0, t1, false);
         t = w0 + 2 * kTileM;
     }
-    // gathered pairs: short rows sorted by (adapter, row)
-    std::sort(gathered.begin(), gathered.end());
+    // gathered pairs: short rows sorted by (adapter, row) -- a counting sort by adapter (base-only rows first) of
+    // the short rows taken in row order
+    std::vector<int32_t> gathered;
+    {
+        std::vector<int64_t> at(p.n_adapters + 2, 0);
+        for (int32_t t = 0; t < p.T; ++t)
+            if (!is_long[t]) at[p.segs[row_seg[t]].adapter_id + 2]++;
+        for (size_t a = 1; a < at.size(); ++a) at[a] += at[a - 1];
+        gathered.resize(at.back());
+        for (int32_t t = 0; t < p.T; ++t)
+            if (!is_long[t]) gathered[at[p.segs[row_seg[t]].adapter_id + 1]++] = t;
+    }
     pl.g_tile0 = int32_t(pl.tiles.size());
     for (size_t g0 = 0; g0 < gathered.size(); g0 += 2 * kTileM) {
-        for (int i = 0; i < 2 * kTileM; ++i) fill(i, (g0 + i < gathered.size()) ? gathered[g0 + i].second : -1);
+        for (int i = 0; i < 2 * kTileM; ++i) fill(i, (g0 + i < gathered.size()) ? gathered[g0 + i] : -1);
         TileDesc t0{}, t1{};
         t0.a_src = t1.a_src = 1;
         t0.a_row0 = pl.n_gtiles * kTileM;
