@@ -880,34 +880,27 @@ static int64_t item_cost(const WorkItem& w) {
 
 void assign_items(const std::vector<WorkItem>& items, const Plan&, int G, std::vector<int32_t>* off,
                   std::vector<int32_t>* list) {
-    // min-heap of (load, CTA) in a flat array: each item goes to the least-loaded CTA (ties: lowest index)
-    struct Slot {
-        int64_t load;
-        int32_t cta;
+    // each item goes to the least-loaded CTA (ties: lowest index), found in a tournament tree over the CTAs: a node
+    // holds the CTA with the least (load, index) below it, and an assignment replays only the grown leaf's path
+    int P2 = 1;
+    while (P2 < G) P2 <<= 1;
+    std::vector<int64_t> load(G, 0);
+    std::vector<int32_t> win(2 * (size_t)P2, -1);      // -1: no CTA below
+    auto better = [&](int32_t a, int32_t b) {
+        if (a < 0) return b;
+        if (b < 0) return a;
+        return (load[b] < load[a] || (load[b] == load[a] && b < a)) ? b : a;
     };
-    auto less = [](const Slot& a, const Slot& b) { return a.load < b.load || (a.load == b.load && a.cta < b.cta); };
-    std::vector<Slot> heap(G);
-    for (int c = 0; c < G; ++c) heap[c] = Slot{0, c};
+    for (int c = 0; c < G; ++c) win[P2 + c] = c;
+    for (int n = P2 - 1; n >= 1; --n) win[n] = better(win[2 * n], win[2 * n + 1]);
     std::vector<int32_t> owner(items.size());
     std::vector<int32_t> count(G + 1, 0);
     for (size_t i = 0; i < items.size(); ++i) {
-        Slot top = heap[0];
-        owner[i] = top.cta;
-        count[top.cta + 1]++;
-        top.load += item_cost(items[i]);
-        // sift the grown root down
-        size_t j = 0;
-        for (;;) {
-            const size_t l = 2 * j + 1, r = l + 1;
-            size_t best = j;
-            const Slot* bs = &top;
-            if (l < heap.size() && less(heap[l], *bs)) { best = l; bs = &heap[l]; }
-            if (r < heap.size() && less(heap[r], *bs)) { best = r; bs = &heap[r]; }
-            if (best == j) break;
-            heap[j] = heap[best];
-            j = best;
-        }
-        heap[j] = top;
+        const int32_t c = win[1];
+        owner[i] = c;
+        count[c + 1]++;
+        load[c] += item_cost(items[i]);
+        for (int n = (P2 + c) >> 1; n >= 1; n >>= 1) win[n] = better(win[2 * n], win[2 * n + 1]);
     }
     off->assign(G + 1, 0);
     for (int c = 0; c < G; ++c) (*off)[c + 1] = (*off)[c] + count[c + 1];
