@@ -878,6 +878,8 @@ static int64_t item_cost(const WorkItem& w) {
     return c + 2000;
 }
 
+int64_t item_cost_estimate(const WorkItem& w) { return item_cost(w); }
+
 void assign_items(const std::vector<WorkItem>& items, const Plan&, int G, std::vector<int32_t>* off,
                   std::vector<int32_t>* list) {
     // each item goes to the least-loaded CTA (ties: lowest index), found in a tournament tree over the CTAs: a node

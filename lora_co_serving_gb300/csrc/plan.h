@@ -89,6 +89,8 @@ int check_plan(const Problem& p, const Plan& pl, bool backward, std::string* err
 // off has G+1 entries; list holds item indices grouped by CTA, each CTA's in increasing order.
 void assign_items(const std::vector<WorkItem>& items, const Plan& plan, int G, std::vector<int32_t>* off,
                   std::vector<int32_t>* list);
+// The estimated cost (cycles) by which assign_items balances the CTAs.
+int64_t item_cost_estimate(const WorkItem& w);
 
 // Byte offsets of everything a call keeps in the workspace.
 struct Layout {

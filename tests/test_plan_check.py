@@ -110,6 +110,39 @@ extern "C" int grad_items(int T, int K, int N, const lora_pool_t* pool, const lo
     lora::plan_backward(p, true, true, true, true, &pl);
     return int(pl.items[2].size());
 }
+// assign_items on n random items over G CTAs against a plain greedy (each item, in order, to the CTA with the least
+// summed estimated cost, the lowest index on a tie): 0 when the two agree
+extern "C" int assign_matches_greedy(int n, int G, unsigned seed) {
+    std::vector<lora::WorkItem> items(n);
+    unsigned x = seed * 2654435761u + 1u;
+    auto rnd = [&](unsigned m) { x ^= x << 13; x ^= x >> 17; x ^= x << 5; return int(x % m); };
+    for (auto& w : items) {
+        w = lora::WorkItem{};
+        w.kind = rnd(7);
+        w.nk = 1 + rnd(200);
+        w.n_ext = rnd(40);
+        w.mma_n = 16 * (1 + rnd(16));
+    }
+    lora::Plan pl;
+    std::vector<int32_t> off, lst;
+    lora::assign_items(items, pl, G, &off, &lst);
+    std::vector<int64_t> load(G, 0);
+    std::vector<std::vector<int32_t>> mine(G);
+    for (int i = 0; i < n; ++i) {
+        int best = 0;
+        for (int c = 1; c < G; ++c)
+            if (load[c] < load[best]) best = c;
+        load[best] += lora::item_cost_estimate(items[i]);
+        mine[best].push_back(i);
+    }
+    if ((int)off.size() != G + 1 || (int)lst.size() != n) return 1;
+    for (int c = 0; c < G; ++c) {
+        if (off[c + 1] - off[c] != (int)mine[c].size()) return 2;
+        for (size_t j = 0; j < mine[c].size(); ++j)
+            if (lst[off[c] + j] != mine[c][j]) return 3;
+    }
+    return 0;
+}
 // backward shrink items: out[0] of the dY B^T passes, out[1] of the x A recompute (-1: the table does not validate)
 extern "C" int bwd_shrink_items(int T, int K, int N, const lora_pool_t* pool, const lora_segment_t* segs, int n,
                                 int* out) {
@@ -137,6 +170,7 @@ def _build_driver(tmp_path, src):
     lib.check_table.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
     lib.grad_items.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3 + [ctypes.c_int]
     lib.bwd_shrink_items.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_void_p]
+    lib.assign_matches_greedy.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint]
     return lib
 
 
@@ -217,3 +251,13 @@ def test_backward_shrink_split_fills_waves(tmp_path, case):
     assert lib.bwd_shrink_items(T, K, N, pool.cptr(), s.ctypes.data, s.shape[0], out) == 0
     assert (out[0], out[1]) == want
     assert lib.check_table(T, K, N, pool.cptr(), s.ctypes.data, s.shape[0], 1) == 0
+
+
+def test_item_assignment_is_the_plain_greedy(tmp_path):
+    """The persistent launches' item lists: every item, in plan order, to the CTA with the least summed estimated
+    cost so far (the lowest index on a tie), for random costs and CTA counts that are and are not powers of two,
+    fewer CTAs than items and more."""
+    lib = _build_driver(tmp_path, open(os.path.join(CSRC, "plan.cpp")).read())
+    for n, G in [(1, 1), (5, 1), (3, 8), (100, 76), (3584, 76), (452, 152), (1000, 7), (64, 64), (129, 128)]:
+        for seed in range(3):
+            assert lib.assign_matches_greedy(n, G, seed) == 0, (n, G, seed)
