@@ -729,26 +729,26 @@ int check_plan(const Problem& p, const Plan& pl, bool backward, std::string* err
     };
     for (int64_t i = 0; i < nt; ++i) {
         const TileDesc& td = pl.tiles[i];
-        const std::string at = "tile " + std::to_string(i) + ": ";
+        auto at = [&] { return "tile " + std::to_string(i) + ": "; };   // built only for a report
         // a window's second tile may start past the last row (its rows then read as zero)
         if (td.a_src == 0 ? (td.a_row0 < 0 || td.a_row0 >= p.T + kTileM) : (td.a_row0 < 0 || td.a_row0 + kTileM > g_rows))
-            return bad(at + "row window outside its source");
-        if (td.chunk0 < 0 || td.nchunk < 0 || td.chunk0 + td.nchunk > n_chunks) return bad(at + "chunk range");
-        if (td.ext_k < 0 || td.ext_k % 16 != 0) return bad(at + "LoRA columns not a multiple of 16");
-        if (td.atom0 < 0 || td.atom0 + cdiv(z_cols(td), 8) > n_atoms) return bad(at + "atom range");
-        if (td.z_blk0 < 0 || td.z_blk0 + cdiv(td.ext_k, kBK) > pl.z_blocks) return bad(at + "Z blocks");
-        if (td.sh_c0 < 0 || td.sh_c0 > td.sh_c1 || td.sh_c1 > td.ext_k) return bad(at + "shrink columns");
+            return bad(at() + "row window outside its source");
+        if (td.chunk0 < 0 || td.nchunk < 0 || td.chunk0 + td.nchunk > n_chunks) return bad(at() + "chunk range");
+        if (td.ext_k < 0 || td.ext_k % 16 != 0) return bad(at() + "LoRA columns not a multiple of 16");
+        if (td.atom0 < 0 || td.atom0 + cdiv(z_cols(td), 8) > n_atoms) return bad(at() + "atom range");
+        if (td.z_blk0 < 0 || td.z_blk0 + cdiv(td.ext_k, kBK) > pl.z_blocks) return bad(at() + "Z blocks");
+        if (td.sh_c0 < 0 || td.sh_c0 > td.sh_c1 || td.sh_c1 > td.ext_k) return bad(at() + "shrink columns");
         if (backward && (td.tpos0 < 0 || td.tpos0 + kTileM > pl.tcols || td.seg < 0 ||
                          td.seg >= int32_t(pl.tsegs.size())))
-            return bad(at + "transposed-buffer columns or segment");
+            return bad(at() + "transposed-buffer columns or segment");
         for (int r = 0; r < kTileM; ++r) {
             const int64_t k = i * kTileM + r;
             const int32_t t = pl.rowmap[k], c = pl.rowchunk[k], aux = pl.rowaux[k];
-            if (t < -1 || t >= p.T) return bad(at + "row " + std::to_string(r) + " maps outside [0, T)");
-            if (c != -1 && (c < td.chunk0 || c >= td.chunk0 + td.nchunk)) return bad(at + "row chunk outside the tile");
+            if (t < -1 || t >= p.T) return bad(at() + "row " + std::to_string(r) + " maps outside [0, T)");
+            if (c != -1 && (c < td.chunk0 || c >= td.chunk0 + td.nchunk)) return bad(at() + "row chunk outside the tile");
             if (aux != -1) {
-                if (c < 0) return bad(at + "saved-activation offset on a row without an adapter");
-                if (aux < 0 || aux + int64_t(p.S) * pl.chunks[c].r > p.xa_elems) return bad(at + "saved-activation offset");
+                if (c < 0) return bad(at() + "saved-activation offset on a row without an adapter");
+                if (aux < 0 || aux + int64_t(p.S) * pl.chunks[c].r > p.xa_elems) return bad(at() + "saved-activation offset");
             }
         }
     }
@@ -784,47 +784,47 @@ int check_plan(const Problem& p, const Plan& pl, bool backward, std::string* err
     for (int k = 0; k < 3; ++k) {
         for (size_t j = 0; j < pl.items[k].size(); ++j) {
             const WorkItem& w = pl.items[k][j];
-            const std::string at = "item " + std::to_string(k) + "." + std::to_string(j) + ": ";
-            if (w.mma_n < 16 || w.mma_n > kPassCols || w.mma_n % 16 != 0) return bad(at + "MMA N");
+            auto at = [&] { return "item " + std::to_string(k) + "." + std::to_string(j) + ": "; };
+            if (w.mma_n < 16 || w.mma_n > kPassCols || w.mma_n % 16 != 0) return bad(at() + "MMA N");
             if (w.kind == kMainFwd || w.kind == kMainDx) {
-                if (w.tile < 0 || w.tile + 1 >= nt) return bad(at + "tile pair");
-                if (w.n0 < 0 || w.n0 >= out_cols) return bad(at + "output columns");
-                if (w.kb0 < 0 || w.nk < 0 || w.kb0 + w.nk > kb_main) return bad(at + "k-blocks");
+                if (w.tile < 0 || w.tile + 1 >= nt) return bad(at() + "tile pair");
+                if (w.n0 < 0 || w.n0 >= out_cols) return bad(at() + "output columns");
+                if (w.kb0 < 0 || w.nk < 0 || w.kb0 + w.nk > kb_main) return bad(at() + "k-blocks");
                 const int32_t ek = pl.tiles[w.tile].ext_k;
-                if (w.ext_c0 < 0 || w.ext_c0 > w.ext_c1 || w.ext_c1 > ek) return bad(at + "LoRA columns");
-                if (w.ext_c0 / kBK + w.n_ext > cdiv(ek, kBK)) return bad(at + "LoRA k-blocks");
-                if (w.nsplit > 1 && (w.part < 0 || w.part + w.split >= pl.main_slots)) return bad(at + "split slot");
+                if (w.ext_c0 < 0 || w.ext_c0 > w.ext_c1 || w.ext_c1 > ek) return bad(at() + "LoRA columns");
+                if (w.ext_c0 / kBK + w.n_ext > cdiv(ek, kBK)) return bad(at() + "LoRA k-blocks");
+                if (w.nsplit > 1 && (w.part < 0 || w.part + w.split >= pl.main_slots)) return bad(at() + "split slot");
             } else if (w.kind == kGradDb || w.kind == kGradDa) {
-                if (w.tile < 0 || w.tile >= int32_t(pl.groups.size())) return bad(at + "gradient group");
+                if (w.tile < 0 || w.tile >= int32_t(pl.groups.size())) return bad(at() + "gradient group");
                 const GradGroup& g = pl.groups[w.tile];
-                if (w.n0 < 0 || w.n0 >= (w.kind == kGradDb ? p.N : p.K)) return bad(at + "gradient rows");
-                if (w.j0 < 0 || w.j0 + w.mma_n > int64_t(p.S) * LORA_MAX_RANK) return bad(at + "transposed rows");
-                if (w.kind == kGradDa && w.j0 >= int64_t(g.nslice) * g.r) return bad(at + "down-factor rows");
+                if (w.n0 < 0 || w.n0 >= (w.kind == kGradDb ? p.N : p.K)) return bad(at() + "gradient rows");
+                if (w.j0 < 0 || w.j0 + w.mma_n > int64_t(p.S) * LORA_MAX_RANK) return bad(at() + "transposed rows");
+                if (w.kind == kGradDa && w.j0 >= int64_t(g.nslice) * g.r) return bad(at() + "down-factor rows");
                 if (g.seg0 < 0 || g.nseg < 1 || g.seg0 + g.nseg > int32_t(pl.tsegs.size()))
-                    return bad(at + "gradient group segments");
+                    return bad(at() + "gradient group segments");
                 int64_t blocks = 0;                  // token blocks of the group's segments
                 for (int32_t q = 0; q < g.nseg; ++q) blocks += cdiv(pl.tsegs[g.seg0 + q].len, kBK);
-                if (w.kb0 < 0 || w.nk < 1 || w.kb0 + w.nk > blocks) return bad(at + "token blocks");
+                if (w.kb0 < 0 || w.nk < 1 || w.kb0 + w.nk > blocks) return bad(at() + "token blocks");
                 if (w.nsplit > 1) {
                     if (w.n_ext < 0 || w.n_ext >= int32_t(pl.units.size()) || pl.units[w.n_ext].kind != w.kind ||
                         pl.units[w.n_ext].tile != w.tile || pl.units[w.n_ext].nsplit != w.nsplit ||
                         w.split < 0 || w.split >= w.nsplit)
-                        return bad(at + "split unit");
+                        return bad(at() + "split unit");
                     const ShrinkUnit& su = pl.units[w.n_ext];
                     if (su.mma_n != w.mma_n || w.part != su.part0 + w.split * w.mma_n)
-                        return bad(at + "partial columns");
+                        return bad(at() + "partial columns");
                 }
             } else {
-                if (w.tile < 0 || w.tile >= nt) return bad(at + "tile");
+                if (w.tile < 0 || w.tile >= nt) return bad(at() + "tile");
                 if (w.n_ext < 0 || w.n_ext >= int32_t(pl.units.size()) || pl.units[w.n_ext].tile != w.tile)
-                    return bad(at + "shrink unit");
+                    return bad(at() + "shrink unit");
                 const TileDesc& td = pl.tiles[w.tile];
                 const int64_t kb_all = cdiv(w.kind == kShrinkDyb ? p.N : p.K, kBK);
-                if (w.kb0 < 0 || w.nk < 1 || w.kb0 + w.nk > kb_all) return bad(at + "k-blocks");
+                if (w.kb0 < 0 || w.nk < 1 || w.kb0 + w.nk > kb_all) return bad(at() + "k-blocks");
                 if (w.n0 < 0 || w.n0 + w.mma_n > cdiv(z_cols(td), 16) * 16 || td.atom0 + (w.n0 + w.mma_n) / 8 > n_atoms)
-                    return bad(at + "LoRA columns");
-                if (w.part < 0 || w.part + w.mma_n > pl.part_cols) return bad(at + "partial columns");
-                if (w.kind != kShrinkXa && td.z_blk0 + cdiv(w.n0 + w.mma_n, kBK) > pl.z_blocks) return bad(at + "Z blocks");
+                    return bad(at() + "LoRA columns");
+                if (w.part < 0 || w.part + w.mma_n > pl.part_cols) return bad(at() + "partial columns");
+                if (w.kind != kShrinkXa && td.z_blk0 + cdiv(w.n0 + w.mma_n, kBK) > pl.z_blocks) return bad(at() + "Z blocks");
             }
         }
     }
@@ -836,16 +836,16 @@ int check_plan(const Problem& p, const Plan& pl, bool backward, std::string* err
     }
     for (size_t i = 0; i < pl.bgmv.size(); ++i) {
         const BgmvGroup& g = pl.bgmv[i];
-        const std::string at = "decode-shrink unit " + std::to_string(i) + ": ";
-        if (g.g_row0 < 0 || g.n_rows < 1 || g.n_rows > kBgmvRows || g.g_row0 + g.n_rows > g_rows) return bad(at + "rows");
-        if (g.tile < pl.g_tile0 || g.tile >= nt || g.row0 < 0 || g.row0 + g.n_rows > kTileM) return bad(at + "tile rows");
+        auto at = [&] { return "decode-shrink unit " + std::to_string(i) + ": "; };
+        if (g.g_row0 < 0 || g.n_rows < 1 || g.n_rows > kBgmvRows || g.g_row0 + g.n_rows > g_rows) return bad(at() + "rows");
+        if (g.tile < pl.g_tile0 || g.tile >= nt || g.row0 < 0 || g.row0 + g.n_rows > kTileM) return bad(at() + "tile rows");
         if (g.chunk >= 0) {
-            if (g.chunk >= n_chunks) return bad(at + "chunk");
+            if (g.chunk >= n_chunks) return bad(at() + "chunk");
             const Chunk& ch = pl.chunks[g.chunk];
-            if (g.j0 < 0 || g.j0 >= int64_t(p.S) * ch.r) return bad(at + "LoRA columns");
+            if (g.j0 < 0 || g.j0 >= int64_t(p.S) * ch.r) return bad(at() + "LoRA columns");
             const TileDesc& td = pl.tiles[g.tile];
             const int64_t last = int64_t(p.S - 1) * td.zstride + ch.zcol + ch.r;   // one past the last Z column
-            if (last > cdiv(z_cols(td), kBK) * kBK) return bad(at + "Z columns");
+            if (last > cdiv(z_cols(td), kBK) * kBK) return bad(at() + "Z columns");
         }
     }
     for (size_t q = 0; q < pl.tsegs.size(); ++q) {
